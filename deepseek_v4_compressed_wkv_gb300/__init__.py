@@ -1,0 +1,265 @@
+"""GB300 (sm_103a) compressed-sparse-attention KV Compressor.
+
+Thin Python binding over the C ABI in ``include/csa.h`` (``libcsa.so``): it only marshals
+arguments.  PyTorch provides device memory and streams; every step of the compressor runs
+in the library's CUDA kernels.  There is no CPU path: if the library is missing or no GPU
+is present, calls fail with an error.
+
+    from deepseek_v4_compressed_wkv_gb300 import Compressor
+    c = Compressor(dim=4096, head_dim=512, ratio=4, overlap=1)
+    c.set_weights(wkv, wgate, gain)          # f32 CUDA tensors [C, dim], [C, dim], [H]
+    out = c.prefill(x)                       # x bf16 CUDA [B, N, dim] -> dict of tensors or None
+    step = c.decode(x_tok, start_pos)        # x_tok bf16 [B, dim], start_pos int32 CUDA [B]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build_mod
+
+__all__ = ["Compressor", "CSAError", "load_library", "fp4_e4m3_roundtrip", "rope_table", "default_options",
+           "library_path", "ABI_FUNCTIONS"]
+
+_lock = threading.Lock()
+_lib = None
+
+# every entry point declared in include/csa.h
+ABI_FUNCTIONS = ("csa_options_default", "csa_compressor_create", "csa_compressor_set_weights",
+                 "csa_compress_prefill", "csa_compress_decode", "csa_state_reset", "csa_state_elems",
+                 "csa_state_export", "csa_device_status", "csa_compressor_destroy", "csa_last_error",
+                 "csa_fp4_e4m3_roundtrip", "csa_rope_table")
+
+
+class CSAError(RuntimeError):
+    pass
+
+
+class Options(ctypes.Structure):
+    _fields_ = [("max_batch", ctypes.c_int), ("rope_dim", ctypes.c_int), ("rope_base", ctypes.c_float),
+                ("rope_factor", ctypes.c_float), ("rope_orig_len", ctypes.c_int), ("beta_fast", ctypes.c_float),
+                ("beta_slow", ctypes.c_float), ("max_pos", ctypes.c_int), ("fp4", ctypes.c_int),
+                ("eps", ctypes.c_float)]
+
+
+class Out(ctypes.Structure):
+    _fields_ = [("latent", ctypes.c_void_p), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("prequant", ctypes.c_void_p)]
+
+
+def library_path() -> str:
+    return _build_mod.LIB
+
+
+def load_library(build_if_missing: bool = True):
+    """Loads libcsa.so (building it first if it is missing and nvcc is available)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build_mod.LIB
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise CSAError(f"{path} is missing: build it with deepseek_v4_compressed_wkv_gb300.build")
+            _build_mod.build()
+        lib = ctypes.CDLL(path)
+        P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        sig = {
+            "csa_options_default": ([P], None),
+            "csa_compressor_create": ([I, I, I, I, P, P], I),
+            "csa_compressor_set_weights": ([P, P, P, P, P], I),
+            "csa_compress_prefill": ([P, P, I, I, I, I, P, P], I),
+            "csa_compress_decode": ([P, P, I, P, P, P, P], I),
+            "csa_state_reset": ([P, I, I, P], I),
+            "csa_state_elems": ([P], I64),
+            "csa_state_export": ([P, P, P, P], I),
+            "csa_device_status": ([P, P], I),
+            "csa_compressor_destroy": ([P], None),
+            "csa_last_error": ([], ctypes.c_char_p),
+            "csa_fp4_e4m3_roundtrip": ([P, I64, P, P, P, P], I),
+            "csa_rope_table": ([P, I, I, P, P], I),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(rc: int, what: str) -> int:
+    if rc < 0:
+        msg = load_library().csa_last_error().decode(errors="replace")
+        raise CSAError(f"{what} failed ({rc}): {msg}")
+    return rc
+
+
+def default_options(**overrides) -> Options:
+    o = Options()
+    load_library().csa_options_default(ctypes.byref(o))
+    for k, v in overrides.items():
+        if not hasattr(o, k):
+            raise TypeError(f"unknown option {k}")
+        setattr(o, k, v)
+    return o
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dptr(t) -> ctypes.c_void_p:
+    if t is None:
+        return ctypes.c_void_p(0)
+    if not t.is_cuda or not t.is_contiguous():
+        raise CSAError("tensors passed to the library must be contiguous CUDA tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _u16(t):
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t
+
+
+class Compressor:
+    """One compressor instance (one attention layer's wkv / wgate / norm / state)."""
+
+    def __init__(self, dim: int, head_dim: int, ratio: int, overlap: int = 0, **options):
+        self._lib = load_library()
+        self.dim, self.head_dim, self.ratio, self.overlap = dim, head_dim, ratio, overlap
+        self.options = default_options(**options)
+        h = ctypes.c_void_p()
+        _check(self._lib.csa_compressor_create(dim, head_dim, ratio, overlap, ctypes.byref(self.options),
+                                               ctypes.byref(h)), "csa_compressor_create")
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.csa_compressor_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self):
+        return self._h
+
+    def set_weights(self, wkv, wgate, gain, stream=None):
+        _check(self._lib.csa_compressor_set_weights(self._h, _dptr(wkv), _dptr(wgate), _dptr(gain),
+                                                    _stream(stream)), "csa_compressor_set_weights")
+
+    def _alloc_out(self, rows, device, prequant=True):
+        H = self.head_dim
+        fp4 = bool(self.options.fp4)
+        d = dict(latent=torch.empty(rows, H, dtype=torch.bfloat16, device=device),
+                 codes=torch.empty(rows, H // 2, dtype=torch.uint8, device=device) if fp4 else None,
+                 scales=torch.empty(rows, H // 16, dtype=torch.uint8, device=device) if fp4 else None,
+                 prequant=torch.empty(rows, H, dtype=torch.bfloat16, device=device) if prequant else None)
+        return d
+
+    @staticmethod
+    def _out_struct(d):
+        return Out(_dptr(d["latent"]).value, _dptr(d["codes"]).value, _dptr(d["scales"]).value,
+                   _dptr(d["prequant"]).value)
+
+    def prefill(self, x, slot_offset: int = 0, out=None, prequant: bool = True, stream=None):
+        """x bf16 [B, N, dim] CUDA.  Returns None when no group completes (N < ratio), else a
+        dict of latent [B, G, H] bf16, codes [B, G, H/2] u8, scales [B, G, H/16] u8 and
+        prequant [B, G, H] bf16 (codes/scales None when fp4 is off)."""
+        B, N, D = x.shape
+        if D != self.dim or x.dtype != torch.bfloat16:
+            raise CSAError("x must be bf16 [B, N, dim]")
+        G = N // self.ratio
+        if out is None:
+            out = self._alloc_out(max(B * G, 1), x.device, prequant)
+        o = self._out_struct(out)
+        g = _check(self._lib.csa_compress_prefill(self._h, _dptr(_u16(x)), B, N, 0, slot_offset,
+                                                  ctypes.byref(o), _stream(stream)), "csa_compress_prefill")
+        if g == 0:
+            return None
+        H = self.head_dim
+        shp = {"latent": (B, g, H), "codes": (B, g, H // 2), "scales": (B, g, H // 16), "prequant": (B, g, H)}
+        return {k: (None if v is None else v[:B * g].view(*shp[k])) for k, v in out.items()}
+
+    def decode(self, x_tok, start_pos, out=None, emitted=None, prequant: bool = True, stream=None):
+        """x_tok bf16 [B, dim], start_pos int32 CUDA [B].  Returns a dict with emitted u8 [B]
+        and latent/codes/scales/prequant [B, ...] (rows valid where emitted)."""
+        B, D = x_tok.shape
+        if D != self.dim or x_tok.dtype != torch.bfloat16 or start_pos.dtype != torch.int32:
+            raise CSAError("x_tok must be bf16 [B, dim] and start_pos int32 [B]")
+        if out is None:
+            out = self._alloc_out(B, x_tok.device, prequant)
+        if emitted is None:
+            emitted = torch.empty(B, dtype=torch.uint8, device=x_tok.device)
+        o = self._out_struct(out)
+        _check(self._lib.csa_compress_decode(self._h, _dptr(_u16(x_tok)), B, _dptr(start_pos), _dptr(emitted),
+                                             ctypes.byref(o), _stream(stream)), "csa_compress_decode")
+        d = dict(out)
+        d["emitted"] = emitted
+        return d
+
+    def state_reset(self, slot_begin: int = 0, slot_count: int | None = None, stream=None):
+        if slot_count is None:
+            slot_count = self.options.max_batch - slot_begin
+        _check(self._lib.csa_state_reset(self._h, slot_begin, slot_count, _stream(stream)), "csa_state_reset")
+
+    def state_export(self, device="cuda", stream=None):
+        n = _check(self._lib.csa_state_elems(self._h), "csa_state_elems")
+        kv = torch.empty(n, dtype=torch.float32, device=device)
+        sc = torch.empty(n, dtype=torch.float32, device=device)
+        _check(self._lib.csa_state_export(self._h, _dptr(kv), _dptr(sc), _stream(stream)), "csa_state_export")
+        mb, H = self.options.max_batch, self.head_dim
+        shape = (mb, 2, 4, 2 * H) if self.overlap else (mb, self.ratio, H)
+        return kv.view(shape), sc.view(shape)
+
+    def device_status(self, stream=None):
+        return _check(self._lib.csa_device_status(self._h, _stream(stream)), "csa_device_status")
+
+
+def fp4_e4m3_roundtrip(x, stream=None):
+    """bf16 CUDA tensor (size a multiple of 16) -> (codes u8 [n/2], scales u8 [n/16], out bf16 [n])."""
+    lib = load_library()
+    x = x.contiguous().view(-1)
+    nb = x.numel() // 16
+    codes = torch.empty(nb * 8, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(nb, dtype=torch.uint8, device=x.device)
+    out = torch.empty(nb * 16, dtype=torch.bfloat16, device=x.device)
+    _check(lib.csa_fp4_e4m3_roundtrip(_dptr(_u16(x)), nb, _dptr(codes), _dptr(scales), _dptr(_u16(out)),
+                                      _stream(stream)), "csa_fp4_e4m3_roundtrip")
+    return codes, scales, out
+
+
+def rope_table(pos0: int, npos: int, **options):
+    """Host-side RoPE table of the library: (cos, sin) float32 numpy [npos, rope_dim/2]."""
+    import numpy as np
+    o = default_options(**options)
+    hr = o.rope_dim // 2
+    cs = np.zeros((npos, hr), np.float32)
+    sn = np.zeros((npos, hr), np.float32)
+    _check(load_library().csa_rope_table(ctypes.byref(o), pos0, npos, cs.ctypes.data, sn.ctypes.data),
+           "csa_rope_table")
+    return cs, sn
+
+
+def state_window_start(pos: int, ratio: int, overlap: int) -> int:
+    """First token whose projection the state at position `pos` still holds.
+
+    Prefilling tokens [state_window_start(pos), pos) of a sequence (as a sequence of its
+    own, in a fresh state slot) leaves exactly the state that prefilling all `pos` tokens
+    leaves: the unfinished group's tokens and, at ratio 4 overlapped, the last complete
+    group's tokens in the parity slot of their absolute group index (so the start is a
+    multiple of 8 tokens there).  Entries that this shorter prefill emits are not the
+    sequence's entries and should be discarded."""
+    g = pos // ratio
+    if not overlap or g == 0:
+        return ratio * g
+    k0 = (g - 1) - ((g - 1) % 2)
+    return 4 * k0

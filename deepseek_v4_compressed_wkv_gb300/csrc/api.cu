@@ -1,0 +1,306 @@
+// C ABI of the compressor: argument checks, ownership of device buffers, the host-built
+// YaRN RoPE table, and the launch sequence of each call.  Declared in include/csa.h.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "csa_internal.cuh"
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(CSA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define CSA_CUDA(call, what)                  \
+  do {                                        \
+    cudaError_t e_ = (call);                  \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+// YaRN NTK-by-parts frequency correction (Peng et al., 2023), as used by the compressed
+// layers' RoPE table ("Module compress", yarn_freqs_cis, built from compress_rope_theta):
+// dims whose wavelength turns more than beta_fast times over the original context keep
+// their frequency, dims turning fewer than beta_slow times are divided by the factor,
+// with a linear ramp between the two correction dims.
+void yarn_inv_freq(const csa_options& o, std::vector<double>& f) {
+  const int d = o.rope_dim;
+  const double base = o.rope_base;
+  auto corr = [&](double turns) {
+    return d * std::log((double)o.rope_orig_len / (turns * 2.0 * M_PI)) / (2.0 * std::log(base));
+  };
+  double lo = std::floor(corr(o.beta_fast)), hi = std::ceil(corr(o.beta_slow));
+  lo = std::max(lo, 0.0);
+  hi = std::min(hi, (double)(d - 1));
+  if (hi == lo) hi += 0.001;
+  f.resize(d / 2);
+  for (int i = 0; i < d / 2; ++i) {
+    const double f0 = std::pow(base, -2.0 * i / d);
+    const double t = std::min(std::max((i - lo) / (hi - lo), 0.0), 1.0);
+    f[i] = f0 / o.rope_factor * t + f0 * (1.0 - t);
+  }
+}
+
+void rope_rows(const csa_options& o, const std::vector<double>& f, int pos0, int npos, float* cs, float* sn) {
+  const int hr = o.rope_dim / 2;
+  for (int p = 0; p < npos; ++p)
+    for (int i = 0; i < hr; ++i) {
+      const double th = (double)(pos0 + p) * f[i];  // angle in double: pos * f reaches ~1e5 rad
+      cs[(size_t)p * hr + i] = (float)std::cos(th);
+      sn[(size_t)p * hr + i] = (float)std::sin(th);
+    }
+}
+
+bool check_options(const csa_options& o, int H, std::string& why) {
+  char buf[256];
+  if (o.max_batch < 1) why = "max_batch must be >= 1";
+  else if (o.rope_dim < 0 || o.rope_dim % 2 || o.rope_dim > H) {
+    snprintf(buf, sizeof buf, "rope_dim %d must be even and in [0, head_dim=%d]", o.rope_dim, H);
+    why = buf;
+  } else if (o.rope_dim > 0 && (o.max_pos < 1 || !(o.rope_base > 1.0f) || !(o.rope_factor > 0.0f) ||
+                                o.rope_orig_len < 1 || !(o.beta_fast > 0.0f) || !(o.beta_slow > 0.0f)))
+    why = "invalid RoPE options (max_pos, rope_base, rope_factor, rope_orig_len, beta_fast, beta_slow)";
+  else if (o.fp4 != 0 && o.fp4 != 1) why = "fp4 must be 0 or 1";
+  else if (!(o.eps >= 0.0f)) why = "eps must be >= 0";
+  else return true;
+  return false;
+}
+
+void free_all(csa_compressor* c) {
+  cudaFree(c->w_packed);
+  cudaFree(c->w_planes);
+  cudaFree(c->gain);
+  cudaFree(c->rope_cos);
+  cudaFree(c->rope_sin);
+  cudaFree(c->state);
+  cudaFree(c->dev_flag);
+  cudaFree(c->scratch);
+}
+
+int ensure_scratch(csa_compressor* c, size_t bytes, cudaStream_t s) {
+  if (c->scratch_bytes >= bytes) return CSA_OK;
+  CSA_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+  cudaFree(c->scratch);
+  c->scratch = nullptr;
+  c->scratch_bytes = 0;
+  CSA_CUDA(cudaMalloc(&c->scratch, bytes), "cudaMalloc(scratch)");
+  c->scratch_bytes = bytes;
+  return CSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void csa_options_default(csa_options* o) {
+  if (!o) return;
+  o->max_batch = 128;
+  o->rope_dim = 64;
+  o->rope_base = 160000.0f;
+  o->rope_factor = 16.0f;
+  o->rope_orig_len = 4096;
+  o->beta_fast = 32.0f;
+  o->beta_slow = 1.0f;
+  o->max_pos = 262144;
+  o->fp4 = 1;
+  o->eps = 1e-6f;
+}
+
+const char* csa_last_error(void) { return g_last_error.c_str(); }
+
+int csa_rope_table(const csa_options* opt, int pos0, int npos, float* cos_out, float* sin_out) {
+  if (!opt || !cos_out || !sin_out || pos0 < 0 || npos < 0 || opt->rope_dim <= 0 || opt->rope_dim % 2)
+    return fail(CSA_ERR_ARG, "csa_rope_table: bad arguments");
+  std::vector<double> f;
+  yarn_inv_freq(*opt, f);
+  rope_rows(*opt, f, pos0, npos, cos_out, sin_out);
+  return CSA_OK;
+}
+
+int csa_compressor_create(int dim, int H, int ratio, int overlap, const csa_options* opt, csa_compressor** out) {
+  try {
+    if (!out) return fail(CSA_ERR_ARG, "csa_compressor_create: out is NULL");
+    *out = nullptr;
+    if (dim <= 0 || dim % 64) return fail(CSA_ERR_ARG, "dim %d must be a positive multiple of 64", dim);
+    if (H < 16 || H > 512 || H % 16) return fail(CSA_ERR_ARG, "head_dim %d must be a multiple of 16 in [16, 512]", H);
+    if (ratio < 1) return fail(CSA_ERR_ARG, "ratio %d must be >= 1", ratio);
+    if (overlap != 0 && overlap != 1) return fail(CSA_ERR_ARG, "overlap must be 0 or 1");
+    if (overlap && ratio != 4) return fail(CSA_ERR_ARG, "the overlapped form exists only at ratio 4 (got %d)", ratio);
+    csa_options o;
+    csa_options_default(&o);
+    if (opt) o = *opt;
+    std::string why;
+    if (!check_options(o, H, why)) return fail(CSA_ERR_ARG, "%s", why.c_str());
+    csa::Packing pk = csa::make_packing(H, overlap);
+    if (H % pk.ft) return fail(CSA_ERR_ARG, "head_dim %d must be a multiple of %d", H, pk.ft);
+
+    auto* c = new (std::nothrow) csa_compressor();
+    if (!c) return fail(CSA_ERR_INTERNAL, "out of host memory");
+    c->dim = dim;
+    c->H = H;
+    c->ratio = ratio;
+    c->overlap = overlap;
+    c->width = (1 + overlap) * H;
+    c->opt = o;
+    c->pk = pk;
+    c->slots = overlap ? 8 : ratio;
+    c->weights_set = false;
+    cudaGetDevice(&c->device);
+    const size_t ncol = pk.cols();
+    cudaError_t e = cudaSuccess;
+    auto alloc = [&](void** p, size_t bytes) {
+      if (e == cudaSuccess) e = cudaMalloc(p, bytes);
+    };
+    alloc((void**)&c->w_packed, ncol * dim * sizeof(float));
+    alloc((void**)&c->w_planes, 3 * ncol * dim * sizeof(__nv_bfloat16));
+    alloc((void**)&c->gain, H * sizeof(float));
+    alloc((void**)&c->state, (size_t)o.max_batch * c->slots * ncol * sizeof(float));
+    alloc((void**)&c->dev_flag, sizeof(int));
+    if (o.rope_dim > 0) {
+      const size_t n = (size_t)o.max_pos * (o.rope_dim / 2);
+      alloc((void**)&c->rope_cos, n * sizeof(float));
+      alloc((void**)&c->rope_sin, n * sizeof(float));
+      if (e == cudaSuccess) {
+        std::vector<double> f;
+        yarn_inv_freq(o, f);
+        std::vector<float> cs(n), sn(n);
+        rope_rows(o, f, 0, o.max_pos, cs.data(), sn.data());
+        e = cudaMemcpy(c->rope_cos, cs.data(), n * sizeof(float), cudaMemcpyHostToDevice);
+        if (e == cudaSuccess) e = cudaMemcpy(c->rope_sin, sn.data(), n * sizeof(float), cudaMemcpyHostToDevice);
+      }
+    }
+    if (e == cudaSuccess) e = cudaMemset(c->dev_flag, 0, sizeof(int));
+    if (e == cudaSuccess && csa::launch_state_reset(c, 0, o.max_batch, 0) != cudaSuccess) e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+      free_all(c);
+      delete c;
+      return cuda_fail(e, "csa_compressor_create");
+    }
+    *out = c;
+    return CSA_OK;
+  } catch (...) {
+    return fail(CSA_ERR_INTERNAL, "csa_compressor_create: unexpected exception");
+  }
+}
+
+int csa_compressor_set_weights(csa_compressor* c, const float* wkv, const float* wgate, const float* gain,
+                               csa_stream_t stream) {
+  if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
+  if (!wkv || !gain) return fail(CSA_ERR_ARG, "wkv and norm_gain are required");
+  if (!wgate && c->ratio > 1) return fail(CSA_ERR_ARG, "wgate is required at ratio > 1");
+  cudaStream_t s = (cudaStream_t)stream;
+  CSA_CUDA(csa::launch_pack_weights(c, wkv, wgate, s), "pack_weights launch");
+  CSA_CUDA(cudaMemcpyAsync(c->gain, gain, c->H * sizeof(float), cudaMemcpyDeviceToDevice, s), "copy gain");
+  c->weights_set = true;
+  return CSA_OK;
+}
+
+int csa_compress_prefill(csa_compressor* c, const uint16_t* x, int B, int N, int start_pos, int slot_offset,
+                         const csa_out* out, csa_stream_t stream) {
+  try {
+    if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
+    if (!c->weights_set) return fail(CSA_ERR_STATE, "weights not set");
+    if (start_pos != 0)
+      return fail(CSA_ERR_ARG, "prefill needs start_pos 0 (got %d); later tokens go through decode", start_pos);
+    if (B < 1 || N < 1) return fail(CSA_ERR_ARG, "B (%d) and N (%d) must be >= 1", B, N);
+    if (slot_offset < 0 || (long long)slot_offset + B > c->opt.max_batch)
+      return fail(CSA_ERR_ARG, "slots [%d, %d) exceed max_batch %d", slot_offset, slot_offset + B, c->opt.max_batch);
+    if (!x) return fail(CSA_ERR_ARG, "x is NULL");
+    const int G = N / c->ratio;
+    if (G > 0 && (!out || !out->latent)) return fail(CSA_ERR_ARG, "out->latent is required");
+    if (G > 0 && c->opt.rope_dim > 0 && (long long)c->ratio * (G - 1) >= c->opt.max_pos)
+      return fail(CSA_ERR_ARG, "entry position %lld exceeds the RoPE table (max_pos %d)",
+                  (long long)c->ratio * (G - 1), c->opt.max_pos);
+    cudaStream_t s = (cudaStream_t)stream;
+    const long long M = (long long)B * N;
+    const size_t bytes = (size_t)M * c->pk.cols() * sizeof(float);
+    int rc = ensure_scratch(c, bytes, s);
+    if (rc) return rc;
+    if (M > 0x7fffffffLL) return fail(CSA_ERR_ARG, "B * N too large");
+    CSA_CUDA(csa::launch_projection_ffma(c, x, (int)M, c->scratch, 0, nullptr, s), "projection launch");
+    if (G > 0) CSA_CUDA(csa::launch_prefill_pool(c, c->scratch, B, N, *out, s), "pool launch");
+    CSA_CUDA(csa::launch_prefill_state(c, c->scratch, B, N, slot_offset, s), "state launch");
+    return G;
+  } catch (...) {
+    return fail(CSA_ERR_INTERNAL, "csa_compress_prefill: unexpected exception");
+  }
+}
+
+int csa_compress_decode(csa_compressor* c, const uint16_t* x_tok, int B, const int32_t* start_pos, uint8_t* emitted,
+                        const csa_out* out, csa_stream_t stream) {
+  if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
+  if (!c->weights_set) return fail(CSA_ERR_STATE, "weights not set");
+  if (B < 1 || B > c->opt.max_batch) return fail(CSA_ERR_ARG, "B %d must be in [1, max_batch=%d]", B, c->opt.max_batch);
+  if (!x_tok || !start_pos || !emitted || !out || !out->latent)
+    return fail(CSA_ERR_ARG, "x_tok, start_pos, emitted and out->latent are required");
+  cudaStream_t s = (cudaStream_t)stream;
+  CSA_CUDA(csa::launch_projection_ffma(c, x_tok, B, c->state, 1, start_pos, s), "decode projection launch");
+  CSA_CUDA(csa::launch_decode_emit(c, start_pos, B, *out, emitted, s), "decode emit launch");
+  return CSA_OK;
+}
+
+int csa_state_reset(csa_compressor* c, int slot_begin, int slot_count, csa_stream_t stream) {
+  if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
+  if (slot_begin < 0 || slot_count < 0 || (long long)slot_begin + slot_count > c->opt.max_batch)
+    return fail(CSA_ERR_ARG, "slots [%d, %d) outside [0, %d)", slot_begin, slot_begin + slot_count, c->opt.max_batch);
+  CSA_CUDA(csa::launch_state_reset(c, slot_begin, slot_count, (cudaStream_t)stream), "state reset launch");
+  return CSA_OK;
+}
+
+int64_t csa_state_elems(const csa_compressor* c) {
+  if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
+  return (int64_t)c->opt.max_batch * c->slots * c->width;
+}
+
+int csa_state_export(const csa_compressor* c, float* kv, float* score, csa_stream_t stream) {
+  if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
+  if (!kv || !score) return fail(CSA_ERR_ARG, "kv and score are required");
+  CSA_CUDA(csa::launch_state_export(c, kv, score, (cudaStream_t)stream), "state export launch");
+  return CSA_OK;
+}
+
+int csa_device_status(csa_compressor* c, csa_stream_t stream) {
+  if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
+  cudaStream_t s = (cudaStream_t)stream;
+  int flag = 0;
+  CSA_CUDA(cudaMemcpyAsync(&flag, c->dev_flag, sizeof(int), cudaMemcpyDeviceToHost, s), "read device flag");
+  CSA_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+  if (!flag) return CSA_OK;
+  CSA_CUDA(cudaMemsetAsync(c->dev_flag, 0, sizeof(int), s), "clear device flag");
+  return fail(CSA_ERR_DEVICE, "device flag 0x%x:%s%s%s", flag, (flag & 1) ? " negative start_pos;" : "",
+              (flag & 2) ? " entry position beyond the RoPE table;" : "", (flag & 4) ? " wait budget exhausted;" : "");
+}
+
+void csa_compressor_destroy(csa_compressor* c) {
+  if (!c) return;
+  cudaDeviceSynchronize();
+  free_all(c);
+  delete c;
+}
+
+int csa_fp4_e4m3_roundtrip(const uint16_t* in, int64_t n_blocks, uint8_t* codes, uint8_t* scales, uint16_t* out,
+                           csa_stream_t stream) {
+  if (n_blocks < 0 || (n_blocks > 0 && (!in || !scales || !out))) return fail(CSA_ERR_ARG, "bad arguments");
+  CSA_CUDA(csa::launch_fp4_roundtrip(in, n_blocks, codes, scales, out, (cudaStream_t)stream), "fp4 launch");
+  return CSA_OK;
+}
+
+}  // extern "C"

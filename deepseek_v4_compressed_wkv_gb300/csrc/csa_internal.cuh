@@ -1,0 +1,202 @@
+// Internal declarations of the CSA KV compressor library: the handle, the packed weight
+// layout, and the device routines shared by the kernels (bf16 rounding, the fp4 round
+// trip, the per-entry epilogue).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/csa.h"
+
+namespace csa {
+
+// ---------------------------------------------------------------------------------------
+// Packed column order.
+//
+// The projection's 2C output columns (kv and score; at ratio 4 overlapped each has branch
+// A and branch B) are stored tile by tile: a tile holds `nk` kinds x `ft` features, kind
+// major.  Kinds: overlapped (kvA, kvB, sA, sB); otherwise (kv, s).  Tile t covers features
+// [t*ft, (t+1)*ft).  All kinds of a feature therefore sit in the same tile, which is what a
+// GEMM tile needs to pool without leaving the chip.  The same order is used for the packed
+// f32 weights, the bf16 weight planes, the projection scratch and the state rows.
+struct Packing {
+  int H, nk, ft, tw, ntiles;  // tw = nk * ft columns per tile
+  __host__ __device__ int col(int kind, int f) const { return (f / ft) * tw + kind * ft + (f % ft); }
+  __host__ __device__ int cols() const { return ntiles * tw; }
+};
+
+enum Kind { KV_A = 0, KV_B = 1, S_A = 2, S_B = 3 };  // overlapped
+enum KindN { KV = 0, S = 1 };                        // non-overlapped
+
+inline __host__ __device__ Packing make_packing(int H, int overlap) {
+  Packing p;
+  p.H = H;
+  p.nk = overlap ? 4 : 2;
+  p.ft = 256 / p.nk;
+  if (p.ft > H) p.ft = H;
+  p.tw = p.nk * p.ft;
+  p.ntiles = H / p.ft;
+  return p;
+}
+
+// Kernel-side view of the epilogue parameters.
+struct EpiParams {
+  const float* gain;      // [H]
+  const float* rope_cos;  // [max_pos][rope_dim/2]
+  const float* rope_sin;
+  int H, rope_dim, fp4, max_pos;
+  float eps;
+};
+
+// ---------------------------------------------------------------------------------------
+// Device number formats.
+
+__device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+  __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// e4m3 bit pattern -> value (exact).  1 sign, 4 exponent bits (bias 7), 3 mantissa bits.
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  float mag = e == 0 ? (float)m * 0.001953125f /* 2^-9 */ : __uint_as_float(((e + 120u) << 23) | (m << 20));
+  return (b & 0x80u) ? -mag : mag;
+}
+
+// Two float32 -> two e2m1 codes packed in one byte, `lo` in bits 0..3, round to nearest
+// even, saturating to +-6 (PTX cvt with .satfinite; the first source goes to the upper
+// nibble).
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+      : "=h"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float e2m1_value(uint32_t code) {
+  // magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 by code: exponent field e = code>>1, mantissa m
+  uint32_t e = (code >> 1) & 3u, m = code & 1u;
+  float mag = e == 0 ? 0.5f * (float)m : (1.0f + 0.5f * (float)m) * (float)(1u << (e - 1));
+  return (code & 8u) ? -mag : mag;
+}
+
+// fp4 round trip of one block of 16 bf16 values held by one thread ("Module compress",
+// fp4_quant_e4m3_inplace): amax floored at 6*2^-9, scale = e4m3(amax / 6) with the
+// division in IEEE f32, values divided by the scale (IEEE f32) to e2m1, dequantised
+// exactly and rounded to bf16.  y[] holds bf16 values (as float); replaced in place by
+// the dequantised values.
+__device__ __forceinline__ void fp4_block16(float y[16], uint8_t codes[8], uint8_t* scale_bits) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(y[i]));
+  const float sq = __fdiv_rn(fmaxf(amax, 0.01171875f /* 6 * 2^-9 */), 6.0f);
+  const __nv_fp8_storage_t sb = __nv_cvt_float_to_fp8(sq, __NV_SATFINITE, __NV_E4M3);
+  const float s = e4m3_value(sb);
+  *scale_bits = sb;
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    uint32_t c2 = e2m1x2(__fdiv_rn(y[i], s), __fdiv_rn(y[i + 1], s));
+    codes[i / 2] = (uint8_t)c2;
+    y[i] = bf16_round(e2m1_value(c2 & 15u) * s);
+    y[i + 1] = bf16_round(e2m1_value(c2 >> 4) * s);
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Epilogue of one entry, one warp per entry: lane l (< H/16) holds pooled features
+// 16l..16l+15 in v[].  bf16 round ("norm(kv.to(bf16))"), RMSNorm in f32 with the f32 gain
+// and one bf16 rounding, YaRN RoPE on the trailing rope_dim features (adjacent pairs,
+// angle pos * f_i from the host-built table), then the fp4 round trip.  All 32 lanes must
+// call it (the RMSNorm sum is a warp reduction); lanes >= H/16 pass zeros and store nothing.
+__device__ __forceinline__ void entry_epilogue(float v[16], int lane, long long pos, const EpiParams& ep,
+                                               uint16_t* latent, uint8_t* codes, uint8_t* scales,
+                                               uint16_t* prequant) {
+  const int nl = ep.H >> 4;
+  const bool act = lane < nl;
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v[i] = act ? bf16_round(v[i]) : 0.0f;
+    ss = fmaf(v[i], v[i], ss);
+  }
+  ss = warp_sum(ss);
+  const float inv = 1.0f / sqrtf(ss / (float)ep.H + ep.eps);
+  if (!act) return;
+  const int f0 = lane * 16;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = bf16_round(v[i] * inv * __ldg(ep.gain + f0 + i));
+  const int r0 = ep.H - ep.rope_dim;
+  if (ep.rope_dim > 0 && f0 + 16 > r0) {
+    const int hr = ep.rope_dim >> 1;
+    const float* cs = ep.rope_cos + pos * hr;
+    const float* sn = ep.rope_sin + pos * hr;
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      const int f = f0 + i;
+      if (f >= r0) {
+        const int k = (f - r0) >> 1;
+        const float c = __ldg(cs + k), s = __ldg(sn + k);
+        const float a = v[i], b = v[i + 1];
+        v[i] = bf16_round(a * c - b * s);
+        v[i + 1] = bf16_round(a * s + b * c);
+      }
+    }
+  }
+  if (prequant) {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = (uint32_t)bf16_bits(v[2 * i]) | ((uint32_t)bf16_bits(v[2 * i + 1]) << 16);
+    uint4* dst = reinterpret_cast<uint4*>(prequant + f0);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+  if (ep.fp4) {
+    uint8_t cd[8], sb;
+    fp4_block16(v, cd, &sb);
+    if (codes) {
+      uint2 pk;
+      pk.x = cd[0] | (cd[1] << 8) | (cd[2] << 16) | ((uint32_t)cd[3] << 24);
+      pk.y = cd[4] | (cd[5] << 8) | (cd[6] << 16) | ((uint32_t)cd[7] << 24);
+      *reinterpret_cast<uint2*>(codes + f0 / 2) = pk;
+    }
+    if (scales) scales[lane] = sb;
+  }
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = (uint32_t)bf16_bits(v[2 * i]) | ((uint32_t)bf16_bits(v[2 * i + 1]) << 16);
+  uint4* dst = reinterpret_cast<uint4*>(latent + f0);
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+}  // namespace csa
+
+// ---------------------------------------------------------------------------------------
+// The handle (host side).
+struct csa_compressor {
+  int dim, H, ratio, overlap, width;  // width = (1 + overlap) * H rows per weight matrix
+  csa_options opt;
+  csa::Packing pk;
+  int slots;        // state slots per sequence: ratio, or 8 (2 parities x 4) overlapped
+  int device;
+  bool weights_set;
+  float* w_packed;  // [2C][dim] f32, packed column order
+  __nv_bfloat16* w_planes;  // [3][2C][dim] bf16 split planes (w = p0 + p1 + p2), packed order
+  float* gain;              // [H]
+  float* rope_cos;          // [max_pos][rope_dim/2]
+  float* rope_sin;
+  float* state;             // [max_batch][slots][2C] f32, packed column order
+  int* dev_flag;            // device-side error flag
+  float* scratch;           // projection scratch [rows][2C] f32 (grown on demand)
+  size_t scratch_bytes;
+};

@@ -1,0 +1,23 @@
+// Launchers of the compressor's kernels (host side, enqueue only).
+#pragma once
+
+#include "csa_internal.cuh"
+
+namespace csa {
+
+EpiParams epi_params(const csa_compressor* c);
+cudaError_t launch_pack_weights(const csa_compressor* c, const float* wkv, const float* wgate, cudaStream_t s);
+cudaError_t launch_projection_ffma(const csa_compressor* c, const uint16_t* x, int M, float* out, int mode,
+                                   const int32_t* start_pos, cudaStream_t s);
+cudaError_t launch_prefill_pool(const csa_compressor* c, const float* proj, int B, int N, const csa_out& out,
+                                cudaStream_t s);
+cudaError_t launch_prefill_state(const csa_compressor* c, const float* proj, int B, int N, int slot_offset,
+                                 cudaStream_t s);
+cudaError_t launch_decode_emit(const csa_compressor* c, const int32_t* start_pos, int B, const csa_out& out,
+                               uint8_t* emitted, cudaStream_t s);
+cudaError_t launch_state_reset(const csa_compressor* c, int slot_begin, int count, cudaStream_t s);
+cudaError_t launch_state_export(const csa_compressor* c, float* kv, float* score, cudaStream_t s);
+cudaError_t launch_fp4_roundtrip(const uint16_t* in, long long nb, uint8_t* codes, uint8_t* scales, uint16_t* out,
+                                 cudaStream_t s);
+
+}  // namespace csa

@@ -1,0 +1,173 @@
+/*
+ * csa.h - C ABI of the GB300 (sm_103a) compressed-sparse-attention KV Compressor.
+ *
+ * What it computes (per compressor instance, i.e. per attention layer):
+ *
+ *   kv, score = x . wkv^T, x . wgate^T        f32, x is bf16 promoted to f32
+ *       ("DeepSeek V4.1 - Pool token pairs", Compressor excerpt, forward: x.float(),
+ *        wkv(x), wgate(x); "Module compress", linear_f32: w is [out_dim][in_dim])
+ *   k^p_j = sum_i softmax_i(score_i) (.) kv_i  per feature, over the candidates of group j
+ *       (same page, pooling formula; "Compressed Sparse Attention - ratio m = 4":
+ *        at ratio 4 overlapped, 8 candidates = branch B of the previous group's 4 tokens
+ *        + branch A of the current group's 4 tokens, the first entry's previous branch
+ *        padded)
+ *   latent = fp4( RoPE( RMSNorm( bf16(k^p_j) ) ) )
+ *       (Pool token pairs: norm(kv.to(bf16)); ratio-4 page: "normalized, rotary position
+ *        is applied"; "Module compress": yarn_freqs_cis with compress_rope_theta, and
+ *        fp4_quant_e4m3_inplace with LATENT_BLOCK = 16: e2m1 values, e4m3 scales)
+ *
+ * Prefill (start_pos 0) emits N / ratio entries per sequence and leaves the trailing
+ * partial group in the per-sequence state; decode (one token per sequence) writes a state
+ * slot and emits an entry when its group completes, (start_pos + 1) % ratio == 0
+ * (Pool token pairs, forward; ratio-4 page, "Prefill and decode use the same rule").
+ *
+ * Conventions
+ *  - All pointers marked "dev" are CUDA device pointers on the current device; "host"
+ *    pointers are ordinary host memory.  The caller owns every buffer it passes in.
+ *    The library owns its weights (copied and re-laid out by set_weights), the state,
+ *    the RoPE table and its scratch memory.
+ *  - Layouts are row-major and dense.  bf16 values are passed as uint16_t bit patterns.
+ *  - Work is enqueued on the given stream and is asynchronous unless stated otherwise.
+ *    A NULL stream is the legacy default stream.
+ *  - Every function returns a status (CSA_OK = 0, or a negative csa_status) unless it
+ *    states otherwise; csa_last_error() then describes the failure (per host thread).
+ *    Nothing aborts and no C++ exception crosses this boundary.
+ *  - A handle is not thread-safe: calls on one handle must be serialised by the caller,
+ *    and work on one handle's state must be ordered on the device (one stream, or
+ *    events), since decode and prefill read and write the state.
+ */
+#ifndef CSA_H
+#define CSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* csa_stream_t; /* the same type as cudaStream_t */
+typedef struct csa_compressor csa_compressor;
+
+typedef enum {
+  CSA_OK = 0,
+  CSA_ERR_ARG = -1,      /* invalid argument or shape */
+  CSA_ERR_CUDA = -2,     /* a CUDA call failed (launch, allocation, copy) */
+  CSA_ERR_STATE = -3,    /* call out of order (weights not set) */
+  CSA_ERR_TIMEOUT = -4,  /* a device-side wait ran out of its iteration budget */
+  CSA_ERR_DEVICE = -5,   /* a kernel reported an input it could not handle (see csa_device_status) */
+  CSA_ERR_INTERNAL = -6
+} csa_status;
+
+/* Options of a compressor instance.  csa_options_default() gives the released Flash
+ * configuration of the ratio-4 page ("Released Flash configuration": RoPE sub-dimension
+ * 64) with compress_rope_theta 160000, YaRN factor 16 over an original length of 4096. */
+typedef struct {
+  int max_batch;       /* state slots (sequences); default 128 */
+  int rope_dim;        /* rotary slice at the end of the latent; 0 disables RoPE; default 64 */
+  float rope_base;     /* compress_rope_theta; default 160000 */
+  float rope_factor;   /* YaRN scaling factor; default 16 */
+  int rope_orig_len;   /* YaRN original context length; default 4096 */
+  float beta_fast;     /* YaRN ramp: dims turning more often than this keep their frequency; 32 */
+  float beta_slow;     /* YaRN ramp: dims turning less often than this are interpolated; 1 */
+  int max_pos;         /* RoPE table length (largest position + 1); default 262144 */
+  int fp4;             /* 1 = fp4 round trip of the latent (default), 0 = off */
+  float eps;           /* RMSNorm epsilon; default 1e-6 */
+} csa_options;
+
+/* Output buffers of one call (dev).  Rows are entries: prefill [B][G][..], decode [B][..].
+ *  latent   [.., H] bf16, required: the final latent (dequantised fp4 values if fp4 is on)
+ *  codes    [.., H/2] u8 or NULL: e2m1 codes, element 2i in the low nibble, sign in bit 3
+ *  scales   [.., H/16] u8 or NULL: e4m3 bit patterns, one per block of 16 features
+ *  prequant [.., H] bf16 or NULL: the latent after RMSNorm and RoPE, before fp4 */
+typedef struct {
+  uint16_t* latent;
+  uint8_t* codes;
+  uint8_t* scales;
+  uint16_t* prequant;
+} csa_out;
+
+/* Fills *opt with the defaults above. */
+void csa_options_default(csa_options* opt);
+
+/* Creates a compressor for x of width dim, latent width head_dim, group size ratio.
+ * overlap = 1 selects the ratio-4 overlapped form (two branches of head_dim each) and
+ * requires ratio == 4.  opt may be NULL (defaults).  Requirements: dim % 64 == 0,
+ * head_dim % 16 == 0 and 16 <= head_dim <= 512, ratio >= 1, rope_dim even and
+ * <= head_dim, max_batch >= 1.  Allocates device memory on the current device (state,
+ * RoPE table) and builds the YaRN table on the host in double precision.
+ * On success *out receives the handle. */
+int csa_compressor_create(int dim, int head_dim, int ratio, int overlap, const csa_options* opt,
+                          csa_compressor** out);
+
+/* Copies the weights into library-owned, re-laid-out buffers.
+ *  wkv   [C][dim] f32 dev, C = (1 + overlap) * head_dim ("Module compress" linear_f32 layout);
+ *        rows 0..head_dim-1 are branch A (or the only branch), rows head_dim.. branch B
+ *  wgate [C][dim] f32 dev, same layout; may be NULL only at ratio 1 (softmax over one
+ *        candidate is 1, so the gate has no effect)
+ *  norm_gain [head_dim] f32 dev: RMSNorm weight
+ * Returns after the re-layout kernels are enqueued; the caller's buffers may be freed once
+ * the stream reaches that point. */
+int csa_compressor_set_weights(csa_compressor* c, const float* wkv, const float* wgate, const float* norm_gain,
+                               csa_stream_t stream);
+
+/* Prefill of B sequences of N tokens each.  x [B][N][dim] bf16 dev.  start_pos must be 0
+ * (only whole-sequence prefill is defined; a later chunk goes through decode).  Sequence b
+ * uses state slot slot_offset + b; needs slot_offset + B <= max_batch.  Writes
+ * G = N / ratio entries per sequence to out ([B][G][..]) and leaves the trailing
+ * N % ratio tokens in the state (at ratio 4 overlapped, also the last complete group's
+ * tokens, whose branch B the next entry pools).  Returns G (0 means "no entry", the
+ * pages' None) or a negative csa_status.  Requires r * (G - 1) < max_pos when RoPE is on. */
+int csa_compress_prefill(csa_compressor* c, const uint16_t* x, int B, int N, int start_pos, int slot_offset,
+                         const csa_out* out, csa_stream_t stream);
+
+/* One decode step for sequences 0..B-1 (state slots 0..B-1), one token each.
+ *  x_tok     [B][dim] bf16 dev
+ *  start_pos [B] int32 dev: position of this token in its sequence (per sequence)
+ *  emitted   [B] u8 dev: set to 1 where the token completed a group, else 0
+ * Row b of out is written only where emitted[b] = 1.  start_pos 0 restarts the sequence
+ * (the pages' prefill branch with one token).  Positions must be >= 0, and for emitted
+ * rows the entry position start_pos + 1 - ratio must be < max_pos; a violation leaves the
+ * row unwritten, sets emitted[b] = 0 and raises the flag read by csa_device_status. */
+int csa_compress_decode(csa_compressor* c, const uint16_t* x_tok, int B, const int32_t* start_pos,
+                        uint8_t* emitted, const csa_out* out, csa_stream_t stream);
+
+/* Resets state slots [slot_begin, slot_begin + slot_count): kv 0, score -inf. */
+int csa_state_reset(csa_compressor* c, int slot_begin, int slot_count, csa_stream_t stream);
+
+/* Number of float elements of each of the two exported state arrays. */
+int64_t csa_state_elems(const csa_compressor* c);
+
+/* Copies the state into kv and score (dev, csa_state_elems floats each), in the logical
+ * layout: non-overlapped [max_batch][ratio][head_dim]; ratio 4 overlapped
+ * [max_batch][2 parities][4 slots][2 * head_dim] (branch A then B; group g of a sequence
+ * lives in parity g % 2).  For tests and for moving a session, not for checkpoints (the
+ * pages keep the state out of checkpoints). */
+int csa_state_export(const csa_compressor* c, float* kv, float* score, csa_stream_t stream);
+
+/* Reads and clears the device-side error flag of the handle (synchronises the stream).
+ * Returns CSA_OK, or CSA_ERR_DEVICE if a kernel flagged an input since the last call. */
+int csa_device_status(csa_compressor* c, csa_stream_t stream);
+
+/* Frees the handle and its device memory (synchronises the device first). NULL is a no-op. */
+void csa_compressor_destroy(csa_compressor* c);
+
+/* Description of the last failure on this host thread ("" if none). */
+const char* csa_last_error(void);
+
+/* The latent's fp4 round trip alone ("Module compress", fp4_quant_e4m3_inplace, block 16):
+ * in [n_blocks][16] bf16 dev -> codes [n_blocks][8] u8 dev (may be NULL),
+ * scales [n_blocks] u8 dev (e4m3 bits), out [n_blocks][16] bf16 dev (dequantised).
+ * Runs the same device routine as the compressor's epilogue. */
+int csa_fp4_e4m3_roundtrip(const uint16_t* in, int64_t n_blocks, uint8_t* codes, uint8_t* scales, uint16_t* out,
+                           csa_stream_t stream);
+
+/* Host-only: the YaRN RoPE table the library uploads ("Module compress", yarn_freqs_cis):
+ * cos_out, sin_out [npos][rope_dim/2] f32 host for positions pos0..pos0+npos-1, computed in
+ * double precision and rounded once to f32. */
+int csa_rope_table(const csa_options* opt, int pos0, int npos, float* cos_out, float* sin_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA_H */

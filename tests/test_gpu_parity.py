@@ -1,0 +1,332 @@
+"""Parity of the CUDA library (through its C ABI) with the CPU oracle, on seeded inputs.
+
+Acceptance (per entry, on the pre-fp4 bf16 latent "prequant"):
+  - at least 99.9% of elements within 2 bf16 ulps of the oracle;
+  - relative error at most 1e-2 on every element whose magnitude is at least 1/16 of the
+    entry's RMS, and absolute error at most 1e-2 * RMS everywhere (near-zero RoPE outputs
+    cancel, so a pure elementwise relative bound is not meaningful there);
+  - the fp4 outputs (codes, scales, dequantised latent) equal the oracle's fp4 round trip
+    of the GPU's own prequant bit for bit (the quantiser is pinned separately on the
+    oracle's bf16 input, bit-exact);
+  - decode emission flags exact.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import deepseek_v4_compressed_wkv_gb300 as csa
+import oracle
+import synthetic
+from _util import bf16_bits_to_f32, layer_inputs, to_bf16_bits, ulp_distance_bf16
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def dev_bits(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(DEV).view(torch.bfloat16)
+
+
+def host_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def opts_of(layer, max_batch=1, max_pos=262144):
+    return dict(max_batch=max_batch, rope_dim=layer.rope_dim, fp4=layer.fp4, max_pos=max_pos)
+
+
+def make_pair(seed, layer, max_batch=1, max_pos=262144):
+    wkv, wgate, gain = synthetic.weights(seed, layer)
+    g = csa.Compressor(layer.dim, layer.head_dim, layer.ratio, layer.overlap, **opts_of(layer, max_batch, max_pos))
+    g.set_weights(torch.from_numpy(wkv).to(DEV), torch.from_numpy(wgate).to(DEV), torch.from_numpy(gain).to(DEV))
+    o = oracle.Compressor(layer.dim, layer.head_dim, layer.ratio, layer.overlap, max_batch=max_batch,
+                          rope_dim=layer.rope_dim, fp4=layer.fp4)
+    o.set_weights(wkv, wgate, gain)
+    return g, o
+
+
+def check_entries(gpu: dict, ref_prequant: np.ndarray, fp4: int, what=""):
+    """gpu: dict of numpy arrays (latent, codes, scales, prequant) [..., H]; ref: oracle prequant."""
+    gp = gpu["prequant"].reshape(-1, ref_prequant.shape[-1])
+    rp = ref_prequant.reshape(gp.shape)
+    ulps = ulp_distance_bf16(gp, rp)
+    frac2 = float(np.mean(ulps <= 2))
+    assert frac2 >= 0.999, f"{what}: only {frac2:.5f} of elements within 2 ulps (max {ulps.max()})"
+    g = bf16_bits_to_f32(gp).astype(np.float64)
+    r = bf16_bits_to_f32(rp).astype(np.float64)
+    rms = np.sqrt(np.mean(r * r, axis=-1, keepdims=True))
+    err = np.abs(g - r)
+    assert np.all(err <= 1e-2 * rms + 1e-30), f"{what}: abs error {np.max(err / rms):.3g} * rms"
+    big = np.abs(r) >= rms / 16
+    rel = err[big] / np.abs(r[big])
+    assert rel.size == 0 or rel.max() <= 1e-2, f"{what}: max relative error {rel.max():.3g}"
+    if fp4:
+        codes, scales, lat = oracle.fp4_e4m3(gp)
+        assert np.array_equal(gpu["scales"].reshape(-1), scales), f"{what}: scales differ from fp4(prequant)"
+        assert np.array_equal(gpu["codes"].reshape(-1), codes), f"{what}: codes differ from fp4(prequant)"
+        assert np.array_equal(gpu["latent"].reshape(-1), lat), f"{what}: latent differs from fp4(prequant)"
+    else:
+        assert np.array_equal(gpu["latent"].reshape(gp.shape), gp)
+    return frac2, int(ulps.max())
+
+
+def to_np(d: dict, rows=None):
+    out = {}
+    for k, v in d.items():
+        if v is None or k == "emitted":
+            continue
+        a = v.contiguous()
+        a = host_bits(a) if a.dtype == torch.bfloat16 else a.cpu().numpy()
+        out[k] = a if rows is None else a[rows]
+    return out
+
+
+# ---- the quantiser alone, fed the oracle's bf16 values ---------------------------------------
+
+def test_fp4_quantiser_bit_exact_on_oracle_input():
+    rng = np.random.default_rng(0)
+    nb = 20000
+    mags = 10.0 ** rng.uniform(-4, 4, size=(nb, 1))
+    vals = (rng.standard_normal((nb, 16)) * mags).astype(np.float32)
+    vals[:50] = 0.0                      # all-zero blocks: floored amax
+    vals[50:60, 3] = 6.375               # tie in the scale rounding
+    vals[60:70] *= 1e-30                 # tiny blocks
+    vals[70:80, 0] = 3.0e38              # saturating scale
+    # the latent prequant of a real run, too
+    bits = to_bf16_bits(vals)
+    pats = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    finite = np.isfinite((pats.astype(np.uint32) << 16).view(np.float32))
+    sweep = np.zeros((int(finite.sum()), 16), np.uint16)
+    sweep[:, 0] = pats[finite]
+    sweep[:, 1:] = to_bf16_bits(np.linspace(-1.5, 1.7, 15, dtype=np.float32))
+    allb = np.concatenate([bits, sweep])
+    codes, scales, out = csa.fp4_e4m3_roundtrip(dev_bits(allb))
+    torch.cuda.synchronize()
+    rc, rs, ro = oracle.fp4_e4m3(allb)
+    assert np.array_equal(scales.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    assert np.array_equal(host_bits(out), ro)
+
+
+# ---- tiny parity workload: prefill, then 64 decode steps from start_pos 0 ---------------------
+
+def test_tiny_prefill_then_decode():
+    wl = synthetic.TINY
+    layer = wl.layers[0]
+    g, o = make_pair(wl.seed, layer)
+    x, *_ = layer_inputs(wl.seed, layer, 1, 64)
+    ref = o.prefill(x)
+    got = g.prefill(dev_bits(x))
+    torch.cuda.synchronize()
+    check_entries(to_np(got), ref["prequant"], layer.fp4, "tiny prefill")
+    g.state_reset()
+    o.state_reset()
+    for p in range(64):
+        sp = np.array([p], np.int32)
+        r = o.decode(x[:, p], sp)
+        d = g.decode(dev_bits(x[:, p]), torch.from_numpy(sp).to(DEV))
+        em = d["emitted"].cpu().numpy()
+        assert np.array_equal(em, r["emitted"]), p
+        if em[0]:
+            check_entries(to_np(d, rows=[0]), r["prequant"][[0]], layer.fp4, f"tiny decode p={p}")
+    assert g.device_status() == 0
+
+
+# ---- small shapes over several tiles, ragged tails, odd batches -------------------------------
+
+SMALL = [
+    # dim, H, ratio, overlap, B, N
+    (256, 128, 4, 1, 3, 4 * 67 + 3),
+    (256, 128, 4, 1, 1, 3),          # no complete group: padded previous branch only
+    (256, 128, 4, 1, 2, 4),
+    (128, 64, 2, 0, 3, 2 * 70 + 1),
+    (256, 512, 4, 1, 2, 128 + 5),
+    (256, 512, 128, 0, 2, 128 * 3 + 77),
+    (192, 256, 8, 0, 1, 8 * 40),
+    (128, 64, 1, 0, 2, 37),
+    (128, 32, 3, 0, 1, 2),
+]
+
+
+@pytest.mark.parametrize("dim,H,ratio,overlap,B,N", SMALL)
+def test_small_prefill_state_and_decode(dim, H, ratio, overlap, B, N):
+    layer = synthetic.Layer(dim, H, ratio, overlap, 1.0 / math.sqrt(dim), gate_scale=2.0,
+                            rope_dim=min(64, H), fp4=1)
+    g, o = make_pair(5, layer, max_batch=B + 1)
+    x, *_ = layer_inputs(5, layer, B, N + 6)
+    xp = np.ascontiguousarray(x[:, :N])
+    ref = o.prefill(xp, slot_offset=1)
+    G = N // ratio
+    canary = 1  # rows past the last entry must stay untouched
+    out = {"latent": torch.full((B * G + canary, H), 7.0, dtype=torch.bfloat16, device=DEV),
+           "codes": torch.full((B * G + canary, H // 2), 0xA5, dtype=torch.uint8, device=DEV),
+           "scales": torch.full((B * G + canary, H // 16), 0x5A, dtype=torch.uint8, device=DEV),
+           "prequant": torch.full((B * G + canary, H), 7.0, dtype=torch.bfloat16, device=DEV)}
+    got = g.prefill(dev_bits(xp), slot_offset=1, out=out)
+    torch.cuda.synchronize()
+    assert (got is None) == (G == 0)
+    if G:
+        check_entries(to_np(got), ref["prequant"], 1, f"prefill {ratio}/{overlap}")
+    assert torch.all(out["latent"][B * G:] == 7.0) and torch.all(out["codes"][B * G:] == 0xA5)
+    assert torch.all(out["scales"][B * G:] == 0x5A) and torch.all(out["prequant"][B * G:] == 7.0)
+    # state after prefill: the meaningful slots equal the oracle's (f32, from f32 projections)
+    kg, sg = (t.cpu().numpy() for t in g.state_export())
+    ko, so = o.state()
+    assert np.allclose(kg, ko, rtol=2e-5, atol=2e-5 * np.abs(ko[np.isfinite(ko)]).max())
+    assert np.array_equal(np.isinf(sg), np.isinf(so))
+    fin = np.isfinite(so)
+    assert np.allclose(sg[fin], so[fin], rtol=2e-5, atol=2e-5 * np.abs(so[fin]).max())
+    # six decode steps continuing every sequence (slots 0..B: slot 0 is fresh, starts at p=0)
+    xall, *_ = layer_inputs(5, layer, B + 1, N + 6)
+    xall[1:] = x
+    for k in range(6):
+        sp = np.array([k] + [N + k] * B, np.int32)
+        xt = np.ascontiguousarray(xall[np.arange(B + 1), sp])
+        r = o.decode(xt, sp)
+        d = g.decode(dev_bits(xt), torch.from_numpy(sp).to(DEV))
+        em = d["emitted"].cpu().numpy()
+        assert np.array_equal(em, r["emitted"]), (k, em, r["emitted"])
+        rows = np.flatnonzero(em)
+        if rows.size:
+            check_entries(to_np(d, rows=rows), r["prequant"][rows], 1, f"decode step {k}")
+    assert g.device_status() == 0
+
+
+# ---- full-size workloads ------------------------------------------------------------------
+
+def test_flash_csa_prefill_full():
+    wl = synthetic.FLASH_CSA
+    layer = wl.layers[0]
+    g, o = make_pair(wl.seed, layer)
+    x, *_ = layer_inputs(wl.seed, layer, 1, 4096)
+    got = g.prefill(dev_bits(x))
+    torch.cuda.synchronize()
+    ref = o.prefill(x)
+    frac, mx = check_entries(to_np(got), ref["prequant"], 1, "Flash CSA prefill")
+    assert ref["G"] == 1024
+
+
+def sampled_groups(G, k, seed):
+    rng = np.random.default_rng(seed)
+    picks = {0, 1, G - 1, G // 2} | set(rng.choice(G, size=min(k, G), replace=False).tolist())
+    return sorted(p for p in picks if 0 <= p < G)
+
+
+def test_hca_prefill_sampled_groups_and_tail_state():
+    wl = synthetic.HCA
+    layer = wl.layers[0]
+    B, N = wl.batch, wl.tokens[0]
+    g, o = make_pair(wl.seed, layer, max_batch=B)
+    x, wkv, wgate, _ = layer_inputs(wl.seed, layer, B, N)
+    got = g.prefill(dev_bits(x))
+    torch.cuda.synchronize()
+    G = N // layer.ratio
+    assert G == 128 and N % layer.ratio == 77
+    gn = to_np(got)
+    for b in range(B):
+        grp = sampled_groups(G, 4, b)
+        ref = o.prefill_groups(x[b], grp)
+        sel = {k: v[b][grp] for k, v in gn.items()}
+        check_entries(sel, ref["prequant"], 1, f"HCA b={b}")
+    # the 77-token tail sits in state slots 0..76 of each sequence
+    kg, sg = (t.cpu().numpy() for t in g.state_export())
+    for b in range(B):
+        tail = x[b, 128 * G:]
+        kv = oracle.linear(tail, wkv, nthreads=8)
+        sc = oracle.linear(tail, wgate, nthreads=8)
+        assert np.allclose(kg[b, :77], kv, rtol=1e-5, atol=1e-5 * np.abs(kv).max())
+        assert np.allclose(sg[b, :77], sc, rtol=1e-5, atol=1e-5 * np.abs(sc).max())
+
+
+@pytest.mark.parametrize("N,layer_idx", [(131072, 0), (131072, 1), (16384, 0)])
+def test_long_prefill_sampled(N, layer_idx):
+    wl = synthetic.LONG
+    layer = wl.layers[layer_idx]
+    g, o = make_pair(wl.seed, layer)
+    x, *_ = layer_inputs(wl.seed, layer, 1, N, outlier_frac=wl.outlier_frac)
+    got = g.prefill(dev_bits(x), prequant=True)
+    torch.cuda.synchronize()
+    G = N // layer.ratio
+    grp = sampled_groups(G, 24, N)
+    # include groups that hold outlier tokens
+    mask = synthetic.outlier_mask(wl.seed, 0, 0, N, wl.outlier_frac)
+    out_groups = np.unique(np.flatnonzero(mask) // layer.ratio)
+    grp = sorted(set(grp) | set(out_groups[:8].tolist()))
+    ref = o.prefill_groups(x[0], grp)
+    gn = {k: v[0][grp] for k, v in to_np(got).items()}
+    check_entries(gn, ref["prequant"], 1, f"long N={N} ratio={layer.ratio}")
+
+
+def test_long_batched_prefill_sampled():
+    wl = synthetic.LONG
+    layer = wl.layers[0]
+    B, N = wl.extra["batched"]
+    g, o = make_pair(wl.seed, layer, max_batch=B)
+    x, *_ = layer_inputs(wl.seed, layer, B, N, outlier_frac=wl.outlier_frac)
+    got = g.prefill(dev_bits(x))
+    torch.cuda.synchronize()
+    gn = to_np(got)
+    G = N // 4
+    for b in (0, 3, 7):
+        grp = sampled_groups(G, 6, b)
+        ref = o.prefill_groups(x[b], grp)
+        check_entries({k: v[b][grp] for k, v in gn.items()}, ref["prequant"], 1, f"B8 b={b}")
+
+
+def test_batched_decode_both_compressors():
+    wl = synthetic.DECODE
+    B = wl.batch
+    sp0 = synthetic.start_positions(wl.seed, B, wl.start_pos_hi)
+    steps = 12
+    for layer in wl.layers:
+        g, o = make_pair(wl.seed, layer, max_batch=B)
+        # bring every sequence's state to its start position
+        for b in range(B):
+            s = int(sp0[b])
+            t0 = csa.state_window_start(s, layer.ratio, layer.overlap)
+            if s > t0:
+                xb = to_bf16_bits(synthetic.tokens(wl.seed, b, t0, s, layer.dim))[None]
+                o.prefill(xb, slot_offset=b)
+                g.prefill(dev_bits(xb), slot_offset=b, prequant=False)
+        for k in range(steps):
+            sp = (sp0 + k).astype(np.int32)
+            xt = to_bf16_bits(np.stack([synthetic.tokens(wl.seed, b, int(sp[b]), int(sp[b]) + 1, layer.dim)[0]
+                                        for b in range(B)]))
+            r = o.decode(xt, sp)
+            d = g.decode(dev_bits(xt), torch.from_numpy(sp).to(DEV))
+            em = d["emitted"].cpu().numpy()
+            assert np.array_equal(em, r["emitted"])
+            assert np.array_equal(em, ((sp + 1) % layer.ratio == 0).astype(np.uint8))
+            rows = np.flatnonzero(em)
+            if rows.size:
+                check_entries(to_np(d, rows=rows), r["prequant"][rows], 1, f"decode r={layer.ratio} k={k}")
+        assert g.device_status() == 0
+
+
+# ---- error paths on the device --------------------------------------------------------------
+
+def test_errors_are_reported_not_raised_on_the_device():
+    layer = synthetic.Layer(128, 64, 4, 1, 0.1, rope_dim=64)
+    g = csa.Compressor(128, 64, 4, 1, max_batch=2, max_pos=64)
+    x = torch.zeros(1, 8, 128, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(csa.CSAError, match="weights not set"):
+        g.prefill(x)
+    wkv, wgate, gain = synthetic.weights(0, layer)
+    g.set_weights(torch.from_numpy(wkv).to(DEV), torch.from_numpy(wgate).to(DEV), torch.from_numpy(gain).to(DEV))
+    with pytest.raises(csa.CSAError, match="max_batch"):
+        g.prefill(torch.zeros(3, 8, 128, dtype=torch.bfloat16, device=DEV))
+    with pytest.raises(csa.CSAError, match="RoPE table"):
+        g.prefill(torch.zeros(1, 4 * 20, 128, dtype=torch.bfloat16, device=DEV))
+    lib = csa.load_library()
+    assert lib.csa_compress_prefill(g.handle, x.data_ptr(), 1, 8, 5, 0, None, None) == -1
+    # decode positions the kernel cannot serve: flagged, rows not emitted, context still usable
+    sp = torch.tensor([-3, 67], dtype=torch.int32, device=DEV)
+    d = g.decode(torch.zeros(2, 128, dtype=torch.bfloat16, device=DEV), sp)
+    assert d["emitted"].cpu().tolist() == [0, 0]
+    with pytest.raises(csa.CSAError, match="device flag"):
+        g.device_status()
+    assert g.device_status() == 0
+    torch.cuda.synchronize()
