@@ -1,0 +1,410 @@
+"""Benchmark of the CSA KV compressor on one GB300 (or N, one process per GPU).
+
+A step is one ratio-4 overlapped prefill of the Flash CSA layer (B=1 sequence of 4096 tokens,
+dim 4096, two branches x 512, fp4 latent): projection, 8-candidate softmax pool, bf16,
+RMSNorm, YaRN RoPE, fp4 round trip and the state update.  `value` is compressed KV entries/s
+over all ranks; tokens/s and the batched-decode rate (B=128, ratio-4 overlapped + ratio-128
+compressors, one token per sequence per step) are reported beside it.  Inputs are seeded
+synthetic data resident in HBM before the timed region; L2 is flushed (a 2x-L2 buffer is
+written) between timed iterations.  Under torchrun every rank runs its own sequences
+(weak scaling, no collective on the data path; the barrier and the max-over-ranks of the
+time are the only communication).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "compressed KV entries/s & input tokens/s (ratio-4 prefill), decode steps/s; % roofline"
+WORKLOAD = "Flash CSA layer prefill: B=1, N=4096, dim=4096, head_dim=512, ratio 4 overlapped, YaRN RoPE 64, fp4"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--decode-steps", type=int, default=64)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(n):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world, device):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the GPU is under load."""
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 6:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if not self.samples:
+            return None
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in self.samples for n, v in zip(names, s[2:6]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------------------------------------
+
+def make_inputs(torch, csa, synthetic, layer, seed, B, N, rank, device):
+    x = np.stack([synthetic.tokens(seed, rank * B + b, 0, N, layer.dim) for b in range(B)])
+    xb = torch.from_numpy(x).to(torch.bfloat16).to(device)
+    wkv, wgate, gain = synthetic.weights(seed, layer)
+    comp = csa.Compressor(layer.dim, layer.head_dim, layer.ratio, layer.overlap, max_batch=max(B, 1),
+                          rope_dim=layer.rope_dim, fp4=layer.fp4)
+    comp.set_weights(torch.from_numpy(wkv).to(device), torch.from_numpy(wgate).to(device),
+                     torch.from_numpy(gain).to(device))
+    return comp, xb
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import deepseek_v4_compressed_wkv_gb300 as csa
+    import synthetic
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    peaks = load_peaks()
+    props = torch.cuda.get_device_properties(device)
+    wl = synthetic.FLASH_CSA
+    layer = wl.layers[0]
+    B, N = 1, wl.tokens[0]
+    G = N // layer.ratio
+    comp, x = make_inputs(torch, csa, synthetic, layer, wl.seed, B, N, rank, device)
+    H = layer.head_dim
+    out = comp._alloc_out(B * G, device, prequant=False)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(int(2 * getattr(props, "L2_cache_size", 128 << 20)) // 4 + 1, dtype=torch.float32,
+                        device=device)
+
+    def step():
+        comp.prefill(x, out=out, prequant=False)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    # keep the GPU busy long enough for the clock sampler to see it under this load
+    t_end = time.time() + 1.0
+    while time.time() < t_end:
+        step()
+        torch.cuda.synchronize()
+    launches0 = comp.kernel_launches()
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(float(i))
+        comp.set_profile_events(*kev[i])
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    comp.set_profile_events(None, None)
+    launches = comp.kernel_launches() - launches0
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    total_ms = max_over_ranks(sum(step_ms), world, device)
+    ms = total_ms / K
+    entries = B * G * world
+    value = entries / (ms * 1e-3)
+    tokens_s = B * N * world / (ms * 1e-3)
+
+    # dominant kernel: the projection (fp32-equivalent: three bf16 products per weight on the
+    # tensor-core path, f32 FMA on the CUDA-core path)
+    flops = 2.0 * B * N * layer.dim * 2 * layer.width
+    kms = statistics.mean(kern_ms)
+    achieved = flops / (kms * 1e-3) / 1e12
+    tc = getattr(csa, "prefill_uses_tensor_cores", lambda c: False)(comp)
+    if tc:
+        peak = peaks["bf16_tflops"] / 3.0
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": None, "kernel": "csa_prefill_tc (projection + fused pool/norm/RoPE/fp4)",
+                "peak_basis": f"{peaks['source']} bf16 dense {peaks['bf16_tflops']} TFLOP/s / 3 bf16 passes"}
+    else:
+        sm_clock = (clk or {}).get("sm_max_mhz") or 2070.0
+        peak = props.multi_processor_count * 128 * 2 * sm_clock * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": None, "kernel": "gemm_ffma_kernel (f32 FMA projection)",
+                "peak_basis": f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 flop x {sm_clock:.0f} MHz"}
+
+    # end to end through the public call with host buffers (pinned): H2D of x, prefill, D2H of
+    # latent + codes + scales
+    x_host = x.cpu().pin_memory()
+    x_dev = torch.empty_like(x)
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items() if v is not None}
+    e2e_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        comp.prefill(x_dev, out=out, prequant=False)
+    torch.cuda.synchronize()
+    e2e_ev[0].record(stream)
+    for i in range(K):
+        x_dev.copy_(x_host, non_blocking=True)
+        comp.prefill(x_dev, out=out, prequant=False)
+        for k, h in host_out.items():
+            h.copy_(out[k], non_blocking=True)
+    e2e_ev[1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e2e_ev[0].elapsed_time(e2e_ev[1]), world, device) / K
+    h2d = x.numel() * 2
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    line = {"metric": METRIC, "value": value, "unit": "entries/s", "n_gpus": world, "steps": K,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": N, "entries_per_step": entries,
+                       "l2": "flushed between timed iterations (2x L2 buffer written)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "tokens_per_s": tokens_s, "kernel_ms": kms, "roofline": roof,
+            "e2e": {"value": entries / (e2e_ms * 1e-3), "unit": "entries/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches, "clocks": clk}
+    comp.close()
+    if not args.no_decode:
+        line["decode"] = bench_decode(args, torch, csa, synthetic, device, peaks, world, rank)
+    return line
+
+
+def bench_decode(args, torch, csa, synthetic, device, peaks, world, rank):
+    """B=128 decode steps through both compressors (ratio 4 overlapped + ratio 128), weights
+    of several layer instances rotated so that each step streams its weights from HBM."""
+    wl = synthetic.DECODE
+    B = wl.batch
+    props = torch.cuda.get_device_properties(device)
+    l2 = getattr(props, "L2_cache_size", 128 << 20)
+    w_bytes = sum(2 * L.width * L.dim * 4 for L in wl.layers)
+    n_layers = max(2, math.ceil(2.5 * l2 / w_bytes))
+    sp0 = synthetic.start_positions(wl.seed, B, wl.start_pos_hi)
+    layers = []
+    for li in range(n_layers):
+        pair = []
+        for L in wl.layers:
+            Ls = synthetic.Layer(L.dim, L.head_dim, L.ratio, L.overlap, L.w_std, L.gate_scale, L.rope_dim, L.fp4,
+                                 weight_stream=L.weight_stream + 2 * li)
+            wkv, wgate, gain = synthetic.weights(wl.seed, Ls)
+            c = csa.Compressor(L.dim, L.head_dim, L.ratio, L.overlap, max_batch=B)
+            c.set_weights(torch.from_numpy(wkv).to(device), torch.from_numpy(wgate).to(device),
+                          torch.from_numpy(gain).to(device))
+            for b in range(B):
+                s = int(sp0[b])
+                t0 = csa.state_window_start(s, L.ratio, L.overlap)
+                if s > t0:
+                    xb = torch.from_numpy(synthetic.tokens(wl.seed, rank * B + b, t0, s, L.dim)).to(torch.bfloat16)
+                    c.prefill(xb[None].to(device), slot_offset=b, prequant=False)
+            outs = c._alloc_out(B, device, prequant=False)
+            pair.append((c, outs))
+        layers.append(pair)
+    steps = args.decode_steps
+    xs = [torch.from_numpy(np.stack([synthetic.tokens(wl.seed, rank * B + b, int(sp0[b]) + k, int(sp0[b]) + k + 1,
+                                                      wl.layers[0].dim)[0] for b in range(B)])).to(torch.bfloat16)
+          .to(device) for k in range(8)]
+    sps = [torch.from_numpy((sp0 + k).astype(np.int32)).to(device) for k in range(steps + 8)]
+    emitted = torch.empty(B, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(k):
+        for c, outs in layers[k % n_layers]:
+            c.decode(xs[k % 8], sps[k], out=outs, emitted=emitted, prequant=False)
+
+    for k in range(8):
+        step(k)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for k in range(steps):
+        step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, device) / steps
+    # algorithmic bytes per step: both weight sets (f32), the two x_tok batches, the state slot
+    # writes, the state read by emitting sequences (expected counts), the outputs
+    wbytes = w_bytes
+    xbytes = 2 * B * wl.layers[0].dim * 2
+    slot_w = sum(B * 2 * L.width * 4 for L in wl.layers)
+    emit_r = sum(B / L.ratio * (8 if L.overlap else L.ratio) * 2 * L.head_dim * 4 for L in wl.layers)
+    outb = sum(B / L.ratio * (L.head_dim * 2 + L.head_dim // 2 + L.head_dim // 16) for L in wl.layers)
+    alg = wbytes + xbytes + slot_w + emit_r + outb
+    gbs = alg / (ms * 1e-3) / 1e9
+    for pair in layers:
+        for c, _ in pair:
+            c.close()
+    return {"steps_per_s": world / (ms * 1e-3) * 1.0, "ms_per_step": ms, "batch": B, "layers_rotated": n_layers,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes_per_step": alg}}
+
+
+# ---------------------------------------------------------------------------------------------
+
+class OracleArm:
+    """The CPU oracle, as it stands, on the Flash CSA prefill workload: one step is the whole
+    4096-token sequence (1024 entries), on all host cores."""
+
+    def __init__(self):
+        import torch
+
+        import oracle
+        import synthetic
+        wl = synthetic.FLASH_CSA
+        layer = wl.layers[0]
+        self.N = wl.tokens[0]
+        x = synthetic.tokens(wl.seed, 0, 0, self.N, layer.dim)
+        self.x = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)[None]
+        wkv, wgate, gain = synthetic.weights(wl.seed, layer)
+        self.o = oracle.Compressor(layer.dim, layer.head_dim, 4, 1, rope_dim=64, fp4=1)
+        self.o.set_weights(wkv, wgate, gain)
+        self.cores = oracle.default_threads()
+
+    def step(self):
+        t0 = time.perf_counter()
+        r = self.o.prefill(self.x, nthreads=self.cores)
+        return r["G"], time.perf_counter() - t0
+
+
+def oracle_sample():
+    arm = OracleArm()
+    g, dt = arm.step()
+    return {"value": g / dt, "unit": "entries/s", "cores": arm.cores, "kind": "oracle",
+            "sample": f"the whole workload: {g} entries ({arm.N} tokens), {dt:.2f} s on {arm.cores} threads"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    arm = OracleArm()
+    for _ in range(args.warmup):
+        arm.step()
+    times = []
+    g = 0
+    for _ in range(args.steps):
+        g, dt = arm.step()
+        times.append(dt)
+    ms = 1e3 * statistics.mean(times)
+    val = g / (ms * 1e-3)
+    cpu = {"value": val, "unit": "entries/s", "cores": arm.cores, "kind": "oracle",
+           "sample": f"the whole workload per step: {g} entries ({arm.N} tokens) on {arm.cores} threads"}
+    return {"impl": "reference", "metric": METRIC, "value": val, "unit": "entries/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD}, "cpu_baseline": cpu,
+            "e2e": {"value": val, "unit": "entries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+        # each step is a few seconds of CPU work: keep the whole run within a few minutes
+        args.steps = max(1, min(args.steps, 30))
+        args.warmup = min(args.warmup, 3)
+        line = run_reference(args, rank, world)
+        if line:
+            print(json.dumps(line), flush=True)
+        return
+    rank, world, local = dist_setup(args.gpus)
+    line = run_ours(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = oracle_sample()
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -31,7 +31,7 @@ _lib = None
 ABI_FUNCTIONS = ("csa_options_default", "csa_compressor_create", "csa_compressor_set_weights",
                  "csa_compress_prefill", "csa_compress_decode", "csa_state_reset", "csa_state_elems",
                  "csa_state_export", "csa_device_status", "csa_compressor_destroy", "csa_last_error",
-                 "csa_fp4_e4m3_roundtrip", "csa_rope_table")
+                 "csa_fp4_e4m3_roundtrip", "csa_rope_table", "csa_set_profile_events", "csa_kernel_launches")
 
 
 class CSAError(RuntimeError):
@@ -81,6 +81,8 @@ def load_library(build_if_missing: bool = True):
             "csa_last_error": ([], ctypes.c_char_p),
             "csa_fp4_e4m3_roundtrip": ([P, I64, P, P, P, P], I),
             "csa_rope_table": ([P, I, I, P, P], I),
+            "csa_set_profile_events": ([P, P, P], I),
+            "csa_kernel_launches": ([P], I64),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -219,6 +221,15 @@ class Compressor:
         mb, H = self.options.max_batch, self.head_dim
         shape = (mb, 2, 4, 2 * H) if self.overlap else (mb, self.ratio, H)
         return kv.view(shape), sc.view(shape)
+
+    def set_profile_events(self, start=None, stop=None):
+        """torch.cuda.Event pair (enable_timing=True) recorded around the dominant kernel."""
+        _check(self._lib.csa_set_profile_events(self._h, ctypes.c_void_p(start.cuda_event if start else 0),
+                                                ctypes.c_void_p(stop.cuda_event if stop else 0)),
+               "csa_set_profile_events")
+
+    def kernel_launches(self) -> int:
+        return _check(self._lib.csa_kernel_launches(self._h), "csa_kernel_launches")
 
     def device_status(self, stream=None):
         return _check(self._lib.csa_device_status(self._h, _stream(stream)), "csa_device_status")

@@ -208,6 +208,7 @@ int csa_compressor_set_weights(csa_compressor* c, const float* wkv, const float*
   if (!wgate && c->ratio > 1) return fail(CSA_ERR_ARG, "wgate is required at ratio > 1");
   cudaStream_t s = (cudaStream_t)stream;
   CSA_CUDA(csa::launch_pack_weights(c, wkv, wgate, s), "pack_weights launch");
+  c->launches += 1;
   CSA_CUDA(cudaMemcpyAsync(c->gain, gain, c->H * sizeof(float), cudaMemcpyDeviceToDevice, s), "copy gain");
   c->weights_set = true;
   return CSA_OK;
@@ -235,9 +236,16 @@ int csa_compress_prefill(csa_compressor* c, const uint16_t* x, int B, int N, int
     int rc = ensure_scratch(c, bytes, s);
     if (rc) return rc;
     if (M > 0x7fffffffLL) return fail(CSA_ERR_ARG, "B * N too large");
+    if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
     CSA_CUDA(csa::launch_projection_ffma(c, x, (int)M, c->scratch, 0, nullptr, s), "projection launch");
-    if (G > 0) CSA_CUDA(csa::launch_prefill_pool(c, c->scratch, B, N, *out, s), "pool launch");
+    if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
+    c->launches += 1;
+    if (G > 0) {
+      CSA_CUDA(csa::launch_prefill_pool(c, c->scratch, B, N, *out, s), "pool launch");
+      c->launches += 1;
+    }
     CSA_CUDA(csa::launch_prefill_state(c, c->scratch, B, N, slot_offset, s), "state launch");
+    c->launches += 1;
     return G;
   } catch (...) {
     return fail(CSA_ERR_INTERNAL, "csa_compress_prefill: unexpected exception");
@@ -252,8 +260,11 @@ int csa_compress_decode(csa_compressor* c, const uint16_t* x_tok, int B, const i
   if (!x_tok || !start_pos || !emitted || !out || !out->latent)
     return fail(CSA_ERR_ARG, "x_tok, start_pos, emitted and out->latent are required");
   cudaStream_t s = (cudaStream_t)stream;
+  if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
   CSA_CUDA(csa::launch_projection_ffma(c, x_tok, B, c->state, 1, start_pos, s), "decode projection launch");
+  if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
   CSA_CUDA(csa::launch_decode_emit(c, start_pos, B, *out, emitted, s), "decode emit launch");
+  c->launches += 2;
   return CSA_OK;
 }
 
@@ -262,6 +273,7 @@ int csa_state_reset(csa_compressor* c, int slot_begin, int slot_count, csa_strea
   if (slot_begin < 0 || slot_count < 0 || (long long)slot_begin + slot_count > c->opt.max_batch)
     return fail(CSA_ERR_ARG, "slots [%d, %d) outside [0, %d)", slot_begin, slot_begin + slot_count, c->opt.max_batch);
   CSA_CUDA(csa::launch_state_reset(c, slot_begin, slot_count, (cudaStream_t)stream), "state reset launch");
+  c->launches += slot_count > 0;
   return CSA_OK;
 }
 
@@ -274,7 +286,21 @@ int csa_state_export(const csa_compressor* c, float* kv, float* score, csa_strea
   if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
   if (!kv || !score) return fail(CSA_ERR_ARG, "kv and score are required");
   CSA_CUDA(csa::launch_state_export(c, kv, score, (cudaStream_t)stream), "state export launch");
+  const_cast<csa_compressor*>(c)->launches += 1;
   return CSA_OK;
+}
+
+int csa_set_profile_events(csa_compressor* c, csa_event_t start, csa_event_t stop) {
+  if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
+  if ((start == nullptr) != (stop == nullptr)) return fail(CSA_ERR_ARG, "set both events or neither");
+  c->prof_start = (cudaEvent_t)start;
+  c->prof_stop = (cudaEvent_t)stop;
+  return CSA_OK;
+}
+
+int64_t csa_kernel_launches(const csa_compressor* c) {
+  if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
+  return c->launches;
 }
 
 int csa_device_status(csa_compressor* c, csa_stream_t stream) {

@@ -199,4 +199,6 @@ struct csa_compressor {
   int* dev_flag;            // device-side error flag
   float* scratch;           // projection scratch [rows][2C] f32 (grown on demand)
   size_t scratch_bytes;
+  cudaEvent_t prof_start, prof_stop;  // optional events around the dominant kernel
+  long long launches;                 // kernels enqueued so far
 };

@@ -47,6 +47,7 @@ extern "C" {
 #endif
 
 typedef struct CUstream_st* csa_stream_t; /* the same type as cudaStream_t */
+typedef struct CUevent_st* csa_event_t;   /* the same type as cudaEvent_t */
 typedef struct csa_compressor csa_compressor;
 
 typedef enum {
@@ -161,6 +162,16 @@ const char* csa_last_error(void);
  * Runs the same device routine as the compressor's epilogue. */
 int csa_fp4_e4m3_roundtrip(const uint16_t* in, int64_t n_blocks, uint8_t* codes, uint8_t* scales, uint16_t* out,
                            csa_stream_t stream);
+
+/* Measurement hook (the pages have no counterpart): while start and stop are set, every
+ * prefill or decode call on this handle records `start` on its stream just before its
+ * dominant kernel (the projection GEMM with its fused epilogue) and `stop` just after it,
+ * so the caller can time that kernel alone with cudaEventElapsedTime.  NULL, NULL turns it
+ * off.  The events stay owned by the caller and must outlive their use. */
+int csa_set_profile_events(csa_compressor* c, csa_event_t start, csa_event_t stop);
+
+/* Number of kernels this handle has enqueued since it was created (all calls). */
+int64_t csa_kernel_launches(const csa_compressor* c);
 
 /* Host-only: the YaRN RoPE table the library uploads ("Module compress", yarn_freqs_cis):
  * cos_out, sin_out [npos][rope_dim/2] f32 host for positions pos0..pos0+npos-1, computed in
