@@ -171,6 +171,9 @@ def run_ours(args, rank, world, local):
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b_ in kev:  # torch creates an event on its first record; the library re-records it
+        a.record(stream)
+        b_.record(stream)
     clocks = ClockSampler(local)
     clocks.start()
     # keep the GPU busy long enough for the clock sampler to see it under this load
@@ -205,7 +208,7 @@ def run_ours(args, rank, world, local):
     flops = 2.0 * B * N * layer.dim * 2 * layer.width
     kms = statistics.mean(kern_ms)
     achieved = flops / (kms * 1e-3) / 1e12
-    tc = getattr(csa, "prefill_uses_tensor_cores", lambda c: False)(comp)
+    tc = comp.uses_tensor_cores()
     if tc:
         peak = peaks["bf16_tflops"] / 3.0
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,

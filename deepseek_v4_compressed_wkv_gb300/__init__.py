@@ -31,7 +31,8 @@ _lib = None
 ABI_FUNCTIONS = ("csa_options_default", "csa_compressor_create", "csa_compressor_set_weights",
                  "csa_compress_prefill", "csa_compress_decode", "csa_state_reset", "csa_state_elems",
                  "csa_state_export", "csa_device_status", "csa_compressor_destroy", "csa_last_error",
-                 "csa_fp4_e4m3_roundtrip", "csa_rope_table", "csa_set_profile_events", "csa_kernel_launches")
+                 "csa_fp4_e4m3_roundtrip", "csa_rope_table", "csa_set_profile_events", "csa_kernel_launches",
+                 "csa_uses_tensor_cores")
 
 
 class CSAError(RuntimeError):
@@ -83,6 +84,7 @@ def load_library(build_if_missing: bool = True):
             "csa_rope_table": ([P, I, I, P, P], I),
             "csa_set_profile_events": ([P, P, P], I),
             "csa_kernel_launches": ([P], I64),
+            "csa_uses_tensor_cores": ([P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -227,6 +229,9 @@ class Compressor:
         _check(self._lib.csa_set_profile_events(self._h, ctypes.c_void_p(start.cuda_event if start else 0),
                                                 ctypes.c_void_p(stop.cuda_event if stop else 0)),
                "csa_set_profile_events")
+
+    def uses_tensor_cores(self) -> bool:
+        return bool(_check(self._lib.csa_uses_tensor_cores(self._h), "csa_uses_tensor_cores"))
 
     def kernel_launches(self) -> int:
         return _check(self._lib.csa_kernel_launches(self._h), "csa_kernel_launches")

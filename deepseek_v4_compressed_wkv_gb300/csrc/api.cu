@@ -92,6 +92,7 @@ void free_all(csa_compressor* c) {
   cudaFree(c->state);
   cudaFree(c->dev_flag);
   cudaFree(c->scratch);
+  cudaFree(c->tc_counters);
 }
 
 int ensure_scratch(csa_compressor* c, size_t bytes, cudaStream_t s) {
@@ -102,6 +103,18 @@ int ensure_scratch(csa_compressor* c, size_t bytes, cudaStream_t s) {
   c->scratch_bytes = 0;
   CSA_CUDA(cudaMalloc(&c->scratch, bytes), "cudaMalloc(scratch)");
   c->scratch_bytes = bytes;
+  return CSA_OK;
+}
+
+int ensure_counters(csa_compressor* c, size_t n, cudaStream_t s) {
+  if (c->tc_counters_n >= n) return CSA_OK;
+  CSA_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+  cudaFree(c->tc_counters);
+  c->tc_counters = nullptr;
+  c->tc_counters_n = 0;
+  CSA_CUDA(cudaMalloc(&c->tc_counters, n * sizeof(int)), "cudaMalloc(counters)");
+  CSA_CUDA(cudaMemset(c->tc_counters, 0, n * sizeof(int)), "cudaMemset(counters)");
+  c->tc_counters_n = n;
   return CSA_OK;
 }
 
@@ -232,10 +245,24 @@ int csa_compress_prefill(csa_compressor* c, const uint16_t* x, int B, int N, int
                   (long long)c->ratio * (G - 1), c->opt.max_pos);
     cudaStream_t s = (cudaStream_t)stream;
     const long long M = (long long)B * N;
+    if (M > 0x7fffffffLL) return fail(CSA_ERR_ARG, "B * N too large");
+    if (csa::prefill_tc_supported(c, x)) {
+      size_t nctr = 0;
+      const size_t bytes = csa::prefill_tc_scratch_bytes(c, B, N, &nctr);
+      int rc = ensure_scratch(c, bytes, s);
+      if (!rc) rc = ensure_counters(c, nctr, s);
+      if (rc) return rc;
+      csa_out o = out ? *out : csa_out{nullptr, nullptr, nullptr, nullptr};
+      if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
+      CSA_CUDA(csa::launch_prefill_tc(c, x, B, N, slot_offset, o, c->scratch, c->tc_counters, s),
+               "tensor-core prefill launch");
+      if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
+      c->launches += 1;
+      return G;
+    }
     const size_t bytes = (size_t)M * c->pk.cols() * sizeof(float);
     int rc = ensure_scratch(c, bytes, s);
     if (rc) return rc;
-    if (M > 0x7fffffffLL) return fail(CSA_ERR_ARG, "B * N too large");
     if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
     CSA_CUDA(csa::launch_projection_ffma(c, x, (int)M, c->scratch, 0, nullptr, s), "projection launch");
     if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
@@ -296,6 +323,12 @@ int csa_set_profile_events(csa_compressor* c, csa_event_t start, csa_event_t sto
   c->prof_start = (cudaEvent_t)start;
   c->prof_stop = (cudaEvent_t)stop;
   return CSA_OK;
+}
+
+int csa_uses_tensor_cores(const csa_compressor* c) {
+  if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
+  static const uint16_t aligned[8] = {};
+  return csa::prefill_tc_supported(c, aligned) ? 1 : 0;
 }
 
 int64_t csa_kernel_launches(const csa_compressor* c) {

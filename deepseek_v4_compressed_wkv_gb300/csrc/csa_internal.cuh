@@ -34,7 +34,7 @@ inline __host__ __device__ Packing make_packing(int H, int overlap) {
   Packing p;
   p.H = H;
   p.nk = overlap ? 4 : 2;
-  p.ft = 256 / p.nk;
+  p.ft = 128 / p.nk;
   if (p.ft > H) p.ft = H;
   p.tw = p.nk * p.ft;
   p.ntiles = H / p.ft;
@@ -199,6 +199,8 @@ struct csa_compressor {
   int* dev_flag;            // device-side error flag
   float* scratch;           // projection scratch [rows][2C] f32 (grown on demand)
   size_t scratch_bytes;
+  int* tc_counters;         // per token tile completion counters of the tensor-core prefill
+  size_t tc_counters_n;     // (kept at zero between calls by the kernel itself)
   cudaEvent_t prof_start, prof_stop;  // optional events around the dominant kernel
   long long launches;                 // kernels enqueued so far
 };

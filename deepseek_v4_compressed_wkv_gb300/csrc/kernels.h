@@ -20,4 +20,10 @@ cudaError_t launch_state_export(const csa_compressor* c, float* kv, float* score
 cudaError_t launch_fp4_roundtrip(const uint16_t* in, long long nb, uint8_t* codes, uint8_t* scales, uint16_t* out,
                                  cudaStream_t s);
 
+// Tensor-core prefill (prefill_tc.cu): projection + pool + norm + RoPE + fp4 + state update.
+bool prefill_tc_supported(const csa_compressor* c, const void* x);
+size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N, size_t* n_counters);
+cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset,
+                              const csa_out& out, void* scratch, int* counters, cudaStream_t s);
+
 }  // namespace csa

@@ -1,0 +1,473 @@
+// Fused prefill on the 5th-generation tensor cores (sm_103a): the projection GEMM with the
+// group softmax pool, bf16 rounding, RMSNorm, YaRN RoPE and the fp4 round trip in its
+// epilogue.  The pre-pool kv / score values live only in TMEM and shared memory.
+//
+// GEMM orientation: the packed weight rows are the MMA's M side (128 rows = one packed tile:
+// ft features x nk kinds), the tokens its N side (256 per tile), K = dim.  The f32 weights
+// enter as three bf16 planes whose sum is exact (w = p0 + p1 + p2), so three bf16 MMAs into
+// one f32 accumulator give the f32 product (x is bf16, so every partial product is exact):
+// the f32 projection of "Pool token pairs" (x.float(), wkv(x), wgate(x)) and the f32 x . w^T
+// of "Module compress" (linear_f32).
+//
+// Roles (192 threads): warp 0 issues the TMA loads (x tile shared by all three planes, one
+// tile per plane), warp 1 owns TMEM and issues tcgen05.mma, warps 2-5 run the epilogue.
+// One CTA computes one (packed tile, token tile); the CTAs of one token tile meet in a global
+// counter, and the last one to finish normalises, rotates and quantises the tile's entries
+// from the pooled values the others left in scratch (the RMSNorm needs all H features).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "csa_internal.cuh"
+#include "kernels.h"
+
+namespace csa {
+namespace tc {
+
+constexpr int kRows = 128;           // packed rows per tile (MMA M)
+constexpr int kTok = 256;            // tokens per tile including the halo (MMA N)
+constexpr int kKb = 64;              // K elements per stage (one 128-byte swizzle row of bf16)
+constexpr int kStages = 2;
+constexpr int kPlaneBytes = kRows * kKb * 2;          // 16 KB
+constexpr int kXBytes = kTok * kKb * 2;               // 32 KB
+constexpr int kStageBytes = 3 * kPlaneBytes + kXBytes;  // 80 KB
+constexpr int kSmemStride = kTok + 1;                 // f32 staging row stride (bank-conflict free)
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 256;
+constexpr uint64_t kWaitNs = 2000000000ull;           // bounded mbarrier waits: 2 s
+
+static_assert(kRows * kSmemStride * 4 <= kStages * kStageBytes, "staging must fit in the stage buffers");
+
+struct Params {
+  int N, K, ratio, overlap, T, GT, halo, ntt, G, ncol, slots, slot_offset;
+  Packing pk;
+  EpiParams ep;
+  csa_out out;
+  float* state;
+  uint16_t* pooled;  // [B][ntt][GT][H] bf16 bits
+  int* counters;     // [B][ntt]
+  int* flag;
+};
+
+// ---- PTX wrappers --------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of `parity` to complete, at most kWaitNs; on time-out raises the CTA's
+// abort flag (so the other roles stop too) and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitNs) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_addr(dst)),
+      "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_addr(dst)),
+      "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with 128-byte swizzle:
+// rows of 128 bytes, 8-row core groups 1024 bytes apart (stride byte offset), descriptor
+// version 1, layout SWIZZLE_128B (2).  The leading byte offset is unused for this layout.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1u << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: bf16 A and B (format 1), f32 accumulator (format 1),
+// both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// ---- the kernel ----------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
+                      const Params P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* full = (uint64_t*)(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_bar = empty + kStages;
+  uint32_t* tmem_slot = (uint32_t*)(acc_bar + 1);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  int* last_flag = (int*)(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ftile = blockIdx.x, tt = blockIdx.y, b = blockIdx.z;
+  const int nkb = P.K / kKb;
+  const int t0 = tt * P.T - P.halo;  // sequence index of the tile's token 0
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_bar, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_map(&map_w);
+    prefetch_map(&map_x);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---- producer: one x tile and three weight-plane tiles per stage
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % kStages;
+        if (kb >= kStages && !mbar_wait(&empty[s], ((kb / kStages) & 1) ^ 1, abort_flag)) break;
+        uint8_t* st = smem + s * kStageBytes;
+        mbar_arrive_expect_tx(&full[s], kStageBytes);
+        for (int p = 0; p < 3; ++p)
+          tma_load_2d(st + p * kPlaneBytes, &map_w, kb * kKb, p * P.ncol + ftile * kRows, &full[s]);
+        tma_load_3d(st + 3 * kPlaneBytes, &map_x, kb * kKb, t0, b, &full[s]);
+        ++issued;
+      }
+      if (*abort_flag) {  // let the copies already in flight land before the CTA exits
+        for (int kb = max(0, issued - kStages); kb < issued; ++kb) {
+          const uint64_t t1 = globaltimer();
+          while (!mbar_try_wait(&full[kb % kStages], (kb / kStages) & 1) && globaltimer() - t1 < kWaitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(kRows, kTok);
+      bool ok = true;
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        const int s = kb % kStages;
+        if (!mbar_wait(&full[s], (kb / kStages) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t st = smem_addr(smem + s * kStageBytes);
+        const uint32_t xs = st + 3 * kPlaneBytes;
+        for (int p = 0; p < 3; ++p)
+          for (int k = 0; k < kKb / 16; ++k)
+            mma_bf16(tmem, sw128_desc(st + p * kPlaneBytes + k * 32), sw128_desc(xs + k * 32), idesc,
+                     (kb | p | k) != 0);
+        mma_commit(&empty[s]);
+      }
+      mma_commit(acc_bar);  // arrives once every MMA issued above has completed
+    }
+  } else {
+    // ---- epilogue (warps 2..5; warp w reads TMEM lanes 32*(w%4) .. +31)
+    const int et = threadIdx.x - 64;  // 0..127
+    const bool have_acc = mbar_wait(acc_bar, 0, abort_flag) && !*abort_flag;
+    if (have_acc) {
+      tc_fence_after();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      float* stg = (float*)smem;  // [128 packed rows][kSmemStride] f32, reuses the stage buffers
+      const int q = warp & 3;
+      const int row = 32 * q + lane;
+      for (int c0 = 0; c0 < kTok; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) stg[row * kSmemStride + c0 + j] = __uint_as_float(r[j]);
+      }
+      epi_sync();
+
+      const Packing& pk = P.pk;
+      const int F = pk.ft, r = P.ratio, G = P.G;
+      const int col0 = ftile * kRows;  // first packed column of this tile
+      // -- state: the tokens of the unfinished group (and, overlapped, of the last complete
+      //    group) that this tile owns; thread et writes packed column col0 + et
+      {
+        float* st = P.state + (size_t)(P.slot_offset + b) * P.slots * P.ncol + col0 + et;
+        const int own0 = tt * P.T, own1 = min(own0 + P.T, P.N);
+        auto put = [&](int tok, int slot) { st[(size_t)slot * P.ncol] = stg[et * kSmemStride + (tok - t0)]; };
+        if (!P.overlap) {
+          for (int tok = max(own0, r * G); tok < own1; ++tok) put(tok, tok - r * G);
+        } else {
+          const int qp = G & 1;
+          for (int tok = max(own0, 4 * G); tok < own1; ++tok) put(tok, 4 * qp + tok - 4 * G);
+          if (G >= 1)
+            for (int tok = max(own0, 4 * G - 4); tok < min(own1, 4 * G); ++tok)
+              put(tok, 4 * (1 - qp) + tok - (4 * G - 4));
+          if (G == 0 && tt == 0) {
+            const int kind = et / F;  // padded previous branch: kv 0, score -inf
+            const float pad = kind < pk.nk / 2 ? 0.0f : -INFINITY;
+            for (int i = 0; i < 4; ++i) st[(size_t)(4 + i) * P.ncol] = pad;
+          }
+        }
+      }
+      // -- pool every (feature, group) pair of the tile into bf16 scratch
+      uint16_t* pooled_tile = P.pooled + ((size_t)b * P.ntt + tt) * P.GT * pk.H;
+      for (int pr = et; pr < P.GT * F; pr += 128) {
+        const int f = pr % F, g = pr / F;
+        const int j = tt * P.GT + g;
+        if (j >= G) break;  // pairs are visited in group order
+        float m = -INFINITY, den = 0.0f, num = 0.0f;
+        if (P.overlap) {
+          const float* kA = stg + (KV_A * F + f) * kSmemStride + 4 * g + 4;
+          const float* sA = stg + (S_A * F + f) * kSmemStride + 4 * g + 4;
+          const float* kB = stg + (KV_B * F + f) * kSmemStride + 4 * g;
+          const float* sB = stg + (S_B * F + f) * kSmemStride + 4 * g;
+          const bool padB = j == 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            m = fmaxf(m, sA[i]);
+            if (!padB) m = fmaxf(m, sB[i]);
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float ea = expf(sA[i] - m);
+            den += ea;
+            num = fmaf(ea, kA[i], num);
+            if (!padB) {
+              const float eb = expf(sB[i] - m);
+              den += eb;
+              num = fmaf(eb, kB[i], num);
+            }
+          }
+        } else {
+          const float* kv = stg + (KV * F + f) * kSmemStride + r * g;
+          const float* sc = stg + (S * F + f) * kSmemStride + r * g;
+          for (int i = 0; i < r; ++i) m = fmaxf(m, sc[i]);
+          for (int i = 0; i < r; ++i) {
+            const float e = expf(sc[i] - m);
+            den += e;
+            num = fmaf(e, kv[i], num);
+          }
+        }
+        pooled_tile[(size_t)g * pk.H + ftile * F + f] = bf16_bits(__fdiv_rn(num, den));
+      }
+      // -- the last CTA of this token tile finishes the entries (RMSNorm needs all features)
+      __threadfence();
+      epi_sync();
+      if (et == 0) {
+        const int prev = atomicAdd(&P.counters[b * P.ntt + tt], 1);
+        *last_flag = prev == pk.ntiles - 1;
+      }
+      epi_sync();
+      if (*last_flag) {
+        __threadfence();
+        const int w = et >> 5;
+        const int ng = min(P.GT, G - tt * P.GT);
+        for (int g = w; g < ng; g += 4) {
+          const int j = tt * P.GT + g;
+          float v[16];
+          const int l = min(lane, (pk.H >> 4) - 1);
+          const uint4* src = (const uint4*)(pooled_tile + (size_t)g * pk.H + 16 * l);
+          const uint4 a = __ldcg(src), c = __ldcg(src + 1);
+          const uint32_t wds[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            v[2 * i] = __uint_as_float(wds[i] << 16);
+            v[2 * i + 1] = __uint_as_float(wds[i] & 0xFFFF0000u);
+          }
+          const size_t e = (size_t)b * G + j;
+          const size_t H = pk.H;
+          entry_epilogue(v, lane, (long long)r * j, P.ep, P.out.latent + e * H,
+                         P.out.codes ? P.out.codes + e * (H / 2) : nullptr,
+                         P.out.scales ? P.out.scales + e * (H / 16) : nullptr,
+                         P.out.prequant ? P.out.prequant + e * H : nullptr);
+        }
+        if (et == 0) P.counters[b * P.ntt + tt] = 0;  // ready for the next call
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) atomicOr(P.flag, 4);
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+}  // namespace tc
+
+// ---- host side ------------------------------------------------------------------------------
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  }
+  return fn;
+}
+
+bool prefill_tc_supported(const csa_compressor* c, const void* x) {
+  return c->pk.tw == tc::kRows && c->dim % tc::kKb == 0 && (c->overlap || c->ratio <= tc::kTok) &&
+         ((uintptr_t)x & 15) == 0 && get_encode() != nullptr;
+}
+
+// Bytes of pooled scratch ([B][token tiles][groups per tile][H] bf16) and the number of
+// completion counters ([B][token tiles]) a prefill of B x N tokens needs.
+size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N, size_t* n_counters) {
+  const int T = c->overlap ? tc::kTok - 4 : (tc::kTok / c->ratio) * c->ratio;
+  const int GT = T / c->ratio;
+  const int ntt = (N + T - 1) / T;
+  *n_counters = (size_t)B * ntt;
+  return (size_t)B * ntt * GT * c->H * sizeof(uint16_t);
+}
+
+cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset,
+                              const csa_out& out, void* scratch, int* counters, cudaStream_t s) {
+  using namespace tc;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
+  if (!encode) return cudaErrorNotSupported;
+  Params P;
+  P.N = N;
+  P.K = c->dim;
+  P.ratio = c->ratio;
+  P.overlap = c->overlap;
+  P.halo = c->overlap ? 4 : 0;
+  P.T = c->overlap ? kTok - 4 : (kTok / c->ratio) * c->ratio;
+  P.GT = P.T / c->ratio;
+  P.ntt = (N + P.T - 1) / P.T;
+  P.G = N / c->ratio;
+  P.ncol = c->pk.cols();
+  P.slots = c->slots;
+  P.slot_offset = slot_offset;
+  P.pk = c->pk;
+  P.ep = epi_params(c);
+  P.out = out;
+  P.state = c->state;
+  P.pooled = (uint16_t*)scratch;
+  P.counters = counters;
+  P.flag = c->dev_flag;
+
+  CUtensorMap mw, mx;
+  {
+    // weights: 3 planes x ncol rows x dim, bf16, K innermost
+    cuuint64_t dims[2] = {(cuuint64_t)c->dim, (cuuint64_t)3 * P.ncol};
+    cuuint64_t strides[1] = {(cuuint64_t)c->dim * 2};
+    cuuint32_t box[2] = {kKb, kRows};
+    cuuint32_t es[2] = {1, 1};
+    if (encode(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)c->w_planes, dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    // x: [B][N][dim] bf16; out-of-range tokens (the halo before token 0, the tail past N) read as 0
+    cuuint64_t dims[3] = {(cuuint64_t)c->dim, (cuuint64_t)N, (cuuint64_t)B};
+    cuuint64_t strides[2] = {(cuuint64_t)c->dim * 2, (cuuint64_t)N * c->dim * 2};
+    cuuint32_t box[3] = {kKb, kTok, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (encode(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)x, dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const size_t smem = (size_t)kStages * kStageBytes + 1024 /* barriers */ + 1024 /* alignment */;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(c->pk.ntiles, P.ntt, B);
+  prefill_tc_kernel<<<grid, kThreads, smem, s>>>(mw, mx, P);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

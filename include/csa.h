@@ -170,6 +170,11 @@ int csa_fp4_e4m3_roundtrip(const uint16_t* in, int64_t n_blocks, uint8_t* codes,
  * off.  The events stay owned by the caller and must outlive their use. */
 int csa_set_profile_events(csa_compressor* c, csa_event_t start, csa_event_t stop);
 
+/* 1 if csa_compress_prefill on this handle runs the tensor-core kernel (for a 16-byte
+ * aligned x), 0 if it runs the CUDA-core projection (packed tiles narrower than 128 rows,
+ * ratio above 256, or no tensor-map encoder in the driver), or a negative csa_status. */
+int csa_uses_tensor_cores(const csa_compressor* c);
+
 /* Number of kernels this handle has enqueued since it was created (all calls). */
 int64_t csa_kernel_launches(const csa_compressor* c);
 
