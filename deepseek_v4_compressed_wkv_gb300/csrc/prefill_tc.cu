@@ -9,8 +9,15 @@
 // the f32 projection of "Pool token pairs" (x.float(), wkv(x), wgate(x)) and the f32 x . w^T
 // of "Module compress" (linear_f32).
 //
-// Roles (192 threads): warp 0 issues the TMA loads (x tile shared by all three planes, one
-// tile per plane), warp 1 owns TMEM and issues tcgen05.mma, warps 2-5 run the epilogue.
+// Accumulation: the tensor cores' f32 accumulator is not IEEE round-to-nearest (truncation per
+// MMA leaves ~2^-16 relative error after 768 steps of K=16), so the MMAs of each K chunk of 128
+// go into a fresh TMEM accumulator (two, alternating) and the epilogue warps add each chunk into
+// f32 registers with ordinary round-to-nearest additions, in chunk order (the promotion to CUDA
+// cores used for low-precision accumulators).  The result is as accurate as an f32 FMA GEMM.
+//
+// Roles (320 threads): warp 0 issues the TMA loads (x tile shared by all three planes, one
+// tile per plane), warp 1 owns TMEM and issues tcgen05.mma, warps 2-9 run the epilogue (warps
+// w and w+4 share TMEM lane quarter w%4 and split the 256 token columns).
 // One CTA computes one (packed tile, token tile); the CTAs of one token tile meet in a global
 // counter, and the last one to finish normalises, rotates and quantises the tile's entries
 // from the pooled values the others left in scratch (the RMSNorm needs all H features).
@@ -31,8 +38,10 @@ constexpr int kPlaneBytes = kRows * kKb * 2;          // 16 KB
 constexpr int kXBytes = kTok * kKb * 2;               // 32 KB
 constexpr int kStageBytes = 3 * kPlaneBytes + kXBytes;  // 80 KB
 constexpr int kSmemStride = kTok + 1;                 // f32 staging row stride (bank-conflict free)
-constexpr int kThreads = 192;
-constexpr int kTmemCols = 256;
+constexpr int kChunkKb = 2;         // K blocks per accumulator chunk (K = 128)
+constexpr int kEpiThreads = 256;
+constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kTmemCols = 2 * kTok;  // two chunk accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;           // bounded mbarrier waits: 2 s
 
 static_assert(kRows * kSmemStride * 4 <= kStages * kStageBytes, "staging must fit in the stage buffers");
@@ -161,7 +170,11 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // ---- the kernel ----------------------------------------------------------------------------
 
@@ -172,14 +185,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* full = (uint64_t*)(smem + kStages * kStageBytes);
   uint64_t* empty = full + kStages;
-  uint64_t* acc_bar = empty + kStages;
-  uint32_t* tmem_slot = (uint32_t*)(acc_bar + 1);
+  uint64_t* chunk_full = empty + kStages;  // [2]: chunk accumulator ready for the epilogue
+  uint64_t* chunk_empty = chunk_full + 2;  // [2]: chunk accumulator drained, free for the MMAs
+  uint32_t* tmem_slot = (uint32_t*)(chunk_empty + 2);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   int* last_flag = (int*)(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ftile = blockIdx.x, tt = blockIdx.y, b = blockIdx.z;
   const int nkb = P.K / kKb;
+  const int nch = (nkb + kChunkKb - 1) / kChunkKb;
   const int t0 = tt * P.T - P.halo;  // sequence index of the tile's token 0
 
   if (threadIdx.x == 0) {
@@ -187,7 +202,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_bar, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&chunk_full[i], 1);
+      mbar_init(&chunk_empty[i], kEpiThreads / 32);
+    }
     *abort_flag = 0;
     *last_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -232,47 +250,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(kRows, kTok);
       bool ok = true;
-      for (int kb = 0; kb < nkb && ok; ++kb) {
-        const int s = kb % kStages;
-        if (!mbar_wait(&full[s], (kb / kStages) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
+      for (int c = 0; c < nch && ok; ++c) {
+        const int buf = c & 1;
+        if (c >= 2 && !mbar_wait(&chunk_empty[buf], ((c >> 1) - 1) & 1, abort_flag)) break;
         tc_fence_after();
-        const uint32_t st = smem_addr(smem + s * kStageBytes);
-        const uint32_t xs = st + 3 * kPlaneBytes;
-        for (int p = 0; p < 3; ++p)
-          for (int k = 0; k < kKb / 16; ++k)
-            mma_bf16(tmem, sw128_desc(st + p * kPlaneBytes + k * 32), sw128_desc(xs + k * 32), idesc,
-                     (kb | p | k) != 0);
-        mma_commit(&empty[s]);
+        const uint32_t d = tmem + (uint32_t)(buf * kTok);
+        const int kb0 = c * kChunkKb, kb1 = min(nkb, kb0 + kChunkKb);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const int s = kb % kStages;
+          if (!mbar_wait(&full[s], (kb / kStages) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_addr(smem + s * kStageBytes);
+          const uint32_t xs = st + 3 * kPlaneBytes;
+          for (int p = 0; p < 3; ++p)
+            for (int k = 0; k < kKb / 16; ++k)
+              mma_bf16(d, sw128_desc(st + p * kPlaneBytes + k * 32), sw128_desc(xs + k * 32), idesc,
+                       (kb != kb0 || p != 0 || k != 0) ? 1u : 0u);
+          mma_commit(&empty[s]);
+        }
+        if (ok) mma_commit(&chunk_full[buf]);  // arrives once this chunk's MMAs have completed
       }
-      mma_commit(acc_bar);  // arrives once every MMA issued above has completed
     }
   } else {
-    // ---- epilogue (warps 2..5; warp w reads TMEM lanes 32*(w%4) .. +31)
-    const int et = threadIdx.x - 64;  // 0..127
-    const bool have_acc = mbar_wait(acc_bar, 0, abort_flag) && !*abort_flag;
-    if (have_acc) {
+    // ---- epilogue (warps 2..9; warp w reads TMEM lanes 32*(w%4) .. +31, columns 128*h .. +127)
+    const int et = threadIdx.x - 64;  // 0..255
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int row = 32 * q + lane;
+    float acc[kTok / 2];
+#pragma unroll
+    for (int i = 0; i < kTok / 2; ++i) acc[i] = 0.0f;
+    bool ok = true;
+    for (int c = 0; c < nch; ++c) {
+      const int buf = c & 1;
+      if (!mbar_wait(&chunk_full[buf], (c >> 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
+      const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * kTok + 128 * h);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t r[32];
+        tmem_ld32(base + 32 * j, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[32 * j + i] += __uint_as_float(r[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&chunk_empty[buf]);
+    }
+    const bool have_acc = ok && !*abort_flag;
+    if (have_acc) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       float* stg = (float*)smem;  // [128 packed rows][kSmemStride] f32, reuses the stage buffers
-      const int q = warp & 3;
-      const int row = 32 * q + lane;
-      for (int c0 = 0; c0 < kTok; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, r);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) stg[row * kSmemStride + c0 + j] = __uint_as_float(r[j]);
-      }
+      for (int i = 0; i < kTok / 2; ++i) stg[row * kSmemStride + 128 * h + i] = acc[i];
       epi_sync();
 
       const Packing& pk = P.pk;
       const int F = pk.ft, r = P.ratio, G = P.G;
       const int col0 = ftile * kRows;  // first packed column of this tile
       // -- state: the tokens of the unfinished group (and, overlapped, of the last complete
-      //    group) that this tile owns; thread et writes packed column col0 + et
-      {
+      //    group) that this tile owns; thread et < 128 writes packed column col0 + et
+      if (et < kRows) {
         float* st = P.state + (size_t)(P.slot_offset + b) * P.slots * P.ncol + col0 + et;
         const int own0 = tt * P.T, own1 = min(own0 + P.T, P.N);
         auto put = [&](int tok, int slot) { st[(size_t)slot * P.ncol] = stg[et * kSmemStride + (tok - t0)]; };
@@ -293,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // -- pool every (feature, group) pair of the tile into bf16 scratch
       uint16_t* pooled_tile = P.pooled + ((size_t)b * P.ntt + tt) * P.GT * pk.H;
-      for (int pr = et; pr < P.GT * F; pr += 128) {
+      for (int pr = et; pr < P.GT * F; pr += kEpiThreads) {
         const int f = pr % F, g = pr / F;
         const int j = tt * P.GT + g;
         if (j >= G) break;  // pairs are visited in group order
@@ -344,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
         const int w = et >> 5;
         const int ng = min(P.GT, G - tt * P.GT);
-        for (int g = w; g < ng; g += 4) {
+        for (int g = w; g < ng; g += kEpiThreads / 32) {
           const int j = tt * P.GT + g;
           float v[16];
           const int l = min(lane, (pk.H >> 4) - 1);
