@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--decode-steps", type=int, default=64)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-seconds", type=float, default=1.0,
+                    help="seconds of untimed steps run under the clock sampler before the timed region")
     return ap.parse_args()
 
 
@@ -177,7 +179,7 @@ def run_ours(args, rank, world, local):
     clocks = ClockSampler(local)
     clocks.start()
     # keep the GPU busy long enough for the clock sampler to see it under this load
-    t_end = time.time() + 1.0
+    t_end = time.time() + args.clock_seconds
     while time.time() < t_end:
         step()
         torch.cuda.synchronize()

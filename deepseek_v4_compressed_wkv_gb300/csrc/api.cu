@@ -120,6 +120,10 @@ int ensure_counters(csa_compressor* c, size_t n, cudaStream_t s) {
 
 }  // namespace
 
+// Used by other translation units of the library to report a failure through
+// csa_last_error (not part of the C ABI).
+__attribute__((visibility("hidden"))) int csa_internal_fail(int code, const char* msg) { return fail(code, "%s", msg); }
+
 extern "C" {
 
 void csa_options_default(csa_options* o) {
@@ -288,7 +292,12 @@ int csa_compress_decode(csa_compressor* c, const uint16_t* x_tok, int B, const i
     return fail(CSA_ERR_ARG, "x_tok, start_pos, emitted and out->latent are required");
   cudaStream_t s = (cudaStream_t)stream;
   if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
-  CSA_CUDA(csa::launch_projection_ffma(c, x_tok, B, c->state, 1, start_pos, s), "decode projection launch");
+  if (csa::decode_tc_supported(c, x_tok)) {
+    CSA_CUDA(csa::launch_decode_tc(c, x_tok, B, start_pos, s), "tensor-core decode projection launch");
+    c->launches += (B + 127) / 128 - 1;
+  } else {
+    CSA_CUDA(csa::launch_projection_ffma(c, x_tok, B, c->state, 1, start_pos, s), "decode projection launch");
+  }
   if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
   CSA_CUDA(csa::launch_decode_emit(c, start_pos, B, *out, emitted, s), "decode emit launch");
   c->launches += 2;

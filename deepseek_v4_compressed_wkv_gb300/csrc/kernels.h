@@ -26,4 +26,9 @@ size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N, size_t* n
 cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset,
                               const csa_out& out, void* scratch, int* counters, cudaStream_t s);
 
+// Tensor-core decode projection (decode_tc.cu): one token per sequence into its state slot.
+bool decode_tc_supported(const csa_compressor* c, const void* x);
+cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, const int32_t* start_pos,
+                             cudaStream_t s);
+
 }  // namespace csa
