@@ -32,7 +32,7 @@ ABI_FUNCTIONS = ("csa_options_default", "csa_compressor_create", "csa_compressor
                  "csa_compress_prefill", "csa_compress_decode", "csa_state_reset", "csa_state_elems",
                  "csa_state_export", "csa_device_status", "csa_compressor_destroy", "csa_last_error",
                  "csa_fp4_e4m3_roundtrip", "csa_rope_table", "csa_set_profile_events", "csa_kernel_launches",
-                 "csa_uses_tensor_cores")
+                 "csa_uses_tensor_cores", "csa_compress_prefill_noalloc")
 
 
 class CSAError(RuntimeError):
@@ -85,6 +85,7 @@ def load_library(build_if_missing: bool = True):
             "csa_set_profile_events": ([P, P, P], I),
             "csa_kernel_launches": ([P], I64),
             "csa_uses_tensor_cores": ([P], I),
+            "csa_compress_prefill_noalloc": ([P, P, I, I, I, I, P, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
