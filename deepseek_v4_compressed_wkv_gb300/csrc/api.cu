@@ -93,6 +93,11 @@ void free_all(csa_compressor* c) {
   cudaFree(c->dev_flag);
   cudaFree(c->scratch);
   cudaFree(c->tc_counters);
+  cudaFree(c->dec_part);
+  cudaFree(c->dec_pooled);
+  cudaFree(c->dec_counters);
+  cudaFree(c->dec_tile_ctr);
+  cudaFree(c->dec_tile_gen);
 }
 
 int ensure_scratch(csa_compressor* c, size_t bytes, cudaStream_t s) {
@@ -190,6 +195,10 @@ int csa_compressor_create(int dim, int H, int ratio, int overlap, const csa_opti
     alloc((void**)&c->gain, H * sizeof(float));
     alloc((void**)&c->state, (size_t)o.max_batch * c->slots * ncol * sizeof(float));
     alloc((void**)&c->dev_flag, sizeof(int));
+    alloc((void**)&c->dec_pooled, (size_t)o.max_batch * H * sizeof(uint16_t));
+    alloc((void**)&c->dec_counters, (size_t)o.max_batch * sizeof(int));
+    alloc((void**)&c->dec_tile_ctr, (size_t)pk.ntiles * sizeof(unsigned));
+    alloc((void**)&c->dec_tile_gen, (size_t)pk.ntiles * sizeof(unsigned));
     if (o.rope_dim > 0) {
       const size_t n = (size_t)o.max_pos * (o.rope_dim / 2);
       alloc((void**)&c->rope_cos, n * sizeof(float));
@@ -204,6 +213,9 @@ int csa_compressor_create(int dim, int H, int ratio, int overlap, const csa_opti
       }
     }
     if (e == cudaSuccess) e = cudaMemset(c->dev_flag, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(c->dec_counters, 0, (size_t)o.max_batch * sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(c->dec_tile_ctr, 0, (size_t)pk.ntiles * sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMemset(c->dec_tile_gen, 0, (size_t)pk.ntiles * sizeof(unsigned));
     if (e == cudaSuccess && csa::launch_state_reset(c, 0, o.max_batch, 0) != cudaSuccess) e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
@@ -291,13 +303,28 @@ int csa_compress_decode(csa_compressor* c, const uint16_t* x_tok, int B, const i
   if (!x_tok || !start_pos || !emitted || !out || !out->latent)
     return fail(CSA_ERR_ARG, "x_tok, start_pos, emitted and out->latent are required");
   cudaStream_t s = (cudaStream_t)stream;
-  if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
   if (csa::decode_tc_supported(c, x_tok)) {
-    CSA_CUDA(csa::launch_decode_tc(c, x_tok, B, start_pos, s), "tensor-core decode projection launch");
-    c->launches += (B + 127) / 128 - 1;
-  } else {
-    CSA_CUDA(csa::launch_projection_ffma(c, x_tok, B, c->state, 1, start_pos, s), "decode projection launch");
+    // split-K partial sums: [slices][B][2C] f32, grown on first use (a later call of the same
+    // or smaller B allocates nothing)
+    const int ks = csa::decode_tc_slices(c);
+    const size_t bytes = (size_t)ks * B * c->pk.cols() * sizeof(float);
+    if (c->dec_part_bytes < bytes) {
+      CSA_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+      cudaFree(c->dec_part);
+      c->dec_part = nullptr;
+      c->dec_part_bytes = 0;
+      CSA_CUDA(cudaMalloc(&c->dec_part, bytes), "cudaMalloc(decode partial sums)");
+      c->dec_part_bytes = bytes;
+    }
+    if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
+    CSA_CUDA(csa::launch_decode_tc(c, x_tok, B, start_pos, c->dec_part, ks, *out, emitted, s),
+             "tensor-core decode launch");
+    if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
+    c->launches += (B + 127) / 128;
+    return CSA_OK;
   }
+  if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
+  CSA_CUDA(csa::launch_projection_ffma(c, x_tok, B, c->state, 1, start_pos, s), "decode projection launch");
   if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
   CSA_CUDA(csa::launch_decode_emit(c, start_pos, B, *out, emitted, s), "decode emit launch");
   c->launches += 2;

@@ -8,7 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/csa.h"
+#include "csa.h"  // include/ is on the include path (see build.py)
 
 namespace csa {
 
@@ -199,6 +199,12 @@ struct csa_compressor {
   int* dev_flag;            // device-side error flag
   float* scratch;           // projection scratch [rows][2C] f32 (grown on demand)
   size_t scratch_bytes;
+  float* dec_part;          // decode split-K partial sums [slices][B][2C] (grown on demand)
+  size_t dec_part_bytes;
+  uint16_t* dec_pooled;     // decode pooled bf16 values [max_batch][H]
+  int* dec_counters;        // decode per-sequence completion counters [max_batch] (kept at zero)
+  unsigned* dec_tile_ctr;   // decode K-slice barrier per packed tile: arrivals (kept at zero)
+  unsigned* dec_tile_gen;   //   and generations
   int* tc_counters;         // per token tile completion counters of the tensor-core prefill
   size_t tc_counters_n;     // (kept at zero between calls by the kernel itself)
   cudaEvent_t prof_start, prof_stop;  // optional events around the dominant kernel

@@ -1,21 +1,28 @@
-// Decode projection on the tensor cores (sm_103a): one token per sequence, written straight
-// into each sequence's state slot ("Pool token pairs", decode branch: kv_state[:, slot] =
-// kv, score_state[:, slot] = score).  The pool and epilogue of the sequences whose group
-// completes run afterwards in decode_emit_kernel.
+// Decode on the tensor cores (sm_103a): one token per sequence, into each sequence's state slot
+// ("Pool token pairs", decode branch: kv_state[:, slot] = kv, score_state[:, slot] = score),
+// then the pool and epilogue of the sequences whose group completes, in one launch.
 //
-// Decode streams every weight once per step for only B tokens, so it is bound by HBM: the
-// f32 weights are read once (4 bytes each) and split into three exact bf16 planes in shared
-// memory by the CUDA cores, which the tensor cores then multiply with the bf16 tokens.
+// Decode streams every weight once per step for only B tokens, so it is bound by HBM.  The
+// kernel streams the three exact bf16 planes of the weights that set_weights prepared (w = p0 +
+// p1 + p2; 6 bytes per weight, 1.5x the f32 weights) straight into the tensor cores: splitting
+// the f32 weights on the CUDA cores instead (4 bytes per weight) made the kernel bound by
+// instruction issue at a quarter of the HBM bandwidth.
 //
-// Work split: packed tile t (128 rows) x K slice.  The K slices of one tile form a thread-block
-// cluster; each CTA accumulates its slice in K chunks of 128 (TMEM, promoted to f32 registers
-// as in the prefill kernel), then the cluster reduces the partial sums through distributed
-// shared memory in a fixed order, each CTA owning 128 / cluster-size tokens, and writes them
-// to the state.
+// Work split: packed tile t (128 rows) x K slice, at most one CTA per SM, launched cooperatively
+// so that all CTAs are resident together.  Each CTA accumulates its slice in K chunks of 128
+// (TMEM, promoted to f32 registers as in the prefill kernel) and writes its partial sums to
+// scratch.  The K slices of a tile then meet at a self-resetting counter barrier (a bounded
+// wait), and each of them finishes a share of the tokens: it adds the slices' partials in a
+// fixed order into the token's state slot (a deterministic split-K reduction), applies the
+// restart at position 0, and, where the token completed a group, pools the tile's features
+// ("Pool token pairs", decode branch; "Compressed Sparse Attention - ratio m = 4", decode
+// rule).  The last tile to finish a sequence (a completion counter, no waiting) runs the
+// entry epilogue, which needs all H features for the RMSNorm.
 //
-// Roles (320 threads): warp 0 lane 0 streams weight tiles (TMA, 3-stage ring), warp 0 lane 1
-// streams token tiles, warp 1 owns TMEM and issues tcgen05.mma, warps 2-9 split the weights
-// into bf16 planes, drain the chunk accumulators and run the reduction.
+// Roles (320 threads) in the projection: warp 0 issues the TMA loads (three plane tiles and one
+// token tile of K = 32 per stage, 64-byte swizzle, 6 stages), warp 1 owns TMEM and issues
+// tcgen05.mma, warps 2-9 drain the chunk accumulators and store the partial sums.  All warps
+// take part in the reduction and pooling.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -28,60 +35,203 @@ namespace dtc {
 
 using namespace tcx;
 
-constexpr int kRows = 128;                       // packed rows per tile (MMA M)
-constexpr int kTok = 128;                        // tokens per launch (MMA N)
-constexpr int kKb = 64;                          // K per block
-constexpr int kWStages = 3;                      // f32 weight ring
-constexpr int kMStages = 2;                      // bf16 planes + token ring
-constexpr int kChunkKb = 2;                      // K blocks per accumulator chunk
-constexpr int kWBytes = kRows * kKb * 4;         // 32 KB
-constexpr int kPlaneBytes = kRows * kKb * 2;     // 16 KB
-constexpr int kXBytes = kTok * kKb * 2;          // 16 KB
-constexpr int kMBytes = 3 * kPlaneBytes + kXBytes;  // 64 KB
-constexpr int kRingBytes = kWStages * kWBytes + kMStages * kMBytes;  // 224 KB
+constexpr int kRows = 128;                              // packed rows per tile (MMA M)
+constexpr int kTok = 128;                               // tokens per launch (MMA N)
+constexpr int kKb = 64;                                 // K granularity of the slice split
+constexpr int kKs = 32;                                 // K per stage (one 64-byte swizzle row of bf16)
+constexpr int kStages = 6;
+constexpr int kChunkSteps = 4;                          // stages per accumulator chunk (K = 128)
+constexpr int kPlaneBytes = kRows * kKs * 2;            // 8 KB
+constexpr int kXBytes = kTok * kKs * 2;                 // 8 KB
+constexpr int kStageBytes = 3 * kPlaneBytes + kXBytes;  // 32 KB
+constexpr int kRingBytes = kStages * kStageBytes;       // 192 KB
 constexpr int kEpiThreads = 256;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kTmemCols = 2 * kTok;
-constexpr int kMaxCluster = 16;
 
 struct Params {
-  int K, ks_kb;          // dim, K blocks per CTA
-  int B, ncol, slots, ratio, overlap;
-  const int32_t* start_pos;
-  float* state;
+  int nkb_total, ks;         // K blocks (of 64) of dim, number of K slices
+  int B, b_total, b0;        // tokens in this launch, in the call, first token of this launch
+  int ncol;                  // packed columns (rows of one weight plane)
+  float* part;               // [ks][b_total][ncol] partial sums
   int* flag;
+  const int32_t* start_pos;  // [b_total]
+  float* state;              // [max_batch][slots][ncol]
+  int slots, ratio, overlap;
+  Packing pk;
+  EpiParams ep;
+  csa_out out;               // rows indexed by sequence
+  uint8_t* emitted;          // [b_total]
+  uint16_t* pooled;          // [b_total][H] bf16 scratch
+  int* seq_ctr;              // [b_total] per-sequence tile counters (kept at zero between calls)
+  unsigned* tile_ctr;        // [ntiles] barrier arrivals (kept at zero between calls)
+  unsigned* tile_gen;        // [ntiles] barrier generations
 };
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
+__device__ __forceinline__ float padded_kind_value(const Packing& pk, int col) {
+  return ((col % pk.tw) / pk.ft) < pk.nk / 2 ? 0.0f : -INFINITY;  // kv kinds first, then scores
 }
 
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
+// After the projection: meet the other K slices of this tile, then reduce, update the state and
+// pool for tokens [ks*B/KS, (ks+1)*B/KS) of this launch.  `scr` is free shared memory.
+__device__ void finish_tokens(const Params& P, int tile, int ks, float* scr) {
+  __shared__ unsigned gen0;
+  __shared__ int go;
+  __shared__ int last;
+  __threadfence();  // this CTA's partial sums are visible before it arrives
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile unsigned* gen = P.tile_gen + tile;
+    gen0 = *gen;
+    __threadfence();
+    go = 1;
+    if (atomicAdd(P.tile_ctr + tile, 1u) == (unsigned)P.ks - 1) {
+      P.tile_ctr[tile] = 0;  // every slice has arrived: reset for the next call, then release
+      __threadfence();
+      atomicAdd(P.tile_gen + tile, 1u);
+    } else {
+      const uint64_t t0 = globaltimer();
+      while (*gen == gen0) {
+        if (globaltimer() - t0 > kWaitNs) {
+          atomicOr(P.flag, 4);
+          go = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  if (!go) return;
 
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-
-__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
+  const Packing& pk = P.pk;
+  const int ncol = pk.cols(), c0 = tile * kRows, f0 = tile * pk.ft;
+  const int tb0 = (int)((long long)ks * P.B / P.ks), tb1 = (int)((long long)(ks + 1) * P.B / P.ks);
+  const int nt = tb1 - tb0;
+  // -- the K-slice partials of each token into its state slot, in slice order
+  for (int it = threadIdx.x; it < nt * (kRows / 4); it += blockDim.x) {
+    const int b = P.b0 + tb0 + it / (kRows / 4), c = c0 + 4 * (it % (kRows / 4));
+    const float* src = P.part + (size_t)b * ncol + c;
+    const size_t stride = (size_t)P.b_total * ncol;
+    float4 a = __ldcg(reinterpret_cast<const float4*>(src));
+    for (int k = 1; k < P.ks; ++k) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + k * stride));
+      a.x += v.x;
+      a.y += v.y;
+      a.z += v.z;
+      a.w += v.w;
+    }
+    const int pp = max(P.start_pos[b], 0);
+    const int slot = P.overlap ? ((pp >> 2) & 1) * 4 + (pp & 3) : pp % P.ratio;
+    *reinterpret_cast<float4*>(P.state + ((size_t)b * P.slots + slot) * ncol + c) = a;
+  }
+  // -- restart padding, emission flags, position checks
+  for (int it = threadIdx.x; it < nt; it += blockDim.x) {
+    const int b = P.b0 + tb0 + it;
+    const int p = P.start_pos[b];
+    if (p == 0 && P.overlap)  // the previous group's branch is the padded one
+      for (int i = 0; i < 4; ++i)
+        for (int c = c0; c < c0 + kRows; ++c)
+          P.state[((size_t)b * P.slots + 4 + i) * ncol + c] = padded_kind_value(pk, c);
+    if (tile == 0) {
+      const bool emit = p >= 0 && (p + 1) % P.ratio == 0;
+      const long long pos = (long long)p + 1 - P.ratio;
+      const bool pos_ok = P.ep.rope_dim == 0 || pos < P.ep.max_pos;
+      P.emitted[b] = (emit && pos_ok) ? 1 : 0;
+      if (p < 0) atomicOr(P.flag, 1);
+      if (emit && !pos_ok) atomicOr(P.flag, 2);
+    }
+  }
+  __syncthreads();  // the slots written above are read below by other threads
+  // -- pool the tile's features for every token of this share that completed a group: groups
+  //    of threads split the candidates (max, then exp sums), merged in a fixed order
+  const int ncand = P.overlap ? 8 : P.ratio;
+  const int ng = (int)blockDim.x / pk.ft;
+  const int f = f0 + (int)threadIdx.x % pk.ft, g = (int)threadIdx.x / pk.ft;
+  float* sm_m = scr;
+  float* sm_d = scr + blockDim.x;
+  float* sm_n = scr + 2 * blockDim.x;
+  for (int it = 0; it < nt; ++it) {
+    const int b = P.b0 + tb0 + it;
+    const int p = P.start_pos[b];
+    if (p < 0 || (p + 1) % P.ratio != 0) continue;
+    const long long pos = (long long)p + 1 - P.ratio;
+    if (P.ep.rope_dim > 0 && pos >= P.ep.max_pos) continue;
+    const float* st = P.state + (size_t)b * P.slots * ncol;
+    const int q = (p >> 2) & 1;
+    auto cand = [&](int i, float& sv, float& kv, bool load_kv) {
+      const float* row;
+      int cs, ck;
+      if (P.overlap) {
+        const bool prevB = i < 4;
+        row = st + (size_t)(prevB ? 4 * (1 - q) + i : 4 * q + i - 4) * ncol;
+        cs = pk.col(prevB ? S_B : S_A, f);
+        ck = pk.col(prevB ? KV_B : KV_A, f);
+      } else {
+        row = st + (size_t)i * ncol;
+        cs = pk.col(S, f);
+        ck = pk.col(KV, f);
+      }
+      sv = row[cs];
+      if (load_kv) kv = row[ck];
+    };
+    float m = -INFINITY, den = 0.0f, num = 0.0f;
+    if (g < ng) {
+      for (int i = g; i < ncand; i += ng) {
+        float sv, kv;
+        cand(i, sv, kv, false);
+        m = fmaxf(m, sv);
+      }
+      for (int i = g; i < ncand; i += ng) {
+        float sv, kv;
+        cand(i, sv, kv, true);
+        const float e = expf(sv - m);
+        den += e;
+        num = fmaf(e, kv, num);
+      }
+    }
+    sm_m[threadIdx.x] = m;
+    sm_d[threadIdx.x] = den;
+    sm_n[threadIdx.x] = num;
+    __syncthreads();
+    if (g == 0) {
+      float M = m;
+      for (int k = 1; k < ng; ++k) M = fmaxf(M, sm_m[k * pk.ft + threadIdx.x]);
+      float D = 0.0f, Nn = 0.0f;
+      for (int k = 0; k < ng; ++k) {
+        const int t = k * pk.ft + threadIdx.x;
+        const float w = sm_m[t] == -INFINITY ? 0.0f : expf(sm_m[t] - M);
+        D = fmaf(sm_d[t], w, D);
+        Nn = fmaf(sm_n[t], w, Nn);
+      }
+      P.pooled[(size_t)b * pk.H + f] = bf16_bits(__fdiv_rn(Nn, D));
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(&P.seq_ctr[b], 1) == pk.ntiles - 1;
+    __syncthreads();
+    if (last && threadIdx.x < 32) {  // the last tile of this sequence: RMSNorm, RoPE, fp4
+      __threadfence();
+      const int lane = threadIdx.x;
+      const int l = min(lane, (pk.H >> 4) - 1);
+      const uint4* src = reinterpret_cast<const uint4*>(P.pooled + (size_t)b * pk.H + 16 * l);
+      const uint4 a = __ldcg(src), c = __ldcg(src + 1);
+      const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+      const size_t H = pk.H;
+      entry_epilogue(v, lane, pos, P.ep, P.out.latent + b * H, P.out.codes ? P.out.codes + b * (H / 2) : nullptr,
+                     P.out.scales ? P.out.scales + b * (H / 16) : nullptr,
+                     P.out.prequant ? P.out.prequant + b * H : nullptr);
+      if (lane == 0) P.seq_ctr[b] = 0;  // ready for the next call
+    }
+    __syncthreads();
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -89,32 +239,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const Params P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t* wring = smem;                               // [kWStages][128 rows][64] f32, row-major
-  uint8_t* mring = smem + kWStages * kWBytes;          // [kMStages]{3 planes, x}, 128-byte swizzle
-  uint64_t* w_full = (uint64_t*)(smem + kRingBytes);
-  uint64_t* w_empty = w_full + kWStages;
-  uint64_t* m_full = w_empty + kWStages;
-  uint64_t* m_empty = m_full + kMStages;
-  uint64_t* c_full = m_empty + kMStages;
+  uint64_t* full = (uint64_t*)(smem + kRingBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* c_full = empty + kStages;
   uint64_t* c_empty = c_full + 2;
   uint32_t* tmem_slot = (uint32_t*)(c_empty + 2);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x;
-  const uint32_t crank = cluster_rank(), csize = cluster_size();
-  const int kb_base = (int)crank * P.ks_kb;
-  const int nkb = P.ks_kb;
-  const int nch = (nkb + kChunkKb - 1) / kChunkKb;
+  const int tile = blockIdx.x, ks = blockIdx.y;
+  const int kb_base = (int)((long long)ks * P.nkb_total / P.ks);
+  const int nkb = (int)((long long)(ks + 1) * P.nkb_total / P.ks) - kb_base;
+  const int nstep = nkb * (kKb / kKs);
+  const int nch = (nstep + kChunkSteps - 1) / kChunkSteps;
+  const int k0 = kb_base * kKb;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kWStages; ++s) {
-      mbar_init(&w_full[s], 1);
-      mbar_init(&w_empty[s], kEpiThreads / 32);
-    }
-    for (int m = 0; m < kMStages; ++m) {
-      mbar_init(&m_full[m], kEpiThreads / 32 + 1);
-      mbar_init(&m_empty[m], 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c_full[i], 1);
@@ -131,24 +274,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  float acc[kTok / 2];
-#pragma unroll
-  for (int i = 0; i < kTok / 2; ++i) acc[i] = 0.0f;
-
   if (warp == 0) {
-    if (lane == 0) {  // weights: HBM -> f32 ring
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kWStages;
-        if (kb >= kWStages && !mbar_wait(&w_empty[s], ((kb / kWStages) - 1) & 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&w_full[s], kWBytes);
-        tma_load_2d(wring + s * kWBytes, &map_w, (kb_base + kb) * kKb, tile * kRows, &w_full[s]);
-      }
-    } else if (lane == 1) {  // tokens: -> x slot of the MMA ring
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int m = kb % kMStages;
-        if (kb >= kMStages && !mbar_wait(&m_empty[m], ((kb / kMStages) - 1) & 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&m_full[m], kXBytes);
-        tma_load_2d(mring + m * kMBytes + 3 * kPlaneBytes, &map_x, (kb_base + kb) * kKb, 0, &m_full[m]);
+    if (lane == 0) {
+      for (int t = 0; t < nstep; ++t) {
+        const int s = t % kStages;
+        if (t >= kStages && !mbar_wait(&empty[s], ((t / kStages) - 1) & 1, abort_flag)) break;
+        uint8_t* st = smem + s * kStageBytes;
+        mbar_arrive_expect_tx(&full[s], kStageBytes);
+        for (int p = 0; p < 3; ++p)
+          tma_load_2d(st + p * kPlaneBytes, &map_w, k0 + t * kKs, p * P.ncol + tile * kRows, &full[s]);
+        tma_load_2d(st + 3 * kPlaneBytes, &map_x, k0 + t * kKs, 0, &full[s]);
       }
     }
   } else if (warp == 1) {
@@ -160,33 +295,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c >= 2 && !mbar_wait(&c_empty[buf], ((c >> 1) - 1) & 1, abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * kTok);
-        const int kb0 = c * kChunkKb, kb1 = min(nkb, kb0 + kChunkKb);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          const int m = kb % kMStages;
-          if (!mbar_wait(&m_full[m], (kb / kMStages) & 1, abort_flag)) {
+        const int t0 = c * kChunkSteps, t1 = min(nstep, t0 + kChunkSteps);
+        for (int t = t0; t < t1; ++t) {
+          const int s = t % kStages;
+          if (!mbar_wait(&full[s], (t / kStages) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t st = smem_addr(mring + m * kMBytes);
-          const uint32_t xs = st + 3 * kPlaneBytes;
+          const uint32_t st = smem_addr(smem + s * kStageBytes);
+          const uint32_t xa = st + 3 * kPlaneBytes;
           for (int p = 0; p < 3; ++p)
-            for (int k = 0; k < kKb / 16; ++k)
-              mma_bf16(d, sw128_desc(st + p * kPlaneBytes + k * 32), sw128_desc(xs + k * 32), idesc,
-                       (kb != kb0 || p != 0 || k != 0) ? 1u : 0u);
-          mma_commit(&m_empty[m]);
+            for (int k = 0; k < kKs / 16; ++k)
+              mma_bf16(d, sw64_desc(st + p * kPlaneBytes + k * 32), sw64_desc(xa + k * 32), idesc,
+                       (t != t0 || p != 0 || k != 0) ? 1u : 0u);
+          mma_commit(&empty[s]);
         }
         if (ok) mma_commit(&c_full[buf]);
       }
     }
   } else {
-    const int et = threadIdx.x - 64;  // 0..255
+    // drain each chunk into f32 registers, in chunk order; then store the partial sums
     const int q = warp & 3, h = (warp - 2) >> 2;
+    const int row = 32 * q + lane;
+    float acc[kTok / 2];
+#pragma unroll
+    for (int i = 0; i < kTok / 2; ++i) acc[i] = 0.0f;
     bool ok = true;
-    int drained = 0;
-    auto drain = [&](int c) {  // add chunk c into the f32 registers
+    for (int c = 0; c < nch; ++c) {
       const int buf = c & 1;
-      if (!mbar_wait(&c_full[buf], (c >> 1) & 1, abort_flag)) return false;
+      if (!mbar_wait(&c_full[buf], (c >> 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * kTok + (kTok / 2) * h);
 #pragma unroll
@@ -199,95 +340,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&c_empty[buf]);
-      return true;
-    };
-    for (int kb = 0; kb < nkb && ok; ++kb) {
-      const int s = kb % kWStages, m = kb % kMStages;
-      if (!mbar_wait(&w_full[s], (kb / kWStages) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      if (kb >= kMStages && !mbar_wait(&m_empty[m], ((kb / kMStages) - 1) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      // split 128 x 64 f32 weights into three bf16 planes, K-major with the 128-byte swizzle:
-      // element (r, k) at r*128 + ((k/8) ^ (r%8))*16 + (k%8)*2
-      const float4* src = (const float4*)(wring + s * kWBytes);
-      uint8_t* planes = mring + m * kMBytes;
-#pragma unroll 4
-      for (int it = 0; it < kWBytes / 16 / kEpiThreads; ++it) {
-        const int idx = it * kEpiThreads + et;  // float4 index: row idx/16, k 4*(idx%16)
-        const float4 w = src[idx];
-        const int r = idx >> 4, k = (idx & 15) * 4;
-        const float wv[4] = {w.x, w.y, w.z, w.w};
-        float r1[4], r2[4];
-        uint32_t p0[2], p1[2], p2[2];
-#pragma unroll
-        for (int e = 0; e < 4; e += 2) {
-          p0[e / 2] = bf16x2_bits(wv[e], wv[e + 1]);
-          r1[e] = wv[e] - __uint_as_float(p0[e / 2] << 16);
-          r1[e + 1] = wv[e + 1] - __uint_as_float(p0[e / 2] & 0xFFFF0000u);
-          p1[e / 2] = bf16x2_bits(r1[e], r1[e + 1]);
-          r2[e] = r1[e] - __uint_as_float(p1[e / 2] << 16);
-          r2[e + 1] = r1[e + 1] - __uint_as_float(p1[e / 2] & 0xFFFF0000u);
-          p2[e / 2] = bf16x2_bits(r2[e], r2[e + 1]);
-        }
-        const int off = r * 128 + ((((k >> 3) ^ (r & 7))) << 4) + (k & 7) * 2;
-        *(uint2*)(planes + off) = make_uint2(p0[0], p0[1]);
-        *(uint2*)(planes + kPlaneBytes + off) = make_uint2(p1[0], p1[1]);
-        *(uint2*)(planes + 2 * kPlaneBytes + off) = make_uint2(p2[0], p2[1]);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&w_empty[s]);
-        mbar_arrive(&m_full[m]);
-      }
-      // drain chunk c once the chunk after it has been fed (keeps one chunk of slack)
-      if ((kb % kChunkKb) == kChunkKb - 1 && kb >= 2 * kChunkKb - 1) {
-        if (!drain(drained)) ok = false;
-        ++drained;
-      }
-    }
-    while (ok && drained < nch) {
-      if (!drain(drained)) ok = false;
-      ++drained;
     }
     if (!ok && threadIdx.x == 64) atomicOr(P.flag, 4);
-  }
-
-  // ---- cluster reduction of the K-slice partial sums (every thread of every CTA takes part)
-  tc_fence_before();
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  __syncthreads();
-  cluster_sync();  // all CTAs of the cluster are past their main loops: ring memory is free
-  const int w = kTok / (int)csize;  // tokens owned per CTA
-  float* recv = (float*)smem;       // [csize][128 rows][w]
-  if (warp >= 2) {
-    const int q = warp & 3, h = (warp - 2) >> 2;
-    const int row = 32 * q + lane;
-    const uint32_t base = smem_addr(recv);
+    float* dst = P.part + ((size_t)ks * P.b_total + P.b0) * P.ncol + tile * kRows + row;
 #pragma unroll
-    for (int i = 0; i < kTok / 2; i += 4) {
-      const int t = (kTok / 2) * h + i;  // first of 4 tokens; w >= 8 keeps them in one owner
-      const uint32_t dst = (uint32_t)(t / w);
-      const uint32_t off = (uint32_t)(((crank * kRows + row) * w + (t % w)) * 4);
-      st_cluster_v4(mapa(base + off, dst), acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+    for (int i = 0; i < kTok / 2; ++i) {
+      const int b = (kTok / 2) * h + i;
+      if (b < P.B) dst[(size_t)b * P.ncol] = acc[i];
     }
   }
-  cluster_sync();
-  // each CTA sums its w tokens over the cluster (in rank order) and writes the state slots
-  for (int o = threadIdx.x; o < kRows * w; o += kThreads) {
-    const int row = o % kRows, tl = o / kRows;
-    const int b = (int)crank * w + tl;
-    if (b >= P.B) continue;
-    float v = 0.0f;
-    for (uint32_t src = 0; src < csize; ++src) v += recv[((int)src * kRows + row) * w + tl];
-    const int p = max(P.start_pos[b], 0);
-    const int slot = P.overlap ? ((p >> 2) & 1) * 4 + (p & 3) : p % P.ratio;
-    P.state[((size_t)b * P.slots + slot) * P.ncol + tile * kRows + row] = v;
-  }
+
   tc_fence_before();
   __syncthreads();
   if (*abort_flag && threadIdx.x == 0) atomicOr(P.flag, 4);
@@ -295,69 +357,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // the ring is free: every stage was consumed by MMAs that completed before the last chunk
+  finish_tokens(P, tile, ks, (float*)smem);
 }
 
 }  // namespace dtc
 
 // ---- host side ------------------------------------------------------------------------------
 
-// Cluster size (K slices per packed tile) for a launch: a power of two that divides the K
-// blocks, keeps at least 2 K blocks per CTA, and brings the CTA count near the SM count.
-static int pick_cluster(const csa_compressor* c) {
+// Number of K slices: at most one CTA per SM (the launch is cooperative), at least one K block
+// per CTA.
+int decode_tc_slices(const csa_compressor* c) {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
+  }
   const int nkb = c->dim / dtc::kKb;
-  int ks = 1;
-  while (ks * 2 <= dtc::kMaxCluster && nkb % (ks * 2) == 0 && nkb / (ks * 2) >= 2 && c->pk.ntiles * ks * 2 <= 160)
-    ks *= 2;
+  int ks = sms / c->pk.ntiles;
+  if (ks < 1) ks = 1;
+  if (ks > nkb) ks = nkb;
   return ks;
 }
 
 bool decode_tc_supported(const csa_compressor* c, const void* x) {
   return c->pk.tw == dtc::kRows && c->dim % dtc::kKb == 0 && ((uintptr_t)x & 15) == 0 &&
-         tcx::get_encode() != nullptr;
+         c->pk.ntiles <= 148 && tcx::get_encode() != nullptr;
 }
 
 cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, const int32_t* start_pos,
-                             cudaStream_t s) {
+                             float* part, int ks, const csa_out& out, uint8_t* emitted, cudaStream_t s) {
   using namespace dtc;
   auto encode = tcx::get_encode();
   if (!encode) return cudaErrorNotSupported;
-  static int ks_cached = 0;
   const size_t smem = (size_t)kRingBytes + 1024 + 1024;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  int ks = pick_cluster(c);
-  // a cluster of 16 is beyond the portable size: use it only if the GPU can place one
-  while (ks > 8) {
-    cudaLaunchConfig_t q = {};
-    q.gridDim = dim3(c->pk.ntiles, ks, 1);
-    q.blockDim = dim3(kThreads, 1, 1);
-    q.dynamicSmemBytes = smem;
-    cudaLaunchAttribute a;
-    a.id = cudaLaunchAttributeClusterDimension;
-    a.val.clusterDim.x = 1;
-    a.val.clusterDim.y = ks;
-    a.val.clusterDim.z = 1;
-    q.attrs = &a;
-    q.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel, &q) == cudaSuccess && n > 0) break;
-    cudaGetLastError();
-    ks /= 2;
-  }
-  (void)ks_cached;
   CUtensorMap mw;
   {
-    cuuint64_t dims[2] = {(cuuint64_t)c->dim, (cuuint64_t)c->pk.cols()};
-    cuuint64_t strides[1] = {(cuuint64_t)c->dim * 4};
-    cuuint32_t box[2] = {kKb, kRows};
+    // the three bf16 weight planes: [3 * ncol rows][dim], K innermost
+    cuuint64_t dims[2] = {(cuuint64_t)c->dim, (cuuint64_t)3 * c->pk.cols()};
+    cuuint64_t strides[1] = {(cuuint64_t)c->dim * 2};
+    cuuint32_t box[2] = {kKs, kRows};
     cuuint32_t es[2] = {1, 1};
-    if (encode(&mw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, (void*)c->w_packed, dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    if (encode(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)c->w_planes, dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -366,34 +415,44 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
     CUtensorMap mx;
     cuuint64_t dims[2] = {(cuuint64_t)c->dim, (cuuint64_t)nb};
     cuuint64_t strides[1] = {(cuuint64_t)c->dim * 2};
-    cuuint32_t box[2] = {kKb, kTok};
+    cuuint32_t box[2] = {kKs, kTok};
     cuuint32_t es[2] = {1, 1};
     if (encode(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)(x + (size_t)b0 * c->dim), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
     Params P;
-    P.K = c->dim;
-    P.ks_kb = c->dim / kKb / ks;
+    P.nkb_total = c->dim / kKb;
+    P.ks = ks;
     P.B = nb;
+    P.b_total = B;
+    P.b0 = b0;
     P.ncol = c->pk.cols();
+    P.part = part;
+    P.flag = c->dev_flag;
+    P.start_pos = start_pos;
+    P.state = c->state;
     P.slots = c->slots;
     P.ratio = c->ratio;
     P.overlap = c->overlap;
-    P.start_pos = start_pos + b0;
-    P.state = c->state + (size_t)b0 * c->slots * c->pk.cols();
-    P.flag = c->dev_flag;
+    P.pk = c->pk;
+    P.ep = epi_params(c);
+    P.out = out;
+    P.emitted = emitted;
+    P.pooled = c->dec_pooled;
+    P.seq_ctr = c->dec_counters;
+    P.tile_ctr = c->dec_tile_ctr;
+    P.tile_gen = c->dec_tile_gen;
+    // the K slices of a tile wait for each other: a cooperative launch keeps the grid resident
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(c->pk.ntiles, ks, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr_c[1];
-    attr_c[0].id = cudaLaunchAttributeClusterDimension;
-    attr_c[0].val.clusterDim.x = 1;
-    attr_c[0].val.clusterDim.y = ks;
-    attr_c[0].val.clusterDim.z = 1;
-    cfg.attrs = attr_c;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
+    cfg.attrs = at;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tc_kernel, mw, mx, P);
     if (e != cudaSuccess) return e;

@@ -26,9 +26,12 @@ size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N, size_t* n
 cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset,
                               const csa_out& out, void* scratch, int* counters, cudaStream_t s);
 
-// Tensor-core decode projection (decode_tc.cu): one token per sequence into its state slot.
+// Tensor-core decode (decode_tc.cu): projection of one token per sequence (split over K),
+// reduction into the state slots, pool and epilogue of the completed groups; one launch per
+// 128 sequences.
 bool decode_tc_supported(const csa_compressor* c, const void* x);
+int decode_tc_slices(const csa_compressor* c);
 cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, const int32_t* start_pos,
-                             cudaStream_t s);
+                             float* part, int nslices, const csa_out& out, uint8_t* emitted, cudaStream_t s);
 
 }  // namespace csa

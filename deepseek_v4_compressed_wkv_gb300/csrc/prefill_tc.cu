@@ -10,10 +10,11 @@
 // of "Module compress" (linear_f32).
 //
 // Accumulation: the tensor cores' f32 accumulator is not IEEE round-to-nearest (truncation per
-// MMA leaves ~2^-16 relative error after 768 steps of K=16), so the MMAs of each K chunk of 128
+// MMA leaves ~2^-16 relative error after 768 steps of K=16), so the MMAs of each K chunk of 256
 // go into a fresh TMEM accumulator (two, alternating) and the epilogue warps add each chunk into
 // f32 registers with ordinary round-to-nearest additions, in chunk order (the promotion to CUDA
-// cores used for low-precision accumulators).  The result is as accurate as an f32 FMA GEMM.
+// cores used for low-precision accumulators).  Chunks of 128 measured a mean projection error of
+// half that of an f32 FMA GEMM; chunks of 256 are 4% faster (chunks of 512: another 2%).
 //
 // Roles (320 threads): warp 0 issues the TMA loads (x tile shared by all three planes, one
 // tile per plane), warp 1 owns TMEM and issues tcgen05.mma, warps 2-9 run the epilogue (warps
@@ -35,13 +36,13 @@ using namespace tcx;
 
 constexpr int kRows = 128;           // packed rows per tile (MMA M)
 constexpr int kTok = 256;            // tokens per tile including the halo (MMA N)
-constexpr int kKb = 64;              // K elements per stage (one 128-byte swizzle row of bf16)
-constexpr int kStages = 2;
-constexpr int kPlaneBytes = kRows * kKb * 2;          // 16 KB
-constexpr int kXBytes = kTok * kKb * 2;               // 32 KB
-constexpr int kStageBytes = 3 * kPlaneBytes + kXBytes;  // 80 KB
+constexpr int kKb = 32;              // K elements per stage (one 64-byte swizzle row of bf16)
+constexpr int kStages = 5;
+constexpr int kPlaneBytes = kRows * kKb * 2;          // 8 KB
+constexpr int kXBytes = kTok * kKb * 2;               // 16 KB
+constexpr int kStageBytes = 3 * kPlaneBytes + kXBytes;  // 40 KB
 constexpr int kSmemStride = kTok + 1;                 // f32 staging row stride (bank-conflict free)
-constexpr int kChunkKb = 2;         // K blocks per accumulator chunk (K = 128)
+constexpr int kChunkKb = 8;         // K blocks per accumulator chunk (K = 256)
 constexpr int kEpiThreads = 256;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kTmemCols = 2 * kTok;  // two chunk accumulators
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t xs = st + 3 * kPlaneBytes;
           for (int p = 0; p < 3; ++p)
             for (int k = 0; k < kKb / 16; ++k)
-              mma_bf16(d, sw128_desc(st + p * kPlaneBytes + k * 32), sw128_desc(xs + k * 32), idesc,
+              mma_bf16(d, sw64_desc(st + p * kPlaneBytes + k * 32), sw64_desc(xs + k * 32), idesc,
                        (kb != kb0 || p != 0 || k != 0) ? 1u : 0u);
           mma_commit(&empty[s]);
         }
@@ -353,7 +354,7 @@ cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B,
     cuuint32_t box[2] = {kKb, kRows};
     cuuint32_t es[2] = {1, 1};
     if (encode(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)c->w_planes, dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -364,7 +365,7 @@ cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B,
     cuuint32_t box[3] = {kKb, kTok, 1};
     cuuint32_t es[3] = {1, 1, 1};
     if (encode(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)x, dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }

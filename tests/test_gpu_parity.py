@@ -328,3 +328,33 @@ def test_errors_are_reported_not_raised_on_the_device():
         g.device_status()
     assert g.device_status() == 0
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("B,ratio,overlap", [(200, 4, 1), (130, 16, 0)])
+def test_decode_batch_beyond_one_token_tile(B, ratio, overlap):
+    """More sequences than one MMA token tile (128): the decode runs in token chunks."""
+    layer = synthetic.Layer(256, 128, ratio, overlap, 1.0 / 16, rope_dim=64, fp4=1)
+    g, o = make_pair(9, layer, max_batch=B)
+    sp0 = (np.arange(B) * 7 % 61).astype(np.int32)
+    for b in range(B):
+        s = int(sp0[b])
+        t0 = csa.state_window_start(s, ratio, overlap)
+        if s > t0:
+            xb = to_bf16_bits(synthetic.tokens(9, b, t0, s, layer.dim))[None]
+            o.prefill(xb, slot_offset=b)
+            g.prefill(dev_bits(xb), slot_offset=b, prequant=False)
+    for k in range(ratio + 1):
+        sp = (sp0 + k).astype(np.int32)
+        xt = to_bf16_bits(np.stack([synthetic.tokens(9, b, int(sp[b]), int(sp[b]) + 1, layer.dim)[0]
+                                    for b in range(B)]))
+        r = o.decode(xt, sp)
+        d = g.decode(dev_bits(xt), torch.from_numpy(sp).to(DEV))
+        em = d["emitted"].cpu().numpy()
+        assert np.array_equal(em, r["emitted"])
+        rows = np.flatnonzero(em)
+        if rows.size:
+            check_entries(to_np(d, rows=rows), r["prequant"][rows], 1, f"decode B={B} k={k}")
+    kg, sg = (t.cpu().numpy() for t in g.state_export())
+    ko, so = o.state()
+    assert np.allclose(kg, ko, rtol=2e-5, atol=2e-5 * np.abs(ko).max(initial=1.0))
+    assert g.device_status() == 0
