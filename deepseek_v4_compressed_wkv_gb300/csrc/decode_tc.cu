@@ -183,7 +183,7 @@ __device__ void finish_tokens(const Params& P, int tile, int ks, float* scr) {
         cand(i, sv, kv, false);
         m = fmaxf(m, sv);
       }
-      for (int i = g; i < ncand; i += ng) {
+      for (int i = g; i < ncand && m != -INFINITY; i += ng) {  // a group of padded slots adds nothing
         float sv, kv;
         cand(i, sv, kv, true);
         const float e = expf(sv - m);
@@ -201,7 +201,8 @@ __device__ void finish_tokens(const Params& P, int tile, int ks, float* scr) {
       float D = 0.0f, Nn = 0.0f;
       for (int k = 0; k < ng; ++k) {
         const int t = k * pk.ft + threadIdx.x;
-        const float w = sm_m[t] == -INFINITY ? 0.0f : expf(sm_m[t] - M);
+        if (sm_m[t] == -INFINITY) continue;  // no live candidate in this group
+        const float w = expf(sm_m[t] - M);
         D = fmaf(sm_d[t], w, D);
         Nn = fmaf(sm_n[t], w, Nn);
       }
