@@ -77,7 +77,6 @@ __device__ __forceinline__ float padded_kind_value(const Packing& pk, int col) {
 __device__ void finish_tokens(const Params& P, int tile, int ks, float* scr) {
   __shared__ unsigned gen0;
   __shared__ int go;
-  __shared__ int last;
   __threadfence();  // this CTA's partial sums are visible before it arrives
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -144,86 +143,106 @@ __device__ void finish_tokens(const Params& P, int tile, int ks, float* scr) {
     }
   }
   __syncthreads();  // the slots written above are read below by other threads
-  // -- pool the tile's features for every token of this share that completed a group: groups
-  //    of threads split the candidates (max, then exp sums), merged in a fixed order
+  // -- pool the tile's features for the tokens of this share that completed a group, in batches
+  //    of up to blockDim / ft tokens at once; within a token, groups of threads split the
+  //    candidates (max, then exp sums) and the group partials are merged in a fixed order
+  __shared__ int elist[kTok];
+  __shared__ int ne;
+  __shared__ int lastv[kThreads / 32];
+  if (threadIdx.x == 0) {
+    int n = 0;
+    for (int it = 0; it < nt; ++it) {
+      const int b = P.b0 + tb0 + it;
+      const int p = P.start_pos[b];
+      const long long pos = (long long)p + 1 - P.ratio;
+      if (p >= 0 && (p + 1) % P.ratio == 0 && (P.ep.rope_dim == 0 || pos < P.ep.max_pos)) elist[n++] = b;
+    }
+    ne = n;
+  }
+  __syncthreads();
   const int ncand = P.overlap ? 8 : P.ratio;
-  const int ng = (int)blockDim.x / pk.ft;
-  const int f = f0 + (int)threadIdx.x % pk.ft, g = (int)threadIdx.x / pk.ft;
+  const int nthr = (int)blockDim.x;
+  const int epb = min(nthr / pk.ft, nthr / 32);  // tokens per batch (one epilogue warp each)
   float* sm_m = scr;
-  float* sm_d = scr + blockDim.x;
-  float* sm_n = scr + 2 * blockDim.x;
-  for (int it = 0; it < nt; ++it) {
-    const int b = P.b0 + tb0 + it;
-    const int p = P.start_pos[b];
-    if (p < 0 || (p + 1) % P.ratio != 0) continue;
-    const long long pos = (long long)p + 1 - P.ratio;
-    if (P.ep.rope_dim > 0 && pos >= P.ep.max_pos) continue;
-    const float* st = P.state + (size_t)b * P.slots * ncol;
-    const int q = (p >> 2) & 1;
-    auto cand = [&](int i, float& sv, float& kv, bool load_kv) {
-      const float* row;
-      int cs, ck;
-      if (P.overlap) {
-        const bool prevB = i < 4;
-        row = st + (size_t)(prevB ? 4 * (1 - q) + i : 4 * q + i - 4) * ncol;
-        cs = pk.col(prevB ? S_B : S_A, f);
-        ck = pk.col(prevB ? KV_B : KV_A, f);
-      } else {
-        row = st + (size_t)i * ncol;
+  float* sm_d = scr + nthr;
+  float* sm_n = scr + 2 * nthr;
+  for (int e0 = 0; e0 < ne; e0 += epb) {
+    const int nbe = min(epb, ne - e0);
+    const int ng = max(1, nthr / (nbe * pk.ft));  // candidate groups per token
+    const int per_tok = ng * pk.ft;
+    const int e = (int)threadIdx.x / per_tok, r = (int)threadIdx.x % per_tok;
+    const int f = f0 + r % pk.ft, g = r / pk.ft;
+    float m = -INFINITY, den = 0.0f, num = 0.0f;
+    if (e < nbe) {
+      const int b = elist[e0 + e];
+      const int q = (P.start_pos[b] >> 2) & 1;
+      const float* st = P.state + (size_t)b * P.slots * ncol;
+      auto row_of = [&](int i, int& cs, int& ck) -> const float* {
+        if (P.overlap) {
+          const bool prevB = i < 4;
+          cs = pk.col(prevB ? S_B : S_A, f);
+          ck = pk.col(prevB ? KV_B : KV_A, f);
+          return st + (size_t)(prevB ? 4 * (1 - q) + i : 4 * q + i - 4) * ncol;
+        }
         cs = pk.col(S, f);
         ck = pk.col(KV, f);
-      }
-      sv = row[cs];
-      if (load_kv) kv = row[ck];
-    };
-    float m = -INFINITY, den = 0.0f, num = 0.0f;
-    if (g < ng) {
+        return st + (size_t)i * ncol;
+      };
+#pragma unroll 8
       for (int i = g; i < ncand; i += ng) {
-        float sv, kv;
-        cand(i, sv, kv, false);
-        m = fmaxf(m, sv);
+        int cs, ck;
+        const float* row = row_of(i, cs, ck);
+        m = fmaxf(m, row[cs]);
       }
-      for (int i = g; i < ncand && m != -INFINITY; i += ng) {  // a group of padded slots adds nothing
-        float sv, kv;
-        cand(i, sv, kv, true);
-        const float e = expf(sv - m);
-        den += e;
-        num = fmaf(e, kv, num);
+      if (m != -INFINITY) {  // a group of padded slots adds nothing
+#pragma unroll 8
+        for (int i = g; i < ncand; i += ng) {
+          int cs, ck;
+          const float* row = row_of(i, cs, ck);
+          const float ex = expf(row[cs] - m);
+          den += ex;
+          num = fmaf(ex, row[ck], num);
+        }
       }
     }
     sm_m[threadIdx.x] = m;
     sm_d[threadIdx.x] = den;
     sm_n[threadIdx.x] = num;
     __syncthreads();
-    if (g == 0) {
-      float M = m;
-      for (int k = 1; k < ng; ++k) M = fmaxf(M, sm_m[k * pk.ft + threadIdx.x]);
+    if (e < nbe && g == 0) {
+      const int base = e * per_tok + r;
+      float M = -INFINITY;
+      for (int k = 0; k < ng; ++k) M = fmaxf(M, sm_m[base + k * pk.ft]);
       float D = 0.0f, Nn = 0.0f;
       for (int k = 0; k < ng; ++k) {
-        const int t = k * pk.ft + threadIdx.x;
-        if (sm_m[t] == -INFINITY) continue;  // no live candidate in this group
+        const int t = base + k * pk.ft;
+        if (sm_m[t] == -INFINITY) continue;
         const float w = expf(sm_m[t] - M);
         D = fmaf(sm_d[t], w, D);
         Nn = fmaf(sm_n[t], w, Nn);
       }
-      P.pooled[(size_t)b * pk.H + f] = bf16_bits(__fdiv_rn(Nn, D));
+      P.pooled[(size_t)elist[e0 + e] * pk.H + f] = bf16_bits(__fdiv_rn(Nn, D));
     }
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) last = atomicAdd(&P.seq_ctr[b], 1) == pk.ntiles - 1;
+    if ((int)threadIdx.x < nbe)
+      lastv[threadIdx.x] = atomicAdd(&P.seq_ctr[elist[e0 + threadIdx.x]], 1) == pk.ntiles - 1;
     __syncthreads();
-    if (last && threadIdx.x < 32) {  // the last tile of this sequence: RMSNorm, RoPE, fp4
+    // the last tile of a sequence runs its RMSNorm, RoPE and fp4: warp w takes token e0 + w
+    const int w = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
+    if (w < nbe && lastv[w]) {
       __threadfence();
-      const int lane = threadIdx.x;
+      const int b = elist[e0 + w];
+      const long long pos = (long long)P.start_pos[b] + 1 - P.ratio;
       const int l = min(lane, (pk.H >> 4) - 1);
       const uint4* src = reinterpret_cast<const uint4*>(P.pooled + (size_t)b * pk.H + 16 * l);
       const uint4 a = __ldcg(src), c = __ldcg(src + 1);
-      const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+      const uint32_t wd[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
       float v[16];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        v[2 * i] = __uint_as_float(w[i] << 16);
-        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        v[2 * i] = __uint_as_float(wd[i] << 16);
+        v[2 * i + 1] = __uint_as_float(wd[i] & 0xFFFF0000u);
       }
       const size_t H = pk.H;
       entry_epilogue(v, lane, pos, P.ep, P.out.latent + b * H, P.out.codes ? P.out.codes + b * (H / 2) : nullptr,
