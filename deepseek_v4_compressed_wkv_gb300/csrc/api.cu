@@ -96,8 +96,6 @@ void free_all(csa_compressor* c) {
   cudaFree(c->dec_part);
   cudaFree(c->dec_pooled);
   cudaFree(c->dec_counters);
-  cudaFree(c->dec_tile_ctr);
-  cudaFree(c->dec_tile_gen);
 }
 
 int ensure_scratch(csa_compressor* c, size_t bytes, cudaStream_t s) {
@@ -195,10 +193,8 @@ int csa_compressor_create(int dim, int H, int ratio, int overlap, const csa_opti
     alloc((void**)&c->gain, H * sizeof(float));
     alloc((void**)&c->state, (size_t)o.max_batch * c->slots * ncol * sizeof(float));
     alloc((void**)&c->dev_flag, sizeof(int));
-    alloc((void**)&c->dec_pooled, (size_t)o.max_batch * H * sizeof(uint16_t));
+    alloc((void**)&c->dec_pooled, (size_t)o.max_batch * H * sizeof(float));
     alloc((void**)&c->dec_counters, (size_t)o.max_batch * sizeof(int));
-    alloc((void**)&c->dec_tile_ctr, (size_t)pk.ntiles * sizeof(unsigned));
-    alloc((void**)&c->dec_tile_gen, (size_t)pk.ntiles * sizeof(unsigned));
     if (o.rope_dim > 0) {
       const size_t n = (size_t)o.max_pos * (o.rope_dim / 2);
       alloc((void**)&c->rope_cos, n * sizeof(float));
@@ -214,8 +210,6 @@ int csa_compressor_create(int dim, int H, int ratio, int overlap, const csa_opti
     }
     if (e == cudaSuccess) e = cudaMemset(c->dev_flag, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(c->dec_counters, 0, (size_t)o.max_batch * sizeof(int));
-    if (e == cudaSuccess) e = cudaMemset(c->dec_tile_ctr, 0, (size_t)pk.ntiles * sizeof(unsigned));
-    if (e == cudaSuccess) e = cudaMemset(c->dec_tile_gen, 0, (size_t)pk.ntiles * sizeof(unsigned));
     if (e == cudaSuccess && csa::launch_state_reset(c, 0, o.max_batch, 0) != cudaSuccess) e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
@@ -240,6 +234,7 @@ int csa_compressor_set_weights(csa_compressor* c, const float* wkv, const float*
   c->launches += 1;
   CSA_CUDA(cudaMemcpyAsync(c->gain, gain, c->H * sizeof(float), cudaMemcpyDeviceToDevice, s), "copy gain");
   c->weights_set = true;
+  c->dec_early_start = false;  // the next decode reads the new planes only after this stream's work
   return CSA_OK;
 }
 
@@ -317,10 +312,11 @@ int csa_compress_decode(csa_compressor* c, const uint16_t* x_tok, int B, const i
       c->dec_part_bytes = bytes;
     }
     if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
-    CSA_CUDA(csa::launch_decode_tc(c, x_tok, B, start_pos, c->dec_part, ks, *out, emitted, s),
+    CSA_CUDA(csa::launch_decode_tc(c, x_tok, B, start_pos, c->dec_part, ks, *out, emitted, c->dec_early_start, s),
              "tensor-core decode launch");
     if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
-    c->launches += (B + 127) / 128;
+    c->dec_early_start = true;
+    c->launches += 2;
     return CSA_OK;
   }
   if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");

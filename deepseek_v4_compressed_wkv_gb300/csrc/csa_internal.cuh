@@ -201,10 +201,10 @@ struct csa_compressor {
   size_t scratch_bytes;
   float* dec_part;          // decode split-K partial sums [slices][B][2C] (grown on demand)
   size_t dec_part_bytes;
-  uint16_t* dec_pooled;     // decode pooled bf16 values [max_batch][H]
-  int* dec_counters;        // decode per-sequence completion counters [max_batch] (kept at zero)
-  unsigned* dec_tile_ctr;   // decode K-slice barrier per packed tile: arrivals (kept at zero)
-  unsigned* dec_tile_gen;   //   and generations
+  float* dec_pooled;        // decode pooled values of the emitting tokens [max_batch][H]
+  int* dec_counters;        // decode per-sequence chunk counters [max_batch] (kept at zero)
+  bool dec_early_start;     // the next decode may start its weight loads before the preceding
+                            // kernel ends (false right after set_weights rewrote the planes)
   int* tc_counters;         // per token tile completion counters of the tensor-core prefill
   size_t tc_counters_n;     // (kept at zero between calls by the kernel itself)
   cudaEvent_t prof_start, prof_stop;  // optional events around the dominant kernel

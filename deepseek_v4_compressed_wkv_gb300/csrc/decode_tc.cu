@@ -1,28 +1,35 @@
 // Decode on the tensor cores (sm_103a): one token per sequence, into each sequence's state slot
 // ("Pool token pairs", decode branch: kv_state[:, slot] = kv, score_state[:, slot] = score),
-// then the pool and epilogue of the sequences whose group completes, in one launch.
+// then the pool and epilogue of the sequences whose group completes.
 //
 // Decode streams every weight once per step for only B tokens, so it is bound by HBM.  The
-// kernel streams the three exact bf16 planes of the weights that set_weights prepared (w = p0 +
-// p1 + p2; 6 bytes per weight, 1.5x the f32 weights) straight into the tensor cores: splitting
-// the f32 weights on the CUDA cores instead (4 bytes per weight) made the kernel bound by
-// instruction issue at a quarter of the HBM bandwidth.
+// projection streams the three exact bf16 planes of the weights that set_weights prepared (w =
+// p0 + p1 + p2; 6 bytes per weight, 1.5x the f32 weights) straight into the tensor cores.
 //
-// Work split: packed tile t (128 rows) x K slice, at most one CTA per SM, launched cooperatively
-// so that all CTAs are resident together.  Each CTA accumulates its slice in K chunks of 128
-// (TMEM, promoted to f32 registers as in the prefill kernel) and writes its partial sums to
-// scratch.  The K slices of a tile then meet at a self-resetting counter barrier (a bounded
-// wait), and each of them finishes a share of the tokens: it adds the slices' partials in a
-// fixed order into the token's state slot (a deterministic split-K reduction), applies the
-// restart at position 0, and, where the token completed a group, pools the tile's features
-// ("Pool token pairs", decode branch; "Compressed Sparse Attention - ratio m = 4", decode
-// rule).  The last tile to finish a sequence (a completion counter, no waiting) runs the
-// entry epilogue, which needs all H features for the RMSNorm.
+// Two launches per call, chained by programmatic dependent launch so that neither waits for
+// the other to be scheduled:
 //
-// Roles (320 threads) in the projection: warp 0 issues the TMA loads (three plane tiles and one
-// token tile of K = 32 per stage, 64-byte swizzle, 6 stages), warp 1 owns TMEM and issues
-// tcgen05.mma, warps 2-9 drain the chunk accumulators and store the partial sums.  All warps
-// take part in the reduction and pooling.
+//  * decode_proj_kernel, grid (packed tile, K slice, 128-token block): accumulates the slice in
+//    K chunks of 128 (TMEM, promoted to f32 registers as in the prefill kernel) and writes its
+//    partial sums.  Roles (320 threads): warp 0 issues the TMA loads (three plane tiles and one
+//    token tile of K = 32 per stage, 64-byte swizzle, 6 stages), warp 1 owns TMEM and issues
+//    tcgen05.mma, warps 2-9 drain the chunk accumulators and store the partial sums.  The
+//    weights are not written by any kernel that can precede a decode launch in early-start
+//    mode, so warp 0 fetches the first stages' weight tiles (and prefetches the rest of the
+//    slice into L2) before it waits for the preceding kernel; the tokens, and every write,
+//    come after that wait.
+//
+//  * decode_finish_kernel, one CTA per (sequence, chunk of 128 features): adds the K slices'
+//    partial sums in slice order (a deterministic split-K reduction) into the token's state
+//    slot, applies the restart at position 0, and where the token completed a group pools the
+//    chunk's features over the group's candidates ("Pool token pairs", decode branch;
+//    "Compressed Sparse Attention - ratio m = 4", decode rule).  The last chunk of a token to
+//    finish (a completion counter; nothing waits) runs the entry epilogue (bf16, RMSNorm, RoPE,
+//    fp4), which needs all features.
+//
+// Each launch lets the next one start as soon as all of its CTAs have begun: the finish kernel
+// at once, the projection right after its own wait.  A CTA only ever waits for a launch whose
+// CTAs have all started, so the chain cannot deadlock whatever the occupancy.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -36,7 +43,7 @@ namespace dtc {
 using namespace tcx;
 
 constexpr int kRows = 128;                              // packed rows per tile (MMA M)
-constexpr int kTok = 128;                               // tokens per launch (MMA N)
+constexpr int kTok = 128;                               // tokens per CTA (MMA N)
 constexpr int kKb = 64;                                 // K granularity of the slice split
 constexpr int kKs = 32;                                 // K per stage (one 64-byte swizzle row of bf16)
 constexpr int kStages = 6;
@@ -48,215 +55,19 @@ constexpr int kRingBytes = kStages * kStageBytes;       // 192 KB
 constexpr int kEpiThreads = 256;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kTmemCols = 2 * kTok;
+constexpr int kFinThreads = 256;
 
-struct Params {
-  int nkb_total, ks;         // K blocks (of 64) of dim, number of K slices
-  int B, b_total, b0;        // tokens in this launch, in the call, first token of this launch
-  int ncol;                  // packed columns (rows of one weight plane)
-  float* part;               // [ks][b_total][ncol] partial sums
+struct ProjParams {
+  int nkb_total, ks;  // K blocks (of 64) of dim, number of K slices
+  int B;              // tokens of the call
+  int ncol;           // packed columns (rows of one weight plane)
+  float* part;        // [ks][B][ncol] partial sums
   int* flag;
-  const int32_t* start_pos;  // [b_total]
-  float* state;              // [max_batch][slots][ncol]
-  int slots, ratio, overlap;
-  Packing pk;
-  EpiParams ep;
-  csa_out out;               // rows indexed by sequence
-  uint8_t* emitted;          // [b_total]
-  uint16_t* pooled;          // [b_total][H] bf16 scratch
-  int* seq_ctr;              // [b_total] per-sequence tile counters (kept at zero between calls)
-  unsigned* tile_ctr;        // [ntiles] barrier arrivals (kept at zero between calls)
-  unsigned* tile_gen;        // [ntiles] barrier generations
 };
 
-__device__ __forceinline__ float padded_kind_value(const Packing& pk, int col) {
-  return ((col % pk.tw) / pk.ft) < pk.nk / 2 ? 0.0f : -INFINITY;  // kv kinds first, then scores
-}
-
-// After the projection: meet the other K slices of this tile, then reduce, update the state and
-// pool for tokens [ks*B/KS, (ks+1)*B/KS) of this launch.  `scr` is free shared memory.
-__device__ void finish_tokens(const Params& P, int tile, int ks, float* scr) {
-  __shared__ unsigned gen0;
-  __shared__ int go;
-  __threadfence();  // this CTA's partial sums are visible before it arrives
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    volatile unsigned* gen = P.tile_gen + tile;
-    gen0 = *gen;
-    __threadfence();
-    go = 1;
-    if (atomicAdd(P.tile_ctr + tile, 1u) == (unsigned)P.ks - 1) {
-      P.tile_ctr[tile] = 0;  // every slice has arrived: reset for the next call, then release
-      __threadfence();
-      atomicAdd(P.tile_gen + tile, 1u);
-    } else {
-      const uint64_t t0 = globaltimer();
-      while (*gen == gen0) {
-        if (globaltimer() - t0 > kWaitNs) {
-          atomicOr(P.flag, 4);
-          go = 0;
-          break;
-        }
-        __nanosleep(64);
-      }
-    }
-    __threadfence();
-  }
-  __syncthreads();
-  if (!go) return;
-
-  const Packing& pk = P.pk;
-  const int ncol = pk.cols(), c0 = tile * kRows, f0 = tile * pk.ft;
-  const int tb0 = (int)((long long)ks * P.B / P.ks), tb1 = (int)((long long)(ks + 1) * P.B / P.ks);
-  const int nt = tb1 - tb0;
-  // -- the K-slice partials of each token into its state slot, in slice order
-  for (int it = threadIdx.x; it < nt * (kRows / 4); it += blockDim.x) {
-    const int b = P.b0 + tb0 + it / (kRows / 4), c = c0 + 4 * (it % (kRows / 4));
-    const float* src = P.part + (size_t)b * ncol + c;
-    const size_t stride = (size_t)P.b_total * ncol;
-    float4 a = __ldcg(reinterpret_cast<const float4*>(src));
-    for (int k = 1; k < P.ks; ++k) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + k * stride));
-      a.x += v.x;
-      a.y += v.y;
-      a.z += v.z;
-      a.w += v.w;
-    }
-    const int pp = max(P.start_pos[b], 0);
-    const int slot = P.overlap ? ((pp >> 2) & 1) * 4 + (pp & 3) : pp % P.ratio;
-    *reinterpret_cast<float4*>(P.state + ((size_t)b * P.slots + slot) * ncol + c) = a;
-  }
-  // -- restart padding, emission flags, position checks
-  for (int it = threadIdx.x; it < nt; it += blockDim.x) {
-    const int b = P.b0 + tb0 + it;
-    const int p = P.start_pos[b];
-    if (p == 0 && P.overlap)  // the previous group's branch is the padded one
-      for (int i = 0; i < 4; ++i)
-        for (int c = c0; c < c0 + kRows; ++c)
-          P.state[((size_t)b * P.slots + 4 + i) * ncol + c] = padded_kind_value(pk, c);
-    if (tile == 0) {
-      const bool emit = p >= 0 && (p + 1) % P.ratio == 0;
-      const long long pos = (long long)p + 1 - P.ratio;
-      const bool pos_ok = P.ep.rope_dim == 0 || pos < P.ep.max_pos;
-      P.emitted[b] = (emit && pos_ok) ? 1 : 0;
-      if (p < 0) atomicOr(P.flag, 1);
-      if (emit && !pos_ok) atomicOr(P.flag, 2);
-    }
-  }
-  __syncthreads();  // the slots written above are read below by other threads
-  // -- pool the tile's features for the tokens of this share that completed a group, in batches
-  //    of up to blockDim / ft tokens at once; within a token, groups of threads split the
-  //    candidates (max, then exp sums) and the group partials are merged in a fixed order
-  __shared__ int elist[kTok];
-  __shared__ int ne;
-  __shared__ int lastv[kThreads / 32];
-  if (threadIdx.x == 0) {
-    int n = 0;
-    for (int it = 0; it < nt; ++it) {
-      const int b = P.b0 + tb0 + it;
-      const int p = P.start_pos[b];
-      const long long pos = (long long)p + 1 - P.ratio;
-      if (p >= 0 && (p + 1) % P.ratio == 0 && (P.ep.rope_dim == 0 || pos < P.ep.max_pos)) elist[n++] = b;
-    }
-    ne = n;
-  }
-  __syncthreads();
-  const int ncand = P.overlap ? 8 : P.ratio;
-  const int nthr = (int)blockDim.x;
-  const int epb = min(nthr / pk.ft, nthr / 32);  // tokens per batch (one epilogue warp each)
-  float* sm_m = scr;
-  float* sm_d = scr + nthr;
-  float* sm_n = scr + 2 * nthr;
-  for (int e0 = 0; e0 < ne; e0 += epb) {
-    const int nbe = min(epb, ne - e0);
-    const int ng = max(1, nthr / (nbe * pk.ft));  // candidate groups per token
-    const int per_tok = ng * pk.ft;
-    const int e = (int)threadIdx.x / per_tok, r = (int)threadIdx.x % per_tok;
-    const int f = f0 + r % pk.ft, g = r / pk.ft;
-    float m = -INFINITY, den = 0.0f, num = 0.0f;
-    if (e < nbe) {
-      const int b = elist[e0 + e];
-      const int q = (P.start_pos[b] >> 2) & 1;
-      const float* st = P.state + (size_t)b * P.slots * ncol;
-      auto row_of = [&](int i, int& cs, int& ck) -> const float* {
-        if (P.overlap) {
-          const bool prevB = i < 4;
-          cs = pk.col(prevB ? S_B : S_A, f);
-          ck = pk.col(prevB ? KV_B : KV_A, f);
-          return st + (size_t)(prevB ? 4 * (1 - q) + i : 4 * q + i - 4) * ncol;
-        }
-        cs = pk.col(S, f);
-        ck = pk.col(KV, f);
-        return st + (size_t)i * ncol;
-      };
-#pragma unroll 8
-      for (int i = g; i < ncand; i += ng) {
-        int cs, ck;
-        const float* row = row_of(i, cs, ck);
-        m = fmaxf(m, row[cs]);
-      }
-      if (m != -INFINITY) {  // a group of padded slots adds nothing
-#pragma unroll 8
-        for (int i = g; i < ncand; i += ng) {
-          int cs, ck;
-          const float* row = row_of(i, cs, ck);
-          const float ex = expf(row[cs] - m);
-          den += ex;
-          num = fmaf(ex, row[ck], num);
-        }
-      }
-    }
-    sm_m[threadIdx.x] = m;
-    sm_d[threadIdx.x] = den;
-    sm_n[threadIdx.x] = num;
-    __syncthreads();
-    if (e < nbe && g == 0) {
-      const int base = e * per_tok + r;
-      float M = -INFINITY;
-      for (int k = 0; k < ng; ++k) M = fmaxf(M, sm_m[base + k * pk.ft]);
-      float D = 0.0f, Nn = 0.0f;
-      for (int k = 0; k < ng; ++k) {
-        const int t = base + k * pk.ft;
-        if (sm_m[t] == -INFINITY) continue;
-        const float w = expf(sm_m[t] - M);
-        D = fmaf(sm_d[t], w, D);
-        Nn = fmaf(sm_n[t], w, Nn);
-      }
-      P.pooled[(size_t)elist[e0 + e] * pk.H + f] = bf16_bits(__fdiv_rn(Nn, D));
-    }
-    __threadfence();
-    __syncthreads();
-    if ((int)threadIdx.x < nbe)
-      lastv[threadIdx.x] = atomicAdd(&P.seq_ctr[elist[e0 + threadIdx.x]], 1) == pk.ntiles - 1;
-    __syncthreads();
-    // the last tile of a sequence runs its RMSNorm, RoPE and fp4: warp w takes token e0 + w
-    const int w = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
-    if (w < nbe && lastv[w]) {
-      __threadfence();
-      const int b = elist[e0 + w];
-      const long long pos = (long long)P.start_pos[b] + 1 - P.ratio;
-      const int l = min(lane, (pk.H >> 4) - 1);
-      const uint4* src = reinterpret_cast<const uint4*>(P.pooled + (size_t)b * pk.H + 16 * l);
-      const uint4 a = __ldcg(src), c = __ldcg(src + 1);
-      const uint32_t wd[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-      float v[16];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        v[2 * i] = __uint_as_float(wd[i] << 16);
-        v[2 * i + 1] = __uint_as_float(wd[i] & 0xFFFF0000u);
-      }
-      const size_t H = pk.H;
-      entry_epilogue(v, lane, pos, P.ep, P.out.latent + b * H, P.out.codes ? P.out.codes + b * (H / 2) : nullptr,
-                     P.out.scales ? P.out.scales + b * (H / 16) : nullptr,
-                     P.out.prequant ? P.out.prequant + b * H : nullptr);
-      if (lane == 0) P.seq_ctr[b] = 0;  // ready for the next call
-    }
-    __syncthreads();
-  }
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
-                     const Params P) {
+    decode_proj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
+                       const ProjParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* full = (uint64_t*)(smem + kRingBytes);
@@ -267,7 +78,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x, ks = blockIdx.y;
+  const int tile = blockIdx.x, ks = blockIdx.y, tb = blockIdx.z * kTok;
   const int kb_base = (int)((long long)ks * P.nkb_total / P.ks);
   const int nkb = (int)((long long)(ks + 1) * P.nkb_total / P.ks) - kb_base;
   const int nstep = nkb * (kKb / kKs);
@@ -296,14 +107,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int t = 0; t < nstep; ++t) {
+      const int npre = min(nstep, kStages);
+      const int wrow = tile * kRows;
+      // weights of the first stages into the ring, the rest of the slice into L2
+      for (int t = 0; t < npre; ++t) {
+        uint8_t* st = smem + t * kStageBytes;
+        mbar_arrive_expect_tx(&full[t], kStageBytes);
+        for (int p = 0; p < 3; ++p)
+          tma_load_2d(st + p * kPlaneBytes, &map_w, k0 + t * kKs, p * P.ncol + wrow, &full[t]);
+      }
+      for (int t = npre; t < nstep; ++t)
+        for (int p = 0; p < 3; ++p) tma_prefetch_l2_2d(&map_w, k0 + t * kKs, p * P.ncol + wrow);
+      griddep_wait();  // the tokens may come from the preceding kernel
+      griddep_launch_dependents();
+      for (int t = 0; t < npre; ++t)
+        tma_load_2d(smem + t * kStageBytes + 3 * kPlaneBytes, &map_x, k0 + t * kKs, tb, &full[t]);
+      for (int t = npre; t < nstep; ++t) {
         const int s = t % kStages;
-        if (t >= kStages && !mbar_wait(&empty[s], ((t / kStages) - 1) & 1, abort_flag)) break;
+        if (!mbar_wait(&empty[s], ((t / kStages) - 1) & 1, abort_flag)) break;
         uint8_t* st = smem + s * kStageBytes;
         mbar_arrive_expect_tx(&full[s], kStageBytes);
         for (int p = 0; p < 3; ++p)
-          tma_load_2d(st + p * kPlaneBytes, &map_w, k0 + t * kKs, p * P.ncol + tile * kRows, &full[s]);
-        tma_load_2d(st + 3 * kPlaneBytes, &map_x, k0 + t * kKs, 0, &full[s]);
+          tma_load_2d(st + p * kPlaneBytes, &map_w, k0 + t * kKs, p * P.ncol + wrow, &full[s]);
+        tma_load_2d(st + 3 * kPlaneBytes, &map_x, k0 + t * kKs, tb, &full[s]);
       }
     }
   } else if (warp == 1) {
@@ -362,11 +188,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&c_empty[buf]);
     }
     if (!ok && threadIdx.x == 64) atomicOr(P.flag, 4);
-    float* dst = P.part + ((size_t)ks * P.b_total + P.b0) * P.ncol + tile * kRows + row;
+    griddep_wait();  // the preceding finish kernel may still be reading this scratch
+    float* dst = P.part + ((size_t)ks * P.B + tb) * P.ncol + tile * kRows + row;
+    const int nb = min(kTok, P.B - tb);
 #pragma unroll
     for (int i = 0; i < kTok / 2; ++i) {
       const int b = (kTok / 2) * h + i;
-      if (b < P.B) dst[(size_t)b * P.ncol] = acc[i];
+      if (b < nb) dst[(size_t)b * P.ncol] = acc[i];
     }
   }
 
@@ -377,16 +205,209 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  // the ring is free: every stage was consumed by MMAs that completed before the last chunk
-  finish_tokens(P, tile, ks, (float*)smem);
+}
+
+struct FinParams {
+  int B, ks, ncol;
+  int fc, nchunk;            // features per chunk (whole tiles), chunks per token
+  const float* part;         // [ks][B][ncol]
+  int* flag;
+  const int32_t* start_pos;  // [B]
+  float* state;              // [max_batch][slots][ncol]
+  int slots, ratio, overlap;
+  Packing pk;
+  EpiParams ep;
+  csa_out out;               // rows indexed by sequence
+  uint8_t* emitted;          // [B]
+  float* pooled;             // [B][H] pooled values of the emitting tokens
+  int* seq_ctr;              // [B] chunks done (kept at zero between calls)
+};
+
+__device__ __forceinline__ float padded_kind_value(const Packing& pk, int col) {
+  return ((col % pk.tw) / pk.ft) < pk.nk / 2 ? 0.0f : -INFINITY;  // kv kinds first, then scores
+}
+
+__device__ __forceinline__ void add4(float4& a, const float4& v) {
+  a.x += v.x;
+  a.y += v.y;
+  a.z += v.z;
+  a.w += v.w;
+}
+
+__device__ __forceinline__ float comp(const float4& v, int e) {
+  return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+
+constexpr int kFinChunk = 128;  // features per finish CTA (a whole number of packed tiles)
+constexpr int kPoolUnroll = 4;  // candidates in flight per thread
+
+// One CTA per (sequence b, chunk j of kFinChunk features): the chunk's packed columns are the
+// contiguous range [j * cw, (j + 1) * cw), cw = fc * nk.
+__global__ void __launch_bounds__(kFinThreads, 4) decode_finish_kernel(const FinParams P) {
+  __shared__ float sm_m[8 * kFinChunk], sm_d[8 * kFinChunk], sm_n[8 * kFinChunk];
+  __shared__ int last;
+  griddep_launch_dependents();  // the next launch may take the SMs this grid leaves free
+  griddep_wait();               // the partial sums of the projection are complete
+
+  const Packing& pk = P.pk;
+  const int b = blockIdx.x, j = blockIdx.y, tid = threadIdx.x, nthr = blockDim.x;
+  const int ncol = P.ncol, cw = P.fc * pk.nk, c0 = j * cw;
+  const int p = P.start_pos[b];
+  const int pp = max(p, 0);
+  const int slot = P.overlap ? ((pp >> 2) & 1) * 4 + (pp & 3) : pp % P.ratio;
+  float* st = P.state + (size_t)b * P.slots * ncol;
+
+  // -- the K-slice partial sums, in slice order, into the state slot
+  {
+    const float* src = P.part + (size_t)b * ncol + c0;
+    const size_t kstride = (size_t)P.B * ncol;
+    for (int i = tid; i < cw / 4; i += nthr) {
+      const float* s0 = src + 4 * i;
+      float4 a = __ldcg(reinterpret_cast<const float4*>(s0));
+      int k = 1;
+      for (; k + 4 <= P.ks; k += 4) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = __ldcg(reinterpret_cast<const float4*>(s0 + (k + u) * kstride));
+#pragma unroll
+        for (int u = 0; u < 4; ++u) add4(a, v[u]);
+      }
+      for (; k < P.ks; ++k) add4(a, __ldcg(reinterpret_cast<const float4*>(s0 + k * kstride)));
+      *reinterpret_cast<float4*>(st + (size_t)slot * ncol + c0 + 4 * i) = a;
+    }
+  }
+  // -- restart at position 0: the previous group's branch is the padded one
+  if (p == 0 && P.overlap)
+    for (int i = tid; i < 4 * cw; i += nthr) {
+      const int r = i / cw, c = c0 + i % cw;
+      st[(size_t)(4 + r) * ncol + c] = padded_kind_value(pk, c);
+    }
+  const bool emit = p >= 0 && (p + 1) % P.ratio == 0;
+  const long long pos = (long long)p + 1 - P.ratio;
+  const bool pos_ok = P.ep.rope_dim == 0 || pos < P.ep.max_pos;
+  if (tid == 0 && j == 0) {
+    P.emitted[b] = (emit && pos_ok) ? 1 : 0;
+    if (p < 0) atomicOr(P.flag, 1);
+    if (emit && !pos_ok) atomicOr(P.flag, 2);
+  }
+  if (!(emit && pos_ok)) return;
+  __threadfence();
+  __syncthreads();  // the slot written above is one of the candidates
+
+  // -- pool: thread (g, fg) takes features f0 + 4fg .. +3 (four adjacent columns of one kind)
+  //    over its contiguous share of the candidates with a running maximum; the shares are
+  //    merged in a fixed order
+  const int fc = P.fc, nfg = fc / 4, f0 = j * fc;
+  const int ncand = P.overlap ? 8 : P.ratio;
+  const int ng = max(1, min(min(nthr / nfg, 8), ncand));
+  const int g = tid / nfg, f = f0 + 4 * (tid % nfg);
+  if (g < ng) {
+    const int i0 = (int)((long long)g * ncand / ng), i1 = (int)((long long)(g + 1) * ncand / ng);
+    const int q = (pp >> 2) & 1;
+    float m[4], den[4], num[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      m[e] = -INFINITY;
+      den[e] = 0.0f;
+      num[e] = 0.0f;
+    }
+    for (int ib = i0; ib < i1; ib += kPoolUnroll) {
+      float4 sv[kPoolUnroll], kv[kPoolUnroll];
+#pragma unroll
+      for (int u = 0; u < kPoolUnroll; ++u) {
+        const int i = ib + u;
+        sv[u] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        kv[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (i < i1) {
+          int srow, cs, ck;
+          if (P.overlap) {
+            const bool prevB = i < 4;  // the previous group's branch B, then this group's branch A
+            srow = prevB ? 4 * (1 - q) + i : 4 * q + i - 4;
+            cs = pk.col(prevB ? S_B : S_A, f);
+            ck = pk.col(prevB ? KV_B : KV_A, f);
+          } else {
+            srow = i;
+            cs = pk.col(S, f);
+            ck = pk.col(KV, f);
+          }
+          const float* row = st + (size_t)srow * ncol;
+          sv[u] = __ldcg(reinterpret_cast<const float4*>(row + cs));
+          kv[u] = __ldcg(reinterpret_cast<const float4*>(row + ck));
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float cm = m[e];
+#pragma unroll
+        for (int u = 0; u < kPoolUnroll; ++u) cm = fmaxf(cm, comp(sv[u], e));
+        if (cm == -INFINITY) continue;  // padded candidates only, so far
+        const float sc = expf(m[e] - cm);  // 0 while m was -inf, 1 when the maximum is unchanged
+        den[e] *= sc;
+        num[e] *= sc;
+#pragma unroll
+        for (int u = 0; u < kPoolUnroll; ++u) {
+          const float ex = expf(comp(sv[u], e) - cm);
+          den[e] += ex;
+          num[e] = fmaf(ex, comp(kv[u], e), num[e]);
+        }
+        m[e] = cm;
+      }
+    }
+    const int o = g * fc + (f - f0);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      sm_m[o + e] = m[e];
+      sm_d[o + e] = den[e];
+      sm_n[o + e] = num[e];
+    }
+  }
+  __syncthreads();
+  for (int ff = tid; ff < fc; ff += nthr) {
+    float M = -INFINITY;
+    for (int k = 0; k < ng; ++k) M = fmaxf(M, sm_m[k * fc + ff]);
+    float D = 0.0f, Nn = 0.0f;
+    for (int k = 0; k < ng; ++k) {
+      const float mk = sm_m[k * fc + ff];
+      if (mk == -INFINITY) continue;  // a share of padded candidates adds nothing
+      const float w = expf(mk - M);
+      D = fmaf(sm_d[k * fc + ff], w, D);
+      Nn = fmaf(sm_n[k * fc + ff], w, Nn);
+    }
+    P.pooled[(size_t)b * pk.H + f0 + ff] = __fdiv_rn(Nn, D);
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last = atomicAdd(P.seq_ctr + b, 1) == P.nchunk - 1;
+  __syncthreads();
+  // -- the last chunk of the token runs the entry epilogue, one warp: lane l holds features
+  //    16l..16l+15
+  if (last && tid < 32) {
+    __threadfence();
+    const int H = pk.H;
+    const int l = min(tid, (H >> 4) - 1);
+    const float4* src = reinterpret_cast<const float4*>(P.pooled + (size_t)b * H + 16 * l);
+    float v[16];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float4 a = __ldcg(src + u);
+      v[4 * u] = a.x;
+      v[4 * u + 1] = a.y;
+      v[4 * u + 2] = a.z;
+      v[4 * u + 3] = a.w;
+    }
+    const size_t Hs = H;
+    entry_epilogue(v, tid, pos, P.ep, P.out.latent + b * Hs, P.out.codes ? P.out.codes + b * (Hs / 2) : nullptr,
+                   P.out.scales ? P.out.scales + b * (Hs / 16) : nullptr,
+                   P.out.prequant ? P.out.prequant + b * Hs : nullptr);
+    if (tid == 0) P.seq_ctr[b] = 0;  // ready for the next call
+  }
 }
 
 }  // namespace dtc
 
 // ---- host side ------------------------------------------------------------------------------
 
-// Number of K slices: at most one CTA per SM (the launch is cooperative), at least one K block
-// per CTA.
+// Number of K slices: about one CTA per SM for a 128-token block, at least one K block per CTA.
 int decode_tc_slices(const csa_compressor* c) {
   static int sms = 0;
   if (!sms) {
@@ -402,23 +423,25 @@ int decode_tc_slices(const csa_compressor* c) {
 }
 
 bool decode_tc_supported(const csa_compressor* c, const void* x) {
-  return c->pk.tw == dtc::kRows && c->dim % dtc::kKb == 0 && ((uintptr_t)x & 15) == 0 &&
-         c->pk.ntiles <= 148 && tcx::get_encode() != nullptr;
+  const int fc = c->H < dtc::kFinChunk ? c->H : dtc::kFinChunk;
+  return c->pk.tw == dtc::kRows && c->dim % dtc::kKb == 0 && ((uintptr_t)x & 15) == 0 && c->H % 16 == 0 &&
+         c->H % fc == 0 && fc % c->pk.ft == 0 && tcx::get_encode() != nullptr;
 }
 
 cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, const int32_t* start_pos,
-                             float* part, int ks, const csa_out& out, uint8_t* emitted, cudaStream_t s) {
+                             float* part, int ks, const csa_out& out, uint8_t* emitted, bool early_start,
+                             cudaStream_t s) {
   using namespace dtc;
   auto encode = tcx::get_encode();
   if (!encode) return cudaErrorNotSupported;
   const size_t smem = (size_t)kRingBytes + 1024 + 1024;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(decode_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  CUtensorMap mw;
+  CUtensorMap mw, mx;
   {
     // the three bf16 weight planes: [3 * ncol rows][dim], K innermost
     cuuint64_t dims[2] = {(cuuint64_t)c->dim, (cuuint64_t)3 * c->pk.cols()};
@@ -430,24 +453,47 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  for (int b0 = 0; b0 < B; b0 += kTok) {
-    const int nb = min(kTok, B - b0);
-    CUtensorMap mx;
-    cuuint64_t dims[2] = {(cuuint64_t)c->dim, (cuuint64_t)nb};
+  {
+    // the tokens: [B rows][dim]; rows past B in the last 128-token block read as zeros
+    cuuint64_t dims[2] = {(cuuint64_t)c->dim, (cuuint64_t)B};
     cuuint64_t strides[1] = {(cuuint64_t)c->dim * 2};
     cuuint32_t box[2] = {kKs, kTok};
     cuuint32_t es[2] = {1, 1};
-    if (encode(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)(x + (size_t)b0 * c->dim), dims, strides, box, es,
+    if (encode(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)x, dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-    Params P;
+  }
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  {
+    ProjParams P;
     P.nkb_total = c->dim / kKb;
     P.ks = ks;
-    P.B = nb;
-    P.b_total = B;
-    P.b0 = b0;
+    P.B = B;
     P.ncol = c->pk.cols();
+    P.part = part;
+    P.flag = c->dev_flag;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(c->pk.ntiles, ks, (B + kTok - 1) / kTok);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    at[0].val.programmaticStreamSerializationAllowed = early_start ? 1 : 0;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_proj_kernel, mw, mx, P);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    FinParams P;
+    P.B = B;
+    P.ks = ks;
+    P.ncol = c->pk.cols();
+    P.fc = c->H < kFinChunk ? c->H : kFinChunk;
+    P.nchunk = c->H / P.fc;
+    P.pooled = c->dec_pooled;
+    P.seq_ctr = c->dec_counters;
     P.part = part;
     P.flag = c->dev_flag;
     P.start_pos = start_pos;
@@ -459,22 +505,15 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
     P.ep = epi_params(c);
     P.out = out;
     P.emitted = emitted;
-    P.pooled = c->dec_pooled;
-    P.seq_ctr = c->dec_counters;
-    P.tile_ctr = c->dec_tile_ctr;
-    P.tile_gen = c->dec_tile_gen;
-    // the K slices of a tile wait for each other: a cooperative launch keeps the grid resident
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(c->pk.ntiles, ks, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.gridDim = dim3(B, P.nchunk, 1);
+    cfg.blockDim = dim3(kFinThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeCooperative;
-    at[0].val.cooperative = 1;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tc_kernel, mw, mx, P);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_finish_kernel, P);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -26,12 +26,14 @@ size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N, size_t* n
 cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset,
                               const csa_out& out, void* scratch, int* counters, cudaStream_t s);
 
-// Tensor-core decode (decode_tc.cu): projection of one token per sequence (split over K),
-// reduction into the state slots, pool and epilogue of the completed groups; one launch per
-// 128 sequences.
+// Tensor-core decode (decode_tc.cu): two launches, the projection of one token per sequence
+// (split over K, partial sums to `part`), then one CTA per sequence for the reduction into its
+// state slot, the pool and the epilogue.  `early_start` lets the projection fetch its weights
+// before the preceding kernel in the stream has finished.
 bool decode_tc_supported(const csa_compressor* c, const void* x);
 int decode_tc_slices(const csa_compressor* c);
 cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, const int32_t* start_pos,
-                             float* part, int nslices, const csa_out& out, uint8_t* emitted, cudaStream_t s);
+                             float* part, int nslices, const csa_out& out, uint8_t* emitted, bool early_start,
+                             cudaStream_t s);
 
 }  // namespace csa

@@ -76,6 +76,22 @@ __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
 }
 
+// Hint: fetch one tile of a tensor map into L2 (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"((uint64_t)map), "r"(c0),
+               "r"(c1)
+               : "memory");
+}
+
+// Programmatic dependent launch.  griddep_wait: block until the grids this launch depends on
+// have completed and their writes are visible (returns at once when the launch did not ask
+// for early start).  griddep_launch_dependents: this CTA no longer holds back the start of
+// the next launch in the stream (it starts once every CTA has said so or exited).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with 128-byte swizzle:
 // rows of 128 bytes, 8-row core groups 1024 bytes apart (stride byte offset), descriptor
 // version 1, layout SWIZZLE_128B (2).  The leading byte offset is unused for this layout.

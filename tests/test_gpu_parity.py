@@ -358,3 +358,117 @@ def test_decode_batch_beyond_one_token_tile(B, ratio, overlap):
     ko, so = o.state()
     assert np.allclose(kg, ko, rtol=2e-5, atol=2e-5 * np.abs(ko).max(initial=1.0))
     assert g.device_status() == 0
+
+
+# ---- decode calls queued back to back (launches that start before the previous one ends) -----
+
+def _decode_setup(seed, layers, B, pos_hi):
+    """Two compressors, every sequence's state brought to its start position on both sides."""
+    sp0 = (np.arange(B) * 37 % pos_hi).astype(np.int32)
+    pairs = []
+    for layer in layers:
+        g, o = make_pair(seed, layer, max_batch=B)
+        for b in range(B):
+            s = int(sp0[b])
+            t0 = csa.state_window_start(s, layer.ratio, layer.overlap)
+            if s > t0:
+                xb = to_bf16_bits(synthetic.tokens(seed, b, t0, s, layer.dim))[None]
+                o.prefill(xb, slot_offset=b)
+                g.prefill(dev_bits(xb), slot_offset=b, prequant=False)
+        pairs.append((g, o))
+    return sp0, pairs
+
+
+def _step_inputs(seed, layer, sp):
+    return to_bf16_bits(np.stack([synthetic.tokens(seed, b, int(sp[b]), int(sp[b]) + 1, layer.dim)[0]
+                                  for b in range(len(sp))]))
+
+
+DECODE_PAIR = [synthetic.Layer(512, 512, 4, 1, 1.0 / 22, gate_scale=2.0, rope_dim=64, fp4=1),
+               synthetic.Layer(512, 512, 16, 0, 1.0 / 22, gate_scale=2.0, rope_dim=64, fp4=1, weight_stream=3)]
+
+
+def _check_steps(pairs, seed, sp0, steps, outs):
+    # the entries of all steps of a layer are checked together: the 2-ulp share is a property
+    # of a sample, and one step may emit a single entry
+    got = [[] for _ in pairs]
+    ref = [[] for _ in pairs]
+    for k in range(steps):
+        sp = (sp0 + k).astype(np.int32)
+        for li, (g, o) in enumerate(pairs):
+            xt = _step_inputs(seed, DECODE_PAIR[li], sp)
+            r = o.decode(xt, sp)
+            d = outs[k][li]
+            em = d["emitted"].cpu().numpy()
+            assert np.array_equal(em, r["emitted"]), (k, li)
+            rows = np.flatnonzero(em)
+            if rows.size:
+                got[li].append(to_np(d, rows=rows))
+                ref[li].append(r["prequant"][rows])
+    for li in range(len(pairs)):
+        assert got[li], li
+        merged = {kk: np.concatenate([gd[kk] for gd in got[li]]) for kk in got[li][0]}
+        check_entries(merged, np.concatenate(ref[li]), 1, f"queued decode layer {li}")
+    for g, o in pairs:
+        kg, sg = (t.cpu().numpy() for t in g.state_export())
+        ko, so = o.state()
+        assert np.allclose(kg, ko, rtol=2e-5, atol=2e-5 * np.abs(ko).max(initial=1.0))
+        assert g.device_status() == 0
+
+
+def test_decode_steps_queued_without_host_sync():
+    """Steps of two compressors enqueued back to back with no synchronisation between them
+    (each call's projection may start while the previous call's kernels run): every step's
+    entries and the final state equal the oracle's step-by-step results."""
+    seed, B, steps = 21, 40, 20
+    sp0, pairs = _decode_setup(seed, DECODE_PAIR, B, 97)
+    xs = {}
+    for k in range(steps):
+        sp = (sp0 + k).astype(np.int32)
+        for li in range(2):
+            xs[k, li] = (dev_bits(_step_inputs(seed, DECODE_PAIR[li], sp)), torch.from_numpy(sp).to(DEV))
+    torch.cuda.synchronize()
+    outs = [[pairs[li][0].decode(*xs[k, li]) for li in range(2)] for k in range(steps)]
+    torch.cuda.synchronize()
+    _check_steps(pairs, seed, sp0, steps, outs)
+
+
+def test_decode_steps_in_a_cuda_graph():
+    """The same steps captured once in a CUDA graph and replayed: identical to the oracle."""
+    seed, B, steps = 23, 40, 12
+    sp0, pairs = _decode_setup(seed, DECODE_PAIR, B, 97)
+    xs = {}
+    for k in range(steps):
+        sp = (sp0 + k).astype(np.int32)
+        for li in range(2):
+            xs[k, li] = (dev_bits(_step_inputs(seed, DECODE_PAIR[li], sp)), torch.from_numpy(sp).to(DEV))
+    outs = [[{"emitted": torch.empty(B, dtype=torch.uint8, device=DEV),
+              **pairs[li][0]._alloc_out(B, DEV, prequant=True)} for li in range(2)] for k in range(steps)]
+
+    def run():
+        for k in range(steps):
+            for li in range(2):
+                o = outs[k][li]
+                pairs[li][0].decode(*xs[k, li], out={kk: v for kk, v in o.items() if kk != "emitted"},
+                                    emitted=o["emitted"])
+
+    # one eager step first (the library sizes its scratch on first use), then back to the start
+    pairs[0][0].decode(*xs[0, 0])
+    pairs[1][0].decode(*xs[0, 1])
+    torch.cuda.synchronize()
+    for li, (g, _) in enumerate(pairs):
+        layer = DECODE_PAIR[li]
+        g.state_reset()
+        for b in range(B):
+            s = int(sp0[b])
+            t0 = csa.state_window_start(s, layer.ratio, layer.overlap)
+            if s > t0:
+                g.prefill(dev_bits(to_bf16_bits(synthetic.tokens(seed, b, t0, s, layer.dim))[None]), slot_offset=b,
+                          prequant=False)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    graph.replay()
+    torch.cuda.synchronize()
+    _check_steps(pairs, seed, sp0, steps, outs)
