@@ -263,7 +263,9 @@ def run_ours(args, rank, world, local):
 
 def bench_decode(args, torch, csa, synthetic, device, peaks, world, rank):
     """B=128 decode steps through both compressors (ratio 4 overlapped + ratio 128), weights
-    of several layer instances rotated so that each step streams its weights from HBM."""
+    of several layer instances rotated so that each step streams its weights from HBM.  As in a
+    model, every layer instance sees consecutive positions: step k runs layer k % L at position
+    start + k // L, and the positions move on between graph replays."""
     wl = synthetic.DECODE
     B = wl.batch
     props = torch.cuda.get_device_properties(device)
@@ -290,11 +292,12 @@ def bench_decode(args, torch, csa, synthetic, device, peaks, world, rank):
             outs = c._alloc_out(B, device, prequant=False)
             pair.append((c, outs))
         layers.append(pair)
-    steps = args.decode_steps
+    steps = n_layers * max(1, -(-args.decode_steps // n_layers))
     xs = [torch.from_numpy(np.stack([synthetic.tokens(wl.seed, rank * B + b, int(sp0[b]) + k, int(sp0[b]) + k + 1,
                                                       wl.layers[0].dim)[0] for b in range(B)])).to(torch.bfloat16)
           .to(device) for k in range(8)]
-    sps = [torch.from_numpy((sp0 + k).astype(np.int32)).to(device) for k in range(steps + 8)]
+    pos_all = torch.from_numpy(np.stack([(sp0 + k // n_layers).astype(np.int32) for k in range(steps)])).to(device)
+    sps = [pos_all[k] for k in range(steps)]
     emitted = torch.empty(B, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
@@ -302,8 +305,9 @@ def bench_decode(args, torch, csa, synthetic, device, peaks, world, rank):
         for c, outs in layers[k % n_layers]:
             c.decode(xs[k % 8], sps[k], out=outs, emitted=emitted, prequant=False)
 
-    for k in range(8):
+    for k in range(n_layers):  # every layer once, at the first position
         step(k)
+    pos_all += 1
     torch.cuda.synchronize()
     # The timed steps run as one captured CUDA graph (the library's decode calls allocate and
     # synchronise nothing once warmed up), so the measurement is of the GPU work rather than of
@@ -318,7 +322,10 @@ def bench_decode(args, torch, csa, synthetic, device, peaks, world, rank):
         torch.cuda.synchronize()
     except Exception:
         graph = None
+        for k in range(steps):
+            step(k)
         torch.cuda.synchronize()
+    pos_all += steps // n_layers  # the timed steps continue where the warm-up stopped
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()

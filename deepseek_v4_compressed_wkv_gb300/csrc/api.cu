@@ -94,8 +94,8 @@ void free_all(csa_compressor* c) {
   cudaFree(c->scratch);
   cudaFree(c->tc_counters);
   cudaFree(c->dec_part);
-  cudaFree(c->dec_pooled);
-  cudaFree(c->dec_counters);
+  cudaFree(c->dec_acc);
+  cudaFree(c->dec_acc_pos);
 }
 
 int ensure_scratch(csa_compressor* c, size_t bytes, cudaStream_t s) {
@@ -193,8 +193,8 @@ int csa_compressor_create(int dim, int H, int ratio, int overlap, const csa_opti
     alloc((void**)&c->gain, H * sizeof(float));
     alloc((void**)&c->state, (size_t)o.max_batch * c->slots * ncol * sizeof(float));
     alloc((void**)&c->dev_flag, sizeof(int));
-    alloc((void**)&c->dec_pooled, (size_t)o.max_batch * H * sizeof(float));
-    alloc((void**)&c->dec_counters, (size_t)o.max_batch * sizeof(int));
+    alloc((void**)&c->dec_acc, (size_t)o.max_batch * 3 * H * sizeof(float));
+    alloc((void**)&c->dec_acc_pos, (size_t)o.max_batch * sizeof(int));
     if (o.rope_dim > 0) {
       const size_t n = (size_t)o.max_pos * (o.rope_dim / 2);
       alloc((void**)&c->rope_cos, n * sizeof(float));
@@ -209,7 +209,7 @@ int csa_compressor_create(int dim, int H, int ratio, int overlap, const csa_opti
       }
     }
     if (e == cudaSuccess) e = cudaMemset(c->dev_flag, 0, sizeof(int));
-    if (e == cudaSuccess) e = cudaMemset(c->dec_counters, 0, (size_t)o.max_batch * sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(c->dec_acc_pos, 0xFF, (size_t)o.max_batch * sizeof(int));
     if (e == cudaSuccess && csa::launch_state_reset(c, 0, o.max_batch, 0) != cudaSuccess) e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
@@ -257,6 +257,7 @@ int csa_compress_prefill(csa_compressor* c, const uint16_t* x, int B, int N, int
     cudaStream_t s = (cudaStream_t)stream;
     const long long M = (long long)B * N;
     if (M > 0x7fffffffLL) return fail(CSA_ERR_ARG, "B * N too large");
+    CSA_CUDA(csa::invalidate_decode_acc(c, slot_offset, B, s), "invalidate decode running values");
     if (csa::prefill_tc_supported(c, x)) {
       size_t nctr = 0;
       const size_t bytes = csa::prefill_tc_scratch_bytes(c, B, N, &nctr);
@@ -298,7 +299,7 @@ int csa_compress_decode(csa_compressor* c, const uint16_t* x_tok, int B, const i
   if (!x_tok || !start_pos || !emitted || !out || !out->latent)
     return fail(CSA_ERR_ARG, "x_tok, start_pos, emitted and out->latent are required");
   cudaStream_t s = (cudaStream_t)stream;
-  if (csa::decode_tc_supported(c, x_tok)) {
+  if (csa::decode_tc_supported(c, x_tok, B)) {
     // split-K partial sums: [slices][B][2C] f32, grown on first use (a later call of the same
     // or smaller B allocates nothing)
     const int ks = csa::decode_tc_slices(c);
@@ -319,6 +320,7 @@ int csa_compress_decode(csa_compressor* c, const uint16_t* x_tok, int B, const i
     c->launches += 2;
     return CSA_OK;
   }
+  CSA_CUDA(csa::invalidate_decode_acc(c, 0, B, s), "invalidate decode running values");
   if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
   CSA_CUDA(csa::launch_projection_ffma(c, x_tok, B, c->state, 1, start_pos, s), "decode projection launch");
   if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
@@ -331,6 +333,8 @@ int csa_state_reset(csa_compressor* c, int slot_begin, int slot_count, csa_strea
   if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
   if (slot_begin < 0 || slot_count < 0 || (long long)slot_begin + slot_count > c->opt.max_batch)
     return fail(CSA_ERR_ARG, "slots [%d, %d) outside [0, %d)", slot_begin, slot_begin + slot_count, c->opt.max_batch);
+  CSA_CUDA(csa::invalidate_decode_acc(c, slot_begin, slot_count, (cudaStream_t)stream),
+           "invalidate decode running values");
   CSA_CUDA(csa::launch_state_reset(c, slot_begin, slot_count, (cudaStream_t)stream), "state reset launch");
   c->launches += slot_count > 0;
   return CSA_OK;

@@ -113,39 +113,26 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Epilogue of one entry, one warp per entry: lane l (< H/16) holds pooled features
-// 16l..16l+15 in v[].  bf16 round ("norm(kv.to(bf16))"), RMSNorm in f32 with the f32 gain
-// and one bf16 rounding, YaRN RoPE on the trailing rope_dim features (adjacent pairs,
-// angle pos * f_i from the host-built table), then the fp4 round trip.  All 32 lanes must
-// call it (the RMSNorm sum is a warp reduction); lanes >= H/16 pass zeros and store nothing.
-__device__ __forceinline__ void entry_epilogue(float v[16], int lane, long long pos, const EpiParams& ep,
-                                               uint16_t* latent, uint8_t* codes, uint8_t* scales,
-                                               uint16_t* prequant) {
-  const int nl = ep.H >> 4;
-  const bool act = lane < nl;
-  float ss = 0.0f;
+// Epilogue of one block of 16 features f0..f0+15 of an entry, after the RMSNorm factor `inv`
+// is known: v[] holds the bf16-rounded pooled values.  RMSNorm in f32 with the f32 gain and one
+// bf16 rounding, YaRN RoPE on the trailing rope_dim features (adjacent pairs, angle pos * f_i
+// from the host-built table), then the fp4 round trip; stores the block's outputs.  gain points
+// at the gain of feature f0; cs / sn at the table row of the entry's position (global or shared
+// memory).
+__device__ __forceinline__ void entry_epilogue_block(float v[16], int f0, float inv, const float* gain,
+                                                     const float* cs, const float* sn, const EpiParams& ep,
+                                                     uint16_t* latent, uint8_t* codes, uint8_t* scales,
+                                                     uint16_t* prequant) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    v[i] = act ? bf16_round(v[i]) : 0.0f;
-    ss = fmaf(v[i], v[i], ss);
-  }
-  ss = warp_sum(ss);
-  const float inv = 1.0f / sqrtf(ss / (float)ep.H + ep.eps);
-  if (!act) return;
-  const int f0 = lane * 16;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = bf16_round(v[i] * inv * __ldg(ep.gain + f0 + i));
+  for (int i = 0; i < 16; ++i) v[i] = bf16_round(v[i] * inv * gain[i]);
   const int r0 = ep.H - ep.rope_dim;
   if (ep.rope_dim > 0 && f0 + 16 > r0) {
-    const int hr = ep.rope_dim >> 1;
-    const float* cs = ep.rope_cos + pos * hr;
-    const float* sn = ep.rope_sin + pos * hr;
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {
       const int f = f0 + i;
       if (f >= r0) {
         const int k = (f - r0) >> 1;
-        const float c = __ldg(cs + k), s = __ldg(sn + k);
+        const float c = cs[k], s = sn[k];
         const float a = v[i], b = v[i + 1];
         v[i] = bf16_round(a * c - b * s);
         v[i + 1] = bf16_round(a * s + b * c);
@@ -169,7 +156,7 @@ __device__ __forceinline__ void entry_epilogue(float v[16], int lane, long long 
       pk.y = cd[4] | (cd[5] << 8) | (cd[6] << 16) | ((uint32_t)cd[7] << 24);
       *reinterpret_cast<uint2*>(codes + f0 / 2) = pk;
     }
-    if (scales) scales[lane] = sb;
+    if (scales) scales[f0 >> 4] = sb;
   }
   uint32_t w[8];
 #pragma unroll
@@ -177,6 +164,34 @@ __device__ __forceinline__ void entry_epilogue(float v[16], int lane, long long 
   uint4* dst = reinterpret_cast<uint4*>(latent + f0);
   dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
   dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// RMSNorm factor from the sum of squares of the bf16-rounded pooled values.
+__device__ __forceinline__ float rms_inv(float ss, const EpiParams& ep) {
+  return 1.0f / sqrtf(ss / (float)ep.H + ep.eps);
+}
+
+// Epilogue of one entry, one warp per entry: lane l (< H/16) holds pooled features
+// 16l..16l+15 in v[].  bf16 round ("norm(kv.to(bf16))"), the sum of squares over the warp,
+// then entry_epilogue_block.  All 32 lanes must call it (the RMSNorm sum is a warp
+// reduction); lanes >= H/16 pass zeros and store nothing.
+__device__ __forceinline__ void entry_epilogue(float v[16], int lane, long long pos, const EpiParams& ep,
+                                               uint16_t* latent, uint8_t* codes, uint8_t* scales,
+                                               uint16_t* prequant) {
+  const int nl = ep.H >> 4;
+  const bool act = lane < nl;
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v[i] = act ? bf16_round(v[i]) : 0.0f;
+    ss = fmaf(v[i], v[i], ss);
+  }
+  ss = warp_sum(ss);
+  const float inv = rms_inv(ss, ep);
+  if (!act) return;
+  const int hr = ep.rope_dim >> 1;
+  entry_epilogue_block(v, lane * 16, inv, ep.gain + lane * 16, hr ? ep.rope_cos + pos * hr : nullptr,
+                       hr ? ep.rope_sin + pos * hr : nullptr, ep, latent, codes, scales, prequant);
 }
 
 }  // namespace csa
@@ -201,8 +216,9 @@ struct csa_compressor {
   size_t scratch_bytes;
   float* dec_part;          // decode split-K partial sums [slices][B][2C] (grown on demand)
   size_t dec_part_bytes;
-  float* dec_pooled;        // decode pooled values of the emitting tokens [max_batch][H]
-  int* dec_counters;        // decode per-sequence chunk counters [max_batch] (kept at zero)
+  float* dec_acc;           // decode, non-overlapped: running softmax max / denominator / numerator
+                            // of each sequence's open group [max_batch][3][H]
+  int* dec_acc_pos;         //   position of the last token folded in [max_batch] (-1: not valid)
   bool dec_early_start;     // the next decode may start its weight loads before the preceding
                             // kernel ends (false right after set_weights rewrote the planes)
   int* tc_counters;         // per token tile completion counters of the tensor-core prefill

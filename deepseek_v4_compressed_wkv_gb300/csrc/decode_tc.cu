@@ -19,19 +19,22 @@
 //    slice into L2) before it waits for the preceding kernel; the tokens, and every write,
 //    come after that wait.
 //
-//  * decode_finish_kernel, one CTA per (sequence, chunk of 128 features): adds the K slices'
-//    partial sums in slice order (a deterministic split-K reduction) into the token's state
-//    slot, applies the restart at position 0, and where the token completed a group pools the
-//    chunk's features over the group's candidates ("Pool token pairs", decode branch;
-//    "Compressed Sparse Attention - ratio m = 4", decode rule).  The last chunk of a token to
-//    finish (a completion counter; nothing waits) runs the entry epilogue (bf16, RMSNorm, RoPE,
-//    fp4), which needs all features.
+//  * decode_finish_kernel, a cluster of CTAs per sequence, one per chunk of 128 features: adds
+//    the K slices' partial sums in slice order (a deterministic split-K reduction) into the
+//    token's state slot, applies the restart at position 0, and where the token completed a
+//    group pools the chunk's features over the group's candidates ("Pool token pairs", decode
+//    branch; "Compressed Sparse Attention - ratio m = 4", decode rule) and runs the entry
+//    epilogue (bf16, RMSNorm, RoPE, fp4) with the RMSNorm's sum of squares exchanged through
+//    distributed shared memory.  The candidates from earlier calls are pooled before the wait
+//    for the projection, while it still runs.
 //
 // Each launch lets the next one start as soon as all of its CTAs have begun: the finish kernel
 // at once, the projection right after its own wait.  A CTA only ever waits for a launch whose
 // CTAs have all started, so the chain cannot deadlock whatever the occupancy.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <cooperative_groups.h>
 
 #include "csa_internal.cuh"
 #include "kernels.h"
@@ -46,16 +49,18 @@ constexpr int kRows = 128;                              // packed rows per tile 
 constexpr int kTok = 128;                               // tokens per CTA (MMA N)
 constexpr int kKb = 64;                                 // K granularity of the slice split
 constexpr int kKs = 32;                                 // K per stage (one 64-byte swizzle row of bf16)
-constexpr int kStages = 6;
+constexpr int kStages = 5;
 constexpr int kChunkSteps = 4;                          // stages per accumulator chunk (K = 128)
 constexpr int kPlaneBytes = kRows * kKs * 2;            // 8 KB
 constexpr int kXBytes = kTok * kKs * 2;                 // 8 KB
 constexpr int kStageBytes = 3 * kPlaneBytes + kXBytes;  // 32 KB
-constexpr int kRingBytes = kStages * kStageBytes;       // 192 KB
+constexpr int kRingBytes = kStages * kStageBytes;       // 160 KB
+constexpr int kPartBytes = kTok * kRows * 4;            // one CTA's partial sums, staged in the ring
+static_assert(kPartBytes <= kRingBytes, "the partial tile is staged in the free ring");
 constexpr int kEpiThreads = 256;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kTmemCols = 2 * kTok;
-constexpr int kFinThreads = 256;
+constexpr int kFinThreads = 128;  // one warp per SM sub-partition: fits beside a projection CTA
 
 struct ProjParams {
   int nkb_total, ks;  // K blocks (of 64) of dim, number of K slices
@@ -67,7 +72,7 @@ struct ProjParams {
 
 __global__ void __launch_bounds__(kThreads, 1)
     decode_proj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
-                       const ProjParams P) {
+                       const __grid_constant__ CUtensorMap map_p, const ProjParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* full = (uint64_t*)(smem + kRingBytes);
@@ -98,6 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_map(&map_w);
     prefetch_map(&map_x);
+    prefetch_map(&map_p);
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
@@ -188,13 +194,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&c_empty[buf]);
     }
     if (!ok && threadIdx.x == 64) atomicOr(P.flag, 4);
-    griddep_wait();  // the preceding finish kernel may still be reading this scratch
-    float* dst = P.part + ((size_t)ks * P.B + tb) * P.ncol + tile * kRows + row;
-    const int nb = min(kTok, P.B - tb);
+    // every MMA has completed and every load has landed: the ring is free.  Stage the partial
+    // sums as [token][packed row] and write them with one TMA store (tokens past B are clipped)
+    float* stg = reinterpret_cast<float*>(smem);
 #pragma unroll
-    for (int i = 0; i < kTok / 2; ++i) {
-      const int b = (kTok / 2) * h + i;
-      if (b < nb) dst[(size_t)b * P.ncol] = acc[i];
+    for (int i = 0; i < kTok / 2; ++i) stg[((kTok / 2) * h + i) * kRows + row] = acc[i];
+    fence_async_shared();
+    named_sync(1, kEpiThreads);
+    if (threadIdx.x == 64) {
+      griddep_wait();  // the preceding finish kernel may still be reading this scratch
+      tma_store_3d(&map_p, stg, tile * kRows, tb, ks);
+      bulk_commit();
+      bulk_wait_read();
     }
   }
 
@@ -209,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 struct FinParams {
   int B, ks, ncol;
-  int fc, nchunk;            // features per chunk (whole tiles), chunks per token
+  int fc, nchunk;            // features per chunk (whole tiles), chunks per token (the cluster)
   const float* part;         // [ks][B][ncol]
   int* flag;
   const int32_t* start_pos;  // [B]
@@ -219,8 +230,9 @@ struct FinParams {
   EpiParams ep;
   csa_out out;               // rows indexed by sequence
   uint8_t* emitted;          // [B]
-  float* pooled;             // [B][H] pooled values of the emitting tokens
-  int* seq_ctr;              // [B] chunks done (kept at zero between calls)
+  float* acc;                // non-overlapped: [max_batch][3][H] running max, denominator and
+                             // numerator of the open group over its tokens so far
+  int* acc_pos;              // [max_batch] position of the last token in acc (-1: not valid)
 };
 
 __device__ __forceinline__ float padded_kind_value(const Packing& pk, int col) {
@@ -239,168 +251,369 @@ __device__ __forceinline__ float comp(const float4& v, int e) {
 }
 
 constexpr int kFinChunk = 128;  // features per finish CTA (a whole number of packed tiles)
+constexpr int kMaxChunks = 8;   // chunks per token: H <= 1024
 constexpr int kPoolUnroll = 4;  // candidates in flight per thread
+constexpr int kMaxFinB = 4096;  // sequences per call (the emitting-first order is built in shared memory)
+constexpr int kStageFloats = 6144;  // partial-sum rows staged per round (24 KB)
 
-// One CTA per (sequence b, chunk j of kFinChunk features): the chunk's packed columns are the
-// contiguous range [j * cw, (j + 1) * cw), cw = fc * nk.
-__global__ void __launch_bounds__(kFinThreads, 4) decode_finish_kernel(const FinParams P) {
-  __shared__ float sm_m[8 * kFinChunk], sm_d[8 * kFinChunk], sm_n[8 * kFinChunk];
-  __shared__ int last;
-  griddep_launch_dependents();  // the next launch may take the SMs this grid leaves free
-  griddep_wait();               // the partial sums of the projection are complete
+// Waits for the phase of `parity` at most kWaitNs; false on time-out.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > kWaitNs) return false;
+  return true;
+}
+
+// Whether the token at position p completes a group that is emitted (a position the RoPE
+// table covers).
+__device__ __forceinline__ bool emits(const FinParams& P, int p) {
+  if (p < 0 || (p + 1) % P.ratio != 0) return false;
+  return P.ep.rope_dim == 0 || (long long)p + 1 - P.ratio < P.ep.max_pos;
+}
+
+// The t-th sequence in the order "emitting sequences, then the others", each by index.  CTAs
+// start in index order, so the ones with pooling to do start first, beside the projection that
+// is still running.  All threads call it; ew is shared scratch of (B + 31) / 32 words.
+__device__ int nth_in_emit_order(const FinParams& P, int t, unsigned* ew, int* s_b) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
+  const int nw = (P.B + 31) >> 5;
+  for (int w = warp; w < nw; w += nwarp) {
+    const int b = 32 * w + lane;
+    const unsigned bal = __ballot_sync(0xffffffffu, b < P.B && emits(P, P.start_pos[b]));
+    if (lane == 0) ew[w] = bal;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    auto valid = [&](int w) -> unsigned {
+      const int n = P.B - 32 * w;
+      return n >= 32 ? 0xffffffffu : ((1u << n) - 1u);
+    };
+    int cnt = 0;
+    for (int w = lane; w < nw; w += 32) cnt += __popc(ew[w] & valid(w));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    const bool want = t < cnt;
+    int r = want ? t : t - cnt;
+    int found = 0;
+    for (int w0 = 0; w0 < nw; w0 += 32) {
+      const int w = w0 + lane;
+      const unsigned bits = w < nw ? (want ? ew[w] : ~ew[w]) & valid(w) : 0u;
+      const int c = __popc(bits);
+      int inc = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      const int tot = __shfl_sync(0xffffffffu, inc, 31);
+      if (r < tot) {
+        const int L = __ffs(__ballot_sync(0xffffffffu, r >= inc - c && r < inc)) - 1;
+        const int rr = r - __shfl_sync(0xffffffffu, inc - c, L);
+        const unsigned wb = __shfl_sync(0xffffffffu, bits, L);
+        const bool mb = ((wb >> lane) & 1u) && __popc(wb & ((1u << lane) - 1u)) == rr;
+        found = 32 * (w0 + L) + __ffs(__ballot_sync(0xffffffffu, mb)) - 1;
+        break;
+      }
+      r -= tot;
+    }
+    if (lane == 0) *s_b = found;
+  }
+  __syncthreads();
+  return *s_b;
+}
+
+// Pools candidates [i0, i1) of the open group(s) for features f .. f+3 with a running maximum.
+// cand(i) gives the state row and the score and kv columns of candidate i.
+template <class Cand>
+__device__ __forceinline__ void pool_range(const float* st, int ncol, int i0, int i1, Cand cand, float m[4],
+                                           float den[4], float num[4]) {
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    m[e] = -INFINITY;
+    den[e] = 0.0f;
+    num[e] = 0.0f;
+  }
+  for (int ib = i0; ib < i1; ib += kPoolUnroll) {
+    float4 sv[kPoolUnroll], kv[kPoolUnroll];
+#pragma unroll
+    for (int u = 0; u < kPoolUnroll; ++u) {
+      const int i = ib + u;
+      sv[u] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      kv[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (i < i1) {
+        int srow, cs, ck;
+        cand(i, srow, cs, ck);
+        const float* row = st + (size_t)srow * ncol;
+        sv[u] = __ldcg(reinterpret_cast<const float4*>(row + cs));
+        kv[u] = __ldcg(reinterpret_cast<const float4*>(row + ck));
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float cm = m[e];
+#pragma unroll
+      for (int u = 0; u < kPoolUnroll; ++u) cm = fmaxf(cm, comp(sv[u], e));
+      if (cm == -INFINITY) continue;  // padded candidates only, so far
+      const float sc = expf(m[e] - cm);  // 0 while m was -inf, 1 when the maximum is unchanged
+      den[e] *= sc;
+      num[e] *= sc;
+#pragma unroll
+      for (int u = 0; u < kPoolUnroll; ++u) {
+        const float ex = expf(comp(sv[u], e) - cm);
+        den[e] += ex;
+        num[e] = fmaf(ex, comp(kv[u], e), num[e]);
+      }
+      m[e] = cm;
+    }
+  }
+}
+
+// Cluster of nchunk CTAs per sequence (the sequence nth_in_emit_order(blockIdx.y)); CTA j takes
+// the features [j * fc, (j + 1) * fc), whose packed columns are the contiguous range
+// [j * cw, (j + 1) * cw), cw = fc * nk.
+//
+// The token of this call always completes the open group last, so every other candidate sits in
+// a state slot written by work that completed before this launch could start (the projection
+// before it only lets it start once its own wait has returned): before its wait a CTA combines
+// them into a running (maximum, denominator, numerator) per feature.  Overlapped (8 candidates)
+// it pools the 7 earlier ones when the token completes a group; otherwise it takes the open
+// group's running values kept from the previous call (acc), or rebuilds them from the state
+// slots when they are not for the previous position.  It also stages the gain and the RoPE row
+// of an emitted entry.  After the wait it adds the token's partial sums into its state slot,
+// folds the token in, keeps the running values (otherwise) or, when the group completes, runs
+// the epilogue, the chunks' sums of squares for the RMSNorm exchanged across the cluster
+// through distributed shared memory.
+__global__ void __launch_bounds__(kFinThreads, 8) decode_finish_kernel(const FinParams P) {
+  namespace cg = cooperative_groups;
+  constexpr int kGrp = 4 * kFinThreads;  // group rows x features of the running values
+  __shared__ float sm_m[kGrp], sm_d[kGrp], sm_n[kGrp];
+  __shared__ float cur[4 * kFinChunk];  // the token's columns of this chunk
+  __shared__ float wss[kFinThreads / 32];
+  __shared__ float gn[kFinChunk];
+  __shared__ float rcs[kFinChunk / 2], rsn[kFinChunk / 2];  // RoPE pairs of the chunk's features
+  __shared__ float ssq[kMaxChunks];
+  __shared__ __align__(16) float pst[kStageFloats];  // staged partial-sum rows
+  __shared__ __align__(8) uint64_t rbar_s;
+  __shared__ unsigned ew[kMaxFinB / 32];
+  __shared__ int s_b;
 
   const Packing& pk = P.pk;
-  const int b = blockIdx.x, j = blockIdx.y, tid = threadIdx.x, nthr = blockDim.x;
-  const int ncol = P.ncol, cw = P.fc * pk.nk, c0 = j * cw;
+  const int j = blockIdx.x, tid = threadIdx.x, nthr = blockDim.x;
+  const int ncol = P.ncol, fc = P.fc, cw = fc * pk.nk, c0 = j * cw, f0 = j * fc, H = pk.H;
+  uint64_t* rbar = &rbar_s;
+  if (tid == 0) {
+    mbar_init(rbar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  const int b = nth_in_emit_order(P, blockIdx.y, ew, &s_b);
   const int p = P.start_pos[b];
   const int pp = max(p, 0);
   const int slot = P.overlap ? ((pp >> 2) & 1) * 4 + (pp & 3) : pp % P.ratio;
+  const int q = (pp >> 2) & 1;
   float* st = P.state + (size_t)b * P.slots * ncol;
-
-  // -- the K-slice partial sums, in slice order, into the state slot
-  {
-    const float* src = P.part + (size_t)b * ncol + c0;
-    const size_t kstride = (size_t)P.B * ncol;
-    for (int i = tid; i < cw / 4; i += nthr) {
-      const float* s0 = src + 4 * i;
-      float4 a = __ldcg(reinterpret_cast<const float4*>(s0));
-      int k = 1;
-      for (; k + 4 <= P.ks; k += 4) {
-        float4 v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = __ldcg(reinterpret_cast<const float4*>(s0 + (k + u) * kstride));
-#pragma unroll
-        for (int u = 0; u < 4; ++u) add4(a, v[u]);
-      }
-      for (; k < P.ks; ++k) add4(a, __ldcg(reinterpret_cast<const float4*>(s0 + k * kstride)));
-      *reinterpret_cast<float4*>(st + (size_t)slot * ncol + c0 + 4 * i) = a;
-    }
-  }
-  // -- restart at position 0: the previous group's branch is the padded one
-  if (p == 0 && P.overlap)
-    for (int i = tid; i < 4 * cw; i += nthr) {
-      const int r = i / cw, c = c0 + i % cw;
-      st[(size_t)(4 + r) * ncol + c] = padded_kind_value(pk, c);
-    }
   const bool emit = p >= 0 && (p + 1) % P.ratio == 0;
   const long long pos = (long long)p + 1 - P.ratio;
-  const bool pos_ok = P.ep.rope_dim == 0 || pos < P.ep.max_pos;
-  if (tid == 0 && j == 0) {
-    P.emitted[b] = (emit && pos_ok) ? 1 : 0;
-    if (p < 0) atomicOr(P.flag, 1);
-    if (emit && !pos_ok) atomicOr(P.flag, 2);
-  }
-  if (!(emit && pos_ok)) return;
-  __threadfence();
-  __syncthreads();  // the slot written above is one of the candidates
+  const bool pool = emits(P, p);
+  float* acc = P.acc + (size_t)b * 3 * H;
 
-  // -- pool: thread (g, fg) takes features f0 + 4fg .. +3 (four adjacent columns of one kind)
-  //    over its contiguous share of the candidates with a running maximum; the shares are
-  //    merged in a fixed order
-  const int fc = P.fc, nfg = fc / 4, f0 = j * fc;
-  const int ncand = P.overlap ? 8 : P.ratio;
-  const int ng = max(1, min(min(nthr / nfg, 8), ncand));
-  const int g = tid / nfg, f = f0 + 4 * (tid % nfg);
-  if (g < ng) {
-    const int i0 = (int)((long long)g * ncand / ng), i1 = (int)((long long)(g + 1) * ncand / ng);
-    const int q = (pp >> 2) & 1;
-    float m[4], den[4], num[4];
+  // -- the earlier candidates, as ngr rows of running values per feature
+  const int nfg = fc / 4;
+  int ngr = 0;
+  if (P.overlap) {
+    if (pool) {
+      ngr = max(1, min(nthr / nfg, 7));
+      const int g = tid / nfg, f = f0 + 4 * (tid % nfg);
+      if (g < ngr) {
+        float m[4], den[4], num[4];
+        pool_range(st, ncol, g * 7 / ngr, (g + 1) * 7 / ngr,
+                   [&](int i, int& srow, int& cs, int& ck) {
+                     const bool prevB = i < 4;  // the previous group's branch B, then this group's A
+                     srow = prevB ? 4 * (1 - q) + i : 4 * q + i - 4;
+                     cs = pk.col(prevB ? S_B : S_A, f);
+                     ck = pk.col(prevB ? KV_B : KV_A, f);
+                   },
+                   m, den, num);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      m[e] = -INFINITY;
-      den[e] = 0.0f;
-      num[e] = 0.0f;
-    }
-    for (int ib = i0; ib < i1; ib += kPoolUnroll) {
-      float4 sv[kPoolUnroll], kv[kPoolUnroll];
-#pragma unroll
-      for (int u = 0; u < kPoolUnroll; ++u) {
-        const int i = ib + u;
-        sv[u] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        kv[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        if (i < i1) {
-          int srow, cs, ck;
-          if (P.overlap) {
-            const bool prevB = i < 4;  // the previous group's branch B, then this group's branch A
-            srow = prevB ? 4 * (1 - q) + i : 4 * q + i - 4;
-            cs = pk.col(prevB ? S_B : S_A, f);
-            ck = pk.col(prevB ? KV_B : KV_A, f);
-          } else {
-            srow = i;
-            cs = pk.col(S, f);
-            ck = pk.col(KV, f);
-          }
-          const float* row = st + (size_t)srow * ncol;
-          sv[u] = __ldcg(reinterpret_cast<const float4*>(row + cs));
-          kv[u] = __ldcg(reinterpret_cast<const float4*>(row + ck));
+        for (int e = 0; e < 4; ++e) {
+          sm_m[g * fc + f - f0 + e] = m[e];
+          sm_d[g * fc + f - f0 + e] = den[e];
+          sm_n[g * fc + f - f0 + e] = num[e];
         }
       }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float cm = m[e];
-#pragma unroll
-        for (int u = 0; u < kPoolUnroll; ++u) cm = fmaxf(cm, comp(sv[u], e));
-        if (cm == -INFINITY) continue;  // padded candidates only, so far
-        const float sc = expf(m[e] - cm);  // 0 while m was -inf, 1 when the maximum is unchanged
-        den[e] *= sc;
-        num[e] *= sc;
-#pragma unroll
-        for (int u = 0; u < kPoolUnroll; ++u) {
-          const float ex = expf(comp(sv[u], e) - cm);
-          den[e] += ex;
-          num[e] = fmaf(ex, comp(kv[u], e), num[e]);
-        }
-        m[e] = cm;
-      }
     }
-    const int o = g * fc + (f - f0);
+  } else if (pp % P.ratio != 0) {
+    const int nprev = pp % P.ratio;
+    if (P.acc_pos[b] == p - 1) {
+      ngr = 1;
+      for (int ff = tid; ff < fc; ff += nthr) {
+        sm_m[ff] = __ldcg(acc + f0 + ff);
+        sm_d[ff] = __ldcg(acc + H + f0 + ff);
+        sm_n[ff] = __ldcg(acc + 2 * H + f0 + ff);
+      }
+    } else {  // rebuild from the state slots of the open group
+      ngr = max(1, min(nthr / nfg, nprev));
+      const int g = tid / nfg, f = f0 + 4 * (tid % nfg);
+      if (g < ngr) {
+        float m[4], den[4], num[4];
+        pool_range(st, ncol, (int)((long long)g * nprev / ngr), (int)((long long)(g + 1) * nprev / ngr),
+                   [&](int i, int& srow, int& cs, int& ck) {
+                     srow = i;
+                     cs = pk.col(S, f);
+                     ck = pk.col(KV, f);
+                   },
+                   m, den, num);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      sm_m[o + e] = m[e];
-      sm_d[o + e] = den[e];
-      sm_n[o + e] = num[e];
+        for (int e = 0; e < 4; ++e) {
+          sm_m[g * fc + f - f0 + e] = m[e];
+          sm_d[g * fc + f - f0 + e] = den[e];
+          sm_n[g * fc + f - f0 + e] = num[e];
+        }
+      }
     }
   }
+  const int hr = P.ep.rope_dim >> 1;
+  const int r0 = H - P.ep.rope_dim;  // even: H is a multiple of 16 and rope_dim is even
+  const int kb = (max(f0, r0) - r0) >> 1;  // first RoPE pair of the chunk
+  if (pool) {  // the epilogue's gain and the chunk's part of the RoPE row
+    for (int ff = tid; ff < fc; ff += nthr) gn[ff] = __ldg(P.ep.gain + f0 + ff);
+    for (int k = kb + tid; k < hr && 2 * k + r0 < f0 + fc; k += nthr) {
+      rcs[k - kb] = __ldg(P.ep.rope_cos + pos * hr + k);
+      rsn[k - kb] = __ldg(P.ep.rope_sin + pos * hr + k);
+    }
+  }
+
+  griddep_launch_dependents();  // the next launch may take the SMs this grid leaves free
+  griddep_wait();               // the partial sums of the projection are complete
+
+  // -- the K-slice partial sums into the state slot: the chunk's row of every slice arrives by
+  //    bulk copy (all in flight at once, as many slices per round as the staging holds), then
+  //    thread i adds column group i over the slices in order
+  {
+    const int nit = cw / 4;
+    const int per_round = max(1, kStageFloats / cw);
+    const float* src = P.part + (size_t)b * ncol + c0;
+    const size_t kstride = (size_t)P.B * ncol;
+    float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    int round = 0;
+    for (int k0 = 0; k0 < P.ks; k0 += per_round, ++round) {
+      const int nr = min(per_round, P.ks - k0);
+      if (tid == 0) {
+        mbar_arrive_expect_tx(rbar, (uint32_t)(nr * cw * 4));
+        for (int r = 0; r < nr; ++r) bulk_load(pst + r * cw, src + (size_t)(k0 + r) * kstride, cw * 4, rbar);
+      }
+      if (!wait_bounded(rbar, round & 1)) atomicOr(P.flag, 4);
+      if (tid < nit)
+        for (int r = 0; r < nr; ++r) add4(a, reinterpret_cast<const float4*>(pst + r * cw)[tid]);
+      __syncthreads();  // the staging is free for the next round
+    }
+    if (tid < nit) {
+      *reinterpret_cast<float4*>(cur + 4 * tid) = a;
+      // an emitting CTA stores the slot after its cluster barrier, so that the barrier has no
+      // global stores to wait for
+      if (!pool) *reinterpret_cast<float4*>(st + (size_t)slot * ncol + c0 + 4 * tid) = a;
+    }
+  }
+  if (!pool) {
+    // -- restart at position 0: the previous group's branch is the padded one
+    if (p == 0 && P.overlap)
+      for (int i = tid; i < 4 * cw; i += nthr) {
+        const int r = i / cw, c = c0 + i % cw;
+        st[(size_t)(4 + r) * ncol + c] = padded_kind_value(pk, c);
+      }
+    if (tid == 0 && j == 0) {
+      P.emitted[b] = 0;
+      if (p < 0) atomicOr(P.flag, 1);
+      if (emit) atomicOr(P.flag, 2);
+      if (!P.overlap) P.acc_pos[b] = p >= 0 ? p : -1;
+    }
+    if (P.overlap) return;  // the same for every CTA of the cluster
+  }
   __syncthreads();
-  for (int ff = tid; ff < fc; ff += nthr) {
-    float M = -INFINITY;
-    for (int k = 0; k < ng; ++k) M = fmaxf(M, sm_m[k * fc + ff]);
+
+  // -- fold the token itself in (the last candidate), the rows merged in a fixed order; thread
+  //    ff takes feature f0 + ff
+  const bool act = tid < fc;
+  const int f = f0 + tid;
+  float pv = 0.0f;
+  if (act) {
+    const float sc = cur[pk.col(P.overlap ? S_A : S, f) - c0];
+    const float kc = cur[pk.col(P.overlap ? KV_A : KV, f) - c0];
+    float M = sc;
+    for (int k = 0; k < ngr; ++k) M = fmaxf(M, sm_m[k * fc + tid]);
     float D = 0.0f, Nn = 0.0f;
-    for (int k = 0; k < ng; ++k) {
-      const float mk = sm_m[k * fc + ff];
-      if (mk == -INFINITY) continue;  // a share of padded candidates adds nothing
+    for (int k = 0; k < ngr; ++k) {
+      const float mk = sm_m[k * fc + tid];
+      if (mk == -INFINITY) continue;  // a row of padded candidates adds nothing
       const float w = expf(mk - M);
-      D = fmaf(sm_d[k * fc + ff], w, D);
-      Nn = fmaf(sm_n[k * fc + ff], w, Nn);
+      D = fmaf(sm_d[k * fc + tid], w, D);
+      Nn = fmaf(sm_n[k * fc + tid], w, Nn);
     }
-    P.pooled[(size_t)b * pk.H + f0 + ff] = __fdiv_rn(Nn, D);
+    const float ex = expf(sc - M);
+    D += ex;
+    Nn = fmaf(ex, kc, Nn);
+    if (pool) {
+      pv = __fdiv_rn(Nn, D);
+    } else {  // the open group's running values for the next call
+      acc[f] = M;
+      acc[H + f] = D;
+      acc[2 * H + f] = Nn;
+    }
   }
-  __threadfence();
+  if (!pool) return;  // the same for every CTA of the cluster
+
+  // -- epilogue, one thread per feature: bf16, the chunk's sum of squares (warps in order),
+  //    exchanged across the cluster and added in chunk order, then RMSNorm, RoPE (the pair
+  //    partner is the neighbouring lane) and the fp4 round trip (a block of 16 features is a
+  //    half warp)
+  cg::cluster_group cluster = cg::this_cluster();
+  const int lane = tid & 31, warp = tid >> 5;
+  const float v = act ? bf16_round(pv) : 0.0f;
+  const float ws = warp_sum(v * v);
+  if (lane == 0) wss[warp] = ws;
   __syncthreads();
-  if (tid == 0) last = atomicAdd(P.seq_ctr + b, 1) == P.nchunk - 1;
-  __syncthreads();
-  // -- the last chunk of the token runs the entry epilogue, one warp: lane l holds features
-  //    16l..16l+15
-  if (last && tid < 32) {
-    __threadfence();
-    const int H = pk.H;
-    const int l = min(tid, (H >> 4) - 1);
-    const float4* src = reinterpret_cast<const float4*>(P.pooled + (size_t)b * H + 16 * l);
-    float v[16];
+  if (tid == 0) {
+    float t = 0.0f;
+    for (int w = 0; w < (nthr >> 5); ++w) t += wss[w];
+    for (int r = 0; r < P.nchunk; ++r) cluster.map_shared_rank(ssq, r)[j] = t;
+  }
+  cluster.sync();
+  // the stores held back until the barrier
+  if (tid < cw / 4)
+    *reinterpret_cast<float4*>(st + (size_t)slot * ncol + c0 + 4 * tid) = *reinterpret_cast<const float4*>(cur + 4 * tid);
+  if (tid == 0 && j == 0) {
+    P.emitted[b] = 1;
+    if (!P.overlap) P.acc_pos[b] = p;
+  }
+  float tot = 0.0f;
+  for (int r = 0; r < P.nchunk; ++r) tot += ssq[r];
+  const float inv = rms_inv(tot, P.ep);
+  float y = act ? bf16_round(v * inv * gn[tid]) : 0.0f;
+  const float partner = __shfl_xor_sync(0xffffffffu, y, 1);
+  if (act && P.ep.rope_dim > 0 && f >= r0) {
+    const int k = ((f - r0) >> 1) - kb;
+    const float c = rcs[k], sn = rsn[k];
+    if ((f & 1) == 0)
+      y = bf16_round(y * c - partner * sn);  // a' = a cos - b sin
+    else
+      y = bf16_round(partner * sn + y * c);  // b' = a sin + b cos
+  }
+  const size_t Hs = H;
+  if (act && P.out.prequant) P.out.prequant[b * Hs + f] = bf16_bits(y);
+  if (P.ep.fp4) {
+    float amax = fabsf(y);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float4 a = __ldcg(src + u);
-      v[4 * u] = a.x;
-      v[4 * u + 1] = a.y;
-      v[4 * u + 2] = a.z;
-      v[4 * u + 3] = a.w;
-    }
-    const size_t Hs = H;
-    entry_epilogue(v, tid, pos, P.ep, P.out.latent + b * Hs, P.out.codes ? P.out.codes + b * (Hs / 2) : nullptr,
-                   P.out.scales ? P.out.scales + b * (Hs / 16) : nullptr,
-                   P.out.prequant ? P.out.prequant + b * Hs : nullptr);
-    if (tid == 0) P.seq_ctr[b] = 0;  // ready for the next call
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float sq = __fdiv_rn(fmaxf(amax, 0.01171875f /* 6 * 2^-9 */), 6.0f);
+    const __nv_fp8_storage_t sb = __nv_cvt_float_to_fp8(sq, __NV_SATFINITE, __NV_E4M3);
+    const float scl = e4m3_value(sb);
+    const float qv = act ? __fdiv_rn(y, scl) : 0.0f;
+    const float qo = __shfl_xor_sync(0xffffffffu, qv, 1);
+    const uint32_t c2 = (lane & 1) ? e2m1x2(qo, qv) : e2m1x2(qv, qo);  // element 2i in the low nibble
+    y = bf16_round(e2m1_value((lane & 1) ? (c2 >> 4) : (c2 & 15u)) * scl);
+    if (act && P.out.codes && !(lane & 1)) P.out.codes[b * (Hs / 2) + f / 2] = (uint8_t)c2;
+    if (act && P.out.scales && (lane & 15) == 0) P.out.scales[b * (Hs / 16) + f / 16] = sb;
   }
+  if (act) P.out.latent[b * Hs + f] = bf16_bits(y);
 }
 
 }  // namespace dtc
@@ -422,10 +635,15 @@ int decode_tc_slices(const csa_compressor* c) {
   return ks;
 }
 
-bool decode_tc_supported(const csa_compressor* c, const void* x) {
+bool decode_tc_supported(const csa_compressor* c, const void* x, int B) {
   const int fc = c->H < dtc::kFinChunk ? c->H : dtc::kFinChunk;
-  return c->pk.tw == dtc::kRows && c->dim % dtc::kKb == 0 && ((uintptr_t)x & 15) == 0 && c->H % 16 == 0 &&
-         c->H % fc == 0 && fc % c->pk.ft == 0 && tcx::get_encode() != nullptr;
+  return B <= dtc::kMaxFinB && c->pk.tw == dtc::kRows && c->dim % dtc::kKb == 0 && ((uintptr_t)x & 15) == 0 && c->H % 16 == 0 &&
+         c->H % fc == 0 && c->H / fc <= dtc::kMaxChunks && fc % c->pk.ft == 0 && tcx::get_encode() != nullptr;
+}
+
+cudaError_t invalidate_decode_acc(const csa_compressor* c, int first, int count, cudaStream_t s) {
+  if (count <= 0) return cudaSuccess;
+  return cudaMemsetAsync(c->dec_acc_pos + first, 0xFF, (size_t)count * sizeof(int), s);
 }
 
 cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, const int32_t* start_pos,
@@ -438,6 +656,14 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(decode_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // both kernels ask for the largest shared-memory carveout, so that finish CTAs can share an
+    // SM with a projection CTA
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_proj_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_finish_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr = true;
   }
@@ -464,6 +690,18 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  CUtensorMap mp;
+  {
+    // the partial sums: [ks][B][ncol] f32, stored as boxes of 128 columns x 128 tokens
+    cuuint64_t dims[3] = {(cuuint64_t)c->pk.cols(), (cuuint64_t)B, (cuuint64_t)ks};
+    cuuint64_t strides[2] = {(cuuint64_t)c->pk.cols() * 4, (cuuint64_t)B * c->pk.cols() * 4};
+    cuuint32_t box[3] = {kRows, kTok, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (encode(&mp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, (void*)part, dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   {
@@ -482,7 +720,7 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
     at[0].val.programmaticStreamSerializationAllowed = early_start ? 1 : 0;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_proj_kernel, mw, mx, P);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_proj_kernel, mw, mx, mp, P);
     if (e != cudaSuccess) return e;
   }
   {
@@ -492,8 +730,6 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
     P.ncol = c->pk.cols();
     P.fc = c->H < kFinChunk ? c->H : kFinChunk;
     P.nchunk = c->H / P.fc;
-    P.pooled = c->dec_pooled;
-    P.seq_ctr = c->dec_counters;
     P.part = part;
     P.flag = c->dev_flag;
     P.start_pos = start_pos;
@@ -505,14 +741,22 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
     P.ep = epi_params(c);
     P.out = out;
     P.emitted = emitted;
+    P.acc = c->dec_acc;
+    P.acc_pos = c->dec_acc_pos;
+    cudaLaunchAttribute fa[2];
+    fa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    fa[0].val.programmaticStreamSerializationAllowed = 1;
+    fa[1].id = cudaLaunchAttributeClusterDimension;
+    fa[1].val.clusterDim.x = P.nchunk;
+    fa[1].val.clusterDim.y = 1;
+    fa[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(B, P.nchunk, 1);
+    cfg.gridDim = dim3(P.nchunk, B, 1);
     cfg.blockDim = dim3(kFinThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.attrs = fa;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, decode_finish_kernel, P);
     if (e != cudaSuccess) return e;
   }

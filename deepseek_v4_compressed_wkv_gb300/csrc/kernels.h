@@ -30,7 +30,10 @@ cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B,
 // (split over K, partial sums to `part`), then one CTA per sequence for the reduction into its
 // state slot, the pool and the epilogue.  `early_start` lets the projection fetch its weights
 // before the preceding kernel in the stream has finished.
-bool decode_tc_supported(const csa_compressor* c, const void* x);
+bool decode_tc_supported(const csa_compressor* c, const void* x, int B);
+// Marks the decode running values of sequences [first, first + count) as not valid (their state
+// slots were rewritten by something other than the tensor-core decode).
+cudaError_t invalidate_decode_acc(const csa_compressor* c, int first, int count, cudaStream_t s);
 int decode_tc_slices(const csa_compressor* c);
 cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, const int32_t* start_pos,
                              float* part, int nslices, const csa_out& out, uint8_t* emitted, bool early_start,

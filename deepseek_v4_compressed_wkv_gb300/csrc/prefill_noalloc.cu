@@ -75,6 +75,8 @@ extern "C" int csa_compress_prefill_noalloc(csa_compressor* c, const uint16_t* x
   // the array keeps the previous call's contents: the counters must start at zero
   if (cudaMemsetAsync(counters, 0, nctr * sizeof(int), s) != cudaSuccess)
     return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: clearing the counters failed");
+  if (csa::invalidate_decode_acc(c, slot_offset, B, s) != cudaSuccess)
+    return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: marking the decode running values failed");
   csa_out o = out ? *out : csa_out{nullptr, nullptr, nullptr, nullptr};
   if (csa::launch_prefill_tc(c, x, B, N, slot_offset, o, base, counters, s) != cudaSuccess)
     return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: kernel launch failed");

@@ -472,3 +472,58 @@ def test_decode_steps_in_a_cuda_graph():
     graph.replay()
     torch.cuda.synchronize()
     _check_steps(pairs, seed, sp0, steps, outs)
+
+
+def test_decode_rollback_and_reset_between_steps():
+    """Positions decoded a second time with other tokens (a rollback), and the state reset and
+    partly prefilled again mid-stream: each decode emits what the oracle emits from the same
+    state.
+    (The non-overlapped decode keeps running softmax values of the open group between calls;
+    they must not outlive a change of the state slots they summarise.)"""
+    seed, B = 31, 24
+    layers = [DECODE_PAIR[1], synthetic.Layer(512, 256, 8, 0, 1.0 / 22, gate_scale=2.0, rope_dim=64, fp4=1,
+                                              weight_stream=5)]
+    got, ref = [[], []], [[], []]
+    for li, layer in enumerate(layers):
+        sp0, (pair,) = _decode_setup(seed, [layer], B, 97)
+        g, o = pair
+
+        def step(k, salt=0):
+            sp = (sp0 + k).astype(np.int32)
+            xt = to_bf16_bits(np.stack([synthetic.tokens(seed + salt, b, int(sp[b]), int(sp[b]) + 1, layer.dim)[0]
+                                        for b in range(B)]))
+            r = o.decode(xt, sp)
+            d = g.decode(dev_bits(xt), torch.from_numpy(sp).to(DEV))
+            em = d["emitted"].cpu().numpy()
+            assert np.array_equal(em, r["emitted"]), (li, k, salt)
+            rows = np.flatnonzero(em)
+            if rows.size:
+                got[li].append(to_np(d, rows=rows))
+                ref[li].append(r["prequant"][rows])
+
+        for k in range(10):
+            step(k)
+        for k in range(4, 14):  # roll back six positions, other tokens
+            step(k, salt=1)
+        # reset every slot, bring half of the sequences back to their start positions; the
+        # other half continues from the reset state
+        half = B // 2
+        g.state_reset()
+        o.state_reset()
+        for b in range(half):
+            s = int(sp0[b])
+            t0 = csa.state_window_start(s, layer.ratio, layer.overlap)
+            if s > t0:
+                xb = to_bf16_bits(synthetic.tokens(seed, b, t0, s, layer.dim))[None]
+                o.prefill(xb, slot_offset=b)
+                g.prefill(dev_bits(xb), slot_offset=b, prequant=False)
+        for k in range(0, 2 * layer.ratio):
+            step(k, salt=2)
+        kg, sg = (t.cpu().numpy() for t in g.state_export())
+        ko, so = o.state()
+        assert np.allclose(kg, ko, rtol=2e-5, atol=2e-5 * np.abs(ko).max(initial=1.0))
+        assert g.device_status() == 0
+    for li in range(2):
+        assert got[li], li
+        merged = {kk: np.concatenate([gd[kk] for gd in got[li]]) for kk in got[li][0]}
+        check_entries(merged, np.concatenate(ref[li]), 1, f"rollback/reset layer {li}")
