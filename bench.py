@@ -41,6 +41,10 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--decode-steps", type=int, default=64)
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="run and print only the decode measurement (for profiling)")
+    ap.add_argument("--decode-layers", type=int, default=0,
+                    help="layer instances rotated in the decode measurement (0: enough to exceed L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clock-seconds", type=float, default=1.0,
                     help="seconds of untimed steps run under the clock sampler before the timed region")
@@ -271,7 +275,7 @@ def bench_decode(args, torch, csa, synthetic, device, peaks, world, rank):
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 128 << 20)
     w_bytes = sum(2 * L.width * L.dim * 4 for L in wl.layers)
-    n_layers = max(2, math.ceil(2.5 * l2 / w_bytes))
+    n_layers = args.decode_layers or max(2, math.ceil(2.5 * l2 / w_bytes))
     sp0 = synthetic.start_positions(wl.seed, B, wl.start_pos_hi)
     layers = []
     for li in range(n_layers):
@@ -426,6 +430,16 @@ def main():
             print(json.dumps(line), flush=True)
         return
     rank, world, local = dist_setup(args.gpus)
+    if args.decode_only:
+        import torch
+
+        import deepseek_v4_compressed_wkv_gb300 as csa
+        import synthetic
+        torch.cuda.set_device(local)
+        d = bench_decode(args, torch, csa, synthetic, torch.device("cuda", local), load_peaks(), world, rank)
+        if rank == 0:
+            print(json.dumps({"decode": d}), flush=True)
+        return
     line = run_ours(args, rank, world, local)
     if rank == 0:
         if not args.no_cpu_baseline:

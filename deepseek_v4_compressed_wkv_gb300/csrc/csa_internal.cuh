@@ -41,6 +41,23 @@ inline __host__ __device__ Packing make_packing(int H, int overlap) {
   return p;
 }
 
+// Tiled layout of the three bf16 weight planes used by the tensor-core kernels.  For packed
+// tile t (128 rows) and K block kb (32 columns) the three planes' 128 x 32 blocks follow each
+// other (24 KB, plane-major), each stored as the image a 64-byte-swizzled shared-memory tile
+// has: row r at byte 64 r, its 16-byte chunk c at chunk position c ^ ((r >> 1) & 3).  One
+// contiguous copy of 24 KB then fills a pipeline stage with operands the MMA reads directly.
+constexpr int kPlaneTileRows = 128, kPlaneTileK = 32;
+__host__ __device__ inline size_t plane_tile_elem(int nkb, int pr, int k, int p) {
+  const int t = pr / kPlaneTileRows, r = pr % kPlaneTileRows, kb = k / kPlaneTileK, kk = k % kPlaneTileK;
+  const int c = kk >> 3, e = kk & 7;
+  const size_t block = ((size_t)t * nkb + kb) * 3 + p;
+  return block * (kPlaneTileRows * kPlaneTileK) + r * kPlaneTileK + ((c ^ ((r >> 1) & 3)) << 3) + e;
+}
+// The stage of (tile t, K block kb): 3 planes x 128 x 32 bf16.
+__host__ __device__ inline size_t plane_stage_elem(int nkb, int t, int kb) {
+  return ((size_t)t * nkb + kb) * 3 * (kPlaneTileRows * kPlaneTileK);
+}
+
 // Kernel-side view of the epilogue parameters.
 struct EpiParams {
   const float* gain;      // [H]
@@ -206,7 +223,7 @@ struct csa_compressor {
   int device;
   bool weights_set;
   float* w_packed;  // [2C][dim] f32, packed column order
-  __nv_bfloat16* w_planes;  // [3][2C][dim] bf16 split planes (w = p0 + p1 + p2), packed order
+  __nv_bfloat16* w_planes;  // 3 bf16 split planes (w = p0 + p1 + p2), tiled (plane_tile_elem)
   float* gain;              // [H]
   float* rope_cos;          // [max_pos][rope_dim/2]
   float* rope_sin;

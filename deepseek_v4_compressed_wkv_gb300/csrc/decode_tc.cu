@@ -19,22 +19,20 @@
 //    slice into L2) before it waits for the preceding kernel; the tokens, and every write,
 //    come after that wait.
 //
-//  * decode_finish_kernel, a cluster of CTAs per sequence, one per chunk of 128 features: adds
-//    the K slices' partial sums in slice order (a deterministic split-K reduction) into the
-//    token's state slot, applies the restart at position 0, and where the token completed a
-//    group pools the chunk's features over the group's candidates ("Pool token pairs", decode
-//    branch; "Compressed Sparse Attention - ratio m = 4", decode rule) and runs the entry
-//    epilogue (bf16, RMSNorm, RoPE, fp4) with the RMSNorm's sum of squares exchanged through
-//    distributed shared memory.  The candidates from earlier calls are pooled before the wait
-//    for the projection, while it still runs.
+//  * decode_finish_kernel, one CTA per sequence: adds the K slices' partial sums in slice order
+//    (a deterministic split-K reduction) into the token's state slot, applies the restart at
+//    position 0, and where the token completed a group pools every feature over the group's
+//    candidates ("Pool token pairs", decode branch; "Compressed Sparse Attention - ratio m =
+//    4", decode rule) and runs the entry epilogue (bf16, RMSNorm, RoPE, fp4).  The candidates
+//    from earlier calls are combined before the wait for the projection, while it still runs;
+//    non-overlapped groups keep running softmax values from call to call instead of re-reading
+//    their earlier tokens.  One CTA per sequence fits on an SM beside a projection CTA.
 //
 // Each launch lets the next one start as soon as all of its CTAs have begun: the finish kernel
 // at once, the projection right after its own wait.  A CTA only ever waits for a launch whose
 // CTAs have all started, so the chain cannot deadlock whatever the occupancy.
 #include <cuda.h>
 #include <cudaTypedefs.h>
-
-#include <cooperative_groups.h>
 
 #include "csa_internal.cuh"
 #include "kernels.h"
@@ -49,12 +47,13 @@ constexpr int kRows = 128;                              // packed rows per tile 
 constexpr int kTok = 128;                               // tokens per CTA (MMA N)
 constexpr int kKb = 64;                                 // K granularity of the slice split
 constexpr int kKs = 32;                                 // K per stage (one 64-byte swizzle row of bf16)
-constexpr int kStages = 5;
+constexpr int kStages = 4;
 constexpr int kChunkSteps = 4;                          // stages per accumulator chunk (K = 128)
 constexpr int kPlaneBytes = kRows * kKs * 2;            // 8 KB
+static_assert(kRows == kPlaneTileRows && kKs == kPlaneTileK, "a stage is one tile of the plane layout");
 constexpr int kXBytes = kTok * kKs * 2;                 // 8 KB
 constexpr int kStageBytes = 3 * kPlaneBytes + kXBytes;  // 32 KB
-constexpr int kRingBytes = kStages * kStageBytes;       // 160 KB
+constexpr int kRingBytes = kStages * kStageBytes;       // 128 KB
 constexpr int kPartBytes = kTok * kRows * 4;            // one CTA's partial sums, staged in the ring
 static_assert(kPartBytes <= kRingBytes, "the partial tile is staged in the free ring");
 constexpr int kEpiThreads = 256;
@@ -63,6 +62,7 @@ constexpr int kTmemCols = 2 * kTok;
 constexpr int kFinThreads = 128;  // one warp per SM sub-partition: fits beside a projection CTA
 
 struct ProjParams {
+  const __nv_bfloat16* w;  // weight planes, tiled (plane_tile_elem)
   int nkb_total, ks;  // K blocks (of 64) of dim, number of K slices
   int B;              // tokens of the call
   int ncol;           // packed columns (rows of one weight plane)
@@ -71,8 +71,8 @@ struct ProjParams {
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_proj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
-                       const __grid_constant__ CUtensorMap map_p, const ProjParams P) {
+    decode_proj_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_p,
+                       const ProjParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* full = (uint64_t*)(smem + kRingBytes);
@@ -101,7 +101,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    prefetch_map(&map_w);
     prefetch_map(&map_x);
     prefetch_map(&map_p);
   }
@@ -114,16 +113,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       const int npre = min(nstep, kStages);
-      const int wrow = tile * kRows;
+      const uint64_t stream_pol = l2_evict_first();  // every weight is read once per call
+      const int nkb32 = P.nkb_total * (kKb / kKs), kb0 = k0 / kKs;
+      const __nv_bfloat16* wt = P.w + plane_stage_elem(nkb32, tile, kb0);  // this slice's stages, contiguous
+      constexpr int kW = 3 * kPlaneBytes;
       // weights of the first stages into the ring, the rest of the slice into L2
       for (int t = 0; t < npre; ++t) {
-        uint8_t* st = smem + t * kStageBytes;
         mbar_arrive_expect_tx(&full[t], kStageBytes);
-        for (int p = 0; p < 3; ++p)
-          tma_load_2d(st + p * kPlaneBytes, &map_w, k0 + t * kKs, p * P.ncol + wrow, &full[t]);
+        bulk_load_hint(smem + t * kStageBytes, wt + (size_t)t * (kW / 2), kW, &full[t], stream_pol);
       }
-      for (int t = npre; t < nstep; ++t)
-        for (int p = 0; p < 3; ++p) tma_prefetch_l2_2d(&map_w, k0 + t * kKs, p * P.ncol + wrow);
+      for (int t = npre; t < nstep; ++t) bulk_prefetch_l2_hint(wt + (size_t)t * (kW / 2), kW, stream_pol);
       griddep_wait();  // the tokens may come from the preceding kernel
       griddep_launch_dependents();
       for (int t = 0; t < npre; ++t)
@@ -133,8 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&empty[s], ((t / kStages) - 1) & 1, abort_flag)) break;
         uint8_t* st = smem + s * kStageBytes;
         mbar_arrive_expect_tx(&full[s], kStageBytes);
-        for (int p = 0; p < 3; ++p)
-          tma_load_2d(st + p * kPlaneBytes, &map_w, k0 + t * kKs, p * P.ncol + wrow, &full[s]);
+        bulk_load_hint(st, wt + (size_t)t * (kW / 2), kW, &full[s], stream_pol);
         tma_load_2d(st + 3 * kPlaneBytes, &map_x, k0 + t * kKs, tb, &full[s]);
       }
     }
@@ -203,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_sync(1, kEpiThreads);
     if (threadIdx.x == 64) {
       griddep_wait();  // the preceding finish kernel may still be reading this scratch
-      tma_store_3d(&map_p, stg, tile * kRows, tb, ks);
+      tma_store_3d_hint(&map_p, stg, tile * kRows, tb, ks, l2_evict_last());  // read back by the finish kernel
       bulk_commit();
       bulk_wait_read();
     }
@@ -220,7 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 struct FinParams {
   int B, ks, ncol;
-  int fc, nchunk;            // features per chunk (whole tiles), chunks per token (the cluster)
+  int order;                 // 1: CTAs take the sequences emitting ones first (more CTAs than SMs)
+  int stage_floats;          // partial-sum rows staged per round (a multiple of ncol)
   const float* part;         // [ks][B][ncol]
   int* flag;
   const int32_t* start_pos;  // [B]
@@ -250,11 +249,11 @@ __device__ __forceinline__ float comp(const float4& v, int e) {
   return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
 }
 
-constexpr int kFinChunk = 128;  // features per finish CTA (a whole number of packed tiles)
-constexpr int kMaxChunks = 8;   // chunks per token: H <= 1024
-constexpr int kPoolUnroll = 4;  // candidates in flight per thread
-constexpr int kMaxFinB = 4096;  // sequences per call (the emitting-first order is built in shared memory)
-constexpr int kStageFloats = 6144;  // partial-sum rows staged per round (24 KB)
+constexpr int kPoolUnroll = 4;          // candidates in flight per thread
+constexpr int kMaxFinB = 4096;          // sequences per call (the emitting-first order is built in shared memory)
+constexpr int kFinGroups = 1;           // feature groups of four per thread: H <= 4 * kFinThreads (head_dim <= 512)
+constexpr int kFinColGroups = 4;        // column groups of four per thread: ncol <= 4 * 4 * kFinThreads
+constexpr int kFinSmemFloats = 22528;   // dynamic shared memory (88 KB): staged partial sums + the token's row
 
 // Waits for the phase of `parity` at most kWaitNs; false on time-out.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
@@ -272,8 +271,9 @@ __device__ __forceinline__ bool emits(const FinParams& P, int p) {
 }
 
 // The t-th sequence in the order "emitting sequences, then the others", each by index.  CTAs
-// start in index order, so the ones with pooling to do start first, beside the projection that
-// is still running.  All threads call it; ew is shared scratch of (B + 31) / 32 words.
+// start in index order, so with more sequences than SMs the ones with pooling to do start
+// first, beside the projection that is still running.  All threads call it; ew is shared
+// scratch of (B + 31) / 32 words.
 __device__ int nth_in_emit_order(const FinParams& P, int t, unsigned* ew, int* s_b) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
   const int nw = (P.B + 31) >> 5;
@@ -322,17 +322,11 @@ __device__ int nth_in_emit_order(const FinParams& P, int t, unsigned* ew, int* s
   return *s_b;
 }
 
-// Pools candidates [i0, i1) of the open group(s) for features f .. f+3 with a running maximum.
+// Pools candidates [i0, i1) for features f .. f+3 with a running maximum, into (m, den, num).
 // cand(i) gives the state row and the score and kv columns of candidate i.
 template <class Cand>
 __device__ __forceinline__ void pool_range(const float* st, int ncol, int i0, int i1, Cand cand, float m[4],
                                            float den[4], float num[4]) {
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    m[e] = -INFINITY;
-    den[e] = 0.0f;
-    num[e] = 0.0f;
-  }
   for (int ib = i0; ib < i1; ib += kPoolUnroll) {
     float4 sv[kPoolUnroll], kv[kPoolUnroll];
 #pragma unroll
@@ -368,44 +362,45 @@ __device__ __forceinline__ void pool_range(const float* st, int ncol, int i0, in
   }
 }
 
-// Cluster of nchunk CTAs per sequence (the sequence nth_in_emit_order(blockIdx.y)); CTA j takes
-// the features [j * fc, (j + 1) * fc), whose packed columns are the contiguous range
-// [j * cw, (j + 1) * cw), cw = fc * nk.
+// One CTA per sequence; thread t takes the features of groups t, t + 128 (four adjacent
+// features, i.e. four adjacent packed columns of each kind).
 //
 // The token of this call always completes the open group last, so every other candidate sits in
 // a state slot written by work that completed before this launch could start (the projection
-// before it only lets it start once its own wait has returned): before its wait a CTA combines
-// them into a running (maximum, denominator, numerator) per feature.  Overlapped (8 candidates)
-// it pools the 7 earlier ones when the token completes a group; otherwise it takes the open
-// group's running values kept from the previous call (acc), or rebuilds them from the state
-// slots when they are not for the previous position.  It also stages the gain and the RoPE row
-// of an emitted entry.  After the wait it adds the token's partial sums into its state slot,
-// folds the token in, keeps the running values (otherwise) or, when the group completes, runs
-// the epilogue, the chunks' sums of squares for the RMSNorm exchanged across the cluster
-// through distributed shared memory.
-__global__ void __launch_bounds__(kFinThreads, 8) decode_finish_kernel(const FinParams P) {
-  namespace cg = cooperative_groups;
-  constexpr int kGrp = 4 * kFinThreads;  // group rows x features of the running values
-  __shared__ float sm_m[kGrp], sm_d[kGrp], sm_n[kGrp];
-  __shared__ float cur[4 * kFinChunk];  // the token's columns of this chunk
-  __shared__ float wss[kFinThreads / 32];
-  __shared__ float gn[kFinChunk];
-  __shared__ float rcs[kFinChunk / 2], rsn[kFinChunk / 2];  // RoPE pairs of the chunk's features
-  __shared__ float ssq[kMaxChunks];
-  __shared__ __align__(16) float pst[kStageFloats];  // staged partial-sum rows
+// before it only lets it start once its own wait has returned).  Before its wait a CTA
+// therefore combines them into a running (maximum, denominator, numerator) per feature:
+// overlapped (8 candidates) it pools the 7 earlier ones when the token completes a group;
+// otherwise it takes the open group's running values kept from the previous call (acc), or
+// rebuilds them from the state slots when they are not for the previous position.  It also
+// loads the gain and RoPE factors of an emitted entry.  After the wait the sequence's rows of
+// the K slices' partial sums arrive by bulk copy and are added in slice order into its state
+// slot; the token is folded in, and the running values are kept (open group) or the entry
+// epilogue runs (completed group: bf16, RMSNorm, RoPE, fp4).
+__global__ void __launch_bounds__(kFinThreads, 5) decode_finish_kernel(const FinParams P) {
+  extern __shared__ __align__(16) float fsm[];  // [stage_floats] staged rows, then [ncol] the token's row
   __shared__ __align__(8) uint64_t rbar_s;
+  __shared__ float wss[kFinThreads / 32];
   __shared__ unsigned ew[kMaxFinB / 32];
   __shared__ int s_b;
-
-  const Packing& pk = P.pk;
-  const int j = blockIdx.x, tid = threadIdx.x, nthr = blockDim.x;
-  const int ncol = P.ncol, fc = P.fc, cw = fc * pk.nk, c0 = j * cw, f0 = j * fc, H = pk.H;
+  float* pst = fsm;
+  float* cur = fsm + P.stage_floats;
   uint64_t* rbar = &rbar_s;
+
+  griddep_launch_dependents();  // the next launch may take the SMs this grid leaves free
+  const Packing& pk = P.pk;
+  const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  const int ncol = P.ncol, H = pk.H, nfg = H / 4;
   if (tid == 0) {
     mbar_init(rbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  const int b = nth_in_emit_order(P, blockIdx.y, ew, &s_b);
+  int b;
+  if (P.order) {
+    b = nth_in_emit_order(P, blockIdx.x, ew, &s_b);
+  } else {
+    b = blockIdx.x;
+    __syncthreads();
+  }
   const int p = P.start_pos[b];
   const int pp = max(p, 0);
   const int slot = P.overlap ? ((pp >> 2) & 1) * 4 + (pp & 3) : pp % P.ratio;
@@ -415,205 +410,223 @@ __global__ void __launch_bounds__(kFinThreads, 8) decode_finish_kernel(const Fin
   const long long pos = (long long)p + 1 - P.ratio;
   const bool pool = emits(P, p);
   float* acc = P.acc + (size_t)b * 3 * H;
+  const int hr = P.ep.rope_dim >> 1;
+  const int r0 = H - P.ep.rope_dim;  // even: H is a multiple of 16 and rope_dim is even
 
-  // -- the earlier candidates, as ngr rows of running values per feature
-  const int nfg = fc / 4;
-  int ngr = 0;
-  if (P.overlap) {
-    if (pool) {
-      ngr = max(1, min(nthr / nfg, 7));
-      const int g = tid / nfg, f = f0 + 4 * (tid % nfg);
-      if (g < ngr) {
-        float m[4], den[4], num[4];
-        pool_range(st, ncol, g * 7 / ngr, (g + 1) * 7 / ngr,
+  // -- before the wait: the earlier candidates, as running values per feature
+  float m[kFinGroups][4], den[kFinGroups][4], num[kFinGroups][4];
+  float gn[kFinGroups][4], rc[kFinGroups][2], rs[kFinGroups][2];
+#pragma unroll
+  for (int gi = 0; gi < kFinGroups; ++gi)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      m[gi][e] = -INFINITY;
+      den[gi][e] = 0.0f;
+      num[gi][e] = 0.0f;
+    }
+  const bool open = !P.overlap && pp % P.ratio != 0;  // running values of an open group to continue
+  const bool use_acc = open && P.acc_pos[b] == p - 1;
+#pragma unroll
+  for (int gi = 0; gi < kFinGroups; ++gi) {
+    const int g = tid + gi * nthr;
+    if (g >= nfg) continue;
+    const int f = 4 * g;
+    if (P.overlap) {
+      if (pool)
+        pool_range(st, ncol, 0, 7,
                    [&](int i, int& srow, int& cs, int& ck) {
                      const bool prevB = i < 4;  // the previous group's branch B, then this group's A
                      srow = prevB ? 4 * (1 - q) + i : 4 * q + i - 4;
                      cs = pk.col(prevB ? S_B : S_A, f);
                      ck = pk.col(prevB ? KV_B : KV_A, f);
                    },
-                   m, den, num);
+                   m[gi], den[gi], num[gi]);
+    } else if (use_acc) {
+      const float4 a0 = __ldcg(reinterpret_cast<const float4*>(acc + f));
+      const float4 a1 = __ldcg(reinterpret_cast<const float4*>(acc + H + f));
+      const float4 a2 = __ldcg(reinterpret_cast<const float4*>(acc + 2 * H + f));
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          sm_m[g * fc + f - f0 + e] = m[e];
-          sm_d[g * fc + f - f0 + e] = den[e];
-          sm_n[g * fc + f - f0 + e] = num[e];
-        }
+      for (int e = 0; e < 4; ++e) {
+        m[gi][e] = comp(a0, e);
+        den[gi][e] = comp(a1, e);
+        num[gi][e] = comp(a2, e);
       }
+    } else if (open) {  // rebuild from the state slots of the open group
+      pool_range(st, ncol, 0, pp % P.ratio,
+                 [&](int i, int& srow, int& cs, int& ck) {
+                   srow = i;
+                   cs = pk.col(S, f);
+                   ck = pk.col(KV, f);
+                 },
+                 m[gi], den[gi], num[gi]);
     }
-  } else if (pp % P.ratio != 0) {
-    const int nprev = pp % P.ratio;
-    if (P.acc_pos[b] == p - 1) {
-      ngr = 1;
-      for (int ff = tid; ff < fc; ff += nthr) {
-        sm_m[ff] = __ldcg(acc + f0 + ff);
-        sm_d[ff] = __ldcg(acc + H + f0 + ff);
-        sm_n[ff] = __ldcg(acc + 2 * H + f0 + ff);
-      }
-    } else {  // rebuild from the state slots of the open group
-      ngr = max(1, min(nthr / nfg, nprev));
-      const int g = tid / nfg, f = f0 + 4 * (tid % nfg);
-      if (g < ngr) {
-        float m[4], den[4], num[4];
-        pool_range(st, ncol, (int)((long long)g * nprev / ngr), (int)((long long)(g + 1) * nprev / ngr),
-                   [&](int i, int& srow, int& cs, int& ck) {
-                     srow = i;
-                     cs = pk.col(S, f);
-                     ck = pk.col(KV, f);
-                   },
-                   m, den, num);
+    if (pool) {  // the epilogue's gain and RoPE factors
+      const float4 gg = __ldg(reinterpret_cast<const float4*>(P.ep.gain + f));
+      gn[gi][0] = gg.x;
+      gn[gi][1] = gg.y;
+      gn[gi][2] = gg.z;
+      gn[gi][3] = gg.w;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          sm_m[g * fc + f - f0 + e] = m[e];
-          sm_d[g * fc + f - f0 + e] = den[e];
-          sm_n[g * fc + f - f0 + e] = num[e];
-        }
+      for (int u = 0; u < 2; ++u) {
+        const int k = (f + 2 * u - r0) >> 1;
+        rc[gi][u] = (hr > 0 && f + 2 * u >= r0) ? __ldg(P.ep.rope_cos + pos * hr + k) : 1.0f;
+        rs[gi][u] = (hr > 0 && f + 2 * u >= r0) ? __ldg(P.ep.rope_sin + pos * hr + k) : 0.0f;
       }
     }
   }
-  const int hr = P.ep.rope_dim >> 1;
-  const int r0 = H - P.ep.rope_dim;  // even: H is a multiple of 16 and rope_dim is even
-  const int kb = (max(f0, r0) - r0) >> 1;  // first RoPE pair of the chunk
-  if (pool) {  // the epilogue's gain and the chunk's part of the RoPE row
-    for (int ff = tid; ff < fc; ff += nthr) gn[ff] = __ldg(P.ep.gain + f0 + ff);
-    for (int k = kb + tid; k < hr && 2 * k + r0 < f0 + fc; k += nthr) {
-      rcs[k - kb] = __ldg(P.ep.rope_cos + pos * hr + k);
-      rsn[k - kb] = __ldg(P.ep.rope_sin + pos * hr + k);
-    }
-  }
 
-  griddep_launch_dependents();  // the next launch may take the SMs this grid leaves free
-  griddep_wait();               // the partial sums of the projection are complete
+  griddep_wait();  // the partial sums of the projection are complete
 
-  // -- the K-slice partial sums into the state slot: the chunk's row of every slice arrives by
-  //    bulk copy (all in flight at once, as many slices per round as the staging holds), then
-  //    thread i adds column group i over the slices in order
+  // -- the K-slice partial sums: the sequence's row of every slice arrives by bulk copy (all in
+  //    flight at once, as many slices per round as the staging holds), then thread t adds
+  //    column groups t, t + 128, ... over the slices in order
   {
-    const int nit = cw / 4;
-    const int per_round = max(1, kStageFloats / cw);
-    const float* src = P.part + (size_t)b * ncol + c0;
+    const int ncg = ncol / 4;
+    const int per_round = P.stage_floats / ncol;
+    const float* src = P.part + (size_t)b * ncol;
     const size_t kstride = (size_t)P.B * ncol;
-    float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    float4 a[kFinColGroups];
+#pragma unroll
+    for (int i = 0; i < kFinColGroups; ++i) a[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     int round = 0;
     for (int k0 = 0; k0 < P.ks; k0 += per_round, ++round) {
       const int nr = min(per_round, P.ks - k0);
       if (tid == 0) {
-        mbar_arrive_expect_tx(rbar, (uint32_t)(nr * cw * 4));
-        for (int r = 0; r < nr; ++r) bulk_load(pst + r * cw, src + (size_t)(k0 + r) * kstride, cw * 4, rbar);
+        mbar_arrive_expect_tx(rbar, (uint32_t)(nr * ncol * 4));
+        const uint64_t once = l2_evict_first();  // the partial sums are dead once read
+        for (int r = 0; r < nr; ++r)
+          bulk_load_hint(pst + r * ncol, src + (size_t)(k0 + r) * kstride, ncol * 4, rbar, once);
       }
       if (!wait_bounded(rbar, round & 1)) atomicOr(P.flag, 4);
-      if (tid < nit)
-        for (int r = 0; r < nr; ++r) add4(a, reinterpret_cast<const float4*>(pst + r * cw)[tid]);
+      const float4* pst4 = reinterpret_cast<const float4*>(pst);
+#pragma unroll
+      for (int i = 0; i < kFinColGroups; ++i) {
+        const int cg = tid + i * nthr;
+        if (cg >= ncg) continue;
+        for (int r0 = 0; r0 < nr; r0 += 8) {  // eight rows in flight, added in order
+          float4 v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v[u] = r0 + u < nr ? pst4[(r0 + u) * ncg + cg] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) add4(a[i], v[u]);
+        }
+      }
       __syncthreads();  // the staging is free for the next round
     }
-    if (tid < nit) {
-      *reinterpret_cast<float4*>(cur + 4 * tid) = a;
-      // an emitting CTA stores the slot after its cluster barrier, so that the barrier has no
-      // global stores to wait for
-      if (!pool) *reinterpret_cast<float4*>(st + (size_t)slot * ncol + c0 + 4 * tid) = a;
-    }
-  }
-  if (!pool) {
-    // -- restart at position 0: the previous group's branch is the padded one
-    if (p == 0 && P.overlap)
-      for (int i = tid; i < 4 * cw; i += nthr) {
-        const int r = i / cw, c = c0 + i % cw;
-        st[(size_t)(4 + r) * ncol + c] = padded_kind_value(pk, c);
-      }
-    if (tid == 0 && j == 0) {
-      P.emitted[b] = 0;
-      if (p < 0) atomicOr(P.flag, 1);
-      if (emit) atomicOr(P.flag, 2);
-      if (!P.overlap) P.acc_pos[b] = p >= 0 ? p : -1;
-    }
-    if (P.overlap) return;  // the same for every CTA of the cluster
-  }
-  __syncthreads();
-
-  // -- fold the token itself in (the last candidate), the rows merged in a fixed order; thread
-  //    ff takes feature f0 + ff
-  const bool act = tid < fc;
-  const int f = f0 + tid;
-  float pv = 0.0f;
-  if (act) {
-    const float sc = cur[pk.col(P.overlap ? S_A : S, f) - c0];
-    const float kc = cur[pk.col(P.overlap ? KV_A : KV, f) - c0];
-    float M = sc;
-    for (int k = 0; k < ngr; ++k) M = fmaxf(M, sm_m[k * fc + tid]);
-    float D = 0.0f, Nn = 0.0f;
-    for (int k = 0; k < ngr; ++k) {
-      const float mk = sm_m[k * fc + tid];
-      if (mk == -INFINITY) continue;  // a row of padded candidates adds nothing
-      const float w = expf(mk - M);
-      D = fmaf(sm_d[k * fc + tid], w, D);
-      Nn = fmaf(sm_n[k * fc + tid], w, Nn);
-    }
-    const float ex = expf(sc - M);
-    D += ex;
-    Nn = fmaf(ex, kc, Nn);
-    if (pool) {
-      pv = __fdiv_rn(Nn, D);
-    } else {  // the open group's running values for the next call
-      acc[f] = M;
-      acc[H + f] = D;
-      acc[2 * H + f] = Nn;
-    }
-  }
-  if (!pool) return;  // the same for every CTA of the cluster
-
-  // -- epilogue, one thread per feature: bf16, the chunk's sum of squares (warps in order),
-  //    exchanged across the cluster and added in chunk order, then RMSNorm, RoPE (the pair
-  //    partner is the neighbouring lane) and the fp4 round trip (a block of 16 features is a
-  //    half warp)
-  cg::cluster_group cluster = cg::this_cluster();
-  const int lane = tid & 31, warp = tid >> 5;
-  const float v = act ? bf16_round(pv) : 0.0f;
-  const float ws = warp_sum(v * v);
-  if (lane == 0) wss[warp] = ws;
-  __syncthreads();
-  if (tid == 0) {
-    float t = 0.0f;
-    for (int w = 0; w < (nthr >> 5); ++w) t += wss[w];
-    for (int r = 0; r < P.nchunk; ++r) cluster.map_shared_rank(ssq, r)[j] = t;
-  }
-  cluster.sync();
-  // the stores held back until the barrier
-  if (tid < cw / 4)
-    *reinterpret_cast<float4*>(st + (size_t)slot * ncol + c0 + 4 * tid) = *reinterpret_cast<const float4*>(cur + 4 * tid);
-  if (tid == 0 && j == 0) {
-    P.emitted[b] = 1;
-    if (!P.overlap) P.acc_pos[b] = p;
-  }
-  float tot = 0.0f;
-  for (int r = 0; r < P.nchunk; ++r) tot += ssq[r];
-  const float inv = rms_inv(tot, P.ep);
-  float y = act ? bf16_round(v * inv * gn[tid]) : 0.0f;
-  const float partner = __shfl_xor_sync(0xffffffffu, y, 1);
-  if (act && P.ep.rope_dim > 0 && f >= r0) {
-    const int k = ((f - r0) >> 1) - kb;
-    const float c = rcs[k], sn = rsn[k];
-    if ((f & 1) == 0)
-      y = bf16_round(y * c - partner * sn);  // a' = a cos - b sin
-    else
-      y = bf16_round(partner * sn + y * c);  // b' = a sin + b cos
-  }
-  const size_t Hs = H;
-  if (act && P.out.prequant) P.out.prequant[b * Hs + f] = bf16_bits(y);
-  if (P.ep.fp4) {
-    float amax = fabsf(y);
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float sq = __fdiv_rn(fmaxf(amax, 0.01171875f /* 6 * 2^-9 */), 6.0f);
-    const __nv_fp8_storage_t sb = __nv_cvt_float_to_fp8(sq, __NV_SATFINITE, __NV_E4M3);
-    const float scl = e4m3_value(sb);
-    const float qv = act ? __fdiv_rn(y, scl) : 0.0f;
-    const float qo = __shfl_xor_sync(0xffffffffu, qv, 1);
-    const uint32_t c2 = (lane & 1) ? e2m1x2(qo, qv) : e2m1x2(qv, qo);  // element 2i in the low nibble
-    y = bf16_round(e2m1_value((lane & 1) ? (c2 >> 4) : (c2 & 15u)) * scl);
-    if (act && P.out.codes && !(lane & 1)) P.out.codes[b * (Hs / 2) + f / 2] = (uint8_t)c2;
-    if (act && P.out.scales && (lane & 15) == 0) P.out.scales[b * (Hs / 16) + f / 16] = sb;
+    for (int i = 0; i < kFinColGroups; ++i) {
+      const int cg = tid + i * nthr;
+      if (cg < ncg) {
+        reinterpret_cast<float4*>(cur)[cg] = a[i];
+        reinterpret_cast<float4*>(st + (size_t)slot * ncol)[cg] = a[i];
+      }
+    }
   }
-  if (act) P.out.latent[b * Hs + f] = bf16_bits(y);
+  // -- restart at position 0: the previous group's branch is the padded one
+  if (p == 0 && P.overlap)
+    for (int i = tid; i < 4 * ncol; i += nthr) st[(size_t)4 * ncol + i] = padded_kind_value(pk, i % ncol);
+  if (tid == 0) {
+    P.emitted[b] = pool ? 1 : 0;
+    if (p < 0) atomicOr(P.flag, 1);
+    if (emit && !pool) atomicOr(P.flag, 2);
+    if (!P.overlap) P.acc_pos[b] = p >= 0 ? p : -1;
+  }
+  if (P.overlap && !pool) return;
+  __syncthreads();  // the token's row is complete in shared memory
+
+  // -- fold the token itself in (the last candidate); keep the running values of an open group,
+  //    or finish the entry
+  float pv[kFinGroups][4];
+#pragma unroll
+  for (int gi = 0; gi < kFinGroups; ++gi) {
+    const int g = tid + gi * nthr;
+    if (g >= nfg) continue;
+    const int f = 4 * g;
+    const float4 sc4 = *reinterpret_cast<const float4*>(cur + pk.col(P.overlap ? S_A : S, f));
+    const float4 kc4 = *reinterpret_cast<const float4*>(cur + pk.col(P.overlap ? KV_A : KV, f));
+    float M[4], D[4], Nn[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float sc = comp(sc4, e), kc = comp(kc4, e), mk = m[gi][e];
+      M[e] = fmaxf(mk, sc);
+      const float w = mk == -INFINITY ? 0.0f : expf(mk - M[e]);  // earlier candidates, rescaled
+      const float ex = expf(sc - M[e]);
+      D[e] = fmaf(den[gi][e], w, ex);
+      Nn[e] = fmaf(num[gi][e], w, ex * kc);
+      pv[gi][e] = __fdiv_rn(Nn[e], D[e]);
+    }
+    if (!pool && !P.overlap) {  // the open group's running values for the next call
+      reinterpret_cast<float4*>(acc + f)[0] = make_float4(M[0], M[1], M[2], M[3]);
+      reinterpret_cast<float4*>(acc + H + f)[0] = make_float4(D[0], D[1], D[2], D[3]);
+      reinterpret_cast<float4*>(acc + 2 * H + f)[0] = make_float4(Nn[0], Nn[1], Nn[2], Nn[3]);
+    }
+  }
+  if (!pool) return;
+
+  // -- the entry epilogue: bf16, the sum of squares over the CTA (warps, then in warp order),
+  //    RMSNorm, RoPE (pairs within a thread), the fp4 round trip (a block of 16 features is
+  //    four adjacent threads)
+  float v[kFinGroups][4];
+  float ss = 0.0f;
+#pragma unroll
+  for (int gi = 0; gi < kFinGroups; ++gi)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[gi][e] = (tid + gi * nthr < nfg) ? bf16_round(pv[gi][e]) : 0.0f;
+      ss = fmaf(v[gi][e], v[gi][e], ss);
+    }
+  ss = warp_sum(ss);
+  if (lane == 0) wss[warp] = ss;
+  __syncthreads();
+  float tot = 0.0f;
+  for (int w = 0; w < (nthr >> 5); ++w) tot += wss[w];
+  const float inv = rms_inv(tot, P.ep);
+  const size_t Hs = H;
+#pragma unroll
+  for (int gi = 0; gi < kFinGroups; ++gi) {
+    const int g = tid + gi * nthr;
+    const bool act = g < nfg;  // the same for the four threads of a block of 16
+    const int f = 4 * g;
+    float y[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) y[e] = bf16_round(v[gi][e] * inv * gn[gi][e]);
+    if (act && P.ep.rope_dim > 0) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (f + 2 * u >= r0) {
+          const float a = y[2 * u], bb = y[2 * u + 1], c = rc[gi][u], sn = rs[gi][u];
+          y[2 * u] = bf16_round(a * c - bb * sn);
+          y[2 * u + 1] = bf16_round(a * sn + bb * c);
+        }
+      }
+    }
+    if (act && P.out.prequant)
+      *reinterpret_cast<uint2*>(P.out.prequant + b * Hs + f) =
+          make_uint2((uint32_t)bf16_bits(y[0]) | ((uint32_t)bf16_bits(y[1]) << 16),
+                     (uint32_t)bf16_bits(y[2]) | ((uint32_t)bf16_bits(y[3]) << 16));
+    if (P.ep.fp4) {
+      float amax = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(y[e]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      const float sq = __fdiv_rn(fmaxf(amax, 0.01171875f /* 6 * 2^-9 */), 6.0f);
+      const __nv_fp8_storage_t sb = __nv_cvt_float_to_fp8(sq, __NV_SATFINITE, __NV_E4M3);
+      const float scl = e4m3_value(sb);
+      const uint32_t c0 = e2m1x2(__fdiv_rn(y[0], scl), __fdiv_rn(y[1], scl));  // element 2i in the low nibble
+      const uint32_t c1 = e2m1x2(__fdiv_rn(y[2], scl), __fdiv_rn(y[3], scl));
+      y[0] = bf16_round(e2m1_value(c0 & 15u) * scl);
+      y[1] = bf16_round(e2m1_value(c0 >> 4) * scl);
+      y[2] = bf16_round(e2m1_value(c1 & 15u) * scl);
+      y[3] = bf16_round(e2m1_value(c1 >> 4) * scl);
+      if (act && P.out.codes) *reinterpret_cast<uint16_t*>(P.out.codes + b * (Hs / 2) + f / 2) = (uint16_t)(c0 | (c1 << 8));
+      if (act && P.out.scales && (g & 3) == 0) P.out.scales[b * (Hs / 16) + f / 16] = sb;
+    }
+    if (act)
+      *reinterpret_cast<uint2*>(P.out.latent + b * Hs + f) =
+          make_uint2((uint32_t)bf16_bits(y[0]) | ((uint32_t)bf16_bits(y[1]) << 16),
+                     (uint32_t)bf16_bits(y[2]) | ((uint32_t)bf16_bits(y[3]) << 16));
+  }
 }
 
 }  // namespace dtc
@@ -636,9 +649,10 @@ int decode_tc_slices(const csa_compressor* c) {
 }
 
 bool decode_tc_supported(const csa_compressor* c, const void* x, int B) {
-  const int fc = c->H < dtc::kFinChunk ? c->H : dtc::kFinChunk;
-  return B <= dtc::kMaxFinB && c->pk.tw == dtc::kRows && c->dim % dtc::kKb == 0 && ((uintptr_t)x & 15) == 0 && c->H % 16 == 0 &&
-         c->H % fc == 0 && c->H / fc <= dtc::kMaxChunks && fc % c->pk.ft == 0 && tcx::get_encode() != nullptr;
+  using namespace dtc;
+  return B <= kMaxFinB && c->pk.tw == kRows && c->dim % kKb == 0 && ((uintptr_t)x & 15) == 0 && c->H % 16 == 0 &&
+         c->H <= 4 * kFinGroups * kFinThreads && c->pk.cols() <= 4 * kFinColGroups * kFinThreads &&
+         2 * c->pk.cols() <= kFinSmemFloats && tcx::get_encode() != nullptr;
 }
 
 cudaError_t invalidate_decode_acc(const csa_compressor* c, int first, int count, cudaStream_t s) {
@@ -664,21 +678,13 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(decode_finish_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kFinSmemFloats * (int)sizeof(float));
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  CUtensorMap mw, mx;
-  {
-    // the three bf16 weight planes: [3 * ncol rows][dim], K innermost
-    cuuint64_t dims[2] = {(cuuint64_t)c->dim, (cuuint64_t)3 * c->pk.cols()};
-    cuuint64_t strides[1] = {(cuuint64_t)c->dim * 2};
-    cuuint32_t box[2] = {kKs, kRows};
-    cuuint32_t es[2] = {1, 1};
-    if (encode(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)c->w_planes, dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  CUtensorMap mx;
   {
     // the tokens: [B rows][dim]; rows past B in the last 128-token block read as zeros
     cuuint64_t dims[2] = {(cuuint64_t)c->dim, (cuuint64_t)B};
@@ -706,6 +712,7 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   {
     ProjParams P;
+    P.w = c->w_planes;
     P.nkb_total = c->dim / kKb;
     P.ks = ks;
     P.B = B;
@@ -720,16 +727,22 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
     at[0].val.programmaticStreamSerializationAllowed = early_start ? 1 : 0;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_proj_kernel, mw, mx, mp, P);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_proj_kernel, mx, mp, P);
     if (e != cudaSuccess) return e;
   }
   {
     FinParams P;
+    static int sms = 0;
+    if (!sms) {
+      int dev = 0;
+      cudaGetDevice(&dev);
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
+    }
     P.B = B;
     P.ks = ks;
     P.ncol = c->pk.cols();
-    P.fc = c->H < kFinChunk ? c->H : kFinChunk;
-    P.nchunk = c->H / P.fc;
+    P.order = B > sms;
+    P.stage_floats = min(ks, max(1, (kFinSmemFloats - P.ncol) / P.ncol)) * P.ncol;
     P.part = part;
     P.flag = c->dev_flag;
     P.start_pos = start_pos;
@@ -743,20 +756,14 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
     P.emitted = emitted;
     P.acc = c->dec_acc;
     P.acc_pos = c->dec_acc_pos;
-    cudaLaunchAttribute fa[2];
-    fa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    fa[0].val.programmaticStreamSerializationAllowed = 1;
-    fa[1].id = cudaLaunchAttributeClusterDimension;
-    fa[1].val.clusterDim.x = P.nchunk;
-    fa[1].val.clusterDim.y = 1;
-    fa[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(P.nchunk, B, 1);
+    cfg.gridDim = dim3(B, 1, 1);
     cfg.blockDim = dim3(kFinThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = (size_t)(P.stage_floats + P.ncol) * sizeof(float);
     cfg.stream = s;
-    cfg.attrs = fa;
-    cfg.numAttrs = 2;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, decode_finish_kernel, P);
     if (e != cudaSuccess) return e;
   }

@@ -11,10 +11,14 @@ namespace csa {
 // ---------------------------------------------------------------------------------------
 // Weight re-layout: logical wkv/wgate [C][dim] -> packed f32 [2C][dim] and three bf16
 // planes whose sum is exactly the f32 weight (each plane takes the next 8 significant bits:
-// w - p0 and w - p0 - p1 are exact in f32, and the last remainder fits a bf16).
+// w - p0 and w - p0 - p1 are exact in f32, and the last remainder fits a bf16), in the tiled
+// layout of plane_tile_elem (only where the tensor-core kernels can run: 128-row packed tiles
+// and dim a multiple of 32).
 __global__ void pack_weights_kernel(const float* __restrict__ wkv, const float* __restrict__ wgate, Packing pk,
                                     int overlap, int dim, float* __restrict__ w_packed,
                                     __nv_bfloat16* __restrict__ planes) {
+  const bool tiled = pk.tw == kPlaneTileRows && dim % kPlaneTileK == 0;
+  const int nkb = dim / kPlaneTileK;
   const int pr = blockIdx.y;  // packed row
   const int tile = pr / pk.tw, within = pr % pk.tw;
   const int kind = within / pk.ft, f = tile * pk.ft + within % pk.ft;
@@ -24,7 +28,6 @@ __global__ void pack_weights_kernel(const float* __restrict__ wkv, const float* 
   else
     src = kind == KV ? wkv : wgate;
   const int row = overlap ? ((kind == KV_B || kind == S_B) ? pk.H + f : f) : f;
-  const size_t plane = (size_t)pk.cols() * dim;
   for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < dim; k += gridDim.x * blockDim.x) {
     const float w = src ? src[(size_t)row * dim + k] : 0.0f;
     const __nv_bfloat16 p0 = __float2bfloat16_rn(w);
@@ -33,9 +36,11 @@ __global__ void pack_weights_kernel(const float* __restrict__ wkv, const float* 
     const float r2 = r1 - __bfloat162float(p1);
     const size_t o = (size_t)pr * dim + k;
     w_packed[o] = w;
-    planes[o] = p0;
-    planes[plane + o] = p1;
-    planes[2 * plane + o] = __float2bfloat16_rn(r2);
+    if (tiled) {
+      planes[plane_tile_elem(nkb, pr, k, 0)] = p0;
+      planes[plane_tile_elem(nkb, pr, k, 1)] = p1;
+      planes[plane_tile_elem(nkb, pr, k, 2)] = __float2bfloat16_rn(r2);
+    }
   }
 }
 

@@ -39,6 +39,7 @@ constexpr int kTok = 256;            // tokens per tile including the halo (MMA 
 constexpr int kKb = 32;              // K elements per stage (one 64-byte swizzle row of bf16)
 constexpr int kStages = 5;
 constexpr int kPlaneBytes = kRows * kKb * 2;          // 8 KB
+static_assert(kRows == kPlaneTileRows && kKb == kPlaneTileK, "a stage is one tile of the plane layout");
 constexpr int kXBytes = kTok * kKb * 2;               // 16 KB
 constexpr int kStageBytes = 3 * kPlaneBytes + kXBytes;  // 40 KB
 constexpr int kSmemStride = kTok + 1;                 // f32 staging row stride (bank-conflict free)
@@ -51,6 +52,7 @@ static_assert(kRows * kSmemStride * 4 <= kStages * kStageBytes, "staging must fi
 
 struct Params {
   int N, K, ratio, overlap, T, GT, halo, ntt, G, ncol, slots, slot_offset;
+  const __nv_bfloat16* w;  // weight planes, tiled (plane_tile_elem)
   Packing pk;
   EpiParams ep;
   csa_out out;
@@ -65,8 +67,7 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" :::
 // ---- the kernel ----------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
-                      const Params P) {
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap map_x, const Params P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* full = (uint64_t*)(smem + kStages * kStageBytes);
@@ -95,7 +96,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     *last_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    prefetch_map(&map_w);
     prefetch_map(&map_x);
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
@@ -113,8 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kb >= kStages && !mbar_wait(&empty[s], ((kb / kStages) & 1) ^ 1, abort_flag)) break;
         uint8_t* st = smem + s * kStageBytes;
         mbar_arrive_expect_tx(&full[s], kStageBytes);
-        for (int p = 0; p < 3; ++p)
-          tma_load_2d(st + p * kPlaneBytes, &map_w, kb * kKb, p * P.ncol + ftile * kRows, &full[s]);
+        bulk_load(st, P.w + plane_stage_elem(P.K / kKb, ftile, kb), 3 * kPlaneBytes, &full[s]);
         tma_load_3d(st + 3 * kPlaneBytes, &map_x, kb * kKb, t0, b, &full[s]);
         ++issued;
       }
@@ -346,18 +345,8 @@ cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B,
   P.counters = counters;
   P.flag = c->dev_flag;
 
-  CUtensorMap mw, mx;
-  {
-    // weights: 3 planes x ncol rows x dim, bf16, K innermost
-    cuuint64_t dims[2] = {(cuuint64_t)c->dim, (cuuint64_t)3 * P.ncol};
-    cuuint64_t strides[1] = {(cuuint64_t)c->dim * 2};
-    cuuint32_t box[2] = {kKb, kRows};
-    cuuint32_t es[2] = {1, 1};
-    if (encode(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)c->w_planes, dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  P.w = c->w_planes;
+  CUtensorMap mx;
   {
     // x: [B][N][dim] bf16; out-of-range tokens (the halo before token 0, the tail past N) read as 0
     cuuint64_t dims[3] = {(cuuint64_t)c->dim, (cuuint64_t)N, (cuuint64_t)B};
@@ -377,7 +366,7 @@ cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B,
     attr_set = true;
   }
   dim3 grid(c->pk.ntiles, P.ntt, B);
-  prefill_tc_kernel<<<grid, kThreads, smem, s>>>(mw, mx, P);
+  prefill_tc_kernel<<<grid, kThreads, smem, s>>>(mx, P);
   return cudaGetLastError();
 }
 
