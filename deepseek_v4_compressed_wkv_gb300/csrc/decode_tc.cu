@@ -61,9 +61,17 @@ constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kTmemCols = 2 * kTok;
 constexpr int kFinThreads = 128;  // one warp per SM sub-partition: fits beside a projection CTA
 
+__device__ __forceinline__ void add4(float4& a, const float4& v) {
+  a.x += v.x;
+  a.y += v.y;
+  a.z += v.z;
+  a.w += v.w;
+}
+
 struct ProjParams {
   const __nv_bfloat16* w;  // weight planes, tiled (plane_tile_elem)
   int nkb_total, ks;  // K blocks (of 64) of dim, number of K slices
+  int cs;             // K slices per cluster, added on chip: 1, 2 or 4 (divides ks and the 128 tokens)
   int B;              // tokens of the call
   int ncol;           // packed columns (rows of one weight plane)
   float* part;        // [ks][B][ncol] partial sums
@@ -193,18 +201,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok && threadIdx.x == 64) atomicOr(P.flag, 4);
     // every MMA has completed and every load has landed: the ring is free.  Stage the partial
-    // sums as [token][packed row] and write them with one TMA store (tokens past B are clipped)
+    // sums as [token][packed row]
     float* stg = reinterpret_cast<float*>(smem);
 #pragma unroll
     for (int i = 0; i < kTok / 2; ++i) stg[((kTok / 2) * h + i) * kRows + row] = acc[i];
-    fence_async_shared();
-    named_sync(1, kEpiThreads);
-    if (threadIdx.x == 64) {
-      griddep_wait();  // the preceding finish kernel may still be reading this scratch
-      tma_store_3d_hint(&map_p, stg, tile * kRows, tb, ks, l2_evict_last());  // read back by the finish kernel
-      bulk_commit();
-      bulk_wait_read();
-    }
   }
 
   tc_fence_before();
@@ -213,6 +213,54 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  // The cs K slices of the cluster are added on chip: CTA r adds tokens [r * 128 / cs, ...) of
+  // the cs staged tiles in slice order (distributed shared memory) and stores that part of the
+  // cluster's partial sums with one TMA store (tokens past B are clipped)
+  const int cs = P.cs, tr = kTok / cs;
+  const int crank = cs > 1 ? (int)cluster_rank() : 0;
+  float* stg = reinterpret_cast<float*>(smem);
+  float* red = cs > 1 ? stg + kTok * kRows : stg + crank * tr * kRows;
+  if (cs > 1) {
+    cluster_arrive();
+    cluster_wait();  // every CTA of the cluster has staged its tile
+    // up to kRedItems items of four floats per thread, every load issued before the additions
+    constexpr int kRedItems = (kTok / 2) * (kRows / 4) / kThreads + 1;  // covers cs >= 2
+    float4 v[kRedItems][4];
+#pragma unroll
+    for (int it = 0; it < kRedItems; ++it) {
+      const int idx = threadIdx.x + it * kThreads;
+      if (idx < tr * (kRows / 4)) {
+        const float* src = stg + (crank * tr + idx / (kRows / 4)) * kRows + 4 * (idx % (kRows / 4));
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q < cs) v[it][q] = ld_cluster_f4(cluster_map(src, q));
+      }
+    }
+#pragma unroll
+    for (int it = 0; it < kRedItems; ++it) {
+      const int idx = threadIdx.x + it * kThreads;
+      if (idx < tr * (kRows / 4)) {
+        float4 a = v[it][0];
+#pragma unroll
+        for (int q = 1; q < 4; ++q)
+          if (q < cs) add4(a, v[it][q]);
+        *reinterpret_cast<float4*>(red + (idx / (kRows / 4)) * kRows + 4 * (idx % (kRows / 4))) = a;
+      }
+    }
+  }
+  fence_async_shared();
+  __syncthreads();
+  if (threadIdx.x == 64) {
+    griddep_wait();  // the preceding finish kernel may still be reading this scratch
+    // read back by the finish kernel
+    tma_store_3d_hint(&map_p, red, tile * kRows, tb + crank * tr, ks / cs, l2_evict_last());
+    bulk_commit();
+    bulk_wait_read();
+  }
+  if (cs > 1) {
+    cluster_arrive();
+    cluster_wait();  // no CTA leaves while another may still read its staged tile
   }
 }
 
@@ -236,13 +284,6 @@ struct FinParams {
 
 __device__ __forceinline__ float padded_kind_value(const Packing& pk, int col) {
   return ((col % pk.tw) / pk.ft) < pk.nk / 2 ? 0.0f : -INFINITY;  // kv kinds first, then scores
-}
-
-__device__ __forceinline__ void add4(float4& a, const float4& v) {
-  a.x += v.x;
-  a.y += v.y;
-  a.z += v.z;
-  a.w += v.w;
 }
 
 __device__ __forceinline__ float comp(const float4& v, int e) {
@@ -643,10 +684,14 @@ int decode_tc_slices(const csa_compressor* c) {
   }
   const int nkb = c->dim / dtc::kKb;
   int ks = sms / c->pk.ntiles;
-  if (ks < 1) ks = 1;
   if (ks > nkb) ks = nkb;
+  if (ks < 1) ks = 1;
+  ks -= ks >= 4 ? ks % 4 : ks % 2;  // whole clusters of K slices (decode_tc_cluster)
   return ks;
 }
+
+// K slices added on chip per cluster: 4 or 2 where they divide the slices, else 1.
+static int decode_tc_cluster(int ks) { return ks % 4 == 0 ? 4 : ks % 2 == 0 ? 2 : 1; }
 
 bool decode_tc_supported(const csa_compressor* c, const void* x, int B) {
   using namespace dtc;
@@ -698,23 +743,25 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
   }
   CUtensorMap mp;
   {
-    // the partial sums: [ks][B][ncol] f32, stored as boxes of 128 columns x 128 tokens
-    cuuint64_t dims[3] = {(cuuint64_t)c->pk.cols(), (cuuint64_t)B, (cuuint64_t)ks};
+    // the partial sums of each cluster of K slices: [ks / cs][B][ncol] f32, stored as boxes of
+    // 128 columns x 128 / cs tokens
+    cuuint64_t dims[3] = {(cuuint64_t)c->pk.cols(), (cuuint64_t)B, (cuuint64_t)(ks / decode_tc_cluster(ks))};
     cuuint64_t strides[2] = {(cuuint64_t)c->pk.cols() * 4, (cuuint64_t)B * c->pk.cols() * 4};
-    cuuint32_t box[3] = {kRows, kTok, 1};
+    cuuint32_t box[3] = {kRows, (cuuint32_t)(kTok / decode_tc_cluster(ks)), 1};
     cuuint32_t es[3] = {1, 1, 1};
     if (encode(&mp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, (void*)part, dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   {
     ProjParams P;
     P.w = c->w_planes;
     P.nkb_total = c->dim / kKb;
     P.ks = ks;
+    P.cs = decode_tc_cluster(ks);
     P.B = B;
     P.ncol = c->pk.cols();
     P.part = part;
@@ -725,8 +772,12 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     at[0].val.programmaticStreamSerializationAllowed = early_start ? 1 : 0;
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = 1;
+    at[1].val.clusterDim.y = P.cs;
+    at[1].val.clusterDim.z = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, decode_proj_kernel, mx, mp, P);
     if (e != cudaSuccess) return e;
   }
@@ -739,10 +790,10 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
       if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
     }
     P.B = B;
-    P.ks = ks;
+    P.ks = ks / decode_tc_cluster(ks);  // partial sums left after the on-chip additions
     P.ncol = c->pk.cols();
     P.order = B > sms;
-    P.stage_floats = min(ks, max(1, (kFinSmemFloats - P.ncol) / P.ncol)) * P.ncol;
+    P.stage_floats = min(P.ks, max(1, (kFinSmemFloats - P.ncol) / P.ncol)) * P.ncol;
     P.part = part;
     P.flag = c->dev_flag;
     P.start_pos = start_pos;
