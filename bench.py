@@ -79,6 +79,30 @@ def max_over_ranks(v, world, device):
     return float(t.item())
 
 
+def profiled_traffic(summary, key):
+    """DRAM bytes (read + write) that an ncu capture measured for a kernel, from its summary under
+    profiles/, or None when the kernel's sources no longer hash as they did at the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", summary)
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            k, _, v = line.strip().partition(": ")
+            if v:
+                fields[k] = v.strip()
+    srcs = {"prefill_tc_flash_csa.md": "prefill_tc.cu", "decode_tc_batched.md": "decode_tc.cu"}[summary]
+    csrc = os.path.join(ROOT, "deepseek_v4_compressed_wkv_gb300", "csrc")
+    m = hashlib.sha256()
+    for fn in (srcs, "tc_common.cuh", "csa_internal.cuh", "kernels.h"):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            m.update(f.read())
+    if m.hexdigest()[:16] != fields.get("sources_sha256_16") or key not in fields:
+        return None
+    return int(fields[key])
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -218,7 +242,8 @@ def run_ours(args, rank, world, local):
     if tc:
         peak = peaks["bf16_tflops"] / 3.0
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None, "kernel": "csa_prefill_tc (projection + fused pool/norm/RoPE/fp4)",
+                "traffic": profiled_traffic("prefill_tc_flash_csa.md", "traffic_bytes_per_launch"),
+                "kernel": "csa_prefill_tc (projection + fused pool/norm/RoPE/fp4)",
                 "peak_basis": f"{peaks['source']} bf16 dense {peaks['bf16_tflops']} TFLOP/s / 3 bf16 passes"}
     else:
         sm_clock = (clk or {}).get("sm_max_mhz") or 2070.0
@@ -358,7 +383,9 @@ def bench_decode(args, torch, csa, synthetic, device, peaks, world, rank):
     return {"steps_per_s": world / (ms * 1e-3) * 1.0, "ms_per_step": ms, "batch": B, "layers_rotated": n_layers,
             "launch": "cuda graph" if graph is not None else "eager",
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes_per_step": alg}}
+                         "frac": gbs / peaks["hbm_gbs"],
+                         "traffic": profiled_traffic("decode_tc_batched.md", "traffic_bytes_per_step"),
+                         "algorithmic_bytes_per_step": alg}}
 
 
 # ---------------------------------------------------------------------------------------------
