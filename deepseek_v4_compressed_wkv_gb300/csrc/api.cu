@@ -269,7 +269,7 @@ int csa_compress_prefill(csa_compressor* c, const uint16_t* x, int B, int N, int
       CSA_CUDA(csa::launch_prefill_tc(c, x, B, N, slot_offset, o, c->scratch, c->tc_counters, s),
                "tensor-core prefill launch");
       if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
-      c->launches += 1;
+      c->launches += G > 0 ? 2 : 1;  // the projection kernel, then the entry kernel
       return G;
     }
     const size_t bytes = (size_t)M * c->pk.cols() * sizeof(float);

@@ -183,6 +183,57 @@ __device__ __forceinline__ void entry_epilogue_block(float v[16], int f0, float 
   dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
+// Epilogue of four adjacent features f..f+3 of entry row `e`, held by one thread, once the
+// RMSNorm factor `inv` is known: v[] holds the bf16-rounded pooled values, gn[] the gain,
+// rc/rs the RoPE cos/sin of the pairs (f, f+1) and (f+2, f+3) (used for pairs at or past
+// H - rope_dim).  RMSNorm with one bf16 rounding, RoPE, then the fp4 round trip, whose block
+// of 16 features is four adjacent lanes (all 32 lanes of the warp must call it; `act` is the
+// same for the four lanes of a block), and the stores.
+__device__ __forceinline__ void entry_epilogue_quad(const float v[4], bool act, int f, int lane, float inv,
+                                                   const float gn[4], const float rc[2], const float rs[2],
+                                                   const EpiParams& ep, size_t e, const csa_out& out) {
+  const size_t H = ep.H;
+  float y[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) y[i] = bf16_round(v[i] * inv * gn[i]);
+  if (act && ep.rope_dim > 0) {
+    const int r0 = ep.H - ep.rope_dim;
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      if (f + 2 * u >= r0) {
+        const float a = y[2 * u], b = y[2 * u + 1];
+        y[2 * u] = bf16_round(a * rc[u] - b * rs[u]);
+        y[2 * u + 1] = bf16_round(a * rs[u] + b * rc[u]);
+      }
+  }
+  if (act && out.prequant)
+    *reinterpret_cast<uint2*>(out.prequant + e * H + f) =
+        make_uint2((uint32_t)bf16_bits(y[0]) | ((uint32_t)bf16_bits(y[1]) << 16),
+                   (uint32_t)bf16_bits(y[2]) | ((uint32_t)bf16_bits(y[3]) << 16));
+  if (ep.fp4) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(y[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float sq = __fdiv_rn(fmaxf(amax, 0.01171875f /* 6 * 2^-9 */), 6.0f);
+    const __nv_fp8_storage_t sb = __nv_cvt_float_to_fp8(sq, __NV_SATFINITE, __NV_E4M3);
+    const float scl = e4m3_value(sb);
+    const uint32_t c0 = e2m1x2(__fdiv_rn(y[0], scl), __fdiv_rn(y[1], scl));  // element 2i in the low nibble
+    const uint32_t c1 = e2m1x2(__fdiv_rn(y[2], scl), __fdiv_rn(y[3], scl));
+    y[0] = bf16_round(e2m1_value(c0 & 15u) * scl);
+    y[1] = bf16_round(e2m1_value(c0 >> 4) * scl);
+    y[2] = bf16_round(e2m1_value(c1 & 15u) * scl);
+    y[3] = bf16_round(e2m1_value(c1 >> 4) * scl);
+    if (act && out.codes) *reinterpret_cast<uint16_t*>(out.codes + e * (H / 2) + f / 2) = (uint16_t)(c0 | (c1 << 8));
+    if (act && out.scales && (lane & 3) == 0) out.scales[e * (H / 16) + f / 16] = sb;
+  }
+  if (act)
+    *reinterpret_cast<uint2*>(out.latent + e * H + f) =
+        make_uint2((uint32_t)bf16_bits(y[0]) | ((uint32_t)bf16_bits(y[1]) << 16),
+                   (uint32_t)bf16_bits(y[2]) | ((uint32_t)bf16_bits(y[3]) << 16));
+}
+
 // RMSNorm factor from the sum of squares of the bf16-rounded pooled values.
 __device__ __forceinline__ float rms_inv(float ss, const EpiParams& ep) {
   return 1.0f / sqrtf(ss / (float)ep.H + ep.eps);

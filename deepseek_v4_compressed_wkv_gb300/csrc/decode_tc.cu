@@ -622,51 +622,10 @@ __global__ void __launch_bounds__(kFinThreads, 5) decode_finish_kernel(const Fin
   float tot = 0.0f;
   for (int w = 0; w < (nthr >> 5); ++w) tot += wss[w];
   const float inv = rms_inv(tot, P.ep);
-  const size_t Hs = H;
 #pragma unroll
   for (int gi = 0; gi < kFinGroups; ++gi) {
     const int g = tid + gi * nthr;
-    const bool act = g < nfg;  // the same for the four threads of a block of 16
-    const int f = 4 * g;
-    float y[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) y[e] = bf16_round(v[gi][e] * inv * gn[gi][e]);
-    if (act && P.ep.rope_dim > 0) {
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        if (f + 2 * u >= r0) {
-          const float a = y[2 * u], bb = y[2 * u + 1], c = rc[gi][u], sn = rs[gi][u];
-          y[2 * u] = bf16_round(a * c - bb * sn);
-          y[2 * u + 1] = bf16_round(a * sn + bb * c);
-        }
-      }
-    }
-    if (act && P.out.prequant)
-      *reinterpret_cast<uint2*>(P.out.prequant + b * Hs + f) =
-          make_uint2((uint32_t)bf16_bits(y[0]) | ((uint32_t)bf16_bits(y[1]) << 16),
-                     (uint32_t)bf16_bits(y[2]) | ((uint32_t)bf16_bits(y[3]) << 16));
-    if (P.ep.fp4) {
-      float amax = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(y[e]));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      const float sq = __fdiv_rn(fmaxf(amax, 0.01171875f /* 6 * 2^-9 */), 6.0f);
-      const __nv_fp8_storage_t sb = __nv_cvt_float_to_fp8(sq, __NV_SATFINITE, __NV_E4M3);
-      const float scl = e4m3_value(sb);
-      const uint32_t c0 = e2m1x2(__fdiv_rn(y[0], scl), __fdiv_rn(y[1], scl));  // element 2i in the low nibble
-      const uint32_t c1 = e2m1x2(__fdiv_rn(y[2], scl), __fdiv_rn(y[3], scl));
-      y[0] = bf16_round(e2m1_value(c0 & 15u) * scl);
-      y[1] = bf16_round(e2m1_value(c0 >> 4) * scl);
-      y[2] = bf16_round(e2m1_value(c1 & 15u) * scl);
-      y[3] = bf16_round(e2m1_value(c1 >> 4) * scl);
-      if (act && P.out.codes) *reinterpret_cast<uint16_t*>(P.out.codes + b * (Hs / 2) + f / 2) = (uint16_t)(c0 | (c1 << 8));
-      if (act && P.out.scales && (g & 3) == 0) P.out.scales[b * (Hs / 16) + f / 16] = sb;
-    }
-    if (act)
-      *reinterpret_cast<uint2*>(P.out.latent + b * Hs + f) =
-          make_uint2((uint32_t)bf16_bits(y[0]) | ((uint32_t)bf16_bits(y[1]) << 16),
-                     (uint32_t)bf16_bits(y[2]) | ((uint32_t)bf16_bits(y[3]) << 16));
+    entry_epilogue_quad(v[gi], g < nfg, 4 * g, lane, inv, gn[gi], rc[gi], rs[gi], P.ep, (size_t)b, P.out);
   }
 }
 

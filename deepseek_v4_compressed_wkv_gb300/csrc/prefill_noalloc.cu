@@ -1,7 +1,7 @@
 // Prefill entry point that allocates no device memory.
 //
-// The ordinary csa_compress_prefill grows its scratch (pooled values and completion
-// counters of the tensor-core kernel) with cudaMalloc on first use.  Some callers cannot
+// The ordinary csa_compress_prefill grows its scratch (the pooled values of the tensor-core
+// kernel) with cudaMalloc on first use.  Some callers cannot
 // allow that: serving runtimes that reserve the whole device memory up front for their own
 // pool (a later cudaMalloc fails, or fragments memory the runtime has already planned), and
 // code that enqueues work while a CUDA graph is being captured on another thread, where
@@ -80,6 +80,6 @@ extern "C" int csa_compress_prefill_noalloc(csa_compressor* c, const uint16_t* x
   csa_out o = out ? *out : csa_out{nullptr, nullptr, nullptr, nullptr};
   if (csa::launch_prefill_tc(c, x, B, N, slot_offset, o, base, counters, s) != cudaSuccess)
     return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: kernel launch failed");
-  c->launches += 1;
+  c->launches += G > 0 ? 2 : 1;
   return G;
 }

@@ -19,9 +19,10 @@
 // Roles (320 threads): warp 0 issues the TMA loads (x tile shared by all three planes, one
 // tile per plane), warp 1 owns TMEM and issues tcgen05.mma, warps 2-9 run the epilogue (warps
 // w and w+4 share TMEM lane quarter w%4 and split the 256 token columns).
-// One CTA computes one (packed tile, token tile); the CTAs of one token tile meet in a global
-// counter, and the last one to finish normalises, rotates and quantises the tile's entries
-// from the pooled values the others left in scratch (the RMSNorm needs all H features).
+// One CTA computes one (packed tile, token tile) and leaves its pooled values in scratch; the
+// entries are then normalised, rotated and quantised by prefill_entry_kernel, one CTA per entry
+// over all SMs (the RMSNorm needs all H features, and one SM finishing a token tile's 63
+// entries alone took about as long as a quarter of the projection).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -54,12 +55,16 @@ struct Params {
   int N, K, ratio, overlap, T, GT, halo, ntt, G, ncol, slots, slot_offset;
   const __nv_bfloat16* w;  // weight planes, tiled (plane_tile_elem)
   Packing pk;
-  EpiParams ep;
-  csa_out out;
   float* state;
   uint16_t* pooled;  // [B][ntt][GT][H] bf16 bits
-  int* counters;     // [B][ntt]
   int* flag;
+};
+
+struct EntryParams {
+  int G, GT, ntt, ratio;
+  const uint16_t* pooled;  // [B][ntt][GT][H] bf16 bits
+  EpiParams ep;
+  csa_out out;
 };
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -76,7 +81,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* chunk_empty = chunk_full + 2;  // [2]: chunk accumulator drained, free for the MMAs
   uint32_t* tmem_slot = (uint32_t*)(chunk_empty + 2);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
-  int* last_flag = (int*)(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ftile = blockIdx.x, tt = blockIdx.y, b = blockIdx.z;
@@ -94,11 +98,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&chunk_empty[i], kEpiThreads / 32);
     }
     *abort_flag = 0;
-    *last_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_map(&map_x);
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  griddep_launch_dependents();  // the entry kernel may be scheduled; it waits for this grid
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -255,39 +259,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         pooled_tile[(size_t)g * pk.H + ftile * F + f] = bf16_bits(__fdiv_rn(num, den));
       }
-      // -- the last CTA of this token tile finishes the entries (RMSNorm needs all features)
-      __threadfence();
-      epi_sync();
-      if (et == 0) {
-        const int prev = atomicAdd(&P.counters[b * P.ntt + tt], 1);
-        *last_flag = prev == pk.ntiles - 1;
-      }
-      epi_sync();
-      if (*last_flag) {
-        __threadfence();
-        const int w = et >> 5;
-        const int ng = min(P.GT, G - tt * P.GT);
-        for (int g = w; g < ng; g += kEpiThreads / 32) {
-          const int j = tt * P.GT + g;
-          float v[16];
-          const int l = min(lane, (pk.H >> 4) - 1);
-          const uint4* src = (const uint4*)(pooled_tile + (size_t)g * pk.H + 16 * l);
-          const uint4 a = __ldcg(src), c = __ldcg(src + 1);
-          const uint32_t wds[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            v[2 * i] = __uint_as_float(wds[i] << 16);
-            v[2 * i + 1] = __uint_as_float(wds[i] & 0xFFFF0000u);
-          }
-          const size_t e = (size_t)b * G + j;
-          const size_t H = pk.H;
-          entry_epilogue(v, lane, (long long)r * j, P.ep, P.out.latent + e * H,
-                         P.out.codes ? P.out.codes + e * (H / 2) : nullptr,
-                         P.out.scales ? P.out.scales + e * (H / 16) : nullptr,
-                         P.out.prequant ? P.out.prequant + e * H : nullptr);
-        }
-        if (et == 0) P.counters[b * P.ntt + tt] = 0;  // ready for the next call
-      }
     }
   }
 
@@ -300,6 +271,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// One CTA of 128 threads per entry (b, j): thread t takes features 4t..4t+3 of its pooled
+// values, then bf16, RMSNorm (the sum of squares over the CTA, warps in order), RoPE and the
+// fp4 round trip (entry_epilogue_quad).  The gain and RoPE factors (written before this launch's
+// predecessor started) are read before the wait for the projection kernel.
+__global__ void __launch_bounds__(128) prefill_entry_kernel(const EntryParams P) {
+  __shared__ float wss[4];
+  const int e = blockIdx.x, t = threadIdx.x, lane = t & 31, f = 4 * t;
+  const int b = e / P.G, j = e % P.G, tt = j / P.GT, g = j % P.GT;
+  const int H = P.ep.H, hr = P.ep.rope_dim >> 1, r0 = H - P.ep.rope_dim;
+  const bool act = f < H;
+  const long long pos = (long long)P.ratio * j;
+  float gn[4] = {0.0f, 0.0f, 0.0f, 0.0f}, rc[2] = {1.0f, 1.0f}, rs[2] = {0.0f, 0.0f};
+  if (act) {
+    const float4 gg = __ldg(reinterpret_cast<const float4*>(P.ep.gain + f));
+    gn[0] = gg.x;
+    gn[1] = gg.y;
+    gn[2] = gg.z;
+    gn[3] = gg.w;
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      if (hr > 0 && f + 2 * u >= r0) {
+        rc[u] = __ldg(P.ep.rope_cos + pos * hr + ((f + 2 * u - r0) >> 1));
+        rs[u] = __ldg(P.ep.rope_sin + pos * hr + ((f + 2 * u - r0) >> 1));
+      }
+  }
+  griddep_wait();  // the pooled values of the projection kernel
+  float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (act) {
+    const uint2 u = __ldcg(reinterpret_cast<const uint2*>(P.pooled + (((size_t)b * P.ntt + tt) * P.GT + g) * H + f));
+    v[0] = __uint_as_float(u.x << 16);
+    v[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(u.y << 16);
+    v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+  }
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) ss = fmaf(v[i], v[i], ss);
+  ss = warp_sum(ss);
+  if (lane == 0) wss[t >> 5] = ss;
+  __syncthreads();
+  const float inv = rms_inv(wss[0] + wss[1] + wss[2] + wss[3], P.ep);
+  entry_epilogue_quad(v, act, f, lane, inv, gn, rc, rs, P.ep, (size_t)e, P.out);
+}
+
 }  // namespace tc
 
 // ---- host side ------------------------------------------------------------------------------
@@ -309,13 +324,13 @@ bool prefill_tc_supported(const csa_compressor* c, const void* x) {
          ((uintptr_t)x & 15) == 0 && tcx::get_encode() != nullptr;
 }
 
-// Bytes of pooled scratch ([B][token tiles][groups per tile][H] bf16) and the number of
-// completion counters ([B][token tiles]) a prefill of B x N tokens needs.
+// Bytes of pooled scratch ([B][token tiles][groups per tile][H] bf16) a prefill of B x N tokens
+// needs; no completion counters (0).
 size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N, size_t* n_counters) {
   const int T = c->overlap ? tc::kTok - 4 : (tc::kTok / c->ratio) * c->ratio;
   const int GT = T / c->ratio;
   const int ntt = (N + T - 1) / T;
-  *n_counters = (size_t)B * ntt;
+  *n_counters = 0;
   return (size_t)B * ntt * GT * c->H * sizeof(uint16_t);
 }
 
@@ -338,12 +353,10 @@ cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B,
   P.slots = c->slots;
   P.slot_offset = slot_offset;
   P.pk = c->pk;
-  P.ep = epi_params(c);
-  P.out = out;
   P.state = c->state;
   P.pooled = (uint16_t*)scratch;
-  P.counters = counters;
   P.flag = c->dev_flag;
+  (void)counters;
 
   P.w = c->w_planes;
   CUtensorMap mx;
@@ -367,7 +380,28 @@ cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B,
   }
   dim3 grid(c->pk.ntiles, P.ntt, B);
   prefill_tc_kernel<<<grid, kThreads, smem, s>>>(mx, P);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || P.G == 0) return e;
+  // the entries: RMSNorm, RoPE and fp4, one CTA each, started early by programmatic dependent
+  // launch (the pooled values are read after its wait)
+  EntryParams Q;
+  Q.G = P.G;
+  Q.GT = P.GT;
+  Q.ntt = P.ntt;
+  Q.ratio = c->ratio;
+  Q.pooled = P.pooled;
+  Q.ep = epi_params(c);
+  Q.out = out;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((long long)B * P.G), 1, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_entry_kernel, Q);
 }
 
 }  // namespace csa
