@@ -3,7 +3,8 @@
 // epilogue.  The pre-pool kv / score values live only in TMEM and shared memory.
 //
 // GEMM orientation: the packed weight rows are the MMA's M side (128 rows = one packed tile:
-// ft features x nk kinds), the tokens its N side (256 per tile), K = dim.  The f32 weights
+// ft features x nk kinds), the tokens its N side (a tile of 256 or 224, whichever fills the
+// SMs in fewer waves), K = dim.  The f32 weights
 // enter as three bf16 planes whose sum is exact (w = p0 + p1 + p2), so three bf16 MMAs into
 // one f32 accumulator give the f32 product (x is bf16, so every partial product is exact):
 // the f32 projection of "Pool token pairs" (x.float(), wkv(x), wgate(x)) and the f32 x . w^T
@@ -36,20 +37,27 @@ namespace tc {
 using namespace tcx;
 
 constexpr int kRows = 128;           // packed rows per tile (MMA M)
-constexpr int kTok = 256;            // tokens per tile including the halo (MMA N)
+constexpr int kTokMax = 256;         // tokens per tile including the halo (MMA N): 256 or 224
 constexpr int kKb = 32;              // K elements per stage (one 64-byte swizzle row of bf16)
 constexpr int kStages = 5;
 constexpr int kPlaneBytes = kRows * kKb * 2;          // 8 KB
 static_assert(kRows == kPlaneTileRows && kKb == kPlaneTileK, "a stage is one tile of the plane layout");
-constexpr int kXBytes = kTok * kKb * 2;               // 16 KB
-constexpr int kStageBytes = 3 * kPlaneBytes + kXBytes;  // 40 KB
-constexpr int kSmemStride = kTok + 1;                 // f32 staging row stride (bank-conflict free)
 constexpr int kChunkKb = 8;         // K blocks per accumulator chunk (K = 256)
 constexpr int kEpiThreads = 256;
 constexpr int kThreads = 64 + kEpiThreads;
-constexpr int kTmemCols = 2 * kTok;  // two chunk accumulators
+constexpr int kTmemCols = 512;      // two chunk accumulators of up to 256 columns (a power of two)
 
-static_assert(kRows * kSmemStride * 4 <= kStages * kStageBytes, "staging must fit in the stage buffers");
+// The sizes that follow from the token tile.  Epilogue warp half h drains token columns
+// [128 h, min(128 h + 128, TOK)).
+template <int TOK>
+struct Tile {
+  static_assert(TOK == 256 || TOK == 224, "token tile");
+  static constexpr int kXBytes = TOK * kKb * 2;                  // 16 KB / 14 KB
+  static constexpr int kStageBytes = 3 * kPlaneBytes + kXBytes;  // 40 KB / 38 KB (multiples of 1 KB)
+  static constexpr int kSmemStride = TOK + 1;                    // f32 staging row stride (bank-conflict free)
+  static_assert(kRows * kSmemStride * 4 <= kStages * kStageBytes, "staging must fit in the stage buffers");
+  static_assert(kStageBytes % 1024 == 0, "stages keep the 1 KB alignment of the swizzled tiles");
+};
 
 struct Params {
   int N, K, ratio, overlap, T, GT, halo, ntt, G, ncol, slots, slot_offset;
@@ -71,8 +79,11 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" :::
 
 // ---- the kernel ----------------------------------------------------------------------------
 
+template <int kTok>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap map_x, const Params P) {
+  constexpr int kStageBytes = Tile<kTok>::kStageBytes;
+  constexpr int kSmemStride = Tile<kTok>::kSmemStride;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* full = (uint64_t*)(smem + kStages * kStageBytes);
@@ -159,13 +170,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---- epilogue (warps 2..9; warp w reads TMEM lanes 32*(w%4) .. +31, columns 128*h .. +127)
+    // ---- epilogue (warps 2..9; warp w reads TMEM lanes 32*(w%4) .. +31, columns 128*h .. up to
+    //      128 columns)
     const int et = threadIdx.x - 64;  // 0..255
     const int q = warp & 3, h = (warp - 2) >> 2;
     const int row = 32 * q + lane;
-    float acc[kTok / 2];
+    const int hcols = h ? kTok - 128 : 128;  // a multiple of 32
+    float acc[128];
 #pragma unroll
-    for (int i = 0; i < kTok / 2; ++i) acc[i] = 0.0f;
+    for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
     bool ok = true;
     for (int c = 0; c < nch; ++c) {
       const int buf = c & 1;
@@ -177,10 +190,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * kTok + 128 * h);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        uint32_t r[32];
-        tmem_ld32(base + 32 * j, r);
+        if (32 * j < hcols) {  // the same for the whole warp
+          uint32_t r[32];
+          tmem_ld32(base + 32 * j, r);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[32 * j + i] += __uint_as_float(r[i]);
+          for (int i = 0; i < 32; ++i) acc[32 * j + i] += __uint_as_float(r[i]);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -191,7 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       float* stg = (float*)smem;  // [128 packed rows][kSmemStride] f32, reuses the stage buffers
 #pragma unroll
-      for (int i = 0; i < kTok / 2; ++i) stg[row * kSmemStride + 128 * h + i] = acc[i];
+      for (int i = 0; i < 128; ++i)
+        if (i < hcols) stg[row * kSmemStride + 128 * h + i] = acc[i];
       epi_sync();
 
       const Packing& pk = P.pk;
@@ -320,22 +336,46 @@ __global__ void __launch_bounds__(128) prefill_entry_kernel(const EntryParams P)
 // ---- host side ------------------------------------------------------------------------------
 
 bool prefill_tc_supported(const csa_compressor* c, const void* x) {
-  return c->pk.tw == tc::kRows && c->dim % tc::kKb == 0 && (c->overlap || c->ratio <= tc::kTok) &&
+  return c->pk.tw == tc::kRows && c->dim % tc::kKb == 0 && (c->overlap || c->ratio <= tc::kTokMax) &&
          ((uintptr_t)x & 15) == 0 && tcx::get_encode() != nullptr;
 }
 
-// Bytes of pooled scratch ([B][token tiles][groups per tile][H] bf16) a prefill of B x N tokens
-// needs; no completion counters (0).
-size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N, size_t* n_counters) {
-  const int T = c->overlap ? tc::kTok - 4 : (tc::kTok / c->ratio) * c->ratio;
-  const int GT = T / c->ratio;
-  const int ntt = (N + T - 1) / T;
-  *n_counters = 0;
-  return (size_t)B * ntt * GT * c->H * sizeof(uint16_t);
+namespace {
+
+// Tokens of a tile owned by it (the overlapped tile also loads the 4 tokens before it).
+int owned_tokens(const csa_compressor* c, int tok) {
+  return c->overlap ? tok - 4 : (tok / c->ratio) * c->ratio;
 }
 
-cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset,
-                              const csa_out& out, void* scratch, int* counters, cudaStream_t s) {
+// The token tile of a launch: the one whose grid takes the fewest waves x tile tokens (one CTA
+// per SM), 256 on a tie.  At the Flash CSA shape the 224-token tile makes 16 x 19 = 304 CTAs,
+// exactly two waves of 152 SMs, where 256 makes 272 (1.79 waves, the second wave a CTA of
+// 256 tokens per SM).
+int prefill_tok(const csa_compressor* c, int B, int N) {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
+  }
+  int best = tc::kTokMax;
+  long long best_cost = -1;
+  for (int tok : {256, 224}) {
+    const int T = owned_tokens(c, tok);
+    if (T < 1) continue;
+    const long long ctas = (long long)c->pk.ntiles * ((N + T - 1) / T) * B;
+    const long long cost = (ctas + sms - 1) / sms * tok;
+    if (best_cost < 0 || cost < best_cost) {
+      best = tok;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+template <int TOK>
+cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset,
+                       const csa_out& out, void* scratch, cudaStream_t s) {
   using namespace tc;
   auto encode = tcx::get_encode();
   if (!encode) return cudaErrorNotSupported;
@@ -345,7 +385,7 @@ cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B,
   P.ratio = c->ratio;
   P.overlap = c->overlap;
   P.halo = c->overlap ? 4 : 0;
-  P.T = c->overlap ? kTok - 4 : (kTok / c->ratio) * c->ratio;
+  P.T = owned_tokens(c, TOK);
   P.GT = P.T / c->ratio;
   P.ntt = (N + P.T - 1) / P.T;
   P.G = N / c->ratio;
@@ -356,30 +396,29 @@ cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B,
   P.state = c->state;
   P.pooled = (uint16_t*)scratch;
   P.flag = c->dev_flag;
-  (void)counters;
-
   P.w = c->w_planes;
   CUtensorMap mx;
   {
     // x: [B][N][dim] bf16; out-of-range tokens (the halo before token 0, the tail past N) read as 0
     cuuint64_t dims[3] = {(cuuint64_t)c->dim, (cuuint64_t)N, (cuuint64_t)B};
     cuuint64_t strides[2] = {(cuuint64_t)c->dim * 2, (cuuint64_t)N * c->dim * 2};
-    cuuint32_t box[3] = {kKb, kTok, 1};
+    cuuint32_t box[3] = {kKb, TOK, 1};
     cuuint32_t es[3] = {1, 1, 1};
     if (encode(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)x, dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const size_t smem = (size_t)kStages * kStageBytes + 1024 /* barriers */ + 1024 /* alignment */;
+  const size_t smem = (size_t)kStages * Tile<TOK>::kStageBytes + 1024 /* barriers */ + 1024 /* alignment */;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(prefill_tc_kernel<TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   dim3 grid(c->pk.ntiles, P.ntt, B);
-  prefill_tc_kernel<<<grid, kThreads, smem, s>>>(mx, P);
+  prefill_tc_kernel<TOK><<<grid, kThreads, smem, s>>>(mx, P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || P.G == 0) return e;
   // the entries: RMSNorm, RoPE and fp4, one CTA each, started early by programmatic dependent
@@ -402,6 +441,25 @@ cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B,
   cfg.attrs = at;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, prefill_entry_kernel, Q);
+}
+
+}  // namespace
+
+// Bytes of pooled scratch ([B][token tiles][groups per tile][H] bf16) a prefill of B x N tokens
+// needs; no completion counters (0).
+size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N, size_t* n_counters) {
+  const int T = owned_tokens(c, prefill_tok(c, B, N));
+  const int GT = T / c->ratio;
+  const int ntt = (N + T - 1) / T;
+  *n_counters = 0;
+  return (size_t)B * ntt * GT * c->H * sizeof(uint16_t);
+}
+
+cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset,
+                              const csa_out& out, void* scratch, int* counters, cudaStream_t s) {
+  (void)counters;
+  return prefill_tok(c, B, N) == 224 ? launch_tok<224>(c, x, B, N, slot_offset, out, scratch, s)
+                                     : launch_tok<256>(c, x, B, N, slot_offset, out, scratch, s);
 }
 
 }  // namespace csa
