@@ -127,17 +127,18 @@ int csa_compress_prefill(csa_compressor* c, const uint16_t* x, int B, int N, int
  * all device memory for their own pool up front, or code that enqueues work while a CUDA
  * graph is being captured.  Same arguments, results and return value as
  * csa_compress_prefill, but the tensor-core kernel's scratch lives in a device array built
- * into the library (16 MiB of pooled values plus 4096 completion counters, held by every GPU
- * that loads the library until the process exits).  It therefore needs:
+ * into the library (16 MiB of pooled values, held by every GPU that loads the library until
+ * the process exits).  It therefore needs:
  *  - a shape that runs the tensor-core kernel (csa_uses_tensor_cores(c) == 1, x 16-byte
  *    aligned); other shapes return CSA_ERR_ARG;
- *  - B * ceil(N / T) * (T / ratio) * head_dim * 2 <= 16 MiB and B * ceil(N / T) <= 4096, with
- *    T = 252 tokens per tile at ratio 4 overlapped, else the largest multiple of ratio
- *    <= 256; larger calls return CSA_ERR_ARG ("too large") without launching anything.
+ *  - B * ceil(N / T) * (T / ratio) * head_dim * 2 <= 16 MiB, with T the tokens a tile owns
+ *    (the launch takes a tile of 224 or 256 tokens: at ratio 4 overlapped T = 220 or 252,
+ *    else the largest multiple of ratio <= the tile); larger calls return CSA_ERR_ARG
+ *    ("too large") without launching anything.
  * The first call on each device looks up the array's device address (with that device
  * current); make that first call before any stream capture.  Every call shares the one
  * array: calls that overlap on the GPU (other streams, other handles) race, so serialise
- * them.  Each call clears the counters it uses before its kernel runs. */
+ * them. */
 int csa_compress_prefill_noalloc(csa_compressor* c, const uint16_t* x, int B, int N, int start_pos,
                                  int slot_offset, const csa_out* out, csa_stream_t stream);
 
