@@ -135,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       griddep_launch_dependents();
       for (int t = 0; t < npre; ++t)
         tma_load_2d(smem + t * kStageBytes + 3 * kPlaneBytes, &map_x, k0 + t * kKs, tb, &full[t]);
+      int issued = npre;
       for (int t = npre; t < nstep; ++t) {
         const int s = t % kStages;
         if (!mbar_wait(&empty[s], ((t / kStages) - 1) & 1, abort_flag)) break;
@@ -142,6 +143,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&full[s], kStageBytes);
         bulk_load_hint(st, wt + (size_t)t * (kW / 2), kW, &full[s], stream_pol);
         tma_load_2d(st + 3 * kPlaneBytes, &map_x, k0 + t * kKs, tb, &full[s]);
+        ++issued;
+      }
+      if (*abort_flag) {  // let the copies already in flight land before the ring is reused or left
+        for (int t = max(0, issued - kStages); t < issued; ++t) {
+          const uint64_t t1 = globaltimer();
+          while (!mbar_try_wait(&full[t % kStages], (t / kStages) & 1) && globaltimer() - t1 < kWaitNs) {
+          }
+        }
       }
     }
   } else if (warp == 1) {
