@@ -252,22 +252,59 @@ def run_ours(args, rank, world, local):
                 "traffic": None, "kernel": "gemm_ffma_kernel (f32 FMA projection)",
                 "peak_basis": f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 flop x {sm_clock:.0f} MHz"}
 
-    # end to end through the public call with host buffers (pinned): H2D of x, prefill, D2H of
-    # latent + codes + scales
+    # end to end through the public call with host buffers (pinned): every step copies its x in
+    # (H2D), runs the prefill and copies latent + codes + scales out (D2H), all inside the timed
+    # region.  As a serving loop would, the steps are pipelined: step i+1's input copy (split over
+    # two copy streams) runs while step i computes, and step i's outputs go back on a third
+    # stream; inputs and outputs are double-buffered.
     x_host = x.cpu().pin_memory()
-    x_dev = torch.empty_like(x)
+    x_dev = [torch.empty_like(x) for _ in range(2)]
+    outs2 = [out, comp._alloc_out(B * G, device, prequant=False)]
     host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items() if v is not None}
-    e2e_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    for _ in range(2):
-        x_dev.copy_(x_host, non_blocking=True)
-        comp.prefill(x_dev, out=out, prequant=False)
+    h2d_streams = [torch.cuda.Stream(device) for _ in range(2)]
+    d2h_stream = torch.cuda.Stream(device)
+    half = x.shape[1] // 2
+
+    def e2e_steps(n):
+        done = [None, None]  # compute of the step that last used buffer 0 / 1
+        outs_done = [None, None]  # D2H of the step that last used output set 0 / 1
+        for i in range(n):
+            j = i % 2
+            copied = []
+            for part, cs in enumerate(h2d_streams):
+                with torch.cuda.stream(cs):
+                    if done[j] is not None:
+                        cs.wait_event(done[j])
+                    sl = slice(0, half) if part == 0 else slice(half, x.shape[1])
+                    x_dev[j][:, sl].copy_(x_host[:, sl], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(cs)
+                    copied.append(ev)
+            for ev in copied:
+                stream.wait_event(ev)
+            if outs_done[j] is not None:
+                stream.wait_event(outs_done[j])
+            comp.prefill(x_dev[j], out=outs2[j], prequant=False)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            done[j] = ev
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(ev)
+                for k, h in host_out.items():
+                    h.copy_(outs2[j][k], non_blocking=True)
+                ev2 = torch.cuda.Event()
+                ev2.record(d2h_stream)
+                outs_done[j] = ev2
+        for cs in h2d_streams + [d2h_stream]:
+            stream.wait_stream(cs)
+
+    e2e_steps(2)
     torch.cuda.synchronize()
+    e2e_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     e2e_ev[0].record(stream)
-    for i in range(K):
-        x_dev.copy_(x_host, non_blocking=True)
-        comp.prefill(x_dev, out=out, prequant=False)
-        for k, h in host_out.items():
-            h.copy_(out[k], non_blocking=True)
+    for cs in h2d_streams + [d2h_stream]:
+        cs.wait_stream(stream)
+    e2e_steps(K)
     e2e_ev[1].record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e2e_ev[0].elapsed_time(e2e_ev[1]), world, device) / K
