@@ -92,7 +92,6 @@ void free_all(csa_compressor* c) {
   cudaFree(c->state);
   cudaFree(c->dev_flag);
   cudaFree(c->scratch);
-  cudaFree(c->tc_counters);
   cudaFree(c->dec_part);
   cudaFree(c->dec_acc);
   cudaFree(c->dec_acc_pos);
@@ -106,18 +105,6 @@ int ensure_scratch(csa_compressor* c, size_t bytes, cudaStream_t s) {
   c->scratch_bytes = 0;
   CSA_CUDA(cudaMalloc(&c->scratch, bytes), "cudaMalloc(scratch)");
   c->scratch_bytes = bytes;
-  return CSA_OK;
-}
-
-int ensure_counters(csa_compressor* c, size_t n, cudaStream_t s) {
-  if (c->tc_counters_n >= n) return CSA_OK;
-  CSA_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
-  cudaFree(c->tc_counters);
-  c->tc_counters = nullptr;
-  c->tc_counters_n = 0;
-  CSA_CUDA(cudaMalloc(&c->tc_counters, n * sizeof(int)), "cudaMalloc(counters)");
-  CSA_CUDA(cudaMemset(c->tc_counters, 0, n * sizeof(int)), "cudaMemset(counters)");
-  c->tc_counters_n = n;
   return CSA_OK;
 }
 
@@ -259,14 +246,12 @@ int csa_compress_prefill(csa_compressor* c, const uint16_t* x, int B, int N, int
     if (M > 0x7fffffffLL) return fail(CSA_ERR_ARG, "B * N too large");
     CSA_CUDA(csa::invalidate_decode_acc(c, slot_offset, B, s), "invalidate decode running values");
     if (csa::prefill_tc_supported(c, x)) {
-      size_t nctr = 0;
-      const size_t bytes = csa::prefill_tc_scratch_bytes(c, B, N, &nctr);
+      const size_t bytes = csa::prefill_tc_scratch_bytes(c, B, N);
       int rc = ensure_scratch(c, bytes, s);
-      if (!rc) rc = ensure_counters(c, nctr, s);
       if (rc) return rc;
       csa_out o = out ? *out : csa_out{nullptr, nullptr, nullptr, nullptr};
       if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
-      CSA_CUDA(csa::launch_prefill_tc(c, x, B, N, slot_offset, o, c->scratch, c->tc_counters, s),
+      CSA_CUDA(csa::launch_prefill_tc(c, x, B, N, slot_offset, o, c->scratch, s),
                "tensor-core prefill launch");
       if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
       c->launches += G > 0 ? 2 : 1;  // the projection kernel, then the entry kernel

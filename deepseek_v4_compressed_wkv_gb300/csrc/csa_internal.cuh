@@ -289,8 +289,6 @@ struct csa_compressor {
   int* dec_acc_pos;         //   position of the last token folded in [max_batch] (-1: not valid)
   bool dec_early_start;     // the next decode may start its weight loads before the preceding
                             // kernel ends (false right after set_weights rewrote the planes)
-  int* tc_counters;         // per token tile completion counters of the tensor-core prefill
-  size_t tc_counters_n;     // (kept at zero between calls by the kernel itself)
   cudaEvent_t prof_start, prof_stop;  // optional events around the dominant kernel
   long long launches;                 // kernels enqueued so far
 };

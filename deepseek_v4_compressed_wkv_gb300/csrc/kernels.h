@@ -22,9 +22,9 @@ cudaError_t launch_fp4_roundtrip(const uint16_t* in, long long nb, uint8_t* code
 
 // Tensor-core prefill (prefill_tc.cu): projection + pool + norm + RoPE + fp4 + state update.
 bool prefill_tc_supported(const csa_compressor* c, const void* x);
-size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N, size_t* n_counters);
+size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N);
 cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset,
-                              const csa_out& out, void* scratch, int* counters, cudaStream_t s);
+                              const csa_out& out, void* scratch, cudaStream_t s);
 
 // Tensor-core decode (decode_tc.cu): two launches, the projection of one token per sequence
 // (split over K, partial sums to `part`), then one CTA per sequence for the reduction into its

@@ -17,9 +17,8 @@ namespace {
 // Largest scratch this entry point can use.  Every GPU that loads the library holds these
 // arrays until the process exits.
 constexpr size_t kPooledBytes = 16u << 20;  // pooled bf16 values: B * token tiles * groups * H * 2
-constexpr size_t kCounters = 4096;          // completion counters: B * token tiles
 
-static __device__ __align__(256) uint8_t g_noalloc_scratch[kPooledBytes + kCounters * sizeof(int)];
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kPooledBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -48,12 +47,11 @@ extern "C" int csa_compress_prefill_noalloc(csa_compressor* c, const uint16_t* x
                              "csa_compress_prefill_noalloc: this shape runs the CUDA-core projection, whose "
                              "scratch is not preallocated (needs 128-row packed tiles, ratio <= 256, 16-byte "
                              "aligned x)");
-  size_t nctr = 0;
-  const size_t bytes = csa::prefill_tc_scratch_bytes(c, B, N, &nctr);
-  if (bytes > kPooledBytes || nctr > kCounters)
+  const size_t bytes = csa::prefill_tc_scratch_bytes(c, B, N);
+  if (bytes > kPooledBytes)
     return csa_internal_fail(CSA_ERR_ARG,
                              "csa_compress_prefill_noalloc: B x N too large for the preallocated scratch "
-                             "(limits: 16 MiB of pooled values, 4096 token tiles)");
+                             "(limit: 16 MiB of pooled values)");
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: no current device");
@@ -70,15 +68,11 @@ extern "C" int csa_compress_prefill_noalloc(csa_compressor* c, const uint16_t* x
     }
     base = g_addr[dev];
   }
-  int* counters = (int*)((uint8_t*)base + kPooledBytes);
   cudaStream_t s = (cudaStream_t)stream;
-  // the array keeps the previous call's contents: the counters must start at zero
-  if (cudaMemsetAsync(counters, 0, nctr * sizeof(int), s) != cudaSuccess)
-    return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: clearing the counters failed");
   if (csa::invalidate_decode_acc(c, slot_offset, B, s) != cudaSuccess)
     return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: marking the decode running values failed");
   csa_out o = out ? *out : csa_out{nullptr, nullptr, nullptr, nullptr};
-  if (csa::launch_prefill_tc(c, x, B, N, slot_offset, o, base, counters, s) != cudaSuccess)
+  if (csa::launch_prefill_tc(c, x, B, N, slot_offset, o, base, s) != cudaSuccess)
     return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: kernel launch failed");
   c->launches += G > 0 ? 2 : 1;
   return G;

@@ -446,18 +446,16 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
 }  // namespace
 
 // Bytes of pooled scratch ([B][token tiles][groups per tile][H] bf16) a prefill of B x N tokens
-// needs; no completion counters (0).
-size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N, size_t* n_counters) {
+// needs.
+size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N) {
   const int T = owned_tokens(c, prefill_tok(c, B, N));
   const int GT = T / c->ratio;
   const int ntt = (N + T - 1) / T;
-  *n_counters = 0;
   return (size_t)B * ntt * GT * c->H * sizeof(uint16_t);
 }
 
 cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset,
-                              const csa_out& out, void* scratch, int* counters, cudaStream_t s) {
-  (void)counters;
+                              const csa_out& out, void* scratch, cudaStream_t s) {
   return prefill_tok(c, B, N) == 224 ? launch_tok<224>(c, x, B, N, slot_offset, out, scratch, s)
                                      : launch_tok<256>(c, x, B, N, slot_offset, out, scratch, s);
 }
