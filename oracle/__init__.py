@@ -66,6 +66,7 @@ def _load():
             "oracle_set_weights": ([P, P, P, P], None),
             "oracle_prefill": ([P, P, I, I, I, P, P, P, P, I], I),
             "oracle_prefill_groups": ([P, P, I, P, I, P, P, P, P, I], I),
+            "oracle_prefill_chunk": ([P, P, I, I, I, I, P, P, P, P, I], I),
             "oracle_decode": ([P, P, I, P, P, P, P, P, P, I], I),
             "oracle_state_reset": ([P], None), "oracle_state_elems": ([P], I64),
             "oracle_state_export": ([P, P, P], None),
@@ -202,14 +203,15 @@ class Compressor:
         return (np.zeros((n, H), np.uint16), np.zeros((n, H // 2), np.uint8), np.zeros((n, H // 16), np.uint8),
                 np.zeros((n, H), np.uint16))
 
-    def prefill(self, x_bf16, slot_offset=0, nthreads=None):
-        """x uint16 [B, N, dim] -> dict(latent [B,G,H], codes, scales, prequant, G)."""
+    def prefill(self, x_bf16, slot_offset=0, nthreads=None, start_pos=0):
+        """x uint16 [B, N, dim] (tokens start_pos .. start_pos+N-1 of each sequence) ->
+        dict(latent [B,G,H], codes, scales, prequant, G), G the groups completing in the chunk."""
         x = np.ascontiguousarray(x_bf16, np.uint16)
         B, N, _ = x.shape
-        G = N // self.ratio
+        G = (start_pos + N) // self.ratio - start_pos // self.ratio
         lat, cd, sc, pq = self._outs(max(B * G, 1))
-        g = self._lib.oracle_prefill(self.h, _ptr(x), B, N, slot_offset, _ptr(lat), _ptr(cd), _ptr(sc), _ptr(pq),
-                                     nthreads or default_threads())
+        g = self._lib.oracle_prefill_chunk(self.h, _ptr(x), B, N, start_pos, slot_offset, _ptr(lat), _ptr(cd),
+                                           _ptr(sc), _ptr(pq), nthreads or default_threads())
         if g < 0:
             raise ValueError("oracle_prefill rejected the arguments")
         H = self.H

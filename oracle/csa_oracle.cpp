@@ -454,6 +454,82 @@ int oracle_prefill_groups(const oracle_compressor* c, const uint16_t* x, int N, 
   return ng;
 }
 
+// A prefill chunk that starts at start_pos > 0 (every sequence at the same position): the N
+// tokens continue sequences whose earlier tokens went through prefill, chunks or decode.
+// The pages define prefill only at start_pos 0 and decode one token at a time; [CSA4]
+// "Prefill and decode use the same rule" fixes what a chunk must compute: the entries of the
+// groups that complete inside [start_pos, start_pos + N), each pooled over its candidates
+// whatever call projected them, and a state that later calls can continue from.  Candidates
+// of earlier calls are read from the state slots the decode rule puts them in (non-overlapped:
+// slot p % r; ratio 4 overlapped: parity (p / 4) % 2, slot p % 4).  The state then receives,
+// as [V41]'s prefill branch does for its remainder, the new tokens of the unfinished group and
+// (overlapped) of the last complete group; no other slot changes.  start_pos 0 is the prefill.
+// Entries go to latent [B][G][H] etc., G = (start_pos + N) / r - start_pos / r.
+int oracle_prefill_chunk(oracle_compressor* c, const uint16_t* x, int B, int N, int start_pos, int slot_offset,
+                         uint16_t* latent, uint8_t* codes, uint8_t* scales, uint16_t* prequant, int nthreads) {
+  if (start_pos == 0) return oracle_prefill(c, x, B, N, slot_offset, latent, codes, scales, prequant, nthreads);
+  if (!c || B < 1 || N < 1 || start_pos < 0 || slot_offset < 0 || slot_offset + B > c->opt.max_batch ||
+      c->wkv.empty())
+    return -1;
+  const int H = c->H, W = c->width(), r = c->ratio, D = c->dim, sw = c->slot_width();
+  const int64_t p0 = start_pos, p1 = p0 + N;
+  const int64_t g_first = p0 / r, g_end = p1 / r, G = g_end - g_first;
+  const int ncand = c->overlap ? 8 : r;
+  auto slot_of = [&](int64_t p) { return c->overlap ? (int)(4 * ((p / 4) % 2) + p % 4) : (int)(p % r); };
+  std::vector<float> kvp((int64_t)N * W), sp((int64_t)N * W);
+  for (int b = 0; b < B; ++b) {
+    const int sb = slot_offset + b;
+    const uint16_t* xs = x + (int64_t)b * N * D;
+    oracle_linear(xs, N, D, c->wkv.data(), W, kvp.data(), nthreads);
+    oracle_linear(xs, N, D, c->wgate.data(), W, sp.data(), nthreads);
+    // the kv / score row (W columns) of token p: this call's projection, or its state slot
+    auto kv_row = [&](int64_t p) -> const float* {
+      return p >= p0 ? &kvp[(p - p0) * W] : state_row(c->kv_state, c, sb, slot_of(p));
+    };
+    auto sc_row = [&](int64_t p) -> const float* {
+      return p >= p0 ? &sp[(p - p0) * W] : state_row(c->score_state, c, sb, slot_of(p));
+    };
+    parallel_for(G, nthreads, [&](int64_t jj) {
+      const int64_t g = g_first + jj;
+      std::vector<float> kv((int64_t)ncand * H), sc((int64_t)ncand * H), pooled(H);
+      for (int i = 0; i < (c->overlap ? 4 : r); ++i)
+        for (int h = 0; h < H; ++h) {
+          if (!c->overlap) {
+            kv[i * H + h] = kv_row(r * g + i)[h];
+            sc[i * H + h] = sc_row(r * g + i)[h];
+            continue;
+          }
+          if (g == 0) {  // [CSA4] padded previous branch
+            kv[i * H + h] = 0.0f;
+            sc[i * H + h] = -std::numeric_limits<float>::infinity();
+          } else {  // branch B (columns H..2H-1) of the previous group's tokens
+            kv[i * H + h] = kv_row(4 * g - 4 + i)[H + h];
+            sc[i * H + h] = sc_row(4 * g - 4 + i)[H + h];
+          }
+          kv[(4 + i) * H + h] = kv_row(4 * g + i)[h];  // branch A of the group's own tokens
+          sc[(4 + i) * H + h] = sc_row(4 * g + i)[h];
+        }
+      oracle_pool(kv.data(), sc.data(), ncand, H, pooled.data(), nullptr);
+      const int64_t e = (int64_t)b * G + jj;
+      finish_entry(c, pooled.data(), r * g, latent ? latent + e * H : nullptr, codes ? codes + e * H / 2 : nullptr,
+                   scales ? scales + e * H / 16 : nullptr, prequant ? prequant + e * H : nullptr);
+    });
+    // state: the new tokens of the unfinished group g_end and, overlapped, of group g_end - 1
+    const int64_t keep_from = std::max(p0, (g_end - c->overlap) * r);
+    for (int64_t p = keep_from; p < p1; ++p) {
+      std::memcpy(state_row(c->kv_state, c, sb, slot_of(p)), &kvp[(p - p0) * W], sw * 4);
+      std::memcpy(state_row(c->score_state, c, sb, slot_of(p)), &sp[(p - p0) * W], sw * 4);
+    }
+    if (c->overlap && g_end == 0)  // no complete group yet: the previous branch stays padded
+      for (int i = 0; i < 4; ++i)
+        for (int h = 0; h < sw; ++h) {
+          state_row(c->kv_state, c, sb, 4 + i)[h] = 0.0f;
+          state_row(c->score_state, c, sb, 4 + i)[h] = -std::numeric_limits<float>::infinity();
+        }
+  }
+  return (int)G;
+}
+
 // [V41] decode branch (start_pos > 0, one token): slot = start_pos % ratio; pool over the
 // state when (start_pos+1) % ratio == 0.  start_pos == 0 takes the prefill branch with one
 // token.  [CSA4] "Prefill and decode use the same rule": at ratio 4 overlapped, the entry

@@ -81,6 +81,13 @@ void oracle_set_weights(oracle_compressor* c, const float* wkv, const float* wga
  * Returns G, or -1 on bad arguments. */
 int oracle_prefill(oracle_compressor* c, const uint16_t* x, int B, int N, int slot_offset, uint16_t* latent,
                    uint8_t* codes, uint8_t* scales, uint16_t* prequant, int nthreads);
+/* Prefill chunk at start_pos >= 0 shared by the B sequences (start_pos 0: oracle_prefill): the
+ * entries of the groups completing in [start_pos, start_pos + N), G = (start_pos + N) / ratio -
+ * start_pos / ratio per sequence, to latent [B][G][H] etc.; earlier candidates come from the
+ * state; the state receives the new tokens of the unfinished group (and, overlapped, of the
+ * last complete group).  Returns G, or -1 on bad arguments. */
+int oracle_prefill_chunk(oracle_compressor* c, const uint16_t* x, int B, int N, int start_pos, int slot_offset,
+                         uint16_t* latent, uint8_t* codes, uint8_t* scales, uint16_t* prequant, int nthreads);
 /* Only the listed groups of one sequence x [N][dim]; outputs [ng][...].  State untouched. */
 int oracle_prefill_groups(const oracle_compressor* c, const uint16_t* x, int N, const int* groups, int ng,
                           uint16_t* latent, uint8_t* codes, uint8_t* scales, uint16_t* prequant, int nthreads);

@@ -228,6 +228,89 @@ def test_prefill_equals_token_by_token_decode(ratio, overlap, N, rope, fp4):
         assert np.array_equal(kp[:, :rem], kd[:, :rem]) and np.array_equal(sp[:, :rem], sd[:, :rem])
 
 
+def live_state_equal(ka, sa, kb, sb, ratio, overlap, P, H):
+    """The state slots a later call can still read after P tokens: non-overlapped the
+    unfinished group's slots; overlapped also the last complete group's parity."""
+    if overlap:
+        q, rem = (P // 4) % 2, P % 4
+        ok = np.array_equal(ka[:, q, :rem], kb[:, q, :rem]) and np.array_equal(sa[:, q, :rem], sb[:, q, :rem])
+        if P >= 4:
+            return ok and np.array_equal(ka[:, 1 - q], kb[:, 1 - q]) and np.array_equal(sa[:, 1 - q], sb[:, 1 - q])
+        return ok and np.all(sa[:, 1, :, H:] == -np.inf) and np.all(sb[:, 1, :, H:] == -np.inf)
+    rem = P % ratio
+    return np.array_equal(ka[:, :rem], kb[:, :rem]) and np.array_equal(sa[:, :rem], sb[:, :rem])
+
+
+# chunk lengths: the first call is a prefill at position 0, the others continue at the position
+# the previous one reached (mid-group, group-aligned, chunks that complete no group, p < ratio)
+CHUNKS = [(4, 1, (5, 2, 9, 1, 7)), (4, 1, (2, 1, 13, 4)), (3, 0, (4, 5, 1, 11)), (16, 0, (7, 20, 3, 40)),
+          (1, 0, (3, 4)), (2, 0, (1, 1, 1, 5))]
+
+
+@pytest.mark.parametrize("ratio,overlap,chunks", CHUNKS)
+def test_prefill_chunks_equal_token_by_token_decode(ratio, overlap, chunks):
+    dim, H, B = 64, 32, 2
+    chk, _ = make(dim, H, ratio, overlap, rope_dim=16, fp4=1, max_batch=B, seed=5)
+    dec, _ = make(dim, H, ratio, overlap, rope_dim=16, fp4=1, max_batch=B, seed=5)
+    P = sum(chunks)
+    x = rand_x(18, B, P, dim)
+    want = {b: [] for b in range(B)}
+    for p in range(P):
+        o = dec.decode(x[:, p], np.full(B, p, np.int32), nthreads=2)
+        for b in range(B):
+            if o["emitted"][b]:
+                want[b].append({k: o[k][b].copy() for k in ("latent", "codes", "scales", "prequant")})
+    got = {b: [] for b in range(B)}
+    p0 = 0
+    for n in chunks:
+        out = chk.prefill(x[:, p0:p0 + n], start_pos=p0, nthreads=2)
+        assert out["G"] == (p0 + n) // ratio - p0 // ratio
+        for b in range(B):
+            for j in range(out["G"]):
+                got[b].append({k: out[k][b, j] for k in ("latent", "codes", "scales", "prequant")})
+        p0 += n
+    for b in range(B):
+        assert len(got[b]) == len(want[b]) == P // ratio
+        for g, w in zip(got[b], want[b]):
+            for k in w:
+                assert np.array_equal(g[k], w[k]), k
+    kc, sc = chk.state()
+    kd, sd = dec.state()
+    assert live_state_equal(kc, sc, kd, sd, ratio, overlap, P, H)
+
+
+@pytest.mark.parametrize("ratio,overlap", [(4, 1), (8, 0)])
+def test_prefill_then_chunks_equal_one_prefill(ratio, overlap):
+    dim, H = 64, 32
+    one, _ = make(dim, H, ratio, overlap, rope_dim=16, fp4=1, max_batch=3, seed=6)
+    parts, _ = make(dim, H, ratio, overlap, rope_dim=16, fp4=1, max_batch=3, seed=6)
+    x = rand_x(19, 2, 11 * ratio + 3, dim)
+    full = one.prefill(x, slot_offset=1)
+    got = []
+    p0 = 0
+    for n in (2 * ratio + 1, 5 * ratio - 2, 4 * ratio + 4):
+        got.append(parts.prefill(x[:, p0:p0 + n], slot_offset=1, start_pos=p0)["latent"])
+        p0 += n
+    assert np.array_equal(np.concatenate(got, axis=1), full["latent"])
+    ka, sa = one.state()
+    kb, sb = parts.state()
+    assert live_state_equal(ka[1:], sa[1:], kb[1:], sb[1:], ratio, overlap, p0, H)
+    assert np.all(ka[0] == 0) and np.all(kb[0] == 0) and np.all(sb[0] == -np.inf)  # slot 0 untouched
+
+
+def test_prefill_chunk_reads_its_own_slots():
+    dim, H, r = 32, 16, 4
+    c, _ = make(dim, H, r, 1, rope_dim=16, fp4=1, max_batch=3, seed=7)
+    x = rand_x(20, 3, 14, dim)
+    c.prefill(x[:, :6])  # three different histories
+    first = c.prefill(x[:, 6:], start_pos=6)
+    d, _ = make(dim, H, r, 1, rope_dim=16, fp4=1, max_batch=3, seed=7)
+    d.prefill(x[1:2, :6], slot_offset=2)
+    second = d.prefill(x[1:2, 6:], slot_offset=2, start_pos=6)
+    assert np.array_equal(first["latent"][1], second["latent"][0])
+    assert not np.array_equal(first["latent"][0], first["latent"][1])
+
+
 def test_prefill_state_holds_the_tail_projections():
     dim, H, r = 48, 16, 8
     c, (wkv, wgate, _) = make(dim, H, r, 0, max_batch=3)
