@@ -322,9 +322,63 @@ def run_ours(args, rank, world, local):
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches, "clocks": clk}
     comp.close()
+    line["chunked_prefill"] = bench_chunked(args, torch, csa, synthetic, device, peaks, world)
     if not args.no_decode:
         line["decode"] = bench_decode(args, torch, csa, synthetic, device, peaks, world, rank)
     return line
+
+
+def bench_chunked(args, torch, csa, synthetic, device, peaks, world):
+    """A prefill chunk that continues a sequence: the Flash CSA layer, 4096 new tokens at position
+    4098 (two tokens into a group, so the first two entries also pool candidates from the state).
+    Every step is the same call on the same input; the state it reads is whatever the previous
+    step left, which changes the values but not the work."""
+    wl = synthetic.FLASH_CSA
+    layer = wl.layers[0]
+    B, N, p0 = 1, wl.tokens[0], wl.tokens[0] + 2
+    comp, x = make_inputs(torch, csa, synthetic, layer, wl.seed, B, N, 0, device)
+    G = (p0 + N) // layer.ratio - p0 // layer.ratio
+    out = comp._alloc_out(B * G, device, prequant=False)
+    stream = torch.cuda.current_stream(device)
+    props = torch.cuda.get_device_properties(device)
+    flush = torch.empty(int(2 * getattr(props, "L2_cache_size", 128 << 20)) // 4 + 1, dtype=torch.float32,
+                        device=device)
+    comp.prefill(torch.cat([x, x[:, :2]], dim=1), out=comp._alloc_out(B * (p0 // 4), device, False), prequant=False)
+
+    def step():
+        comp.prefill(x, out=out, prequant=False, start_pos=p0)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b_ in kev:
+        a.record(stream)
+        b_.record(stream)
+    launches0 = comp.kernel_launches()
+    for i in range(K):
+        flush.fill_(float(i))
+        comp.set_profile_events(*kev[i])
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    comp.set_profile_events(None, None)
+    launches = comp.kernel_launches() - launches0
+    ms = max_over_ranks(sum(a.elapsed_time(b_) for a, b_ in ev), world, device) / K
+    kms = statistics.mean(a.elapsed_time(b_) for a, b_ in kev)
+    flops = 2.0 * B * N * layer.dim * 2 * layer.width
+    achieved = flops / (kms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"] / 3.0
+    comp.close()
+    return {"workload": f"Flash CSA chunk: B={B}, {N} tokens at start_pos {p0} after a {p0}-token prefill",
+            "value": B * G * world / (ms * 1e-3), "unit": "entries/s", "ms_per_step": ms, "steps": K,
+            "tokens_per_s": B * N * world / (ms * 1e-3), "kernel_ms": kms, "gpu_launches": launches,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "kernel": "chunk_carry_kernel + csa_prefill_tc (projection + fused pool)"}}
 
 
 def bench_decode(args, torch, csa, synthetic, device, peaks, world, rank):

@@ -32,7 +32,7 @@ ABI_FUNCTIONS = ("csa_options_default", "csa_compressor_create", "csa_compressor
                  "csa_compress_prefill", "csa_compress_decode", "csa_state_reset", "csa_state_elems",
                  "csa_state_export", "csa_device_status", "csa_compressor_destroy", "csa_last_error",
                  "csa_fp4_e4m3_roundtrip", "csa_rope_table", "csa_set_profile_events", "csa_kernel_launches",
-                 "csa_uses_tensor_cores", "csa_compress_prefill_noalloc")
+                 "csa_uses_tensor_cores", "csa_compress_prefill_noalloc", "csa_compress_prefill_into")
 
 
 class CSAError(RuntimeError):
@@ -86,6 +86,7 @@ def load_library(build_if_missing: bool = True):
             "csa_kernel_launches": ([P], I64),
             "csa_uses_tensor_cores": ([P], I),
             "csa_compress_prefill_noalloc": ([P, P, I, I, I, I, P, P], I),
+            "csa_compress_prefill_into": ([P, P, I, I, I, I, P, I, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -175,24 +176,40 @@ class Compressor:
         return Out(_dptr(d["latent"]).value, _dptr(d["codes"]).value, _dptr(d["scales"]).value,
                    _dptr(d["prequant"]).value)
 
-    def prefill(self, x, slot_offset: int = 0, out=None, prequant: bool = True, stream=None):
-        """x bf16 [B, N, dim] CUDA.  Returns None when no group completes (N < ratio), else a
-        dict of latent [B, G, H] bf16, codes [B, G, H/2] u8, scales [B, G, H/16] u8 and
+    def prefill(self, x, slot_offset: int = 0, out=None, prequant: bool = True, stream=None, start_pos: int = 0):
+        """x bf16 [B, N, dim] CUDA: tokens start_pos .. start_pos+N-1 of each sequence (start_pos > 0:
+        a chunk continuing the sequences in the state).  Returns None when no group completes,
+        else a dict of latent [B, G, H] bf16, codes [B, G, H/2] u8, scales [B, G, H/16] u8 and
         prequant [B, G, H] bf16 (codes/scales None when fp4 is off)."""
         B, N, D = x.shape
         if D != self.dim or x.dtype != torch.bfloat16:
             raise CSAError("x must be bf16 [B, N, dim]")
-        G = N // self.ratio
+        G = (start_pos + N) // self.ratio - start_pos // self.ratio
         if out is None:
             out = self._alloc_out(max(B * G, 1), x.device, prequant)
         o = self._out_struct(out)
-        g = _check(self._lib.csa_compress_prefill(self._h, _dptr(_u16(x)), B, N, 0, slot_offset,
+        g = _check(self._lib.csa_compress_prefill(self._h, _dptr(_u16(x)), B, N, start_pos, slot_offset,
                                                   ctypes.byref(o), _stream(stream)), "csa_compress_prefill")
         if g == 0:
             return None
         H = self.head_dim
         shp = {"latent": (B, g, H), "codes": (B, g, H // 2), "scales": (B, g, H // 16), "prequant": (B, g, H)}
         return {k: (None if v is None else v[:B * g].view(*shp[k])) for k, v in out.items()}
+
+    def prefill_into(self, x, cache, start_pos: int = 0, slot_offset: int = 0, stream=None) -> int:
+        """Prefill (or a chunk at start_pos) writing entry g of sequence b into row g of
+        cache["latent"][b] ([B, rows, H] bf16; optional "codes" [B, rows, H/2], "scales"
+        [B, rows, H/16], "prequant" [B, rows, H]).  Returns the entries written per sequence."""
+        B, N, D = x.shape
+        if D != self.dim or x.dtype != torch.bfloat16:
+            raise CSAError("x must be bf16 [B, N, dim]")
+        lat = cache["latent"]
+        if lat.dim() != 3 or lat.shape[0] != B or lat.shape[2] != self.head_dim:
+            raise CSAError("cache['latent'] must be [B, rows, head_dim]")
+        o = self._out_struct({k: cache.get(k) for k in ("latent", "codes", "scales", "prequant")})
+        return _check(self._lib.csa_compress_prefill_into(self._h, _dptr(_u16(x)), B, N, start_pos, slot_offset,
+                                                          ctypes.byref(o), lat.shape[1], _stream(stream)),
+                      "csa_compress_prefill_into")
 
     def decode(self, x_tok, start_pos, out=None, emitted=None, prequant: bool = True, stream=None):
         """x_tok bf16 [B, dim], start_pos int32 CUDA [B].  Returns a dict with emitted u8 [B]

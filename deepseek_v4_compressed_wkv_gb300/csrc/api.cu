@@ -108,7 +108,83 @@ int ensure_scratch(csa_compressor* c, size_t bytes, cudaStream_t s) {
   return CSA_OK;
 }
 
+// Checks shared by the prefill entry points; on success fills the call geometry.  cache_rows < 0:
+// entries go to out [B][G][..]; else to rows start_pos / ratio .. of a cache [B][cache_rows][..].
+int check_prefill(const csa_compressor* c, const uint16_t* x, int B, int N, int start_pos, int slot_offset,
+                  const csa_out* out, int cache_rows, const char* what, csa::Chunk* ck) {
+  if (!c) return fail(CSA_ERR_ARG, "%s: handle is NULL", what);
+  if (!c->weights_set) return fail(CSA_ERR_STATE, "%s: weights not set", what);
+  if (B < 1 || N < 1) return fail(CSA_ERR_ARG, "%s: B (%d) and N (%d) must be >= 1", what, B, N);
+  if (start_pos < 0 || (long long)start_pos + N > 0x7fffffffLL)
+    return fail(CSA_ERR_ARG, "%s: start_pos %d must be >= 0 and start_pos + N must fit in int32", what, start_pos);
+  if (slot_offset < 0 || (long long)slot_offset + B > c->opt.max_batch)
+    return fail(CSA_ERR_ARG, "%s: slots [%d, %d) exceed max_batch %d", what, slot_offset, slot_offset + B,
+                c->opt.max_batch);
+  if (!x) return fail(CSA_ERR_ARG, "%s: x is NULL", what);
+  if ((long long)B * N > 0x7fffffffLL) return fail(CSA_ERR_ARG, "%s: B * N too large", what);
+  const int r = c->ratio;
+  const int gend = (int)(((long long)start_pos + N) / r);
+  if (cache_rows >= 0 && gend > cache_rows)
+    return fail(CSA_ERR_ARG, "%s: group %d does not fit a cache of %d rows", what, gend - 1, cache_rows);
+  *ck = csa::make_chunk(start_pos, N, r);
+  if (cache_rows >= 0) {
+    ck->bstride = cache_rows;
+    ck->row0 = ck->g0;
+  }
+  if (ck->G > 0 && (!out || !out->latent)) return fail(CSA_ERR_ARG, "%s: out->latent is required", what);
+  if (ck->G > 0 && c->opt.rope_dim > 0 && (long long)r * (gend - 1) >= c->opt.max_pos)
+    return fail(CSA_ERR_ARG, "%s: entry position %lld exceeds the RoPE table (max_pos %d)", what,
+                (long long)r * (gend - 1), c->opt.max_pos);
+  return CSA_OK;
+}
+
+int prefill_call(csa_compressor* c, const uint16_t* x, int B, int N, int start_pos, int slot_offset,
+                 const csa_out* out, int cache_rows, csa_stream_t stream, const char* what) {
+  try {
+    csa::Chunk ck;
+    int rc = check_prefill(c, x, B, N, start_pos, slot_offset, out, cache_rows, what, &ck);
+    if (rc) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    const long long M = (long long)B * N;
+    const csa_out o = out ? *out : csa_out{nullptr, nullptr, nullptr, nullptr};
+    CSA_CUDA(csa::invalidate_decode_acc(c, slot_offset, B, s), "invalidate decode running values");
+    if (csa::prefill_tc_supported(c, x)) {
+      rc = ensure_scratch(c, csa::prefill_tc_scratch_bytes(c, B, N, ck), s);
+      if (rc) return rc;
+      if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
+      CSA_CUDA(csa::launch_prefill_tc(c, x, B, N, slot_offset, ck, o, c->scratch, s), "tensor-core prefill launch");
+      if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
+      // the carry kernel (a chunk), the projection kernel, the entry kernel
+      c->launches += csa::chunk_needs_carry(ck, c->overlap) + 1 + (ck.G > 0);
+      return ck.G;
+    }
+    rc = ensure_scratch(c, (size_t)M * c->pk.cols() * sizeof(float), s);
+    if (rc) return rc;
+    if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
+    CSA_CUDA(csa::launch_projection_ffma(c, x, (int)M, c->scratch, 0, nullptr, s), "projection launch");
+    if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
+    c->launches += 1;
+    if (ck.G > 0) {
+      CSA_CUDA(csa::launch_prefill_pool(c, c->scratch, B, N, slot_offset, ck, o, s), "pool launch");
+      c->launches += 1;
+    }
+    CSA_CUDA(csa::launch_prefill_state(c, c->scratch, B, N, slot_offset, ck, s), "state launch");
+    c->launches += 1;
+    return ck.G;
+  } catch (...) {
+    return fail(CSA_ERR_INTERNAL, "%s: unexpected exception", what);
+  }
+}
+
 }  // namespace
+
+// Argument checks of a prefill call, shared with the no-alloc entry point (not part of the C ABI).
+__attribute__((visibility("hidden"))) int csa_internal_check_prefill(const csa_compressor* c, const uint16_t* x, int B,
+                                                                  int N, int start_pos, int slot_offset,
+                                                                  const csa_out* out, const char* what,
+                                                                  csa::Chunk* ck) {
+  return check_prefill(c, x, B, N, start_pos, slot_offset, out, -1, what, ck);
+}
 
 // Used by other translation units of the library to report a failure through
 // csa_last_error (not part of the C ABI).
@@ -227,53 +303,13 @@ int csa_compressor_set_weights(csa_compressor* c, const float* wkv, const float*
 
 int csa_compress_prefill(csa_compressor* c, const uint16_t* x, int B, int N, int start_pos, int slot_offset,
                          const csa_out* out, csa_stream_t stream) {
-  try {
-    if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
-    if (!c->weights_set) return fail(CSA_ERR_STATE, "weights not set");
-    if (start_pos != 0)
-      return fail(CSA_ERR_ARG, "prefill needs start_pos 0 (got %d); later tokens go through decode", start_pos);
-    if (B < 1 || N < 1) return fail(CSA_ERR_ARG, "B (%d) and N (%d) must be >= 1", B, N);
-    if (slot_offset < 0 || (long long)slot_offset + B > c->opt.max_batch)
-      return fail(CSA_ERR_ARG, "slots [%d, %d) exceed max_batch %d", slot_offset, slot_offset + B, c->opt.max_batch);
-    if (!x) return fail(CSA_ERR_ARG, "x is NULL");
-    const int G = N / c->ratio;
-    if (G > 0 && (!out || !out->latent)) return fail(CSA_ERR_ARG, "out->latent is required");
-    if (G > 0 && c->opt.rope_dim > 0 && (long long)c->ratio * (G - 1) >= c->opt.max_pos)
-      return fail(CSA_ERR_ARG, "entry position %lld exceeds the RoPE table (max_pos %d)",
-                  (long long)c->ratio * (G - 1), c->opt.max_pos);
-    cudaStream_t s = (cudaStream_t)stream;
-    const long long M = (long long)B * N;
-    if (M > 0x7fffffffLL) return fail(CSA_ERR_ARG, "B * N too large");
-    CSA_CUDA(csa::invalidate_decode_acc(c, slot_offset, B, s), "invalidate decode running values");
-    if (csa::prefill_tc_supported(c, x)) {
-      const size_t bytes = csa::prefill_tc_scratch_bytes(c, B, N);
-      int rc = ensure_scratch(c, bytes, s);
-      if (rc) return rc;
-      csa_out o = out ? *out : csa_out{nullptr, nullptr, nullptr, nullptr};
-      if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
-      CSA_CUDA(csa::launch_prefill_tc(c, x, B, N, slot_offset, o, c->scratch, s),
-               "tensor-core prefill launch");
-      if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
-      c->launches += G > 0 ? 2 : 1;  // the projection kernel, then the entry kernel
-      return G;
-    }
-    const size_t bytes = (size_t)M * c->pk.cols() * sizeof(float);
-    int rc = ensure_scratch(c, bytes, s);
-    if (rc) return rc;
-    if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
-    CSA_CUDA(csa::launch_projection_ffma(c, x, (int)M, c->scratch, 0, nullptr, s), "projection launch");
-    if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
-    c->launches += 1;
-    if (G > 0) {
-      CSA_CUDA(csa::launch_prefill_pool(c, c->scratch, B, N, *out, s), "pool launch");
-      c->launches += 1;
-    }
-    CSA_CUDA(csa::launch_prefill_state(c, c->scratch, B, N, slot_offset, s), "state launch");
-    c->launches += 1;
-    return G;
-  } catch (...) {
-    return fail(CSA_ERR_INTERNAL, "csa_compress_prefill: unexpected exception");
-  }
+  return prefill_call(c, x, B, N, start_pos, slot_offset, out, -1, stream, "csa_compress_prefill");
+}
+
+int csa_compress_prefill_into(csa_compressor* c, const uint16_t* x, int B, int N, int start_pos, int slot_offset,
+                              const csa_out* cache, int cache_rows, csa_stream_t stream) {
+  if (cache_rows < 1) return fail(CSA_ERR_ARG, "csa_compress_prefill_into: cache_rows %d must be >= 1", cache_rows);
+  return prefill_call(c, x, B, N, start_pos, slot_offset, cache, cache_rows, stream, "csa_compress_prefill_into");
 }
 
 int csa_compress_decode(csa_compressor* c, const uint16_t* x_tok, int B, const int32_t* start_pos, uint8_t* emitted,

@@ -58,6 +58,49 @@ __host__ __device__ inline size_t plane_stage_elem(int nkb, int t, int kb) {
   return ((size_t)t * nkb + kb) * 3 * (kPlaneTileRows * kPlaneTileK);
 }
 
+// State slot of the token at position p of a sequence ("Pool token pairs", decode branch:
+// p % ratio; ratio 4 overlapped: group p / 4 lives in parity (p / 4) % 2, slot p % 4 of it).
+__host__ __device__ inline int state_slot(long long p, int ratio, int overlap) {
+  return overlap ? (int)(((p >> 2) & 1) * 4 + (p & 3)) : (int)(p % ratio);
+}
+
+// Geometry of one prefill call over tokens [p0, p0 + N) of each sequence (all sequences at the
+// same position).  p0 = 0 is the whole-sequence prefill of the pages; p0 > 0 a chunk that
+// continues sequences whose earlier tokens are in the state (the same rule as decode, token by
+// token).  The kernels index tokens from the start of the open group: virtual token v is
+// position p0 - a + v, so v < a are the open group's earlier tokens, read from the state.
+struct Chunk {
+  int p0;              // position of the call's first token
+  int a;               // p0 % ratio
+  int g0;              // p0 / ratio: absolute index of the first group the call can complete
+  int G;               // groups completing in the call: (p0 + N) / ratio - g0
+  int gend;            // (p0 + N) / ratio: the group left unfinished
+  long long bstride;   // output rows per sequence
+  long long row0;      // output row of the call's first entry
+  // entry j of sequence b goes to output row b * bstride + row0 + j
+  __host__ __device__ long long row(int b, int j) const { return (long long)b * bstride + row0 + j; }
+};
+
+// Entries to out [B][G][..] (set bstride and row0 for other layouts).
+inline Chunk make_chunk(int p0, int N, int ratio) {
+  Chunk k;
+  k.p0 = p0;
+  k.a = p0 % ratio;
+  k.g0 = p0 / ratio;
+  k.gend = (int)(((long long)p0 + N) / ratio);
+  k.G = k.gend - k.g0;
+  k.bstride = k.G;
+  k.row0 = 0;
+  return k;
+}
+
+// The earlier candidates a chunk's first group pools besides its new tokens (the open group's
+// tokens before p0 and, overlapped, branch B of the previous group; overlapped, the second
+// group's branch B of those same tokens) are reduced by chunk_carry_kernel to running softmax
+// values (max, denominator, numerator) per feature, [B][1 + overlap][3][H] f32, before the
+// projection kernel overwrites any state slot.
+inline bool chunk_needs_carry(const Chunk& k, int overlap) { return k.G > 0 && (k.a > 0 || (overlap && k.g0 > 0)); }
+
 // Kernel-side view of the epilogue parameters.
 struct EpiParams {
   const float* gain;      // [H]

@@ -9,10 +9,10 @@ EpiParams epi_params(const csa_compressor* c);
 cudaError_t launch_pack_weights(const csa_compressor* c, const float* wkv, const float* wgate, cudaStream_t s);
 cudaError_t launch_projection_ffma(const csa_compressor* c, const uint16_t* x, int M, float* out, int mode,
                                    const int32_t* start_pos, cudaStream_t s);
-cudaError_t launch_prefill_pool(const csa_compressor* c, const float* proj, int B, int N, const csa_out& out,
-                                cudaStream_t s);
+cudaError_t launch_prefill_pool(const csa_compressor* c, const float* proj, int B, int N, int slot_offset,
+                                const Chunk& ck, const csa_out& out, cudaStream_t s);
 cudaError_t launch_prefill_state(const csa_compressor* c, const float* proj, int B, int N, int slot_offset,
-                                 cudaStream_t s);
+                                 const Chunk& ck, cudaStream_t s);
 cudaError_t launch_decode_emit(const csa_compressor* c, const int32_t* start_pos, int B, const csa_out& out,
                                uint8_t* emitted, cudaStream_t s);
 cudaError_t launch_state_reset(const csa_compressor* c, int slot_begin, int count, cudaStream_t s);
@@ -22,9 +22,9 @@ cudaError_t launch_fp4_roundtrip(const uint16_t* in, long long nb, uint8_t* code
 
 // Tensor-core prefill (prefill_tc.cu): projection + pool + norm + RoPE + fp4 + state update.
 bool prefill_tc_supported(const csa_compressor* c, const void* x);
-size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N);
+size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N, const Chunk& ck);
 cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset,
-                              const csa_out& out, void* scratch, cudaStream_t s);
+                              const Chunk& ck, const csa_out& out, void* scratch, cudaStream_t s);
 
 // Tensor-core decode (decode_tc.cu): two launches, the projection of one token per sequence
 // (split over K, partial sums to `part`), then one CTA per sequence for the reduction into its

@@ -55,8 +55,7 @@ struct RowMap {
   int slots, ratio, overlap;
   __device__ size_t row(int m, int ncol) const {
     if (mode == 0) return (size_t)m * ncol;
-    const int p = max(start_pos[m], 0);
-    const int slot = overlap ? ((p >> 2) & 1) * 4 + (p & 3) : p % ratio;
+    const int slot = state_slot(max(start_pos[m], 0), ratio, overlap);
     return ((size_t)m * slots + slot) * ncol;
   }
 };
@@ -155,27 +154,37 @@ __device__ __forceinline__ void pool16(int ncand, Cand cand, float out[16]) {
   for (int i = 0; i < 16; ++i) out[i] = __fdiv_rn(num[i], den[i]);
 }
 
-// Prefill pool + epilogue from the projection scratch, one warp per entry (b, j).
-__global__ __launch_bounds__(128) void prefill_pool_kernel(const float* __restrict__ proj, int B, int N, int G,
-                                                           int ratio, int overlap, Packing pk, EpiParams ep,
-                                                           csa_out out) {
+// Prefill pool + epilogue from the projection scratch, one warp per entry (b, j): entry j of
+// the call is absolute group g0 + j; a candidate token before the call's first position p0
+// (a chunk) is read from its state slot, which prefill_state_kernel rewrites only after this
+// kernel.
+__global__ __launch_bounds__(128) void prefill_pool_kernel(const float* __restrict__ proj, int B, int N, Chunk ck,
+                                                           int ratio, int overlap, Packing pk,
+                                                           const float* __restrict__ state, int slots,
+                                                           int slot_offset, EpiParams ep, csa_out out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = ck.G;
   const long long e = (long long)blockIdx.x * 4 + warp;
   if (e >= (long long)B * G) return;
   const int b = (int)(e / G), j = (int)(e % G);
+  const long long g = (long long)ck.g0 + j;
   const int ncol = pk.cols();
   const float* seq = proj + (size_t)b * N * ncol;
+  const float* st = state + (size_t)(slot_offset + b) * slots * ncol;
+  auto row_of = [&](long long p) {  // projected row of the token at position p
+    return p >= ck.p0 ? seq + (size_t)(p - ck.p0) * ncol : st + (size_t)state_slot(p, ratio, overlap) * ncol;
+  };
   const int f0 = min(lane, (pk.H >> 4) - 1) * 16;
   float v[16];
   if (overlap) {
     pool16(8, [&](int c, const float*& kvp, const float*& sp) {
       if (c < 4) {
-        if (j == 0) return false;
-        const float* row = seq + (size_t)(4 * j - 4 + c) * ncol;
+        if (g == 0) return false;
+        const float* row = row_of(4 * g - 4 + c);
         kvp = row + pk.col(KV_B, f0);
         sp = row + pk.col(S_B, f0);
       } else {
-        const float* row = seq + (size_t)(4 * j + c - 4) * ncol;
+        const float* row = row_of(4 * g + c - 4);
         kvp = row + pk.col(KV_A, f0);
         sp = row + pk.col(S_A, f0);
       }
@@ -183,15 +192,16 @@ __global__ __launch_bounds__(128) void prefill_pool_kernel(const float* __restri
     }, v);
   } else {
     pool16(ratio, [&](int c, const float*& kvp, const float*& sp) {
-      const float* row = seq + (size_t)(ratio * j + c) * ncol;
+      const float* row = row_of(ratio * g + c);
       kvp = row + pk.col(KV, f0);
       sp = row + pk.col(S, f0);
       return true;
     }, v);
   }
   const size_t H = pk.H;
-  entry_epilogue(v, lane, (long long)ratio * j, ep, out.latent + e * H, out.codes ? out.codes + e * (H / 2) : nullptr,
-                 out.scales ? out.scales + e * (H / 16) : nullptr, out.prequant ? out.prequant + e * H : nullptr);
+  const size_t o = (size_t)ck.row(b, j);
+  entry_epilogue(v, lane, (long long)ratio * g, ep, out.latent + o * H, out.codes ? out.codes + o * (H / 2) : nullptr,
+                 out.scales ? out.scales + o * (H / 16) : nullptr, out.prequant ? out.prequant + o * H : nullptr);
 }
 
 __device__ __forceinline__ float padded_value(const Packing& pk, int col) {
@@ -200,30 +210,24 @@ __device__ __forceinline__ float padded_value(const Packing& pk, int col) {
 }
 
 // Prefill state update ("Pool token pairs": the trailing partial group waits in the state;
-// at ratio 4 overlapped also the last complete group, whose branch B the next entry pools).
-__global__ void prefill_state_kernel(const float* __restrict__ proj, int N, int ratio, int overlap, Packing pk,
-                                     float* __restrict__ state, int slots, int slot_offset) {
+// at ratio 4 overlapped also the last complete group, whose branch B the next entry pools):
+// the call's tokens of those groups go to their slots (a chunk's earlier tokens are there
+// already).
+__global__ void prefill_state_kernel(const float* __restrict__ proj, int N, Chunk ck, int ratio, int overlap,
+                                     Packing pk, float* __restrict__ state, int slots, int slot_offset) {
   const int b = blockIdx.x;
   const int ncol = pk.cols();
-  const int G = N / ratio, rem = N % ratio;
   const float* seq = proj + (size_t)b * N * ncol;
   float* st = state + (size_t)(slot_offset + b) * slots * ncol;
-  auto copy_row = [&](int token, int slot) {
-    for (int c = threadIdx.x; c < ncol; c += blockDim.x) st[(size_t)slot * ncol + c] = seq[(size_t)token * ncol + c];
-  };
-  if (!overlap) {
-    for (int i = 0; i < rem; ++i) copy_row(G * ratio + i, i);
-    return;
+  const long long p1 = (long long)ck.p0 + N;
+  const long long keep = max((long long)ck.p0, ((long long)ck.gend - overlap) * ratio);
+  for (long long p = keep; p < p1; ++p) {
+    const float* src = seq + (size_t)(p - ck.p0) * ncol;
+    float* dst = st + (size_t)state_slot(p, ratio, overlap) * ncol;
+    for (int c = threadIdx.x; c < ncol; c += blockDim.x) dst[c] = src[c];
   }
-  const int q = G & 1;
-  for (int i = 0; i < rem; ++i) copy_row(4 * G + i, 4 * q + i);
-  for (int i = 0; i < 4; ++i) {
-    if (G >= 1) {
-      copy_row(4 * (G - 1) + i, 4 * (1 - q) + i);
-    } else {
-      for (int c = threadIdx.x; c < ncol; c += blockDim.x) st[(size_t)(4 + i) * ncol + c] = padded_value(pk, c);
-    }
-  }
+  if (overlap && ck.gend == 0)  // no complete group yet: the previous branch stays padded
+    for (int c = threadIdx.x; c < 4 * ncol; c += blockDim.x) st[(size_t)4 * ncol + c] = padded_value(pk, c % ncol);
 }
 
 // Decode: pool + epilogue for the sequences whose token completed a group; one warp per
@@ -353,19 +357,18 @@ EpiParams epi_params(const csa_compressor* c) {
   return ep;
 }
 
-cudaError_t launch_prefill_pool(const csa_compressor* c, const float* proj, int B, int N, const csa_out& out,
-                                cudaStream_t s) {
-  const int G = N / c->ratio;
-  const long long E = (long long)B * G;
+cudaError_t launch_prefill_pool(const csa_compressor* c, const float* proj, int B, int N, int slot_offset,
+                                const Chunk& ck, const csa_out& out, cudaStream_t s) {
+  const long long E = (long long)B * ck.G;
   if (E > 0)
-    prefill_pool_kernel<<<(unsigned)((E + 3) / 4), 128, 0, s>>>(proj, B, N, G, c->ratio, c->overlap, c->pk,
-                                                              epi_params(c), out);
+    prefill_pool_kernel<<<(unsigned)((E + 3) / 4), 128, 0, s>>>(proj, B, N, ck, c->ratio, c->overlap, c->pk, c->state,
+                                                              c->slots, slot_offset, epi_params(c), out);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_state(const csa_compressor* c, const float* proj, int B, int N, int slot_offset,
-                                 cudaStream_t s) {
-  prefill_state_kernel<<<B, 256, 0, s>>>(proj, N, c->ratio, c->overlap, c->pk, c->state, c->slots, slot_offset);
+                                 const Chunk& ck, cudaStream_t s) {
+  prefill_state_kernel<<<B, 256, 0, s>>>(proj, N, ck, c->ratio, c->overlap, c->pk, c->state, c->slots, slot_offset);
   return cudaGetLastError();
 }
 

@@ -24,6 +24,12 @@
 // entries are then normalised, rotated and quantised by prefill_entry_kernel, one CTA per entry
 // over all SMs (the RMSNorm needs all H features, and one SM finishing a token tile's 63
 // entries alone took about as long as a quarter of the projection).
+//
+// A chunk at position p0 > 0 (Chunk) tiles the tokens from the start of the open group: the
+// first tile's leading a = p0 % ratio token columns (and the overlapped halo) are earlier
+// tokens, whose contribution to the first group (overlapped: the first two groups) arrives as
+// running softmax values computed from the state before this kernel (chunk_carry_kernel);
+// their x rows read as zeros and their columns are not pooled.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -61,15 +67,19 @@ struct Tile {
 
 struct Params {
   int N, K, ratio, overlap, T, GT, halo, ntt, G, ncol, slots, slot_offset;
+  int a, g0, gend;         // chunk geometry (Chunk): all 0 / G for a prefill from position 0
   const __nv_bfloat16* w;  // weight planes, tiled (plane_tile_elem)
   Packing pk;
   float* state;
-  uint16_t* pooled;  // [B][ntt][GT][H] bf16 bits
+  uint16_t* pooled;        // [B][ntt][GT][H] bf16 bits
+  const float* carry;      // [B][1 + overlap][3][H] running softmax values of the candidates
+                           // of the first groups that are earlier than the chunk, or null
   int* flag;
 };
 
 struct EntryParams {
   int G, GT, ntt, ratio;
+  Chunk ck;
   const uint16_t* pooled;  // [B][ntt][GT][H] bf16 bits
   EpiParams ep;
   csa_out out;
@@ -97,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ftile = blockIdx.x, tt = blockIdx.y, b = blockIdx.z;
   const int nkb = P.K / kKb;
   const int nch = (nkb + kChunkKb - 1) / kChunkKb;
-  const int t0 = tt * P.T - P.halo;  // sequence index of the tile's token 0
+  const int t0 = tt * P.T - P.halo;  // virtual index (from the open group's start) of the tile's token 0
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -129,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* st = smem + s * kStageBytes;
         mbar_arrive_expect_tx(&full[s], kStageBytes);
         bulk_load(st, P.w + plane_stage_elem(P.K / kKb, ftile, kb), 3 * kPlaneBytes, &full[s]);
-        tma_load_3d(st + 3 * kPlaneBytes, &map_x, kb * kKb, t0, b, &full[s]);
+        tma_load_3d(st + 3 * kPlaneBytes, &map_x, kb * kKb, t0 - P.a, b, &full[s]);
         ++issued;
       }
       if (*abort_flag) {  // let the copies already in flight land before the CTA exits
@@ -203,6 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const bool have_acc = ok && !*abort_flag;
     if (have_acc) {
+      // a chunk's carry kernel (the grid this launch may overlap) has finished reading the state
+      // and written the carried values; a no-op for a launch without that predecessor
+      griddep_wait();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       float* stg = (float*)smem;  // [128 packed rows][kSmemStride] f32, reuses the stage buffers
 #pragma unroll
@@ -213,21 +226,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Packing& pk = P.pk;
       const int F = pk.ft, r = P.ratio, G = P.G;
       const int col0 = ftile * kRows;  // first packed column of this tile
-      // -- state: the tokens of the unfinished group (and, overlapped, of the last complete
-      //    group) that this tile owns; thread et < 128 writes packed column col0 + et
+      // -- state: the new tokens (virtual index >= a) of the unfinished group and, overlapped,
+      //    of the last complete group that this tile owns; thread et < 128 writes packed
+      //    column col0 + et.  Virtual group G is absolute group gend.
       if (et < kRows) {
         float* st = P.state + (size_t)(P.slot_offset + b) * P.slots * P.ncol + col0 + et;
-        const int own0 = tt * P.T, own1 = min(own0 + P.T, P.N);
+        const int own0 = max(tt * P.T, P.a), own1 = min(tt * P.T + P.T, P.a + P.N);
         auto put = [&](int tok, int slot) { st[(size_t)slot * P.ncol] = stg[et * kSmemStride + (tok - t0)]; };
         if (!P.overlap) {
           for (int tok = max(own0, r * G); tok < own1; ++tok) put(tok, tok - r * G);
         } else {
-          const int qp = G & 1;
+          const int qp = P.gend & 1;
           for (int tok = max(own0, 4 * G); tok < own1; ++tok) put(tok, 4 * qp + tok - 4 * G);
           if (G >= 1)
             for (int tok = max(own0, 4 * G - 4); tok < min(own1, 4 * G); ++tok)
               put(tok, 4 * (1 - qp) + tok - (4 * G - 4));
-          if (G == 0 && tt == 0) {
+          if (P.gend == 0 && tt == 0) {
             const int kind = et / F;  // padded previous branch: kv 0, score -inf
             const float pad = kind < pk.nk / 2 ? 0.0f : -INFINITY;
             for (int i = 0; i < 4; ++i) st[(size_t)(4 + i) * P.ncol] = pad;
@@ -241,12 +255,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = tt * P.GT + g;
         if (j >= G) break;  // pairs are visited in group order
         float m = -INFINITY, den = 0.0f, num = 0.0f;
-        if (P.overlap) {
+        if (P.carry && j < 1 + P.overlap) {
+          // the chunk's first groups hold tokens earlier than the chunk (virtual index < a, or the
+          // halo): those arrive as running values; the rest are this tile's columns.  Group 0:
+          // branch A of tokens a..3 (non-overlapped: tokens a..ratio-1); overlapped group 1:
+          // branch B of tokens a..3 and branch A of tokens 4..7.
+          const float* cr = P.carry + ((size_t)b * (1 + P.overlap) + j) * 3 * pk.H + ftile * F + f;
+          const float mc = cr[0], dc = cr[pk.H], nc = cr[2 * pk.H];  // max, denominator, numerator
+          const int kk = P.overlap ? (KV_A * F + f) : (KV * F + f), ks = P.overlap ? (S_A * F + f) : (S * F + f);
+          const float* kv = stg + kk * kSmemStride + P.halo + 4 * j;
+          const float* sc = stg + ks * kSmemStride + P.halo + 4 * j;
+          const float* kB = stg + (KV_B * F + f) * kSmemStride + P.halo;
+          const float* sB = stg + (S_B * F + f) * kSmemStride + P.halo;
+          const int n = P.overlap ? 4 : r, i0 = j == 0 ? P.a : 0, iB = j == 1 ? P.a : 4;
+          m = mc;
+          for (int i = i0; i < n; ++i) m = fmaxf(m, sc[i]);
+          for (int i = iB; i < 4; ++i) m = fmaxf(m, sB[i]);
+          const float rs = expf(mc - m);  // 0 when nothing was carried (mc = -inf)
+          den = dc * rs;
+          num = nc * rs;
+          for (int i = iB; i < 4; ++i) {
+            const float e = expf(sB[i] - m);
+            den += e;
+            num = fmaf(e, kB[i], num);
+          }
+          for (int i = i0; i < n; ++i) {
+            const float e = expf(sc[i] - m);
+            den += e;
+            num = fmaf(e, kv[i], num);
+          }
+        } else if (P.overlap) {
           const float* kA = stg + (KV_A * F + f) * kSmemStride + 4 * g + 4;
           const float* sA = stg + (S_A * F + f) * kSmemStride + 4 * g + 4;
           const float* kB = stg + (KV_B * F + f) * kSmemStride + 4 * g;
           const float* sB = stg + (S_B * F + f) * kSmemStride + 4 * g;
-          const bool padB = j == 0;
+          const bool padB = P.g0 + j == 0;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             m = fmaxf(m, sA[i]);
@@ -287,6 +330,53 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Running softmax values (max, denominator, numerator) per feature of the candidates of a
+// chunk's first groups that are earlier than the chunk, from the state (absolute group g0 is
+// the open group, its tokens before p0 in slots 0 .. a-1, overlapped of parity g0 % 2):
+//  [b][0]: group g0 - the open group's earlier tokens (overlapped: their branch A) and,
+//          overlapped, branch B of group g0 - 1 (parity (g0 - 1) % 2; none for g0 = 0, the
+//          padded branch);
+//  [b][1]: overlapped only, group g0 + 1 - branch B of the open group's earlier tokens.
+// Layout [B][1 + overlap][3][H] f32; an empty set gives (-inf, 0, 0).  Grid (H / 128, B), one
+// thread per feature.  The projection kernel that follows starts at once (programmatic
+// dependent launch): it reads these values, and writes state slots, only after its wait.
+template <class Cand>
+__device__ __forceinline__ void running_softmax(int n, Cand cand, float* out, int H) {
+  float m = -INFINITY, den = 0.0f, num = 0.0f;
+  for (int i = 0; i < n; ++i) m = fmaxf(m, *cand(i, true));
+  if (m > -INFINITY)
+    for (int i = 0; i < n; ++i) {
+      const float e = expf(*cand(i, true) - m);
+      den += e;
+      num = fmaf(e, *cand(i, false), num);
+    }
+  out[0] = m;
+  out[H] = den;
+  out[2 * H] = num;
+}
+
+__global__ void __launch_bounds__(128) chunk_carry_kernel(const float* __restrict__ state, Packing pk, int overlap,
+                                                          int slots, int slot_offset, Chunk ck,
+                                                          float* __restrict__ carry) {
+  griddep_launch_dependents();
+  const int b = blockIdx.y, f = blockIdx.x * blockDim.x + threadIdx.x;
+  const int ncol = pk.cols(), H = pk.H;
+  if (f >= H) return;
+  const float* st = state + (size_t)(slot_offset + b) * slots * ncol;
+  float* out = carry + (size_t)b * (1 + overlap) * 3 * H + f;
+  if (!overlap) {
+    running_softmax(ck.a, [&](int i, bool score) { return st + (size_t)i * ncol + pk.col(score ? S : KV, f); }, out, H);
+    return;
+  }
+  const int open = 4 * (ck.g0 & 1), prev = 4 * ((ck.g0 + 1) & 1), nprev = ck.g0 > 0 ? 4 : 0;
+  running_softmax(nprev + ck.a, [&](int i, bool score) {
+    return i < nprev ? st + (size_t)(prev + i) * ncol + pk.col(score ? S_B : KV_B, f)
+                     : st + (size_t)(open + i - nprev) * ncol + pk.col(score ? S_A : KV_A, f);
+  }, out, H);
+  running_softmax(ck.a, [&](int i, bool score) { return st + (size_t)(open + i) * ncol + pk.col(score ? S_B : KV_B, f); },
+                  out + 3 * H, H);
+}
+
 // One CTA of 128 threads per entry (b, j): thread t takes features 4t..4t+3 of its pooled
 // values, then bf16, RMSNorm (the sum of squares over the CTA, warps in order), RoPE and the
 // fp4 round trip (entry_epilogue_quad).  The gain and RoPE factors (written before this launch's
@@ -297,7 +387,7 @@ __global__ void __launch_bounds__(128) prefill_entry_kernel(const EntryParams P)
   const int b = e / P.G, j = e % P.G, tt = j / P.GT, g = j % P.GT;
   const int H = P.ep.H, hr = P.ep.rope_dim >> 1, r0 = H - P.ep.rope_dim;
   const bool act = f < H;
-  const long long pos = (long long)P.ratio * j;
+  const long long pos = (long long)P.ratio * (P.ck.g0 + j);
   float gn[4] = {0.0f, 0.0f, 0.0f, 0.0f}, rc[2] = {1.0f, 1.0f}, rs[2] = {0.0f, 0.0f};
   if (act) {
     const float4 gg = __ldg(reinterpret_cast<const float4*>(P.ep.gain + f));
@@ -328,7 +418,7 @@ __global__ void __launch_bounds__(128) prefill_entry_kernel(const EntryParams P)
   if (lane == 0) wss[t >> 5] = ss;
   __syncthreads();
   const float inv = rms_inv(wss[0] + wss[1] + wss[2] + wss[3], P.ep);
-  entry_epilogue_quad(v, act, f, lane, inv, gn, rc, rs, P.ep, (size_t)e, P.out);
+  entry_epilogue_quad(v, act, f, lane, inv, gn, rc, rs, P.ep, (size_t)P.ck.row(b, j), P.out);
 }
 
 }  // namespace tc
@@ -341,6 +431,10 @@ bool prefill_tc_supported(const csa_compressor* c, const void* x) {
 }
 
 namespace {
+
+// Offset of the carried running softmax values ([B][1 + overlap][3][H] f32) after the pooled
+// scratch.
+size_t carry_offset(size_t pooled_bytes) { return (pooled_bytes + 255) & ~(size_t)255; }
 
 // Tokens of a tile owned by it (the overlapped tile also loads the 4 tokens before it).
 int owned_tokens(const csa_compressor* c, int tok) {
@@ -374,7 +468,7 @@ int prefill_tok(const csa_compressor* c, int B, int N) {
 }
 
 template <int TOK>
-cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset,
+cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset, const Chunk& ck,
                        const csa_out& out, void* scratch, cudaStream_t s) {
   using namespace tc;
   auto encode = tcx::get_encode();
@@ -387,16 +481,28 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
   P.halo = c->overlap ? 4 : 0;
   P.T = owned_tokens(c, TOK);
   P.GT = P.T / c->ratio;
-  P.ntt = (N + P.T - 1) / P.T;
-  P.G = N / c->ratio;
+  P.ntt = (ck.a + N + P.T - 1) / P.T;
+  P.G = ck.G;
+  P.a = ck.a;
+  P.g0 = ck.g0;
+  P.gend = ck.gend;
   P.ncol = c->pk.cols();
   P.slots = c->slots;
   P.slot_offset = slot_offset;
   P.pk = c->pk;
   P.state = c->state;
   P.pooled = (uint16_t*)scratch;
+  P.carry = nullptr;
   P.flag = c->dev_flag;
   P.w = c->w_planes;
+  if (chunk_needs_carry(ck, c->overlap)) {
+    float* carry = (float*)((uint8_t*)scratch + carry_offset((size_t)B * P.ntt * P.GT * c->H * sizeof(uint16_t)));
+    chunk_carry_kernel<<<dim3((c->H + 127) / 128, B), 128, 0, s>>>(c->state, c->pk, c->overlap, c->slots, slot_offset,
+                                                                  ck, carry);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    P.carry = carry;
+  }
   CUtensorMap mx;
   {
     // x: [B][N][dim] bf16; out-of-range tokens (the halo before token 0, the tail past N) read as 0
@@ -417,9 +523,17 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(c->pk.ntiles, P.ntt, B);
-  prefill_tc_kernel<TOK><<<grid, kThreads, smem, s>>>(mx, P);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t pc = {};
+  pc.gridDim = dim3(c->pk.ntiles, P.ntt, B);
+  pc.blockDim = dim3(kThreads, 1, 1);
+  pc.dynamicSmemBytes = smem;
+  pc.stream = s;
+  pc.attrs = pdl;
+  pc.numAttrs = P.carry ? 1 : 0;  // started early only behind a chunk's carry kernel
+  cudaError_t e = cudaLaunchKernelEx(&pc, prefill_tc_kernel<TOK>, mx, P);
   if (e != cudaSuccess || P.G == 0) return e;
   // the entries: RMSNorm, RoPE and fp4, one CTA each, started early by programmatic dependent
   // launch (the pooled values are read after its wait)
@@ -428,6 +542,7 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
   Q.GT = P.GT;
   Q.ntt = P.ntt;
   Q.ratio = c->ratio;
+  Q.ck = ck;
   Q.pooled = P.pooled;
   Q.ep = epi_params(c);
   Q.out = out;
@@ -445,19 +560,22 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
 
 }  // namespace
 
-// Bytes of pooled scratch ([B][token tiles][groups per tile][H] bf16) a prefill of B x N tokens
-// needs.
-size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N) {
-  const int T = owned_tokens(c, prefill_tok(c, B, N));
+// Bytes of scratch a prefill call of B x N tokens needs: the pooled values ([B][token tiles]
+// [groups per tile][H] bf16) and, for a chunk whose first group has earlier candidates, their
+// running softmax values ([B][1 + overlap][3][H] f32).
+size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N, const Chunk& ck) {
+  const int T = owned_tokens(c, prefill_tok(c, B, ck.a + N));
   const int GT = T / c->ratio;
-  const int ntt = (N + T - 1) / T;
-  return (size_t)B * ntt * GT * c->H * sizeof(uint16_t);
+  const int ntt = (ck.a + N + T - 1) / T;
+  const size_t pooled = (size_t)B * ntt * GT * c->H * sizeof(uint16_t);
+  return chunk_needs_carry(ck, c->overlap) ? carry_offset(pooled) + (size_t)B * (1 + c->overlap) * 3 * c->H * 4
+                                           : pooled;
 }
 
 cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset,
-                              const csa_out& out, void* scratch, cudaStream_t s) {
-  return prefill_tok(c, B, N) == 224 ? launch_tok<224>(c, x, B, N, slot_offset, out, scratch, s)
-                                     : launch_tok<256>(c, x, B, N, slot_offset, out, scratch, s);
+                              const Chunk& ck, const csa_out& out, void* scratch, cudaStream_t s) {
+  return prefill_tok(c, B, ck.a + N) == 224 ? launch_tok<224>(c, x, B, N, slot_offset, ck, out, scratch, s)
+                                            : launch_tok<256>(c, x, B, N, slot_offset, ck, out, scratch, s);
 }
 
 }  // namespace csa

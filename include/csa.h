@@ -112,15 +112,33 @@ int csa_compressor_create(int dim, int head_dim, int ratio, int overlap, const c
 int csa_compressor_set_weights(csa_compressor* c, const float* wkv, const float* wgate, const float* norm_gain,
                                csa_stream_t stream);
 
-/* Prefill of B sequences of N tokens each.  x [B][N][dim] bf16 dev.  start_pos must be 0
- * (only whole-sequence prefill is defined; a later chunk goes through decode).  Sequence b
- * uses state slot slot_offset + b; needs slot_offset + B <= max_batch.  Writes
- * G = N / ratio entries per sequence to out ([B][G][..]) and leaves the trailing
- * N % ratio tokens in the state (at ratio 4 overlapped, also the last complete group's
- * tokens, whose branch B the next entry pools).  Returns G (0 means "no entry", the
- * pages' None) or a negative csa_status.  Requires r * (G - 1) < max_pos when RoPE is on. */
+/* Prefill of B sequences, tokens start_pos .. start_pos + N - 1 of each ("Pool token pairs",
+ * Compressor forward, prefill branch).  x [B][N][dim] bf16 dev.  Sequence b uses state slot
+ * slot_offset + b; needs slot_offset + B <= max_batch.
+ *  - start_pos 0: the whole-sequence prefill of the pages.  Writes G = N / ratio entries per
+ *    sequence and leaves the trailing N % ratio tokens in the state (at ratio 4 overlapped, also
+ *    the last complete group's tokens, whose branch B the next entry pools).
+ *  - start_pos > 0: a chunk continuing sequences whose earlier tokens went through prefill,
+ *    chunks or decode (all B at the same position).  The pages define this only one token at a
+ *    time (the decode branch); a chunk gives the results of N such steps ("Compressed Sparse
+ *    Attention", "prefill and decode use the same rule"): the entries of the groups that
+ *    complete inside the chunk, G = (start_pos + N) / ratio - start_pos / ratio, their earlier
+ *    candidates read from the state, and a state holding the chunk's tokens of the unfinished
+ *    group (and, overlapped, of the last complete group).
+ * Entry j of sequence b (group start_pos / ratio + j, RoPE position ratio * that group) goes to
+ * row b * G + j of out ([B][G][..]).  Returns G (0 means "no entry", the pages' None) or a
+ * negative csa_status.  Requires ratio * (last group) < max_pos when RoPE is on. */
 int csa_compress_prefill(csa_compressor* c, const uint16_t* x, int B, int N, int start_pos, int slot_offset,
                          const csa_out* out, csa_stream_t stream);
+
+/* The same prefill (whole sequence or chunk), writing each entry straight into the caller's
+ * compressed-KV cache at its group index: group g of sequence b goes to row b * cache_rows + g
+ * of each array of *cache ([B][cache_rows][..], same element layouts as csa_out; codes, scales
+ * and prequant may be NULL).  The pages have no such call; it saves the copy from out into a
+ * cache.  Needs (start_pos + N) / ratio <= cache_rows; rows of other groups are not touched.
+ * Returns the number of entries written per sequence, or a negative csa_status. */
+int csa_compress_prefill_into(csa_compressor* c, const uint16_t* x, int B, int N, int start_pos, int slot_offset,
+                              const csa_out* cache, int cache_rows, csa_stream_t stream);
 
 /* Prefill that allocates no device memory.  The pages have no counterpart: this exists for
  * callers that cannot let the library call cudaMalloc, such as serving runtimes that reserve
@@ -131,10 +149,11 @@ int csa_compress_prefill(csa_compressor* c, const uint16_t* x, int B, int N, int
  * the process exits).  It therefore needs:
  *  - a shape that runs the tensor-core kernel (csa_uses_tensor_cores(c) == 1, x 16-byte
  *    aligned); other shapes return CSA_ERR_ARG;
- *  - B * ceil(N / T) * (T / ratio) * head_dim * 2 <= 16 MiB, with T the tokens a tile owns
- *    (the launch takes a tile of 224 or 256 tokens: at ratio 4 overlapped T = 220 or 252,
- *    else the largest multiple of ratio <= the tile); larger calls return CSA_ERR_ARG
- *    ("too large") without launching anything.
+ *  - B * ceil((a + N) / T) * (T / ratio) * head_dim * 2 <= 16 MiB, with a = start_pos % ratio
+ *    and T the tokens a tile owns (the launch takes a tile of 224 or 256 tokens: at ratio 4
+ *    overlapped T = 220 or 252, else the largest multiple of ratio <= the tile), plus, for a
+ *    chunk whose first group has earlier candidates, B * head_dim * 12 bytes (rounded up to
+ *    256); larger calls return CSA_ERR_ARG ("too large") without launching anything.
  * The first call on each device looks up the array's device address (with that device
  * current); make that first call before any stream capture.  Every call shares the one
  * array: calls that overlap on the GPU (other streams, other handles) race, so serialise

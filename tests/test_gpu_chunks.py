@@ -1,0 +1,147 @@
+"""Prefill chunks at start_pos > 0 and prefill straight into a caller's compressed-KV cache.
+
+A chunk continues sequences whose earlier tokens are in the state: its entries and the state
+it leaves must be those of the oracle's chunk (itself pinned to token-by-token decode and to
+one whole prefill).  Each call of a chain is compared with the oracle (entries within the
+parity tolerance of the other tests, state within f32 rounding), then decode steps continue
+the chain.  Shapes cover both projection paths (tensor-core and CUDA-core), chunks that start
+mid-group, complete no group, span several token tiles, and the ratios 1, 3, 4 (overlapped),
+8, 128 and 300.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+from _util import layer_inputs
+from test_gpu_parity import DEV, check_entries, dev_bits, make_pair, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def check_state(g, o, what):
+    kg, sg = (t.cpu().numpy() for t in g.state_export())
+    ko, so = o.state()
+    assert np.allclose(kg, ko, rtol=2e-5, atol=2e-5 * np.abs(ko).max(initial=1.0)), what
+    assert np.array_equal(np.isinf(sg), np.isinf(so)), what
+    fin = np.isfinite(so)
+    assert np.allclose(sg[fin], so[fin], rtol=2e-5, atol=2e-5 * np.abs(so[fin]).max(initial=1.0)), what
+
+
+CHAINS = [
+    # dim, H, ratio, overlap, B, chunk lengths (the first call starts at position 0)
+    (256, 128, 4, 1, 2, (6, 1, 2, 4 * 70 + 3, 9, 500)),
+    (256, 512, 4, 1, 1, (1, 2, 260, 4)),
+    (256, 512, 128, 0, 2, (100, 30, 128 * 3 + 77, 5)),
+    (192, 256, 8, 0, 2, (13, 8 * 40 + 3, 4, 8)),
+    (128, 64, 1, 0, 2, (5, 7)),
+    (128, 32, 3, 0, 2, (4, 3 * 90 + 2, 1)),      # packed tile narrower than 128 rows: CUDA-core path
+    (128, 64, 300, 0, 1, (310, 300 * 2 + 7, 5)),  # ratio above one token tile: CUDA-core path
+]
+
+
+@pytest.mark.parametrize("dim,H,ratio,overlap,B,chunks", CHAINS)
+def test_prefill_chunks_then_decode(dim, H, ratio, overlap, B, chunks):
+    layer = synthetic.Layer(dim, H, ratio, overlap, 1.0 / math.sqrt(dim), gate_scale=2.0, rope_dim=min(64, H), fp4=1)
+    g, o = make_pair(11, layer, max_batch=B + 1)
+    P = sum(chunks)
+    x, *_ = layer_inputs(11, layer, B, P + 5)
+    p0 = 0
+    for n in chunks:
+        xc = np.ascontiguousarray(x[:, p0:p0 + n])
+        ref = o.prefill(xc, slot_offset=1, start_pos=p0)
+        got = g.prefill(dev_bits(xc), slot_offset=1, start_pos=p0)
+        torch.cuda.synchronize()
+        G = (p0 + n) // ratio - p0 // ratio
+        assert ref["G"] == G and (got is None) == (G == 0)
+        if G:
+            check_entries(to_np(got), ref["prequant"], 1, f"chunk at {p0} (+{n})")
+        check_state(g, o, f"state after the chunk at {p0}")
+        p0 += n
+    # decode continues the chained sequences
+    for k in range(5):
+        sp = np.full(B, P + k, np.int32)
+        xt = np.ascontiguousarray(x[:, P + k])
+        xt_all = np.concatenate([np.zeros((1, dim), np.uint16), xt])  # slot 0 restarts at position 0
+        sp_all = np.concatenate([[0], sp]).astype(np.int32)
+        r = o.decode(xt_all, sp_all)
+        d = g.decode(dev_bits(xt_all), torch.from_numpy(sp_all).to(DEV))
+        em = d["emitted"].cpu().numpy()
+        assert np.array_equal(em, r["emitted"])
+        rows = np.flatnonzero(em)
+        if rows.size:
+            check_entries(to_np(d, rows=rows), r["prequant"][rows], 1, f"decode after chunks, step {k}")
+    assert g.device_status() == 0
+
+
+def test_prefill_into_cache_rows():
+    layer = synthetic.Layer(256, 128, 4, 1, 1.0 / 16, gate_scale=2.0, rope_dim=64, fp4=1)
+    B, rows = 2, 100
+    g, _ = make_pair(12, layer, max_batch=B)
+    h, _ = make_pair(12, layer, max_batch=B)
+    x, *_ = layer_inputs(12, layer, B, 300)
+    H = layer.head_dim
+    cache = {"latent": torch.full((B, rows, H), 7.0, dtype=torch.bfloat16, device=DEV),
+             "codes": torch.full((B, rows, H // 2), 0xA5, dtype=torch.uint8, device=DEV),
+             "scales": torch.full((B, rows, H // 16), 0x5A, dtype=torch.uint8, device=DEV),
+             "prequant": torch.full((B, rows, H), 7.0, dtype=torch.bfloat16, device=DEV)}
+    p0 = 0
+    for n in (10, 50, 3, 201):
+        xc = dev_bits(np.ascontiguousarray(x[:, p0:p0 + n]))
+        wrote = g.prefill_into(xc, cache, start_pos=p0)
+        ref = h.prefill(xc, start_pos=p0)
+        g0, g1 = p0 // 4, (p0 + n) // 4
+        assert wrote == g1 - g0
+        if ref is not None:
+            for k in cache:  # the same kernels: identical bits
+                assert torch.equal(cache[k][:, g0:g1], ref[k]), (p0, k)
+        p0 += n
+    end = p0 // 4
+    assert torch.all(cache["latent"][:, end:] == 7.0) and torch.all(cache["codes"][:, end:] == 0xA5)
+    assert torch.all(cache["scales"][:, end:] == 0x5A) and torch.all(cache["prequant"][:, end:] == 7.0)
+    ka, sa = g.state_export()
+    kb, sb = h.state_export()
+    assert torch.equal(ka, kb) and torch.equal(sa, sb)
+    small = {k: v[:, :10].contiguous() for k, v in cache.items()}
+    with pytest.raises(Exception, match="does not fit"):
+        g.prefill_into(dev_bits(np.ascontiguousarray(x[:, :44])), small, start_pos=0)
+    assert g.device_status() == 0
+
+
+def test_flash_csa_chunked_prefill_full():
+    """Flash CSA shapes: a prefill of 1001 tokens, then a chunk of 2000 starting mid-group
+    (several token tiles), every entry against the oracle."""
+    wl = synthetic.FLASH_CSA
+    layer = wl.layers[0]
+    g, o = make_pair(wl.seed, layer)
+    x, *_ = layer_inputs(wl.seed, layer, 1, 3001)
+    p0 = 0
+    for n in (1001, 2000):
+        xc = np.ascontiguousarray(x[:, p0:p0 + n])
+        got = g.prefill(dev_bits(xc), start_pos=p0)
+        torch.cuda.synchronize()
+        ref = o.prefill(xc, start_pos=p0)
+        check_entries(to_np(got), ref["prequant"], 1, f"Flash CSA chunk at {p0}")
+        p0 += n
+    check_state(g, o, "Flash CSA state after the chunks")
+
+
+def test_hca_chunked_prefill():
+    """HCA shapes (ratio 128): a chunk that completes no group, then one starting 74 tokens into a
+    group and spanning three token tiles."""
+    wl = synthetic.HCA
+    layer = wl.layers[0]
+    g, o = make_pair(wl.seed, layer, max_batch=2)
+    x, *_ = layer_inputs(wl.seed, layer, 2, 1000)
+    p0 = 0
+    for n in (300, 30, 670):
+        xc = np.ascontiguousarray(x[:, p0:p0 + n])
+        got = g.prefill(dev_bits(xc), start_pos=p0)
+        torch.cuda.synchronize()
+        ref = o.prefill(xc, start_pos=p0)
+        if ref["G"]:
+            check_entries(to_np(got), ref["prequant"], 1, f"HCA chunk at {p0}")
+        p0 += n
+    check_state(g, o, "HCA state after the chunks")

@@ -319,7 +319,8 @@ def test_errors_are_reported_not_raised_on_the_device():
     with pytest.raises(csa.CSAError, match="RoPE table"):
         g.prefill(torch.zeros(1, 4 * 20, 128, dtype=torch.bfloat16, device=DEV))
     lib = csa.load_library()
-    assert lib.csa_compress_prefill(g.handle, x.data_ptr(), 1, 8, 5, 0, None, None) == -1
+    assert lib.csa_compress_prefill(g.handle, x.data_ptr(), 1, 8, -1, 0, None, None) == -1  # negative start_pos
+    assert lib.csa_compress_prefill(g.handle, x.data_ptr(), 1, 8, 5, 0, None, None) == -1  # entries but no out
     # decode positions the kernel cannot serve: flagged, rows not emitted, context still usable
     sp = torch.tensor([-3, 67], dtype=torch.int32, device=DEV)
     d = g.decode(torch.zeros(2, 128, dtype=torch.bfloat16, device=DEV), sp)
