@@ -57,6 +57,7 @@ def _load():
             "oracle_bf16_to_f32": ([U16], F), "oracle_e4m3_from_f32": ([F], U8),
             "oracle_e4m3_to_f64": ([U8], D), "oracle_e2m1_from_f32": ([F], U8), "oracle_e2m1_to_f64": ([U8], D),
             "oracle_fp4_e4m3": ([P, I64, P, P, P], None),
+            "oracle_fp4_e8m0": ([P, I64, P, P, P], None),
             "oracle_yarn_freqs": ([I, D, D, I, D, D, P], None),
             "oracle_yarn_bounds": ([I, D, I, D, D, P, P], None),
             "oracle_pool": ([P, P, I, I, P, P], None),
@@ -134,6 +135,19 @@ def fp4_e4m3(bf16_bits: np.ndarray):
     return codes, scales, out
 
 
+def fp4_e8m0(bf16_bits: np.ndarray):
+    """The indexer's fp4 round trip (power-of-two scales, block 32) of a uint16 (bf16 bits)
+    array whose size is a multiple of 32.  Returns (codes uint8 [n/2], scales uint8 [n/32]
+    e8m0 bytes, out uint16 [n])."""
+    x = np.ascontiguousarray(bf16_bits, dtype=np.uint16).reshape(-1)
+    nb = x.size // 32
+    codes = np.zeros(nb * 16, np.uint8)
+    scales = np.zeros(nb, np.uint8)
+    out = np.zeros(nb * 32, np.uint16)
+    _load().oracle_fp4_e8m0(_ptr(x), nb, _ptr(codes), _ptr(scales), _ptr(out))
+    return codes, scales, out
+
+
 def yarn_freqs(rope_dim=64, base=160000.0, factor=16.0, orig_len=4096, beta_fast=32.0, beta_slow=1.0):
     f = np.zeros(rope_dim // 2, np.float64)
     _load().oracle_yarn_freqs(rope_dim, base, factor, orig_len, beta_fast, beta_slow, _ptr(f))
@@ -198,10 +212,15 @@ class Compressor:
                    np.ascontiguousarray(gain, np.float32))
         self._lib.oracle_set_weights(self.h, _ptr(self._w[0]), _ptr(self._w[1]), _ptr(self._w[2]))
 
+    @property
+    def scale_block(self):
+        """Values per fp4 scale: 16 (e4m3 scales, the latent) or 32 (power-of-two scales)."""
+        return 32 if self.fp4 == 2 else 16
+
     def _outs(self, n):
         H = self.H
-        return (np.zeros((n, H), np.uint16), np.zeros((n, H // 2), np.uint8), np.zeros((n, H // 16), np.uint8),
-                np.zeros((n, H), np.uint16))
+        return (np.zeros((n, H), np.uint16), np.zeros((n, H // 2), np.uint8),
+                np.zeros((n, H // self.scale_block), np.uint8), np.zeros((n, H), np.uint16))
 
     def prefill(self, x_bf16, slot_offset=0, nthreads=None, start_pos=0):
         """x uint16 [B, N, dim] (tokens start_pos .. start_pos+N-1 of each sequence) ->
@@ -216,7 +235,7 @@ class Compressor:
             raise ValueError("oracle_prefill rejected the arguments")
         H = self.H
         return dict(G=g, latent=lat[:B * G].reshape(B, G, H), codes=cd[:B * G].reshape(B, G, H // 2),
-                    scales=sc[:B * G].reshape(B, G, H // 16), prequant=pq[:B * G].reshape(B, G, H))
+                    scales=sc[:B * G].reshape(B, G, H // self.scale_block), prequant=pq[:B * G].reshape(B, G, H))
 
     def prefill_groups(self, x_seq_bf16, groups, nthreads=None):
         """x uint16 [N, dim] (one sequence); groups: list of group indices -> outputs [ng, ...]."""

@@ -131,6 +131,30 @@ void fp4_block(const uint16_t* in, uint8_t* codes, uint8_t* scale, uint16_t* out
   }
 }
 
+// [RUST] fp4_quant_e8m0_inplace with block FP4_BLOCK = 32 (the indexer's fp4 round trip):
+// amax floored at 6*2^-126; scale = the power-of-two ceiling of amax/6 (float32 division),
+// kept as an e8m0 byte (an 8-bit biased exponent, bias 127, value 2^(byte-127)); each value
+// divided by the scale (exact: a power of two) to e2m1; dequantised and rounded to bf16.
+void fp4_block_e8m0(const uint16_t* in, uint8_t* codes, uint8_t* scale, uint16_t* out) {
+  float amax = 0.0f;
+  for (int i = 0; i < 32; ++i) amax = std::fmax(amax, (float)std::fabs(bf16_value(in[i])));
+  const float q = std::fmax(amax, std::ldexp(6.0f, -126)) / 6.0f;
+  int e = binade((double)q);                 // 2^e <= q < 2^(e+1)
+  if (std::ldexp(1.0, e) < (double)q) ++e;   // the smallest power of two >= q
+  const double s = std::ldexp(1.0, e);
+  *scale = (uint8_t)(e + 127);
+  for (int i = 0; i < 32; ++i) {
+    uint8_t c = e2m1_round((float)(bf16_value(in[i]) / s));
+    if (codes) {
+      if (i % 2 == 0)
+        codes[i / 2] = c;
+      else
+        codes[i / 2] |= (uint8_t)(c << 4);
+    }
+    out[i] = bf16_round(e2m1_value(c) * s);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // YaRN RoPE ([RUST] yarn_freqs_cis; [CSA4] "RoPE sub-dimension 64", applied
 // after normalisation).  NTK-by-parts frequency correction of Peng et al.
@@ -190,6 +214,7 @@ struct oracle_compressor {
   int width() const { return (1 + overlap) * H; }
   int slots() const { return overlap ? 8 : ratio; }  // overlap: 2 parities x 4
   int slot_width() const { return overlap ? 2 * H : H; }
+  int scale_block() const { return opt.fp4 == 2 ? 32 : 16; }  // values per fp4 scale
 };
 
 extern "C" {
@@ -205,6 +230,11 @@ double oracle_e2m1_to_f64(uint8_t c) { return e2m1_value(c); }
 void oracle_fp4_e4m3(const uint16_t* in, int64_t n_blocks, uint8_t* codes, uint8_t* scales, uint16_t* out) {
   for (int64_t b = 0; b < n_blocks; ++b)
     fp4_block(in + 16 * b, codes ? codes + 8 * b : nullptr, scales + b, out + 16 * b);
+}
+
+void oracle_fp4_e8m0(const uint16_t* in, int64_t n_blocks, uint8_t* codes, uint8_t* scales, uint16_t* out) {
+  for (int64_t b = 0; b < n_blocks; ++b)
+    fp4_block_e8m0(in + 32 * b, codes ? codes + 16 * b : nullptr, scales + b, out + 32 * b);
 }
 
 void oracle_yarn_freqs(int d, double base, double factor, int orig_len, double bf, double bs, double* f) {
@@ -275,6 +305,7 @@ void oracle_epilogue(const oracle_compressor* c, const float* pooled, int64_t po
 oracle_compressor* oracle_create(int dim, int H, int ratio, int overlap, const oracle_options* opt) {
   if (dim <= 0 || H <= 0 || H % 16 != 0 || ratio < 1 || (overlap && ratio != 4) || !opt) return nullptr;
   if (opt->rope_dim < 0 || opt->rope_dim % 2 || opt->rope_dim > H || opt->max_batch < 1) return nullptr;
+  if (opt->fp4 < 0 || opt->fp4 > 2 || (opt->fp4 == 2 && H % 32)) return nullptr;
   auto* c = new oracle_compressor();
   c->dim = dim;
   c->H = H;
@@ -359,14 +390,16 @@ void finish_entry(const oracle_compressor* c, const float* pooled, int64_t pos, 
   std::vector<uint16_t> pq(H), lat(H);
   std::vector<uint8_t> cd(H / 2), sc(H / 16);
   oracle_epilogue(c, pooled, pos, pq.data());
-  if (c->opt.fp4)
+  if (c->opt.fp4 == 1)  // the latent: e4m3 scales, block 16
     oracle_fp4_e4m3(pq.data(), H / 16, cd.data(), sc.data(), lat.data());
+  else if (c->opt.fp4 == 2)  // the indexer's keys: power-of-two scales, block 32
+    oracle_fp4_e8m0(pq.data(), H / 32, cd.data(), sc.data(), lat.data());
   else
     lat = pq;
   if (latent) std::memcpy(latent, lat.data(), H * 2);
   if (prequant) std::memcpy(prequant, pq.data(), H * 2);
   if (codes && c->opt.fp4) std::memcpy(codes, cd.data(), H / 2);
-  if (scales && c->opt.fp4) std::memcpy(scales, sc.data(), H / 16);
+  if (scales && c->opt.fp4) std::memcpy(scales, sc.data(), H / c->scale_block());
 }
 
 float* state_row(std::vector<float>& st, const oracle_compressor* c, int b, int slot) {
@@ -394,7 +427,7 @@ int oracle_prefill(oracle_compressor* c, const uint16_t* x, int B, int N, int sl
       oracle_pool(kv.data(), sc.data(), ncand, H, pooled.data(), nullptr);
       int64_t e = (int64_t)b * G + j;
       finish_entry(c, pooled.data(), r * j, latent ? latent + e * H : nullptr, codes ? codes + e * H / 2 : nullptr,
-                   scales ? scales + e * H / 16 : nullptr, prequant ? prequant + e * H : nullptr);
+                   scales ? scales + e * H / c->scale_block() : nullptr, prequant ? prequant + e * H : nullptr);
     });
     // [V41] the trailing partial group waits in the state (slots 0..rem-1).
     const int sb = slot_offset + b, sw = c->slot_width();
@@ -449,7 +482,7 @@ int oracle_prefill_groups(const oracle_compressor* c, const uint16_t* x, int N, 
     gather_group(c, kvp.data(), sp.data(), t0, j, kv.data(), sc.data());
     oracle_pool(kv.data(), sc.data(), ncand, H, pooled.data(), nullptr);
     finish_entry(c, pooled.data(), r * j, latent ? latent + g * H : nullptr, codes ? codes + g * H / 2 : nullptr,
-                 scales ? scales + g * H / 16 : nullptr, prequant ? prequant + g * H : nullptr);
+                 scales ? scales + g * H / c->scale_block() : nullptr, prequant ? prequant + g * H : nullptr);
   });
   return ng;
 }
@@ -512,7 +545,7 @@ int oracle_prefill_chunk(oracle_compressor* c, const uint16_t* x, int B, int N, 
       oracle_pool(kv.data(), sc.data(), ncand, H, pooled.data(), nullptr);
       const int64_t e = (int64_t)b * G + jj;
       finish_entry(c, pooled.data(), r * g, latent ? latent + e * H : nullptr, codes ? codes + e * H / 2 : nullptr,
-                   scales ? scales + e * H / 16 : nullptr, prequant ? prequant + e * H : nullptr);
+                   scales ? scales + e * H / c->scale_block() : nullptr, prequant ? prequant + e * H : nullptr);
     });
     // state: the new tokens of the unfinished group g_end and, overlapped, of group g_end - 1
     const int64_t keep_from = std::max(p0, (g_end - c->overlap) * r);
@@ -554,7 +587,7 @@ int oracle_decode(oracle_compressor* c, const uint16_t* x_tok, int B, const int3
         if (latent) std::memcpy(latent + b * H, lat.data(), H * 2);
         if (prequant) std::memcpy(prequant + b * H, pq.data(), H * 2);
         if (codes && c->opt.fp4) std::memcpy(codes + b * H / 2, cd.data(), H / 2);
-        if (scales && c->opt.fp4) std::memcpy(scales + b * H / 16, sc.data(), H / 16);
+        if (scales && c->opt.fp4) std::memcpy(scales + b * H / c->scale_block(), sc.data(), H / c->scale_block());
       }
       return;
     }
@@ -572,7 +605,7 @@ int oracle_decode(oracle_compressor* c, const uint16_t* x_tok, int B, const int3
                   pooled.data(), nullptr);
       emit[b] = 1;
       finish_entry(c, pooled.data(), p + 1 - r, latent ? latent + b * H : nullptr,
-                   codes ? codes + b * H / 2 : nullptr, scales ? scales + b * H / 16 : nullptr,
+                   codes ? codes + b * H / 2 : nullptr, scales ? scales + b * H / c->scale_block() : nullptr,
                    prequant ? prequant + b * H : nullptr);
       return;
     }
@@ -591,7 +624,7 @@ int oracle_decode(oracle_compressor* c, const uint16_t* x_tok, int B, const int3
     oracle_pool(ck.data(), cs.data(), 8, H, pooled.data(), nullptr);
     emit[b] = 1;
     finish_entry(c, pooled.data(), p - 3, latent ? latent + b * H : nullptr, codes ? codes + b * H / 2 : nullptr,
-                 scales ? scales + b * H / 16 : nullptr, prequant ? prequant + b * H : nullptr);
+                 scales ? scales + b * H / c->scale_block() : nullptr, prequant ? prequant + b * H : nullptr);
   });
   int n = 0;
   for (int b = 0; b < B; ++b) {

@@ -38,7 +38,8 @@ typedef struct {
   double rope_factor;
   int rope_orig_len;
   double beta_fast, beta_slow;
-  int fp4;           /* 1 = e2m1 values / e4m3 scales round trip on the latent */
+  int fp4;           /* 1 = e2m1 values / e4m3 scales per 16 (the latent); 2 = e2m1 values /
+                        power-of-two (e8m0) scales per 32 (the indexer's keys); 0 = off */
   double eps;        /* RMSNorm epsilon */
 } oracle_options;
 
@@ -54,6 +55,9 @@ uint8_t oracle_e2m1_from_f32(float v);             /* RNE ties to even code, sig
 double oracle_e2m1_to_f64(uint8_t code);
 /* fp4 round trip of n consecutive blocks of 16 bf16 values. */
 void oracle_fp4_e4m3(const uint16_t* in, int64_t n_blocks, uint8_t* codes, uint8_t* scales, uint16_t* out);
+/* The indexer's fp4 round trip of n consecutive blocks of 32 bf16 values: codes [n][16],
+ * scales [n] e8m0 bytes (2^(byte - 127)), out [n][32] bf16. */
+void oracle_fp4_e8m0(const uint16_t* in, int64_t n_blocks, uint8_t* codes, uint8_t* scales, uint16_t* out);
 
 /* ---- RoPE ---- */
 /* corrected inverse frequencies f'_i, i < rope_dim/2 */

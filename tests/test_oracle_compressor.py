@@ -190,7 +190,8 @@ def test_worked_example_ratio4_overlap():
 # ---- prefill == decode ----------------------------------------------------------------------
 
 @pytest.mark.parametrize("ratio,overlap,N,rope,fp4", [(2, 0, 64, 0, 0), (4, 1, 37, 16, 1), (4, 1, 3, 16, 1),
-                                                      (3, 0, 29, 16, 1), (1, 0, 6, 16, 1), (16, 0, 50, 16, 1)])
+                                                      (3, 0, 29, 16, 1), (1, 0, 6, 16, 1), (16, 0, 50, 16, 1),
+                                                      (4, 1, 21, 16, 2)])
 def test_prefill_equals_token_by_token_decode(ratio, overlap, N, rope, fp4):
     dim, H = 64, 32
     B = 2
@@ -309,6 +310,17 @@ def test_prefill_chunk_reads_its_own_slots():
     second = d.prefill(x[1:2, 6:], slot_offset=2, start_pos=6)
     assert np.array_equal(first["latent"][1], second["latent"][0])
     assert not np.array_equal(first["latent"][0], first["latent"][1])
+
+
+def test_indexer_quantiser_applies_to_the_prequant_latent():
+    """fp4 = 2 (the indexer's keys): the latent is the e8m0 / block-32 round trip of prequant,
+    one scale per 32 features."""
+    c, _ = make(64, 64, 4, 1, rope_dim=16, fp4=2)
+    out = c.prefill(rand_x(21, 1, 4 * 9 + 1, 64))
+    codes, scales, lat = oracle.fp4_e8m0(out["prequant"])
+    assert out["scales"].shape == (1, 9, 2)
+    assert np.array_equal(out["scales"].reshape(-1), scales) and np.array_equal(out["codes"].reshape(-1), codes)
+    assert np.array_equal(out["latent"].reshape(-1), lat)
 
 
 def test_prefill_state_holds_the_tail_projections():

@@ -177,3 +177,55 @@ def test_fp4_block_all_bf16_patterns_against_search():
         c0 = int(codes[r, 0] & 0xF)
         assert c0 == e2m1_by_search(float(q)), (hex(blocks[r, 0]), float(q), c0)
         assert oracle.bf16_to_f32(int(out[r, 0])) == np.float32(E2M1_GRID[c0 & 7] * (1 - 2 * (c0 >> 3)) * s)
+
+
+# ---- the indexer's fp4 block: power-of-two (e8m0) scales, block 32 ------------------------
+
+def test_e8m0_scale_examples():
+    for amax, byte, val in _rows("e8m0_scale_examples.txt"):
+        blk = np.zeros(32, np.uint16)
+        blk[5] = oracle.bf16_from_f32(float(amax))
+        blk[30] = oracle.bf16_from_f32(-float(amax) / 3)
+        _, scales, _ = oracle.fp4_e8m0(blk)
+        assert scales[0] == int(byte), (amax, scales[0], byte)
+        assert Fraction(2) ** (int(scales[0]) - 127) == Fraction(float(val))
+
+
+def test_fp4_e8m0_blocks_against_exact_arithmetic():
+    """Random blocks over 60 decades: the scale is the least power of two at or above the
+    float32 quotient amax/6 (exact rationals), every code is the search-based e2m1 of
+    value/scale, the dequantised value is code * scale, and codes pack two per byte."""
+    rng = np.random.default_rng(4)
+    nb = 3000
+    mags = 10.0 ** rng.uniform(-30, 30, size=(nb, 1))
+    vals = (rng.standard_normal((nb, 32)) * mags).astype(np.float32)
+    vals[:20] = 0.0
+    vals[20:40, 7] = 6.0 * 2.0 ** rng.integers(-20, 20, size=20)  # amax / 6 a power of two
+    bits = np.stack([[oracle.bf16_from_f32(float(v)) for v in row] for row in vals]).astype(np.uint16)
+    codes, scales, out = oracle.fp4_e8m0(bits)
+    codes = codes.reshape(nb, 16)
+    out = out.reshape(nb, 32)
+    floor = Fraction(6) * Fraction(2) ** -126
+    for r in range(nb):
+        v = (bits[r].astype(np.uint32) << 16).view(np.float32)
+        amax = max(Fraction(float(np.max(np.abs(v)))), floor)
+        q = Fraction(float(np.float32(float(amax)) / np.float32(6.0)))  # the float32 quotient
+        s = Fraction(2) ** (int(scales[r]) - 127)
+        assert s >= q and s / 2 < q, (r, float(q), float(s))
+        for i in range(32):
+            c = int(codes[r, i // 2] >> (4 * (i % 2))) & 0xF
+            assert c == e2m1_by_search(float(Fraction(float(v[i])) / s)), (r, i)
+            want = Fraction(float(E2M1_GRID[c & 7])) * s * (-1 if c & 8 else 1)
+            assert Fraction(float(oracle.bf16_to_f32(int(out[r, i])))) == want, (r, i)
+
+
+def test_fp4_e8m0_exact_powers():
+    # amax = 6 * 2^k: scale 2^k, the largest value maps to code 7 (6.0), half of it to 3.0
+    for k in (-100, -3, 0, 5, 100):
+        blk = np.zeros(32, np.uint16)
+        blk[0] = oracle.bf16_from_f32(6.0 * 2.0 ** k)
+        blk[1] = oracle.bf16_from_f32(-3.0 * 2.0 ** k)
+        codes, scales, out = oracle.fp4_e8m0(blk)
+        assert scales[0] == 127 + k
+        assert codes[0] == (0x7 | (0xD << 4))
+        assert oracle.bf16_to_f32(int(out[0])) == 6.0 * 2.0 ** k
