@@ -21,7 +21,8 @@ import torch
 
 from . import build as _build_mod
 
-__all__ = ["Compressor", "CSAError", "load_library", "fp4_e4m3_roundtrip", "rope_table", "default_options",
+__all__ = ["Compressor", "CSAError", "load_library", "fp4_e4m3_roundtrip", "fp4_e8m0_roundtrip", "rope_table",
+           "default_options",
            "library_path", "ABI_FUNCTIONS"]
 
 _lock = threading.Lock()
@@ -32,7 +33,8 @@ ABI_FUNCTIONS = ("csa_options_default", "csa_compressor_create", "csa_compressor
                  "csa_compress_prefill", "csa_compress_decode", "csa_state_reset", "csa_state_elems",
                  "csa_state_export", "csa_device_status", "csa_compressor_destroy", "csa_last_error",
                  "csa_fp4_e4m3_roundtrip", "csa_rope_table", "csa_set_profile_events", "csa_kernel_launches",
-                 "csa_uses_tensor_cores", "csa_compress_prefill_noalloc", "csa_compress_prefill_into")
+                 "csa_uses_tensor_cores", "csa_compress_prefill_noalloc", "csa_compress_prefill_into",
+                 "csa_fp4_e8m0_roundtrip")
 
 
 class CSAError(RuntimeError):
@@ -81,6 +83,7 @@ def load_library(build_if_missing: bool = True):
             "csa_compressor_destroy": ([P], None),
             "csa_last_error": ([], ctypes.c_char_p),
             "csa_fp4_e4m3_roundtrip": ([P, I64, P, P, P, P], I),
+            "csa_fp4_e8m0_roundtrip": ([P, I64, P, P, P, P], I),
             "csa_rope_table": ([P, I, I, P, P], I),
             "csa_set_profile_events": ([P, P, P], I),
             "csa_kernel_launches": ([P], I64),
@@ -162,12 +165,17 @@ class Compressor:
         _check(self._lib.csa_compressor_set_weights(self._h, _dptr(wkv), _dptr(wgate), _dptr(gain),
                                                     _stream(stream)), "csa_compressor_set_weights")
 
+    @property
+    def scale_block(self) -> int:
+        """Features per fp4 scale: 16 (e4m3 scales, fp4 = 1) or 32 (power-of-two scales, fp4 = 2)."""
+        return 32 if self.options.fp4 == 2 else 16
+
     def _alloc_out(self, rows, device, prequant=True):
         H = self.head_dim
         fp4 = bool(self.options.fp4)
         d = dict(latent=torch.empty(rows, H, dtype=torch.bfloat16, device=device),
                  codes=torch.empty(rows, H // 2, dtype=torch.uint8, device=device) if fp4 else None,
-                 scales=torch.empty(rows, H // 16, dtype=torch.uint8, device=device) if fp4 else None,
+                 scales=torch.empty(rows, H // self.scale_block, dtype=torch.uint8, device=device) if fp4 else None,
                  prequant=torch.empty(rows, H, dtype=torch.bfloat16, device=device) if prequant else None)
         return d
 
@@ -193,7 +201,8 @@ class Compressor:
         if g == 0:
             return None
         H = self.head_dim
-        shp = {"latent": (B, g, H), "codes": (B, g, H // 2), "scales": (B, g, H // 16), "prequant": (B, g, H)}
+        shp = {"latent": (B, g, H), "codes": (B, g, H // 2), "scales": (B, g, H // self.scale_block),
+               "prequant": (B, g, H)}
         return {k: (None if v is None else v[:B * g].view(*shp[k])) for k, v in out.items()}
 
     def prefill_into(self, x, cache, start_pos: int = 0, slot_offset: int = 0, stream=None) -> int:
@@ -268,6 +277,20 @@ def fp4_e4m3_roundtrip(x, stream=None):
     out = torch.empty(nb * 16, dtype=torch.bfloat16, device=x.device)
     _check(lib.csa_fp4_e4m3_roundtrip(_dptr(_u16(x)), nb, _dptr(codes), _dptr(scales), _dptr(_u16(out)),
                                       _stream(stream)), "csa_fp4_e4m3_roundtrip")
+    return codes, scales, out
+
+
+def fp4_e8m0_roundtrip(x, stream=None):
+    """The indexer's fp4 round trip: bf16 CUDA tensor (size a multiple of 32) -> (codes u8 [n/2],
+    scales u8 [n/32] e8m0 bytes, out bf16 [n])."""
+    lib = load_library()
+    x = x.contiguous().view(-1)
+    nb = x.numel() // 32
+    codes = torch.empty(nb * 16, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(nb, dtype=torch.uint8, device=x.device)
+    out = torch.empty(nb * 32, dtype=torch.bfloat16, device=x.device)
+    _check(lib.csa_fp4_e8m0_roundtrip(_dptr(_u16(x)), nb, _dptr(codes), _dptr(scales), _dptr(_u16(out)),
+                                      _stream(stream)), "csa_fp4_e8m0_roundtrip")
     return codes, scales, out
 
 

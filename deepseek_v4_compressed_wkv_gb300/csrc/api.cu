@@ -77,7 +77,11 @@ bool check_options(const csa_options& o, int H, std::string& why) {
   } else if (o.rope_dim > 0 && (o.max_pos < 1 || !(o.rope_base > 1.0f) || !(o.rope_factor > 0.0f) ||
                                 o.rope_orig_len < 1 || !(o.beta_fast > 0.0f) || !(o.beta_slow > 0.0f)))
     why = "invalid RoPE options (max_pos, rope_base, rope_factor, rope_orig_len, beta_fast, beta_slow)";
-  else if (o.fp4 != 0 && o.fp4 != 1) why = "fp4 must be 0 or 1";
+  else if (o.fp4 < 0 || o.fp4 > 2) why = "fp4 must be 0 (off), 1 (e4m3 scales, block 16) or 2 (power-of-two scales, block 32)";
+  else if (o.fp4 == 2 && H % 32) {
+    snprintf(buf, sizeof buf, "fp4 = 2 quantises blocks of 32 features: head_dim %d must be a multiple of 32", H);
+    why = buf;
+  }
   else if (!(o.eps >= 0.0f)) why = "eps must be >= 0";
   else return true;
   return false;
@@ -416,6 +420,13 @@ int csa_fp4_e4m3_roundtrip(const uint16_t* in, int64_t n_blocks, uint8_t* codes,
                            csa_stream_t stream) {
   if (n_blocks < 0 || (n_blocks > 0 && (!in || !scales || !out))) return fail(CSA_ERR_ARG, "bad arguments");
   CSA_CUDA(csa::launch_fp4_roundtrip(in, n_blocks, codes, scales, out, (cudaStream_t)stream), "fp4 launch");
+  return CSA_OK;
+}
+
+int csa_fp4_e8m0_roundtrip(const uint16_t* in, int64_t n_blocks, uint8_t* codes, uint8_t* scales, uint16_t* out,
+                           csa_stream_t stream) {
+  if (n_blocks < 0 || (n_blocks > 0 && (!in || !scales || !out))) return fail(CSA_ERR_ARG, "bad arguments");
+  CSA_CUDA(csa::launch_fp4_e8m0_roundtrip(in, n_blocks, codes, scales, out, (cudaStream_t)stream), "fp4 launch");
   return CSA_OK;
 }
 

@@ -106,7 +106,7 @@ struct EpiParams {
   const float* gain;      // [H]
   const float* rope_cos;  // [max_pos][rope_dim/2]
   const float* rope_sin;
-  int H, rope_dim, fp4, max_pos;
+  int H, rope_dim, fp4, max_pos;  // fp4: 0 off, 1 e4m3 scale per 16, 2 power-of-two scale per 32
   float eps;
 };
 
@@ -167,6 +167,41 @@ __device__ __forceinline__ void fp4_block16(float y[16], uint8_t codes[8], uint8
   }
 }
 
+// Power-of-two scale of the indexer's fp4 round trip ("Module compress", fp4_quant_e8m0_inplace):
+// the smallest power of two >= max(amax, 6 * 2^-126) / 6, the division in IEEE f32.  The
+// quotient is a normal float (>= 2^-126), so the ceiling is its exponent, plus one unless the
+// mantissa is zero.  *byte receives the e8m0 encoding (the biased exponent, value 2^(byte-127)).
+__device__ __forceinline__ float e8m0_scale(float amax, uint32_t* byte) {
+  const float q = __fdiv_rn(fmaxf(amax, 6.0f * 1.17549435082228750797e-38f /* 6 * 2^-126 */), 6.0f);
+  const uint32_t u = __float_as_uint(q);
+  const uint32_t e = (u >> 23) + ((u & 0x7FFFFFu) != 0u ? 1u : 0u);
+  *byte = e;
+  return __uint_as_float(e << 23);
+}
+
+// fp4 round trip of one block of 32 bf16 values with a power-of-two scale ("Module compress",
+// fp4_quant_e8m0_inplace, FP4_BLOCK = 32): values divided by the scale (exact) to e2m1,
+// dequantised and rounded to bf16 in place.
+__device__ __forceinline__ void fp4_block32_e8m0(float y[32], uint8_t codes[16], uint8_t* scale_byte) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(y[i]));
+  uint32_t sb;
+  const float s = e8m0_scale(amax, &sb);
+  *scale_byte = (uint8_t)sb;
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const uint32_t c2 = e2m1x2(__fdiv_rn(y[i], s), __fdiv_rn(y[i + 1], s));
+    codes[i / 2] = (uint8_t)c2;
+    y[i] = bf16_round(e2m1_value(c2 & 15u) * s);
+    y[i + 1] = bf16_round(e2m1_value(c2 >> 4) * s);
+  }
+}
+
+// Values per fp4 scale of the compressor's output: 16 (e4m3 scales, the latent) or 32
+// (power-of-two scales, the indexer's keys).
+__host__ __device__ inline int fp4_scale_block(int fp4) { return fp4 == 2 ? 32 : 16; }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -182,7 +217,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ void entry_epilogue_block(float v[16], int f0, float inv, const float* gain,
                                                      const float* cs, const float* sn, const EpiParams& ep,
                                                      uint16_t* latent, uint8_t* codes, uint8_t* scales,
-                                                     uint16_t* prequant) {
+                                                     uint16_t* prequant, unsigned lanes) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = bf16_round(v[i] * inv * gain[i]);
   const int r0 = ep.H - ep.rope_dim;
@@ -207,7 +242,29 @@ __device__ __forceinline__ void entry_epilogue_block(float v[16], int f0, float 
     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
   }
-  if (ep.fp4) {
+  if (ep.fp4 == 2) {  // power-of-two scale over 32 features: this lane and its neighbour
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(lanes, amax, 1));
+    uint32_t sb;
+    const float s = e8m0_scale(amax, &sb);
+    uint8_t cd[8];
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      const uint32_t c2 = e2m1x2(__fdiv_rn(v[i], s), __fdiv_rn(v[i + 1], s));
+      cd[i / 2] = (uint8_t)c2;
+      v[i] = bf16_round(e2m1_value(c2 & 15u) * s);
+      v[i + 1] = bf16_round(e2m1_value(c2 >> 4) * s);
+    }
+    if (codes) {
+      uint2 pk;
+      pk.x = cd[0] | (cd[1] << 8) | (cd[2] << 16) | ((uint32_t)cd[3] << 24);
+      pk.y = cd[4] | (cd[5] << 8) | (cd[6] << 16) | ((uint32_t)cd[7] << 24);
+      *reinterpret_cast<uint2*>(codes + f0 / 2) = pk;
+    }
+    if (scales && (f0 & 31) == 0) scales[f0 >> 5] = (uint8_t)sb;
+  } else if (ep.fp4) {
     uint8_t cd[8], sb;
     fp4_block16(v, cd, &sb);
     if (codes) {
@@ -230,8 +287,9 @@ __device__ __forceinline__ void entry_epilogue_block(float v[16], int f0, float 
 // RMSNorm factor `inv` is known: v[] holds the bf16-rounded pooled values, gn[] the gain,
 // rc/rs the RoPE cos/sin of the pairs (f, f+1) and (f+2, f+3) (used for pairs at or past
 // H - rope_dim).  RMSNorm with one bf16 rounding, RoPE, then the fp4 round trip, whose block
-// of 16 features is four adjacent lanes (all 32 lanes of the warp must call it; `act` is the
-// same for the four lanes of a block), and the stores.
+// is four adjacent lanes (16 features, e4m3 scale) or eight (32 features, power-of-two scale)
+// (all 32 lanes of the warp must call it; `act` is the same for the lanes of a block), and the
+// stores.
 __device__ __forceinline__ void entry_epilogue_quad(const float v[4], bool act, int f, int lane, float inv,
                                                    const float gn[4], const float rc[2], const float rs[2],
                                                    const EpiParams& ep, size_t e, const csa_out& out) {
@@ -259,9 +317,16 @@ __device__ __forceinline__ void entry_epilogue_quad(const float v[4], bool act, 
     for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(y[i]));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    const float sq = __fdiv_rn(fmaxf(amax, 0.01171875f /* 6 * 2^-9 */), 6.0f);
-    const __nv_fp8_storage_t sb = __nv_cvt_float_to_fp8(sq, __NV_SATFINITE, __NV_E4M3);
-    const float scl = e4m3_value(sb);
+    uint32_t sb;
+    float scl;
+    if (ep.fp4 == 2) {  // power-of-two scale over 32 features: eight lanes
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+      scl = e8m0_scale(amax, &sb);
+    } else {  // e4m3 scale over 16 features: four lanes
+      const float sq = __fdiv_rn(fmaxf(amax, 0.01171875f /* 6 * 2^-9 */), 6.0f);
+      sb = __nv_cvt_float_to_fp8(sq, __NV_SATFINITE, __NV_E4M3);
+      scl = e4m3_value(sb);
+    }
     const uint32_t c0 = e2m1x2(__fdiv_rn(y[0], scl), __fdiv_rn(y[1], scl));  // element 2i in the low nibble
     const uint32_t c1 = e2m1x2(__fdiv_rn(y[2], scl), __fdiv_rn(y[3], scl));
     y[0] = bf16_round(e2m1_value(c0 & 15u) * scl);
@@ -269,7 +334,8 @@ __device__ __forceinline__ void entry_epilogue_quad(const float v[4], bool act, 
     y[2] = bf16_round(e2m1_value(c1 & 15u) * scl);
     y[3] = bf16_round(e2m1_value(c1 >> 4) * scl);
     if (act && out.codes) *reinterpret_cast<uint16_t*>(out.codes + e * (H / 2) + f / 2) = (uint16_t)(c0 | (c1 << 8));
-    if (act && out.scales && (lane & 3) == 0) out.scales[e * (H / 16) + f / 16] = sb;
+    const int blk = fp4_scale_block(ep.fp4);
+    if (act && out.scales && (lane & (blk / 4 - 1)) == 0) out.scales[e * (H / blk) + f / blk] = (uint8_t)sb;
   }
   if (act)
     *reinterpret_cast<uint2*>(out.latent + e * H + f) =
@@ -301,8 +367,9 @@ __device__ __forceinline__ void entry_epilogue(float v[16], int lane, long long 
   const float inv = rms_inv(ss, ep);
   if (!act) return;
   const int hr = ep.rope_dim >> 1;
+  const unsigned lanes = nl >= 32 ? 0xffffffffu : (1u << nl) - 1u;  // the lanes that reach here
   entry_epilogue_block(v, lane * 16, inv, ep.gain + lane * 16, hr ? ep.rope_cos + pos * hr : nullptr,
-                       hr ? ep.rope_sin + pos * hr : nullptr, ep, latent, codes, scales, prequant);
+                       hr ? ep.rope_sin + pos * hr : nullptr, ep, latent, codes, scales, prequant, lanes);
 }
 
 }  // namespace csa

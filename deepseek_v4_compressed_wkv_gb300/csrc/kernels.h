@@ -19,6 +19,8 @@ cudaError_t launch_state_reset(const csa_compressor* c, int slot_begin, int coun
 cudaError_t launch_state_export(const csa_compressor* c, float* kv, float* score, cudaStream_t s);
 cudaError_t launch_fp4_roundtrip(const uint16_t* in, long long nb, uint8_t* codes, uint8_t* scales, uint16_t* out,
                                  cudaStream_t s);
+cudaError_t launch_fp4_e8m0_roundtrip(const uint16_t* in, long long nb, uint8_t* codes, uint8_t* scales,
+                                      uint16_t* out, cudaStream_t s);
 
 // Tensor-core prefill (prefill_tc.cu): projection + pool + norm + RoPE + fp4 + state update.
 bool prefill_tc_supported(const csa_compressor* c, const void* x);

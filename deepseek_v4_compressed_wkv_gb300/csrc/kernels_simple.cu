@@ -201,7 +201,8 @@ __global__ __launch_bounds__(128) void prefill_pool_kernel(const float* __restri
   const size_t H = pk.H;
   const size_t o = (size_t)ck.row(b, j);
   entry_epilogue(v, lane, (long long)ratio * g, ep, out.latent + o * H, out.codes ? out.codes + o * (H / 2) : nullptr,
-                 out.scales ? out.scales + o * (H / 16) : nullptr, out.prequant ? out.prequant + o * H : nullptr);
+                 out.scales ? out.scales + o * (H / fp4_scale_block(ep.fp4)) : nullptr,
+                 out.prequant ? out.prequant + o * H : nullptr);
 }
 
 __device__ __forceinline__ float padded_value(const Packing& pk, int col) {
@@ -280,7 +281,8 @@ __global__ __launch_bounds__(128) void decode_emit_kernel(const int32_t* __restr
   }
   const size_t H = pk.H;
   entry_epilogue(v, lane, pos, ep, out.latent + b * H, out.codes ? out.codes + b * (H / 2) : nullptr,
-                 out.scales ? out.scales + b * (H / 16) : nullptr, out.prequant ? out.prequant + b * H : nullptr);
+                 out.scales ? out.scales + b * (H / fp4_scale_block(ep.fp4)) : nullptr,
+                 out.prequant ? out.prequant + b * H : nullptr);
 }
 
 __global__ void state_reset_kernel(float* __restrict__ state, Packing pk, size_t first, size_t count) {
@@ -318,6 +320,24 @@ __global__ void fp4_roundtrip_kernel(const uint16_t* __restrict__ in, long long 
       for (int i = 0; i < 8; ++i) codes[b * 8 + i] = cd[i];
 #pragma unroll
     for (int i = 0; i < 16; ++i) out[b * 16 + i] = bf16_bits(y[i]);
+  }
+}
+
+// The indexer's fp4 round trip alone: one thread per block of 32 values.
+__global__ void fp4_e8m0_roundtrip_kernel(const uint16_t* __restrict__ in, long long nb, uint8_t* __restrict__ codes,
+                                          uint8_t* __restrict__ scales, uint16_t* __restrict__ out) {
+  for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nb; b += (long long)gridDim.x * blockDim.x) {
+    float y[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) y[i] = __uint_as_float((uint32_t)in[b * 32 + i] << 16);
+    uint8_t cd[16], sb;
+    fp4_block32_e8m0(y, cd, &sb);
+    scales[b] = sb;
+    if (codes)
+#pragma unroll
+      for (int i = 0; i < 16; ++i) codes[b * 16 + i] = cd[i];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) out[b * 32 + i] = bf16_bits(y[i]);
   }
 }
 
@@ -395,6 +415,12 @@ cudaError_t launch_state_export(const csa_compressor* c, float* kv, float* score
 cudaError_t launch_fp4_roundtrip(const uint16_t* in, long long nb, uint8_t* codes, uint8_t* scales, uint16_t* out,
                                  cudaStream_t s) {
   if (nb > 0) fp4_roundtrip_kernel<<<grid_cap((size_t)nb, 256), 256, 0, s>>>(in, nb, codes, scales, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp4_e8m0_roundtrip(const uint16_t* in, long long nb, uint8_t* codes, uint8_t* scales,
+                                      uint16_t* out, cudaStream_t s) {
+  if (nb > 0) fp4_e8m0_roundtrip_kernel<<<grid_cap((size_t)nb, 128), 128, 0, s>>>(in, nb, codes, scales, out);
   return cudaGetLastError();
 }
 

@@ -72,14 +72,18 @@ typedef struct {
   float beta_fast;     /* YaRN ramp: dims turning more often than this keep their frequency; 32 */
   float beta_slow;     /* YaRN ramp: dims turning less often than this are interpolated; 1 */
   int max_pos;         /* RoPE table length (largest position + 1); default 262144 */
-  int fp4;             /* 1 = fp4 round trip of the latent (default), 0 = off */
+  int fp4;             /* fp4 round trip of the output: 1 = e2m1 values with an e4m3 scale per 16
+                          features, the latent's (default); 2 = e2m1 values with a power-of-two
+                          (e8m0) scale per 32 features, the indexer's keys (head_dim % 32 == 0);
+                          0 = off */
   float eps;           /* RMSNorm epsilon; default 1e-6 */
 } csa_options;
 
 /* Output buffers of one call (dev).  Rows are entries: prefill [B][G][..], decode [B][..].
  *  latent   [.., H] bf16, required: the final latent (dequantised fp4 values if fp4 is on)
  *  codes    [.., H/2] u8 or NULL: e2m1 codes, element 2i in the low nibble, sign in bit 3
- *  scales   [.., H/16] u8 or NULL: e4m3 bit patterns, one per block of 16 features
+ *  scales   [.., H/16] u8 or NULL: e4m3 bit patterns, one per block of 16 features (fp4 = 1);
+ *           [.., H/32] u8: e8m0 bytes (2^(byte - 127)), one per block of 32 features (fp4 = 2)
  *  prequant [.., H] bf16 or NULL: the latent after RMSNorm and RoPE, before fp4 */
 typedef struct {
   uint16_t* latent;
@@ -200,6 +204,14 @@ const char* csa_last_error(void);
  * scales [n_blocks] u8 dev (e4m3 bits), out [n_blocks][16] bf16 dev (dequantised).
  * Runs the same device routine as the compressor's epilogue. */
 int csa_fp4_e4m3_roundtrip(const uint16_t* in, int64_t n_blocks, uint8_t* codes, uint8_t* scales, uint16_t* out,
+                           csa_stream_t stream);
+
+/* The indexer's fp4 round trip alone ("Module compress", fp4_quant_e8m0_inplace, FP4_BLOCK 32:
+ * scale = the power-of-two ceiling of max(amax, 6 * 2^-126) / 6, values to e2m1, dequantised
+ * and rounded to bf16): in [n_blocks][32] bf16 dev -> codes [n_blocks][16] u8 dev (may be
+ * NULL), scales [n_blocks] u8 dev (e8m0 bytes), out [n_blocks][32] bf16 dev.  Runs the same
+ * device routine as the compressor's epilogue with fp4 = 2. */
+int csa_fp4_e8m0_roundtrip(const uint16_t* in, int64_t n_blocks, uint8_t* codes, uint8_t* scales, uint16_t* out,
                            csa_stream_t stream);
 
 /* Measurement hook (the pages have no counterpart): while start and stop are set, every

@@ -139,7 +139,15 @@ LONG = Workload("long-context prefill sweep", 4,
                 (16384, 65536, 131072), outlier_frac=0.01, outlier_scale=20.0,
                 extra={"batched": (8, 8192)})
 
-WORKLOADS = {"tiny": TINY, "flash_csa": FLASH_CSA, "hca": HCA, "decode": DECODE, "long": LONG}
+# the indexer's 128-wide compressor of a CSA layer (its keys take the power-of-two fp4 round
+# trip), and the ratio-2 "pool token pairs" layers, at the Flash width
+INDEXER = Workload("Flash CSA indexer compressor: B=1 N=4096 dim=4096 head_dim=128 ratio=4 overlapped", 5,
+                   (Layer(FLASH_DIM, 128, 4, 1, 1.0 / 64, fp4=2),), 1, (4096,))
+PAIRS = Workload("pool token pairs: B=2 N=4096 dim=4096 head_dim=512 ratio=2", 6,
+                 (Layer(FLASH_DIM, FLASH_H, 2, 0, 1.0 / 64),), 2, (4096,))
+
+WORKLOADS = {"tiny": TINY, "flash_csa": FLASH_CSA, "hca": HCA, "decode": DECODE, "long": LONG,
+             "indexer": INDEXER, "pairs": PAIRS}
 
 
 def weights(seed: int, layer: Layer):

@@ -56,9 +56,13 @@ def test_create_rejects_bad_shapes_without_a_device(args, frag):
 def test_create_rejects_bad_options():
     lib = csa.load_library()
     h = ctypes.c_void_p()
-    for kw in (dict(rope_dim=63), dict(rope_dim=1024), dict(max_batch=0), dict(fp4=2)):
+    for kw in (dict(rope_dim=63), dict(rope_dim=1024), dict(max_batch=0), dict(fp4=3), dict(fp4=-1)):
         o = csa.default_options(**kw)
         assert lib.csa_compressor_create(4096, 512, 4, 1, ctypes.byref(o), ctypes.byref(h)) == -1
+    # the power-of-two quantiser takes blocks of 32 features
+    o = csa.default_options(fp4=2, rope_dim=16)
+    assert lib.csa_compressor_create(4096, 48, 4, 0, ctypes.byref(o), ctypes.byref(h)) == -1
+    assert "multiple of 32" in lib.csa_last_error().decode()
 
 
 def test_null_handle_calls_fail_cleanly():
