@@ -323,9 +323,53 @@ def run_ours(args, rank, world, local):
             "gpu_launches": launches, "clocks": clk}
     comp.close()
     line["chunked_prefill"] = bench_chunked(args, torch, csa, synthetic, device, peaks, world)
+    line["other_prefill"] = [bench_prefill_workload(args, torch, csa, synthetic, device, peaks, world, wl)
+                             for wl in (synthetic.HCA, synthetic.INDEXER, synthetic.PAIRS)]
     if not args.no_decode:
         line["decode"] = bench_decode(args, torch, csa, synthetic, device, peaks, world, rank)
     return line
+
+
+def bench_prefill_workload(args, torch, csa, synthetic, device, peaks, world, wl):
+    """Prefill throughput of another compressor instance of the model (same kernels): the HCA
+    layer (ratio 128), the indexer's 128-wide compressor, the ratio-2 layers."""
+    layer = wl.layers[0]
+    B, N = wl.batch, wl.tokens[0]
+    G = N // layer.ratio
+    comp, x = make_inputs(torch, csa, synthetic, layer, wl.seed, B, N, 0, device)
+    out = comp._alloc_out(B * G, device, prequant=False)
+    stream = torch.cuda.current_stream(device)
+    props = torch.cuda.get_device_properties(device)
+    flush = torch.empty(int(2 * getattr(props, "L2_cache_size", 128 << 20)) // 4 + 1, dtype=torch.float32,
+                        device=device)
+    for _ in range(max(args.warmup, 3)):
+        comp.prefill(x, out=out, prequant=False)
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b_ in kev:
+        a.record(stream)
+        b_.record(stream)
+    for i in range(K):
+        flush.fill_(float(i))
+        comp.set_profile_events(*kev[i])
+        ev[i][0].record(stream)
+        comp.prefill(x, out=out, prequant=False)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    comp.set_profile_events(None, None)
+    ms = max_over_ranks(sum(a.elapsed_time(b_) for a, b_ in ev), world, device) / K
+    kms = statistics.mean(a.elapsed_time(b_) for a, b_ in kev)
+    flops = 2.0 * B * N * layer.dim * 2 * layer.width
+    achieved = flops / (kms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"] / 3.0
+    tc = comp.uses_tensor_cores()
+    comp.close()
+    return {"workload": wl.name, "value": B * G * world / (ms * 1e-3), "unit": "entries/s", "ms_per_step": ms,
+            "tokens_per_s": B * N * world / (ms * 1e-3), "kernel_ms": kms, "tensor_cores": bool(tc),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak}}
 
 
 def bench_chunked(args, torch, csa, synthetic, device, peaks, world):

@@ -3,8 +3,8 @@
 // epilogue.  The pre-pool kv / score values live only in TMEM and shared memory.
 //
 // GEMM orientation: the packed weight rows are the MMA's M side (128 rows = one packed tile:
-// ft features x nk kinds), the tokens its N side (a tile of 256 or 224, whichever fills the
-// SMs in fewer waves), K = dim.  The f32 weights
+// ft features x nk kinds), the tokens its N side (a tile of 256, 224 or 128, whichever fills
+// the SMs in fewer waves x tile tokens), K = dim.  The f32 weights
 // enter as three bf16 planes whose sum is exact (w = p0 + p1 + p2), so three bf16 MMAs into
 // one f32 accumulator give the f32 product (x is bf16, so every partial product is exact):
 // the f32 projection of "Pool token pairs" (x.float(), wkv(x), wgate(x)) and the f32 x . w^T
@@ -43,7 +43,7 @@ namespace tc {
 using namespace tcx;
 
 constexpr int kRows = 128;           // packed rows per tile (MMA M)
-constexpr int kTokMax = 256;         // tokens per tile including the halo (MMA N): 256 or 224
+constexpr int kTokMax = 256;         // tokens per tile including the halo (MMA N): 256, 224 or 128
 constexpr int kKb = 32;              // K elements per stage (one 64-byte swizzle row of bf16)
 constexpr int kStages = 5;
 constexpr int kPlaneBytes = kRows * kKb * 2;          // 8 KB
@@ -57,9 +57,9 @@ constexpr int kTmemCols = 512;      // two chunk accumulators of up to 256 colum
 // [128 h, min(128 h + 128, TOK)).
 template <int TOK>
 struct Tile {
-  static_assert(TOK == 256 || TOK == 224, "token tile");
-  static constexpr int kXBytes = TOK * kKb * 2;                  // 16 KB / 14 KB
-  static constexpr int kStageBytes = 3 * kPlaneBytes + kXBytes;  // 40 KB / 38 KB (multiples of 1 KB)
+  static_assert(TOK == 256 || TOK == 224 || TOK == 128, "token tile");
+  static constexpr int kXBytes = TOK * kKb * 2;                  // 16 / 14 / 8 KB
+  static constexpr int kStageBytes = 3 * kPlaneBytes + kXBytes;  // 40 / 38 / 32 KB (multiples of 1 KB)
   static constexpr int kSmemStride = TOK + 1;                    // f32 staging row stride (bank-conflict free)
   static_assert(kRows * kSmemStride * 4 <= kStages * kStageBytes, "staging must fit in the stage buffers");
   static_assert(kStageBytes % 1024 == 0, "stages keep the 1 KB alignment of the swizzled tiles");
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int et = threadIdx.x - 64;  // 0..255
     const int q = warp & 3, h = (warp - 2) >> 2;
     const int row = 32 * q + lane;
-    const int hcols = h ? kTok - 128 : 128;  // a multiple of 32
+    const int hcols = h ? kTok - 128 : 128;  // a multiple of 32 (0: the 128-token tile's second half idles)
     float acc[128];
 #pragma unroll
     for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
@@ -442,9 +442,10 @@ int owned_tokens(const csa_compressor* c, int tok) {
 }
 
 // The token tile of a launch: the one whose grid takes the fewest waves x tile tokens (one CTA
-// per SM), 256 on a tie.  At the Flash CSA shape the 224-token tile makes 16 x 19 = 304 CTAs,
-// exactly two waves of 152 SMs, where 256 makes 272 (1.79 waves, the second wave a CTA of
-// 256 tokens per SM).
+// per SM), the larger on a tie.  At the Flash CSA shape the 224-token tile makes 16 x 19 = 304
+// CTAs, exactly two waves of 152 SMs, where 256 makes 272 (1.79 waves, the second wave a CTA
+// of 256 tokens per SM); the indexer's 128-wide compressor (4 packed tiles) takes the 128-token
+// tile, 4 x 34 = 136 CTAs in one wave instead of 76 CTAs of 224 tokens.
 int prefill_tok(const csa_compressor* c, int B, int N) {
   static int sms = 0;
   if (!sms) {
@@ -454,7 +455,7 @@ int prefill_tok(const csa_compressor* c, int B, int N) {
   }
   int best = tc::kTokMax;
   long long best_cost = -1;
-  for (int tok : {256, 224}) {
+  for (int tok : {256, 224, 128}) {
     const int T = owned_tokens(c, tok);
     if (T < 1) continue;
     const long long ctas = (long long)c->pk.ntiles * ((N + T - 1) / T) * B;
@@ -574,8 +575,14 @@ size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N, const Chu
 
 cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset,
                               const Chunk& ck, const csa_out& out, void* scratch, cudaStream_t s) {
-  return prefill_tok(c, B, ck.a + N) == 224 ? launch_tok<224>(c, x, B, N, slot_offset, ck, out, scratch, s)
-                                            : launch_tok<256>(c, x, B, N, slot_offset, ck, out, scratch, s);
+  switch (prefill_tok(c, B, ck.a + N)) {
+    case 224:
+      return launch_tok<224>(c, x, B, N, slot_offset, ck, out, scratch, s);
+    case 128:
+      return launch_tok<128>(c, x, B, N, slot_offset, ck, out, scratch, s);
+    default:
+      return launch_tok<256>(c, x, B, N, slot_offset, ck, out, scratch, s);
+  }
 }
 
 }  // namespace csa
