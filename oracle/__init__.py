@@ -70,6 +70,7 @@ def _load():
             "oracle_prefill_chunk": ([P, P, I, I, I, I, P, P, P, P, I], I),
             "oracle_decode": ([P, P, I, P, P, P, P, P, P, I], I),
             "oracle_state_reset": ([P], None), "oracle_state_elems": ([P], I64),
+            "oracle_set_gate_bias": ([P, P], None),
             "oracle_state_export": ([P, P, P], None),
         }
         for name, (args, res) in sig.items():
@@ -216,6 +217,12 @@ class Compressor:
     def scale_block(self):
         """Values per fp4 scale: 16 (e4m3 scales, the latent) or 32 (power-of-two scales)."""
         return 32 if self.fp4 == 2 else 16
+
+    def set_gate_bias(self, ape):
+        """ape float32 [ratio, (1 + overlap) * H] added to the gate logits by position within the
+        group, or None to remove it."""
+        self._ape = None if ape is None else np.ascontiguousarray(ape, np.float32)
+        self._lib.oracle_set_gate_bias(self.h, None if self._ape is None else _ptr(self._ape))
 
     def _outs(self, n):
         H = self.H

@@ -209,6 +209,7 @@ struct oracle_compressor {
   int dim, H, ratio, overlap;
   oracle_options opt;
   std::vector<float> wkv, wgate, gain;  // [C][dim], [C][dim], [H]
+  std::vector<float> ape;               // gate positional bias [ratio][C], empty = none
   std::vector<double> freqs;            // [rope_dim/2]
   std::vector<float> kv_state, score_state;
   int width() const { return (1 + overlap) * H; }
@@ -216,6 +217,20 @@ struct oracle_compressor {
   int slot_width() const { return overlap ? 2 * H : H; }
   int scale_block() const { return opt.fp4 == 2 ? 32 : 16; }  // values per fp4 scale
 };
+
+namespace {
+
+// [CSA4] "wgate(x) + positional bias": the gate logits of n projected tokens at positions
+// p0, p0 + 1, ... get the bias row of their position within the group, ape[p % ratio][c],
+// one float32 addition each.  No bias set: unchanged.
+void add_gate_bias(const oracle_compressor* c, float* sp, int64_t n, int64_t p0) {
+  if (c->ape.empty()) return;
+  const int W = c->width();
+  for (int64_t t = 0; t < n; ++t)
+    for (int k = 0; k < W; ++k) sp[t * W + k] = sp[t * W + k] + c->ape[((p0 + t) % c->ratio) * W + k];
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -335,6 +350,13 @@ void oracle_set_weights(oracle_compressor* c, const float* wkv, const float* wga
   c->gain.assign(gain, gain + c->H);
 }
 
+void oracle_set_gate_bias(oracle_compressor* c, const float* ape) {
+  if (ape)
+    c->ape.assign(ape, ape + (int64_t)c->ratio * c->width());
+  else
+    c->ape.clear();
+}
+
 int64_t oracle_state_elems(const oracle_compressor* c) {
   return (int64_t)c->opt.max_batch * c->slots() * c->slot_width();
 }
@@ -421,6 +443,7 @@ int oracle_prefill(oracle_compressor* c, const uint16_t* x, int B, int N, int sl
     const uint16_t* xs = x + (int64_t)b * N * D;
     oracle_linear(xs, N, D, c->wkv.data(), W, kvp.data(), nthreads);
     oracle_linear(xs, N, D, c->wgate.data(), W, sp.data(), nthreads);
+    add_gate_bias(c, sp.data(), N, 0);
     parallel_for(G, nthreads, [&](int64_t j) {
       std::vector<float> kv((int64_t)ncand * H), sc((int64_t)ncand * H), pooled(H);
       gather_group(c, kvp.data(), sp.data(), 0, j, kv.data(), sc.data());
@@ -478,6 +501,7 @@ int oracle_prefill_groups(const oracle_compressor* c, const uint16_t* x, int N, 
     std::vector<float> kvp(nt * W), sp(nt * W);
     oracle_linear(x + t0 * D, nt, D, c->wkv.data(), W, kvp.data(), 1);
     oracle_linear(x + t0 * D, nt, D, c->wgate.data(), W, sp.data(), 1);
+    add_gate_bias(c, sp.data(), nt, t0);
     std::vector<float> kv((int64_t)ncand * H), sc((int64_t)ncand * H), pooled(H);
     gather_group(c, kvp.data(), sp.data(), t0, j, kv.data(), sc.data());
     oracle_pool(kv.data(), sc.data(), ncand, H, pooled.data(), nullptr);
@@ -515,6 +539,7 @@ int oracle_prefill_chunk(oracle_compressor* c, const uint16_t* x, int B, int N, 
     const uint16_t* xs = x + (int64_t)b * N * D;
     oracle_linear(xs, N, D, c->wkv.data(), W, kvp.data(), nthreads);
     oracle_linear(xs, N, D, c->wgate.data(), W, sp.data(), nthreads);
+    add_gate_bias(c, sp.data(), N, p0);
     // the kv / score row (W columns) of token p: this call's projection, or its state slot
     auto kv_row = [&](int64_t p) -> const float* {
       return p >= p0 ? &kvp[(p - p0) * W] : state_row(c->kv_state, c, sb, slot_of(p));
@@ -594,6 +619,7 @@ int oracle_decode(oracle_compressor* c, const uint16_t* x_tok, int B, const int3
     std::vector<float> kv(W), sc(W);
     oracle_linear(xt, 1, D, c->wkv.data(), W, kv.data(), 1);
     oracle_linear(xt, 1, D, c->wgate.data(), W, sc.data(), 1);
+    add_gate_bias(c, sc.data(), 1, p);
     const int sw = c->slot_width();
     if (!c->overlap) {
       const int slot = (int)(p % r);

@@ -101,6 +101,10 @@ int oracle_decode(oracle_compressor* c, const uint16_t* x_tok, int B, const int3
                   uint16_t* latent, uint8_t* codes, uint8_t* scales, uint16_t* prequant, uint8_t* emitted,
                   int nthreads);
 void oracle_state_reset(oracle_compressor* c);
+/* Gate positional bias ([CSA4] "wgate(x) + positional bias"): ape [ratio][C] f32 (C = (1 +
+ * overlap) * H, branch A then B), added to the gate logits of a token at position p as
+ * ape[p % ratio]; NULL removes it. */
+void oracle_set_gate_bias(oracle_compressor* c, const float* ape);
 /* state layout: non-overlap [max_batch][ratio][H]; overlap [max_batch][2][4][2H] */
 int64_t oracle_state_elems(const oracle_compressor* c);
 void oracle_state_export(const oracle_compressor* c, float* kv, float* score);

@@ -323,6 +323,73 @@ def test_indexer_quantiser_applies_to_the_prequant_latent():
     assert np.array_equal(out["latent"].reshape(-1), lat)
 
 
+# ---- gate positional bias ([CSA4] "wgate(x) + positional bias") ------------------------------
+
+@pytest.mark.parametrize("ratio,overlap,s0", [(4, 0, 2), (4, 1, 1), (8, 0, 7)])
+def test_gate_bias_on_one_slot_selects_that_token(ratio, overlap, s0):
+    """A bias of 1000 on one position of the group (branch A when overlapped) gives that token
+    softmax weight 1 (the others exp(-1000) = 0), so each entry is the epilogue of that token's
+    kv row, computed here from numpy's float64 projection rounded to float32."""
+    dim, H = 64, 32
+    c, (wkv, _, _) = make(dim, H, ratio, overlap, rope_dim=16)
+    ape = np.zeros((ratio, (1 + overlap) * H), np.float32)
+    ape[s0, :H] = 1000.0
+    c.set_gate_bias(ape)
+    x = rand_x(22, 1, 5 * ratio + 1, dim)
+    out = c.prefill(x)
+    xf = bf16_bits_to_f32(x[0]).astype(np.float64)
+    for j in range(5):
+        kv = (xf[ratio * j + s0] @ wkv.astype(np.float64).T).astype(np.float32)[:H]
+        assert np.array_equal(out["prequant"][0, j], c.epilogue(kv, ratio * j)), j
+
+
+@pytest.mark.parametrize("ratio,overlap", [(4, 1), (3, 0)])
+def test_gate_bias_constant_per_feature_changes_nothing(ratio, overlap):
+    """The softmax is unchanged by adding one constant to every candidate's logit: a bias that
+    depends only on the feature (same for every position and both branches) leaves the entries
+    as they are, up to the float32 rounding of the shifted logits."""
+    dim, H = 64, 32
+    a, _ = make(dim, H, ratio, overlap, rope_dim=16, fp4=1, max_batch=2)
+    b, _ = make(dim, H, ratio, overlap, rope_dim=16, fp4=1, max_batch=2)
+    cf = np.random.default_rng(5).standard_normal(H).astype(np.float32) * 3
+    b.set_gate_bias(np.tile(np.concatenate([cf] * (1 + overlap)), (ratio, 1)))
+    x = rand_x(23, 2, 40 * ratio + 2, dim)
+    pa, pb = a.prefill(x)["prequant"], b.prefill(x)["prequant"]
+    u = ulp_distance_bf16(pa, pb)
+    assert u.max() <= 1 and np.mean(u == 0) >= 0.99
+
+
+@pytest.mark.parametrize("ratio,overlap,chunks", [(4, 1, (6, 5, 13)), (3, 0, (4, 8, 1, 9))])
+def test_gate_bias_prefill_chunks_equal_decode(ratio, overlap, chunks):
+    """With a random bias, prefill chunks still equal token-by-token decode, bit for bit: both
+    add the bias of the token's position within its group."""
+    dim, H, B = 64, 32, 2
+    ape = np.random.default_rng(6).standard_normal((ratio, (1 + overlap) * H)).astype(np.float32)
+    chk, _ = make(dim, H, ratio, overlap, rope_dim=16, fp4=1, max_batch=B, seed=8)
+    dec, _ = make(dim, H, ratio, overlap, rope_dim=16, fp4=1, max_batch=B, seed=8)
+    chk.set_gate_bias(ape)
+    dec.set_gate_bias(ape)
+    P = sum(chunks)
+    x = rand_x(24, B, P, dim)
+    want = []
+    for p in range(P):
+        o = dec.decode(x[:, p], np.full(B, p, np.int32))
+        if o["emitted"][0]:
+            want.append(o["latent"].copy())
+    got = []
+    p0 = 0
+    for n in chunks:
+        out = chk.prefill(x[:, p0:p0 + n], start_pos=p0)
+        got += [out["latent"][:, j] for j in range(out["G"])]
+        p0 += n
+    assert len(got) == len(want) == P // ratio
+    for g, w in zip(got, want):
+        assert np.array_equal(g, w)
+    # the bias matters: without it the entries differ
+    plain, _ = make(dim, H, ratio, overlap, rope_dim=16, fp4=1, max_batch=B, seed=8)
+    assert not np.array_equal(plain.prefill(x)["latent"][:, 0], got[0])
+
+
 def test_prefill_state_holds_the_tail_projections():
     dim, H, r = 48, 16, 8
     c, (wkv, wgate, _) = make(dim, H, r, 0, max_batch=3)
