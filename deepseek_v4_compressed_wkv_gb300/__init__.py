@@ -34,7 +34,7 @@ ABI_FUNCTIONS = ("csa_options_default", "csa_compressor_create", "csa_compressor
                  "csa_state_export", "csa_device_status", "csa_compressor_destroy", "csa_last_error",
                  "csa_fp4_e4m3_roundtrip", "csa_rope_table", "csa_set_profile_events", "csa_kernel_launches",
                  "csa_uses_tensor_cores", "csa_compress_prefill_noalloc", "csa_compress_prefill_into",
-                 "csa_fp4_e8m0_roundtrip")
+                 "csa_fp4_e8m0_roundtrip", "csa_compressor_set_gate_bias")
 
 
 class CSAError(RuntimeError):
@@ -84,6 +84,7 @@ def load_library(build_if_missing: bool = True):
             "csa_last_error": ([], ctypes.c_char_p),
             "csa_fp4_e4m3_roundtrip": ([P, I64, P, P, P, P], I),
             "csa_fp4_e8m0_roundtrip": ([P, I64, P, P, P, P], I),
+            "csa_compressor_set_gate_bias": ([P, P, P], I),
             "csa_rope_table": ([P, I, I, P, P], I),
             "csa_set_profile_events": ([P, P, P], I),
             "csa_kernel_launches": ([P], I64),
@@ -164,6 +165,12 @@ class Compressor:
     def set_weights(self, wkv, wgate, gain, stream=None):
         _check(self._lib.csa_compressor_set_weights(self._h, _dptr(wkv), _dptr(wgate), _dptr(gain),
                                                     _stream(stream)), "csa_compressor_set_weights")
+
+    def set_gate_bias(self, ape, stream=None):
+        """ape f32 CUDA [ratio, (1 + overlap) * head_dim] added to the gate logits by position within
+        the group, or None to remove it."""
+        _check(self._lib.csa_compressor_set_gate_bias(self._h, _dptr(ape), _stream(stream)),
+               "csa_compressor_set_gate_bias")
 
     @property
     def scale_block(self) -> int:

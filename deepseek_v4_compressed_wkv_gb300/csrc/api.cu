@@ -91,6 +91,7 @@ void free_all(csa_compressor* c) {
   cudaFree(c->w_packed);
   cudaFree(c->w_planes);
   cudaFree(c->gain);
+  cudaFree(c->ape);
   cudaFree(c->rope_cos);
   cudaFree(c->rope_sin);
   cudaFree(c->state);
@@ -165,7 +166,7 @@ int prefill_call(csa_compressor* c, const uint16_t* x, int B, int N, int start_p
     rc = ensure_scratch(c, (size_t)M * c->pk.cols() * sizeof(float), s);
     if (rc) return rc;
     if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
-    CSA_CUDA(csa::launch_projection_ffma(c, x, (int)M, c->scratch, 0, nullptr, s), "projection launch");
+    CSA_CUDA(csa::launch_projection_ffma(c, x, (int)M, c->scratch, 0, nullptr, N, start_pos, s), "projection launch");
     if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
     c->launches += 1;
     if (ck.G > 0) {
@@ -305,6 +306,20 @@ int csa_compressor_set_weights(csa_compressor* c, const float* wkv, const float*
   return CSA_OK;
 }
 
+int csa_compressor_set_gate_bias(csa_compressor* c, const float* ape, csa_stream_t stream) {
+  if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
+  if (!ape) {
+    c->ape_set = false;
+    return CSA_OK;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!c->ape) CSA_CUDA(cudaMalloc(&c->ape, (size_t)c->ratio * c->pk.cols() * sizeof(float)), "cudaMalloc(gate bias)");
+  CSA_CUDA(csa::launch_pack_ape(c, ape, s), "gate bias launch");
+  c->launches += 1;
+  c->ape_set = true;
+  return CSA_OK;
+}
+
 int csa_compress_prefill(csa_compressor* c, const uint16_t* x, int B, int N, int start_pos, int slot_offset,
                          const csa_out* out, csa_stream_t stream) {
   return prefill_call(c, x, B, N, start_pos, slot_offset, out, -1, stream, "csa_compress_prefill");
@@ -347,7 +362,7 @@ int csa_compress_decode(csa_compressor* c, const uint16_t* x_tok, int B, const i
   }
   CSA_CUDA(csa::invalidate_decode_acc(c, 0, B, s), "invalidate decode running values");
   if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
-  CSA_CUDA(csa::launch_projection_ffma(c, x_tok, B, c->state, 1, start_pos, s), "decode projection launch");
+  CSA_CUDA(csa::launch_projection_ffma(c, x_tok, B, c->state, 1, start_pos, 0, 0, s), "decode projection launch");
   if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
   CSA_CUDA(csa::launch_decode_emit(c, start_pos, B, *out, emitted, s), "decode emit launch");
   c->launches += 2;

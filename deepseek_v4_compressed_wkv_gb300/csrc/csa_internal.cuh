@@ -386,6 +386,9 @@ struct csa_compressor {
   float* w_packed;  // [2C][dim] f32, packed column order
   __nv_bfloat16* w_planes;  // 3 bf16 split planes (w = p0 + p1 + p2), tiled (plane_tile_elem)
   float* gain;              // [H]
+  float* ape;               // gate positional bias [ratio][2C] f32, packed order, zero at the kv
+                            // columns (allocated by the first csa_compressor_set_gate_bias)
+  bool ape_set;             // the bias is in use
   float* rope_cos;          // [max_pos][rope_dim/2]
   float* rope_sin;
   float* state;             // [max_batch][slots][2C] f32, packed column order

@@ -289,6 +289,7 @@ struct FinParams {
   float* acc;                // non-overlapped: [max_batch][3][H] running max, denominator and
                              // numerator of the open group over its tokens so far
   int* acc_pos;              // [max_batch] position of the last token in acc (-1: not valid)
+  const float* ape;          // packed gate positional bias [ratio][ncol] (zero at kv columns), or null
 };
 
 __device__ __forceinline__ float padded_kind_value(const Packing& pk, int col) {
@@ -567,6 +568,10 @@ __global__ void __launch_bounds__(kFinThreads, 5) decode_finish_kernel(const Fin
     for (int i = 0; i < kFinColGroups; ++i) {
       const int cg = tid + i * nthr;
       if (cg < ncg) {
+        // wgate(x) + the positional bias of the token's place in its group, at the score columns
+        // (a float4 never straddles two kinds: a kind spans ft >= 16 columns)
+        if (P.ape && ((4 * cg) % pk.tw) / pk.ft >= pk.nk / 2)
+          add4(a[i], __ldg(reinterpret_cast<const float4*>(P.ape + (size_t)(pp % P.ratio) * ncol) + cg));
         reinterpret_cast<float4*>(cur)[cg] = a[i];
         reinterpret_cast<float4*>(st + (size_t)slot * ncol)[cg] = a[i];
       }
@@ -775,6 +780,7 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
     P.emitted = emitted;
     P.acc = c->dec_acc;
     P.acc_pos = c->dec_acc_pos;
+    P.ape = c->ape_set ? c->ape : nullptr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(B, 1, 1);
     cfg.blockDim = dim3(kFinThreads, 1, 1);

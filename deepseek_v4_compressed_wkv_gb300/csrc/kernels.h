@@ -7,8 +7,11 @@ namespace csa {
 
 EpiParams epi_params(const csa_compressor* c);
 cudaError_t launch_pack_weights(const csa_compressor* c, const float* wkv, const float* wgate, cudaStream_t s);
+// Dense rows (mode 0, prefill: row m is token m % N at position p0 + m % N) or decode state
+// slots (mode 1, positions start_pos); the gate positional bias, if set, is added.
 cudaError_t launch_projection_ffma(const csa_compressor* c, const uint16_t* x, int M, float* out, int mode,
-                                   const int32_t* start_pos, cudaStream_t s);
+                                   const int32_t* start_pos, int N, int p0, cudaStream_t s);
+cudaError_t launch_pack_ape(const csa_compressor* c, const float* ape, cudaStream_t s);
 cudaError_t launch_prefill_pool(const csa_compressor* c, const float* proj, int B, int N, int slot_offset,
                                 const Chunk& ck, const csa_out& out, cudaStream_t s);
 cudaError_t launch_prefill_state(const csa_compressor* c, const float* proj, int B, int N, int slot_offset,

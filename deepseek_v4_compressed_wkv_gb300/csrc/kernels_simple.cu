@@ -44,6 +44,20 @@ __global__ void pack_weights_kernel(const float* __restrict__ wkv, const float* 
   }
 }
 
+// Gate positional bias: logical ape [ratio][C] (the gate's columns, branch A then B) -> packed
+// [ratio][2C] with the bias at the score columns and zero at the kv columns.
+__global__ void pack_ape_kernel(const float* __restrict__ src, Packing pk, int overlap, int ratio,
+                                float* __restrict__ dst) {
+  const int ncol = pk.cols(), C = (1 + overlap) * pk.H;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ratio * ncol; i += gridDim.x * blockDim.x) {
+    const int r = i / ncol, pc = i % ncol;
+    const int within = pc % pk.tw, kind = within / pk.ft, f = (pc / pk.tw) * pk.ft + within % pk.ft;
+    float v = 0.0f;
+    if (kind >= pk.nk / 2) v = src[(size_t)r * C + ((overlap && kind == S_B) ? pk.H + f : f)];
+    dst[i] = v;
+  }
+}
+
 // ---------------------------------------------------------------------------------------
 // CUDA-core projection: out[m][n] = sum_k x[m][k] * w[n][k], f32 accumulation in k order.
 // Rows go to out + m*ncol (prefill) or, for decode, to the state slot of sequence m.
@@ -53,6 +67,10 @@ struct RowMap {
   int mode;  // 0: dense rows; 1: decode state slots
   const int32_t* start_pos;
   int slots, ratio, overlap;
+  const float* ape;  // packed gate positional bias [ratio][2C], or null
+  int N, p0;         // dense rows: row m is token m % N of its sequence, at position p0 + m % N
+  // position of the token of row m (for the bias)
+  __device__ long long pos(int m) const { return mode == 0 ? (long long)p0 + m % N : (long long)max(start_pos[m], 0); }
   __device__ size_t row(int m, int ncol) const {
     if (mode == 0) return (size_t)m * ncol;
     const int slot = state_slot(max(start_pos[m], 0), ratio, overlap);
@@ -100,10 +118,13 @@ __global__ __launch_bounds__(256) void gemm_ffma_kernel(const uint16_t* __restri
     const int m = m0 + ty * 4 + i;
     if (m >= M) continue;
     float* dst = out + map.row(m, ncol);
+    const float* ab = map.ape ? map.ape + (size_t)(map.pos(m) % map.ratio) * ncol : nullptr;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int n = n0 + tx * 4 + j;
-      if (n < ncol) dst[n] = acc[i][j];
+      // wgate(x) + bias at the score columns ("Compressed Sparse Attention": positional bias);
+      // the packed bias is zero at the kv columns, where nothing is added
+      if (n < ncol) dst[n] = (ab && ab[n] != 0.0f) ? acc[i][j] + ab[n] : acc[i][j];
     }
   }
 }
@@ -355,9 +376,15 @@ cudaError_t launch_pack_weights(const csa_compressor* c, const float* wkv, const
   return cudaGetLastError();
 }
 
+cudaError_t launch_pack_ape(const csa_compressor* c, const float* ape, cudaStream_t s) {
+  const int n = c->ratio * c->pk.cols();
+  pack_ape_kernel<<<grid_cap((size_t)n, 256), 256, 0, s>>>(ape, c->pk, c->overlap, c->ratio, c->ape);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_projection_ffma(const csa_compressor* c, const uint16_t* x, int M, float* out, int mode,
-                                   const int32_t* start_pos, cudaStream_t s) {
-  RowMap map{mode, start_pos, c->slots, c->ratio, c->overlap};
+                                   const int32_t* start_pos, int N, int p0, cudaStream_t s) {
+  RowMap map{mode, start_pos, c->slots, c->ratio, c->overlap, c->ape_set ? c->ape : nullptr, N, p0};
   const int ncol = c->pk.cols();
   dim3 grid((ncol + GN - 1) / GN, (M + GM - 1) / GM);
   gemm_ffma_kernel<<<grid, 256, 0, s>>>(x, c->w_packed, M, ncol, c->dim, out, map);

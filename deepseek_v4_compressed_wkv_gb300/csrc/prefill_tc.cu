@@ -68,6 +68,7 @@ struct Tile {
 struct Params {
   int N, K, ratio, overlap, T, GT, halo, ntt, G, ncol, slots, slot_offset;
   int a, g0, gend;         // chunk geometry (Chunk): all 0 / G for a prefill from position 0
+  const float* ape;        // packed gate positional bias [ratio][ncol] (zero at kv columns), or null
   const __nv_bfloat16* w;  // weight planes, tiled (plane_tile_elem)
   Packing pk;
   float* state;
@@ -221,6 +222,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 128; ++i)
         if (i < hcols) stg[row * kSmemStride + 128 * h + i] = acc[i];
+      if (P.ape && row / P.pk.ft >= P.pk.nk / 2) {
+        // wgate(x) + the positional bias of each token's place in its group (score rows only):
+        // column c holds the token at position ratio * g0 + t0 + c (halo columns wrap harmlessly)
+        const float* ab = P.ape + ftile * kRows + row;
+        const int r = P.ratio;
+        int sl = ((P.ratio * P.g0 + t0 + 128 * h) % r + r) % r;
+        for (int i = 0; i < hcols; ++i) {
+          stg[row * kSmemStride + 128 * h + i] += __ldg(ab + (size_t)sl * P.ncol);
+          sl = sl + 1 == r ? 0 : sl + 1;
+        }
+      }
       epi_sync();
 
       const Packing& pk = P.pk;
@@ -494,6 +506,7 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
   P.state = c->state;
   P.pooled = (uint16_t*)scratch;
   P.carry = nullptr;
+  P.ape = c->ape_set ? c->ape : nullptr;
   P.flag = c->dev_flag;
   P.w = c->w_planes;
   if (chunk_needs_carry(ck, c->overlap)) {

@@ -116,6 +116,15 @@ int csa_compressor_create(int dim, int head_dim, int ratio, int overlap, const c
 int csa_compressor_set_weights(csa_compressor* c, const float* wkv, const float* wgate, const float* norm_gain,
                                csa_stream_t stream);
 
+/* Gate positional bias ("Compressed Sparse Attention": the pooling logits are "wgate(x) +
+ * positional bias"; the pages give neither its shape nor its values).  ape [ratio][C] f32 dev,
+ * C = (1 + overlap) * head_dim (the gate's columns, branch A then B): a token at position p
+ * gets score = wgate(x) + ape[p % ratio], one f32 addition, before it is pooled or stored in
+ * the state.  The library keeps its own re-laid-out copy (the caller's buffer may be freed once
+ * the stream reaches this call); NULL removes the bias (the default: none).  Applies to calls
+ * enqueued after this one; tokens already in the state keep the bias they were given. */
+int csa_compressor_set_gate_bias(csa_compressor* c, const float* ape, csa_stream_t stream);
+
 /* Prefill of B sequences, tokens start_pos .. start_pos + N - 1 of each ("Pool token pairs",
  * Compressor forward, prefill branch).  x [B][N][dim] bf16 dev.  Sequence b uses state slot
  * slot_offset + b; needs slot_offset + B <= max_batch.
