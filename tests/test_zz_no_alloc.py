@@ -28,13 +28,13 @@ def _bits(t):
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def _call_noalloc(lib, comp, x, out, slot_offset=0):
+def _call_noalloc(lib, comp, x, out, slot_offset=0, start_pos=0):
     B, N, _ = x.shape
     o = csa.Out(out["latent"].data_ptr(), out["codes"].data_ptr(), out["scales"].data_ptr(),
                 out["prequant"].data_ptr())
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    return lib.csa_compress_prefill_noalloc(comp.handle, ctypes.c_void_p(x.data_ptr()), B, N, 0, slot_offset,
-                                            ctypes.byref(o), stream)
+    return lib.csa_compress_prefill_noalloc(comp.handle, ctypes.c_void_p(x.data_ptr()), B, N, start_pos,
+                                            slot_offset, ctypes.byref(o), stream)
 
 
 def test_noalloc_prefill_matches_the_allocating_entry_point_twice():
@@ -65,6 +65,17 @@ def test_noalloc_prefill_matches_the_allocating_entry_point_twice():
         ka, sa = na_c.state_export()
         kb, sb = ref_c.state_export()
         assert torch.equal(ka, kb) and torch.equal(sa, sb), call
+    # a chunk continuing the last call's sequences (its carried values also live in the array)
+    B, p0, N = 3, 4 * 151 + 1, 4 * 60 + 2
+    x = torch.from_numpy(np.stack([synthetic.tokens(9, b, p0, p0 + N, layer.dim) for b in range(B)])) \
+        .to(torch.bfloat16).to(DEV)
+    G = (p0 + N) // 4 - p0 // 4
+    ref = ref_c.prefill(x, start_pos=p0)
+    out = ref_c._alloc_out(B * G, x.device, prequant=True)
+    assert _call_noalloc(lib, na_c, x, out, start_pos=p0) == G, lib.csa_last_error().decode()
+    torch.cuda.synchronize()
+    for k in ("latent", "prequant", "codes", "scales"):
+        assert torch.equal(out[k].view(B, G, -1), ref[k]), ("chunk", k)
     assert na_c.device_status() == 0
 
 
