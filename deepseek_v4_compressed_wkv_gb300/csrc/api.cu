@@ -434,6 +434,7 @@ void csa_compressor_destroy(csa_compressor* c) {
 int csa_fp4_e4m3_roundtrip(const uint16_t* in, int64_t n_blocks, uint8_t* codes, uint8_t* scales, uint16_t* out,
                            csa_stream_t stream) {
   if (n_blocks < 0 || (n_blocks > 0 && (!in || !scales || !out))) return fail(CSA_ERR_ARG, "bad arguments");
+  if (n_blocks == 0) return CSA_OK;  // nothing to do, nothing enqueued
   CSA_CUDA(csa::launch_fp4_roundtrip(in, n_blocks, codes, scales, out, (cudaStream_t)stream), "fp4 launch");
   return CSA_OK;
 }
@@ -441,6 +442,7 @@ int csa_fp4_e4m3_roundtrip(const uint16_t* in, int64_t n_blocks, uint8_t* codes,
 int csa_fp4_e8m0_roundtrip(const uint16_t* in, int64_t n_blocks, uint8_t* codes, uint8_t* scales, uint16_t* out,
                            csa_stream_t stream) {
   if (n_blocks < 0 || (n_blocks > 0 && (!in || !scales || !out))) return fail(CSA_ERR_ARG, "bad arguments");
+  if (n_blocks == 0) return CSA_OK;  // nothing to do, nothing enqueued
   CSA_CUDA(csa::launch_fp4_e8m0_roundtrip(in, n_blocks, codes, scales, out, (cudaStream_t)stream), "fp4 launch");
   return CSA_OK;
 }

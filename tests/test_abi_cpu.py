@@ -71,6 +71,13 @@ def test_null_handle_calls_fail_cleanly():
     assert lib.csa_compress_decode(None, None, 1, None, None, None, None) == -1
     assert lib.csa_state_reset(None, 0, 1, None) == -1
     assert lib.csa_state_elems(None) == -1
+    assert lib.csa_compress_prefill_into(None, None, 1, 4, 0, 0, None, 8, None) == -1
+    assert lib.csa_compress_prefill_noalloc(None, None, 1, 4, 0, 0, None, None) == -1
+    assert lib.csa_compressor_set_gate_bias(None, None, None) == -1
+    assert lib.csa_fp4_e8m0_roundtrip(None, -1, None, None, None, None) == -1
+    assert lib.csa_fp4_e8m0_roundtrip(None, 4, None, None, None, None) == -1  # buffers required
+    assert lib.csa_fp4_e4m3_roundtrip(None, 4, None, None, None, None) == -1
+    assert lib.csa_fp4_e8m0_roundtrip(None, 0, None, None, None, None) == 0  # nothing to do
     lib.csa_compressor_destroy(None)
 
 
