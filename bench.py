@@ -335,18 +335,24 @@ def run_ours(args, rank, world, local):
     line["chunked_prefill"] = bench_chunked(args, torch, csa, synthetic, device, peaks, world)
     line["other_prefill"] = [bench_prefill_workload(args, torch, csa, synthetic, device, peaks, world, wl)
                              for wl in (synthetic.HCA, synthetic.INDEXER, synthetic.PAIRS)]
+    line["other_prefill"].append(bench_prefill_workload(args, torch, csa, synthetic, device, peaks, world,
+                                                        synthetic.FLASH_CSA, gate_bias=True))
     if not args.no_decode:
         line["decode"] = bench_decode(args, torch, csa, synthetic, device, peaks, world, rank)
     return line
 
 
-def bench_prefill_workload(args, torch, csa, synthetic, device, peaks, world, wl):
+def bench_prefill_workload(args, torch, csa, synthetic, device, peaks, world, wl, gate_bias=False):
     """Prefill throughput of another compressor instance of the model (same kernels): the HCA
-    layer (ratio 128), the indexer's 128-wide compressor, the ratio-2 layers."""
+    layer (ratio 128), the indexer's 128-wide compressor, the ratio-2 layers; or of the Flash CSA
+    layer with a gate positional bias set (random, std 1)."""
     layer = wl.layers[0]
     B, N = wl.batch, wl.tokens[0]
     G = N // layer.ratio
     comp, x = make_inputs(torch, csa, synthetic, layer, wl.seed, B, N, 0, device)
+    if gate_bias:
+        ape = torch.randn(layer.ratio, layer.width, generator=torch.Generator().manual_seed(7)).to(device)
+        comp.set_gate_bias(ape)
     out = comp._alloc_out(B * G, device, prequant=False)
     stream = torch.cuda.current_stream(device)
     props = torch.cuda.get_device_properties(device)
@@ -377,7 +383,8 @@ def bench_prefill_workload(args, torch, csa, synthetic, device, peaks, world, wl
     peak = peaks["bf16_tflops"] / 3.0
     tc = comp.uses_tensor_cores()
     comp.close()
-    return {"workload": wl.name, "value": B * G * world / (ms * 1e-3), "unit": "entries/s", "ms_per_step": ms,
+    name = wl.name + (", gate positional bias set" if gate_bias else "")
+    return {"workload": name, "value": B * G * world / (ms * 1e-3), "unit": "entries/s", "ms_per_step": ms,
             "tokens_per_s": B * N * world / (ms * 1e-3), "kernel_ms": kms, "tensor_cores": bool(tc),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak}}
