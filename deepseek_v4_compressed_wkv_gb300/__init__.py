@@ -53,8 +53,13 @@ class Out(ctypes.Structure):
                 ("prequant", ctypes.c_void_p)]
 
 
+def _variant() -> str:
+    # CSA_LIBRARY_VARIANT=bounds selects the bounds-checked build (for tests)
+    return os.environ.get("CSA_LIBRARY_VARIANT", "")
+
+
 def library_path() -> str:
-    return _build_mod.LIB
+    return _build_mod.lib_path(_variant())
 
 
 def load_library(build_if_missing: bool = True):
@@ -63,11 +68,11 @@ def load_library(build_if_missing: bool = True):
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build_mod.LIB
+        path = _build_mod.lib_path(_variant())
         if not os.path.exists(path):
             if not build_if_missing:
                 raise CSAError(f"{path} is missing: build it with deepseek_v4_compressed_wkv_gb300.build")
-            _build_mod.build()
+            _build_mod.build(variant=_variant())
         lib = ctypes.CDLL(path)
         P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
         sig = {

@@ -2,6 +2,11 @@
 
 Each translation unit under csrc/ is compiled in parallel to an object file in
 csrc/_build/, then linked into csrc/_build/libcsa.so.  Nothing is installed.
+
+build(variant="bounds") builds the bounds-checked library instead (csrc/_build_bounds/,
+-DCSA_DEBUG_BOUNDS): every kernel store with a computed index is checked against its buffer's
+extent, skipped if outside and reported through the handle's device flag (bit 8).  The tests
+run the parity cases against it; the binding loads it when CSA_LIBRARY_VARIANT=bounds.
 """
 from __future__ import annotations
 
@@ -45,17 +50,28 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def lib_path(variant: str = "") -> str:
+    """Path of the library of a variant: "" (the product) or "bounds" (bounds-checked)."""
+    return LIB if not variant else os.path.join(CSRC, "_build_" + variant, "libcsa.so")
+
+
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, variant: str = "") -> str:
+    if variant not in ("", "bounds"):
+        raise ValueError(f"unknown variant {variant!r}")
+    bdir = os.path.dirname(lib_path(variant))
+    lib = lib_path(variant)
+    extra = ["-DCSA_DEBUG_BOUNDS"] if variant == "bounds" else []
+    os.makedirs(bdir, exist_ok=True)
     srcs = sources()
     hdrs = headers()
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(bdir, os.path.basename(s)[:-3] + ".o") for s in srcs]
     nv = nvcc()
 
     def compile_one(src, obj):
         if not force and not _stale(obj, [src] + hdrs + [__file__]):
             return None
-        cmd = [nv, *ARCH, *FLAGS, *(["-Xptxas", "-v"] if ptxas_info else []), "-c", src, "-o", obj + ".tmp"]
+        cmd = [nv, *ARCH, *FLAGS, *extra, *(["-Xptxas", "-v"] if ptxas_info else []), "-c", src, "-o",
+               obj + ".tmp"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
@@ -66,16 +82,16 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         for out in ex.map(lambda so: compile_one(*so), zip(srcs, objs)):
             if out:
                 sys.stderr.write(out)
-    if force or _stale(LIB, objs):
-        tmp = LIB + f".{os.getpid()}.tmp"
+    if force or _stale(lib, objs):
+        tmp = lib + f".{os.getpid()}.tmp"
         cmd = [nv, *ARCH, "-shared", "-o", tmp, *objs, "-lcuda"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv)
-    print(LIB)
+    v = "bounds" if "--bounds" in sys.argv else ""
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv, variant=v))

@@ -111,6 +111,20 @@ struct EpiParams {
 };
 
 // ---------------------------------------------------------------------------------------
+// Index checks of the bounds-checked build (compiled with -DCSA_DEBUG_BOUNDS): a store whose
+// element index falls outside its buffer's extent [0, n) is skipped and raises bit 8 of the
+// handle's device flag, instead of writing out of bounds.  Compiled out otherwise.
+#ifdef CSA_DEBUG_BOUNDS
+__device__ __forceinline__ bool in_bounds(long long i, long long n, int* flag) {
+  if (i >= 0 && i < n) return true;
+  atomicOr(flag, 8);
+  return false;
+}
+#else
+__device__ __forceinline__ bool in_bounds(long long, long long, int*) { return true; }
+#endif
+
+// ---------------------------------------------------------------------------------------
 // Device number formats.
 
 __device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }

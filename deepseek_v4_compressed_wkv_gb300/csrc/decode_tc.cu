@@ -290,6 +290,7 @@ struct FinParams {
                              // numerator of the open group over its tokens so far
   int* acc_pos;              // [max_batch] position of the last token in acc (-1: not valid)
   const float* ape;          // packed gate positional bias [ratio][ncol] (zero at kv columns), or null
+  long long state_elems, acc_elems;  // extents checked by the bounds-checked build
 };
 
 __device__ __forceinline__ float padded_kind_value(const Packing& pk, int col) {
@@ -573,13 +574,16 @@ __global__ void __launch_bounds__(kFinThreads, 5) decode_finish_kernel(const Fin
         if (P.ape && ((4 * cg) % pk.tw) / pk.ft >= pk.nk / 2)
           add4(a[i], __ldg(reinterpret_cast<const float4*>(P.ape + (size_t)(pp % P.ratio) * ncol) + cg));
         reinterpret_cast<float4*>(cur)[cg] = a[i];
-        reinterpret_cast<float4*>(st + (size_t)slot * ncol)[cg] = a[i];
+        if (in_bounds((long long)((st - P.state) + (size_t)slot * ncol + 4 * cg + 3), P.state_elems, P.flag))
+          reinterpret_cast<float4*>(st + (size_t)slot * ncol)[cg] = a[i];
       }
     }
   }
   // -- restart at position 0: the previous group's branch is the padded one
   if (p == 0 && P.overlap)
-    for (int i = tid; i < 4 * ncol; i += nthr) st[(size_t)4 * ncol + i] = padded_kind_value(pk, i % ncol);
+    for (int i = tid; i < 4 * ncol; i += nthr)
+      if (in_bounds((long long)((st - P.state) + (size_t)4 * ncol + i), P.state_elems, P.flag))
+        st[(size_t)4 * ncol + i] = padded_kind_value(pk, i % ncol);
   if (tid == 0) {
     P.emitted[b] = pool ? 1 : 0;
     if (p < 0) atomicOr(P.flag, 1);
@@ -610,7 +614,8 @@ __global__ void __launch_bounds__(kFinThreads, 5) decode_finish_kernel(const Fin
       Nn[e] = fmaf(num[gi][e], w, ex * kc);
       pv[gi][e] = __fdiv_rn(Nn[e], D[e]);
     }
-    if (!pool && !P.overlap) {  // the open group's running values for the next call
+    if (!pool && !P.overlap &&
+        in_bounds((long long)((acc - P.acc) + 2 * H + f + 3), P.acc_elems, P.flag)) {  // running values for the next call
       reinterpret_cast<float4*>(acc + f)[0] = make_float4(M[0], M[1], M[2], M[3]);
       reinterpret_cast<float4*>(acc + H + f)[0] = make_float4(D[0], D[1], D[2], D[3]);
       reinterpret_cast<float4*>(acc + 2 * H + f)[0] = make_float4(Nn[0], Nn[1], Nn[2], Nn[3]);
@@ -781,6 +786,8 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
     P.acc = c->dec_acc;
     P.acc_pos = c->dec_acc_pos;
     P.ape = c->ape_set ? c->ape : nullptr;
+    P.state_elems = (long long)c->opt.max_batch * c->slots * P.ncol;
+    P.acc_elems = (long long)c->opt.max_batch * 3 * c->H;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(B, 1, 1);
     cfg.blockDim = dim3(kFinThreads, 1, 1);

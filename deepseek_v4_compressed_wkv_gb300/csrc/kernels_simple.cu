@@ -69,6 +69,8 @@ struct RowMap {
   int slots, ratio, overlap;
   const float* ape;  // packed gate positional bias [ratio][2C], or null
   int N, p0;         // dense rows: row m is token m % N of its sequence, at position p0 + m % N
+  long long extent;  // elements of the destination (checked by the bounds-checked build)
+  int* flag;
   // position of the token of row m (for the bias)
   __device__ long long pos(int m) const { return mode == 0 ? (long long)p0 + m % N : (long long)max(start_pos[m], 0); }
   __device__ size_t row(int m, int ncol) const {
@@ -124,7 +126,8 @@ __global__ __launch_bounds__(256) void gemm_ffma_kernel(const uint16_t* __restri
       const int n = n0 + tx * 4 + j;
       // wgate(x) + bias at the score columns ("Compressed Sparse Attention": positional bias);
       // the packed bias is zero at the kv columns, where nothing is added
-      if (n < ncol) dst[n] = (ab && ab[n] != 0.0f) ? acc[i][j] + ab[n] : acc[i][j];
+      if (n < ncol && in_bounds((long long)((dst - out) + n), map.extent, map.flag))
+        dst[n] = (ab && ab[n] != 0.0f) ? acc[i][j] + ab[n] : acc[i][j];
     }
   }
 }
@@ -182,7 +185,7 @@ __device__ __forceinline__ void pool16(int ncand, Cand cand, float out[16]) {
 __global__ __launch_bounds__(128) void prefill_pool_kernel(const float* __restrict__ proj, int B, int N, Chunk ck,
                                                            int ratio, int overlap, Packing pk,
                                                            const float* __restrict__ state, int slots,
-                                                           int slot_offset, EpiParams ep, csa_out out) {
+                                                           int slot_offset, EpiParams ep, csa_out out, int* flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = ck.G;
   const long long e = (long long)blockIdx.x * 4 + warp;
@@ -221,6 +224,7 @@ __global__ __launch_bounds__(128) void prefill_pool_kernel(const float* __restri
   }
   const size_t H = pk.H;
   const size_t o = (size_t)ck.row(b, j);
+  if (!in_bounds((long long)o, (long long)B * ck.bstride, flag)) return;  // the same for the whole warp
   entry_epilogue(v, lane, (long long)ratio * g, ep, out.latent + o * H, out.codes ? out.codes + o * (H / 2) : nullptr,
                  out.scales ? out.scales + o * (H / fp4_scale_block(ep.fp4)) : nullptr,
                  out.prequant ? out.prequant + o * H : nullptr);
@@ -236,7 +240,8 @@ __device__ __forceinline__ float padded_value(const Packing& pk, int col) {
 // the call's tokens of those groups go to their slots (a chunk's earlier tokens are there
 // already).
 __global__ void prefill_state_kernel(const float* __restrict__ proj, int N, Chunk ck, int ratio, int overlap,
-                                     Packing pk, float* __restrict__ state, int slots, int slot_offset) {
+                                     Packing pk, float* __restrict__ state, int slots, int slot_offset,
+                                     long long state_elems, int* flag) {
   const int b = blockIdx.x;
   const int ncol = pk.cols();
   const float* seq = proj + (size_t)b * N * ncol;
@@ -246,9 +251,10 @@ __global__ void prefill_state_kernel(const float* __restrict__ proj, int N, Chun
   for (long long p = keep; p < p1; ++p) {
     const float* src = seq + (size_t)(p - ck.p0) * ncol;
     float* dst = st + (size_t)state_slot(p, ratio, overlap) * ncol;
+    if (!in_bounds((long long)((dst - state) + ncol - 1), state_elems, flag)) continue;
     for (int c = threadIdx.x; c < ncol; c += blockDim.x) dst[c] = src[c];
   }
-  if (overlap && ck.gend == 0)  // no complete group yet: the previous branch stays padded
+  if (overlap && ck.gend == 0 && in_bounds((long long)((st - state) + 8 * ncol - 1), state_elems, flag))
     for (int c = threadIdx.x; c < 4 * ncol; c += blockDim.x) st[(size_t)4 * ncol + c] = padded_value(pk, c % ncol);
 }
 
@@ -384,7 +390,8 @@ cudaError_t launch_pack_ape(const csa_compressor* c, const float* ape, cudaStrea
 
 cudaError_t launch_projection_ffma(const csa_compressor* c, const uint16_t* x, int M, float* out, int mode,
                                    const int32_t* start_pos, int N, int p0, cudaStream_t s) {
-  RowMap map{mode, start_pos, c->slots, c->ratio, c->overlap, c->ape_set ? c->ape : nullptr, N, p0};
+  const long long extent = mode == 0 ? (long long)M * c->pk.cols() : (long long)c->opt.max_batch * c->slots * c->pk.cols();
+  RowMap map{mode, start_pos, c->slots, c->ratio, c->overlap, c->ape_set ? c->ape : nullptr, N, p0, extent, c->dev_flag};
   const int ncol = c->pk.cols();
   dim3 grid((ncol + GN - 1) / GN, (M + GM - 1) / GM);
   gemm_ffma_kernel<<<grid, 256, 0, s>>>(x, c->w_packed, M, ncol, c->dim, out, map);
@@ -409,13 +416,14 @@ cudaError_t launch_prefill_pool(const csa_compressor* c, const float* proj, int 
   const long long E = (long long)B * ck.G;
   if (E > 0)
     prefill_pool_kernel<<<(unsigned)((E + 3) / 4), 128, 0, s>>>(proj, B, N, ck, c->ratio, c->overlap, c->pk, c->state,
-                                                              c->slots, slot_offset, epi_params(c), out);
+                                                              c->slots, slot_offset, epi_params(c), out, c->dev_flag);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_state(const csa_compressor* c, const float* proj, int B, int N, int slot_offset,
                                  const Chunk& ck, cudaStream_t s) {
-  prefill_state_kernel<<<B, 256, 0, s>>>(proj, N, ck, c->ratio, c->overlap, c->pk, c->state, c->slots, slot_offset);
+  prefill_state_kernel<<<B, 256, 0, s>>>(proj, N, ck, c->ratio, c->overlap, c->pk, c->state, c->slots, slot_offset,
+                                         (long long)c->opt.max_batch * c->slots * c->pk.cols(), c->dev_flag);
   return cudaGetLastError();
 }
 

@@ -76,6 +76,7 @@ struct Params {
   const float* carry;      // [B][1 + overlap][3][H] running softmax values of the candidates
                            // of the first groups that are earlier than the chunk, or null
   int* flag;
+  long long state_elems, pooled_elems;  // extents checked by the bounds-checked build
 };
 
 struct EntryParams {
@@ -84,6 +85,8 @@ struct EntryParams {
   const uint16_t* pooled;  // [B][ntt][GT][H] bf16 bits
   EpiParams ep;
   csa_out out;
+  long long out_rows;      // rows of the outputs (checked by the bounds-checked build)
+  int* flag;
 };
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -242,9 +245,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       //    of the last complete group that this tile owns; thread et < 128 writes packed
       //    column col0 + et.  Virtual group G is absolute group gend.
       if (et < kRows) {
-        float* st = P.state + (size_t)(P.slot_offset + b) * P.slots * P.ncol + col0 + et;
+        const size_t st0 = (size_t)(P.slot_offset + b) * P.slots * P.ncol + col0 + et;
+        float* st = P.state + st0;
         const int own0 = max(tt * P.T, P.a), own1 = min(tt * P.T + P.T, P.a + P.N);
-        auto put = [&](int tok, int slot) { st[(size_t)slot * P.ncol] = stg[et * kSmemStride + (tok - t0)]; };
+        auto put = [&](int tok, int slot) {
+          if (in_bounds((long long)(st0 + (size_t)slot * P.ncol), P.state_elems, P.flag))
+            st[(size_t)slot * P.ncol] = stg[et * kSmemStride + (tok - t0)];
+        };
         if (!P.overlap) {
           for (int tok = max(own0, r * G); tok < own1; ++tok) put(tok, tok - r * G);
         } else {
@@ -256,7 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (P.gend == 0 && tt == 0) {
             const int kind = et / F;  // padded previous branch: kv 0, score -inf
             const float pad = kind < pk.nk / 2 ? 0.0f : -INFINITY;
-            for (int i = 0; i < 4; ++i) st[(size_t)(4 + i) * P.ncol] = pad;
+            for (int i = 0; i < 4; ++i)
+              if (in_bounds((long long)(st0 + (size_t)(4 + i) * P.ncol), P.state_elems, P.flag))
+                st[(size_t)(4 + i) * P.ncol] = pad;
           }
         }
       }
@@ -328,7 +337,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             num = fmaf(e, kv[i], num);
           }
         }
-        pooled_tile[(size_t)g * pk.H + ftile * F + f] = bf16_bits(__fdiv_rn(num, den));
+        const size_t pi = (size_t)g * pk.H + ftile * F + f;
+        if (in_bounds((long long)((pooled_tile - P.pooled) + pi), P.pooled_elems, P.flag))
+          pooled_tile[pi] = bf16_bits(__fdiv_rn(num, den));
       }
     }
   }
@@ -369,13 +380,15 @@ __device__ __forceinline__ void running_softmax(int n, Cand cand, float* out, in
 
 __global__ void __launch_bounds__(128) chunk_carry_kernel(const float* __restrict__ state, Packing pk, int overlap,
                                                           int slots, int slot_offset, Chunk ck,
-                                                          float* __restrict__ carry) {
+                                                          float* __restrict__ carry, long long carry_elems,
+                                                          int* flag) {
   griddep_launch_dependents();
   const int b = blockIdx.y, f = blockIdx.x * blockDim.x + threadIdx.x;
   const int ncol = pk.cols(), H = pk.H;
   if (f >= H) return;
   const float* st = state + (size_t)(slot_offset + b) * slots * ncol;
   float* out = carry + (size_t)b * (1 + overlap) * 3 * H + f;
+  if (!in_bounds((long long)((size_t)(b + 1) * (1 + overlap) * 3 * H) - 1, carry_elems, flag)) return;
   if (!overlap) {
     running_softmax(ck.a, [&](int i, bool score) { return st + (size_t)i * ncol + pk.col(score ? S : KV, f); }, out, H);
     return;
@@ -430,7 +443,9 @@ __global__ void __launch_bounds__(128) prefill_entry_kernel(const EntryParams P)
   if (lane == 0) wss[t >> 5] = ss;
   __syncthreads();
   const float inv = rms_inv(wss[0] + wss[1] + wss[2] + wss[3], P.ep);
-  entry_epilogue_quad(v, act, f, lane, inv, gn, rc, rs, P.ep, (size_t)P.ck.row(b, j), P.out);
+  const long long row = P.ck.row(b, j);
+  if (!in_bounds(row, P.out_rows, P.flag)) return;  // the same for the whole CTA
+  entry_epilogue_quad(v, act, f, lane, inv, gn, rc, rs, P.ep, (size_t)row, P.out);
 }
 
 }  // namespace tc
@@ -508,11 +523,14 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
   P.carry = nullptr;
   P.ape = c->ape_set ? c->ape : nullptr;
   P.flag = c->dev_flag;
+  P.state_elems = (long long)c->opt.max_batch * c->slots * P.ncol;
+  P.pooled_elems = (long long)B * P.ntt * P.GT * c->H;
   P.w = c->w_planes;
   if (chunk_needs_carry(ck, c->overlap)) {
     float* carry = (float*)((uint8_t*)scratch + carry_offset((size_t)B * P.ntt * P.GT * c->H * sizeof(uint16_t)));
     chunk_carry_kernel<<<dim3((c->H + 127) / 128, B), 128, 0, s>>>(c->state, c->pk, c->overlap, c->slots, slot_offset,
-                                                                  ck, carry);
+                                                                  ck, carry, (long long)B * (1 + c->overlap) * 3 * c->H,
+                                                                  c->dev_flag);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     P.carry = carry;
@@ -558,6 +576,8 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
   Q.ratio = c->ratio;
   Q.ck = ck;
   Q.pooled = P.pooled;
+  Q.out_rows = (long long)B * ck.bstride;
+  Q.flag = c->dev_flag;
   Q.ep = epi_params(c);
   Q.out = out;
   cudaLaunchAttribute at[1];

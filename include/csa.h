@@ -199,7 +199,9 @@ int64_t csa_state_elems(const csa_compressor* c);
 int csa_state_export(const csa_compressor* c, float* kv, float* score, csa_stream_t stream);
 
 /* Reads and clears the device-side error flag of the handle (synchronises the stream).
- * Returns CSA_OK, or CSA_ERR_DEVICE if a kernel flagged an input since the last call. */
+ * Returns CSA_OK, or CSA_ERR_DEVICE if a kernel flagged something since the last call: bit 1 a
+ * negative start_pos, bit 2 an entry position beyond the RoPE table, bit 4 a wait that gave up,
+ * bit 8 (only in the bounds-checked build of the library) a store outside its buffer, skipped. */
 int csa_device_status(csa_compressor* c, csa_stream_t stream);
 
 /* Frees the handle and its device memory (synchronises the device first). NULL is a no-op. */
