@@ -37,6 +37,7 @@ CHAINS = [
     (256, 512, 128, 0, 2, (100, 30, 128 * 3 + 77, 5)),
     (192, 256, 8, 0, 2, (13, 8 * 40 + 3, 4, 8)),
     (128, 64, 1, 0, 2, (5, 7)),
+    (1024, 128, 4, 1, 1, (9, 4 * 100 + 2, 301)),
     (128, 32, 3, 0, 2, (4, 3 * 90 + 2, 1)),      # packed tile narrower than 128 rows: CUDA-core path
     (128, 64, 300, 0, 1, (310, 300 * 2 + 7, 5)),  # ratio above one token tile: CUDA-core path
 ]

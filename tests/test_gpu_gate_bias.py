@@ -18,6 +18,7 @@ SHAPES = [
     (256, 128, 4, 1, 2, 4 * 60 + 1, 4 * 20 + 3),
     (256, 512, 128, 0, 2, 128 * 2 + 30, 128 + 9),
     (192, 256, 8, 0, 1, 8 * 40 + 3, 13),
+    (1024, 128, 4, 1, 1, 4 * 120 + 1, 4 * 30 + 2),
     (128, 32, 3, 0, 2, 3 * 40 + 2, 7),           # CUDA-core path
     (128, 64, 300, 0, 1, 300 * 2 + 7, 301),      # CUDA-core path
 ]

@@ -182,6 +182,9 @@ SMALL_FP4 = [(d, H, r, ov, B, N, 1) for d, H, r, ov, B, N in SMALL] + [
     (256, 128, 4, 1, 2, 4 * 60 + 1, 2),
     (128, 32, 3, 0, 2, 3 * 40 + 2, 2),   # CUDA-core path with the block-32 quantiser (lane pairs)
     (256, 64, 8, 0, 1, 8 * 30 + 5, 2),
+    # few packed tiles at a wider dim (the 128-token tile)
+    (1024, 128, 4, 1, 2, 4 * 150 + 3, 2),
+    (1024, 128, 8, 0, 1, 8 * 70 + 5, 1),
 ]
 
 
