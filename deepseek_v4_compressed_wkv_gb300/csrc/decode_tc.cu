@@ -11,9 +11,10 @@
 //
 //  * decode_proj_kernel, grid (packed tile, K slice, 128-token block): accumulates the slice in
 //    K chunks of 128 (TMEM, promoted to f32 registers as in the prefill kernel) and writes its
-//    partial sums.  Roles (320 threads): warp 0 issues the TMA loads (three plane tiles and one
-//    token tile of K = 32 per stage, 64-byte swizzle, 6 stages), warp 1 owns TMEM and issues
-//    tcgen05.mma, warps 2-9 drain the chunk accumulators and store the partial sums.  The
+//    partial sums.  Roles (320 threads): warp 0 issues the loads (one bulk copy of the three
+//    pre-swizzled plane tiles and one TMA token tile of K = 32 per stage, 4 stages), warp 1 owns
+//    TMEM and issues tcgen05.mma, warps 2-9 drain the chunk accumulators, the cluster of 4 K
+//    slices adds its sums through distributed shared memory and stores them with TMA.  The
 //    weights are not written by any kernel that can precede a decode launch in early-start
 //    mode, so warp 0 fetches the first stages' weight tiles (and prefetches the rest of the
 //    slice into L2) before it waits for the preceding kernel; the tokens, and every write,
