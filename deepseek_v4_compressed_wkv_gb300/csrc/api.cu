@@ -3,15 +3,24 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "csa_internal.cuh"
 #include "kernels.h"
 
 namespace {
+
+// An NVTX range around an ABI call, for timelines taken with the CUDA tools (a no-op otherwise).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 thread_local std::string g_last_error;
 
@@ -104,6 +113,10 @@ void free_all(csa_compressor* c) {
 
 int ensure_scratch(csa_compressor* c, size_t bytes, cudaStream_t s) {
   if (c->scratch_bytes >= bytes) return CSA_OK;
+  // failure injection on the host, for tests of the error path: CSA_TEST_FAIL_ALLOC set makes
+  // growing the scratch fail as a cudaMalloc failure would (nothing is freed or enqueued)
+  if (getenv("CSA_TEST_FAIL_ALLOC"))
+    return fail(CSA_ERR_CUDA, "cudaMalloc(scratch): forced failure (CSA_TEST_FAIL_ALLOC is set)");
   CSA_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
   cudaFree(c->scratch);
   c->scratch = nullptr;
@@ -145,6 +158,7 @@ int check_prefill(const csa_compressor* c, const uint16_t* x, int B, int N, int 
 
 int prefill_call(csa_compressor* c, const uint16_t* x, int B, int N, int start_pos, int slot_offset,
                  const csa_out* out, int cache_rows, csa_stream_t stream, const char* what) {
+  NvtxRange range(what);
   try {
     csa::Chunk ck;
     int rc = check_prefill(c, x, B, N, start_pos, slot_offset, out, cache_rows, what, &ck);
@@ -294,6 +308,7 @@ int csa_compressor_create(int dim, int H, int ratio, int overlap, const csa_opti
 
 int csa_compressor_set_weights(csa_compressor* c, const float* wkv, const float* wgate, const float* gain,
                                csa_stream_t stream) {
+  NvtxRange range("csa_compressor_set_weights");
   if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
   if (!wkv || !gain) return fail(CSA_ERR_ARG, "wkv and norm_gain are required");
   if (!wgate && c->ratio > 1) return fail(CSA_ERR_ARG, "wgate is required at ratio > 1");
@@ -333,6 +348,7 @@ int csa_compress_prefill_into(csa_compressor* c, const uint16_t* x, int B, int N
 
 int csa_compress_decode(csa_compressor* c, const uint16_t* x_tok, int B, const int32_t* start_pos, uint8_t* emitted,
                         const csa_out* out, csa_stream_t stream) {
+  NvtxRange range("csa_compress_decode");
   if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
   if (!c->weights_set) return fail(CSA_ERR_STATE, "weights not set");
   if (B < 1 || B > c->opt.max_batch) return fail(CSA_ERR_ARG, "B %d must be in [1, max_batch=%d]", B, c->opt.max_batch);
@@ -370,6 +386,7 @@ int csa_compress_decode(csa_compressor* c, const uint16_t* x_tok, int B, const i
 }
 
 int csa_state_reset(csa_compressor* c, int slot_begin, int slot_count, csa_stream_t stream) {
+  NvtxRange range("csa_state_reset");
   if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
   if (slot_begin < 0 || slot_count < 0 || (long long)slot_begin + slot_count > c->opt.max_batch)
     return fail(CSA_ERR_ARG, "slots [%d, %d) outside [0, %d)", slot_begin, slot_begin + slot_count, c->opt.max_batch);

@@ -9,6 +9,8 @@
 // in a fixed file-scope device array instead.
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "csa_internal.cuh"
 #include "kernels.h"
 
@@ -35,8 +37,23 @@ int csa_internal_fail(int code, const char* msg);
 int csa_internal_check_prefill(const csa_compressor* c, const uint16_t* x, int B, int N, int start_pos,
                                int slot_offset, const csa_out* out, const char* what, csa::Chunk* ck);
 
+namespace {
+int noalloc_call(csa_compressor* c, const uint16_t* x, int B, int N, int start_pos, int slot_offset,
+                 const csa_out* out, csa_stream_t stream);
+}  // namespace
+
 extern "C" int csa_compress_prefill_noalloc(csa_compressor* c, const uint16_t* x, int B, int N, int start_pos,
                                             int slot_offset, const csa_out* out, csa_stream_t stream) {
+  nvtxRangePushA("csa_compress_prefill_noalloc");
+  const int rc = noalloc_call(c, x, B, N, start_pos, slot_offset, out, stream);
+  nvtxRangePop();
+  return rc;
+}
+
+namespace {
+
+int noalloc_call(csa_compressor* c, const uint16_t* x, int B, int N, int start_pos, int slot_offset,
+                 const csa_out* out, csa_stream_t stream) {
   csa::Chunk ck;
   const int rc =
       csa_internal_check_prefill(c, x, B, N, start_pos, slot_offset, out, "csa_compress_prefill_noalloc", &ck);
@@ -76,3 +93,5 @@ extern "C" int csa_compress_prefill_noalloc(csa_compressor* c, const uint16_t* x
   c->launches += csa::chunk_needs_carry(ck, c->overlap) + 1 + (ck.G > 0);
   return ck.G;
 }
+
+}  // namespace
