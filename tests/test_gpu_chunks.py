@@ -146,3 +146,28 @@ def test_hca_chunked_prefill():
             check_entries(to_np(got), ref["prequant"], 1, f"HCA chunk at {p0}")
         p0 += n
     check_state(g, o, "HCA state after the chunks")
+
+
+@pytest.mark.parametrize("layer_idx,split", [(0, 65537), (1, 70000)])
+def test_long_context_in_two_chunks_sampled(layer_idx, split):
+    """The long-context workload (131072 tokens, 1 % outlier tokens) as a prefill and a chunk
+    split mid-group: sampled entries of both calls against the oracle's groups of the whole
+    sequence (a chunk gives the entries a whole prefill gives)."""
+    from test_gpu_parity import sampled_groups
+    wl = synthetic.LONG
+    layer = wl.layers[layer_idx]
+    N = 131072
+    g, o = make_pair(wl.seed, layer)
+    x, *_ = layer_inputs(wl.seed, layer, 1, N, outlier_frac=wl.outlier_frac)
+    r = layer.ratio
+    got = []
+    for p0, p1 in ((0, split), (split, N)):
+        out = g.prefill(dev_bits(np.ascontiguousarray(x[:, p0:p1])), start_pos=p0, prequant=True)
+        torch.cuda.synchronize()
+        got.append((p0 // r, to_np(out)))
+    for gfirst, gn in got:
+        G = gn["prequant"].shape[1]
+        loc = sampled_groups(G, 12, gfirst)
+        ref = o.prefill_groups(x[0], [gfirst + j for j in loc])
+        check_entries({k: v[0][loc] for k, v in gn.items()}, ref["prequant"], 1, f"long chunk from group {gfirst}")
+    assert g.device_status() == 0
