@@ -691,9 +691,10 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
   auto encode = tcx::get_encode();
   if (!encode) return cudaErrorNotSupported;
   const size_t smem = (size_t)kRingBytes + 1024 + 1024;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(decode_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<unsigned long long> attr{0};
+  cudaError_t ea = tcx::once_per_device(attr, [] {
+    cudaError_t e = cudaFuncSetAttribute(decode_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)((size_t)kRingBytes + 1024 + 1024));
     // both kernels ask for the largest shared-memory carveout, so that finish CTAs can share an
     // SM with a projection CTA
     if (e == cudaSuccess)
@@ -705,9 +706,9 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(decode_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kFinSmemFloats * (int)sizeof(float));
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+    return e;
+  });
+  if (ea != cudaSuccess) return ea;
   CUtensorMap mx;
   {
     // the tokens: [B rows][dim]; rows past B in the last 128-token block read as zeros

@@ -548,13 +548,12 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
       return cudaErrorInvalidValue;
   }
   const size_t smem = (size_t)kStages * Tile<TOK>::kStageBytes + 1024 /* barriers */ + 1024 /* alignment */;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(prefill_tc_kernel<TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_set{0};
+  cudaError_t ea = tcx::once_per_device(attr_set, [] {
+    return cudaFuncSetAttribute(prefill_tc_kernel<TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)((size_t)kStages * Tile<TOK>::kStageBytes + 1024 + 1024));
+  });
+  if (ea != cudaSuccess) return ea;
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;

@@ -7,8 +7,24 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace csa {
 namespace tcx {
+
+// Function attributes (dynamic shared memory, carveout) belong to a device: `done` keeps one bit
+// per device; set() runs once on each device the process launches on (setting an attribute twice
+// is harmless, so two threads racing to the first launch need no lock).
+inline cudaError_t once_per_device(std::atomic<unsigned long long>& done, cudaError_t (*set)()) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (done.load() & bit) return cudaSuccess;
+  e = set();
+  if (e == cudaSuccess) done.fetch_or(bit);
+  return e;
+}
 
 constexpr uint64_t kWaitNs = 2000000000ull;  // bounded mbarrier waits: 2 s
 
