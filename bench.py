@@ -454,7 +454,8 @@ def bench_decode(args, torch, csa, synthetic, device, peaks, world, rank):
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 128 << 20)
     w_bytes = sum(2 * L.width * L.dim * 4 for L in wl.layers)
-    n_layers = args.decode_layers or max(2, math.ceil(2.5 * l2 / w_bytes))
+    # at least 8 instances, and at least 2.5 x L2 of f32 weight bytes (the planes read are 1.5 x that)
+    n_layers = args.decode_layers or max(8, math.ceil(2.5 * l2 / w_bytes))
     sp0 = synthetic.start_positions(wl.seed, B, wl.start_pos_hi)
     layers = []
     for li in range(n_layers):
