@@ -127,7 +127,8 @@ int csa_compressor_set_gate_bias(csa_compressor* c, const float* ape, csa_stream
 
 /* Prefill of B sequences, tokens start_pos .. start_pos + N - 1 of each ("Pool token pairs",
  * Compressor forward, prefill branch).  x [B][N][dim] bf16 dev.  Sequence b uses state slot
- * slot_offset + b; needs slot_offset + B <= max_batch.
+ * slot_offset + b; needs B >= 1, N >= 1 and slot_offset + B <= max_batch (an empty call returns
+ * CSA_ERR_ARG and enqueues nothing).
  *  - start_pos 0: the whole-sequence prefill of the pages.  Writes G = N / ratio entries per
  *    sequence and leaves the trailing N % ratio tokens in the state (at ratio 4 overlapped, also
  *    the last complete group's tokens, whose branch B the next entry pools).
@@ -174,7 +175,8 @@ int csa_compress_prefill_into(csa_compressor* c, const uint16_t* x, int B, int N
 int csa_compress_prefill_noalloc(csa_compressor* c, const uint16_t* x, int B, int N, int start_pos,
                                  int slot_offset, const csa_out* out, csa_stream_t stream);
 
-/* One decode step for sequences 0..B-1 (state slots 0..B-1), one token each.
+/* One decode step for sequences 0..B-1 (state slots 0..B-1), one token each; 1 <= B <= max_batch
+ * (B = 0 returns CSA_ERR_ARG and enqueues nothing).
  *  x_tok     [B][dim] bf16 dev
  *  start_pos [B] int32 dev: position of this token in its sequence (per sequence)
  *  emitted   [B] u8 dev: set to 1 where the token completed a group, else 0

@@ -361,6 +361,14 @@ def test_errors_are_reported_not_raised_on_the_device():
     lib = csa.load_library()
     assert lib.csa_compress_prefill(g.handle, x.data_ptr(), 1, 8, -1, 0, None, None) == -1  # negative start_pos
     assert lib.csa_compress_prefill(g.handle, x.data_ptr(), 1, 8, 5, 0, None, None) == -1  # entries but no out
+    # empty calls are argument errors that enqueue nothing (the oracle rejects them alike)
+    n0 = g.kernel_launches()
+    assert lib.csa_compress_prefill(g.handle, x.data_ptr(), 1, 0, 0, 0, None, None) == -1
+    assert lib.csa_compress_prefill(g.handle, x.data_ptr(), 0, 8, 0, 0, None, None) == -1
+    sp1 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    em1 = torch.zeros(1, dtype=torch.uint8, device=DEV)
+    assert lib.csa_compress_decode(g.handle, x.data_ptr(), 0, sp1.data_ptr(), em1.data_ptr(), None, None) == -1
+    assert g.kernel_launches() == n0
     # decode positions the kernel cannot serve: flagged, rows not emitted, context still usable
     sp = torch.tensor([-3, 67], dtype=torch.int32, device=DEV)
     d = g.decode(torch.zeros(2, 128, dtype=torch.bfloat16, device=DEV), sp)

@@ -403,6 +403,23 @@ def test_prefill_state_holds_the_tail_projections():
     assert np.all(kv[0] == 0) and np.all(sc[0] == -np.inf)  # slot 0 untouched
 
 
+def test_empty_calls_are_rejected_and_change_nothing():
+    """Empty batches and zero-token prefills are argument errors (the library's ABI returns
+    CSA_ERR_ARG for the same calls); the state keeps what an earlier prefill left."""
+    dim, H, r = 32, 16, 4
+    c, _ = make(dim, H, r, 1, max_batch=2)
+    c.prefill(rand_x(17, 2, 2 * r + 3, dim))
+    kv0, sc0 = (a.copy() for a in c.state())
+    with pytest.raises(ValueError):
+        c.prefill(np.zeros((2, 0, dim), np.uint16))
+    with pytest.raises(ValueError):
+        c.prefill(np.zeros((0, 5, dim), np.uint16))
+    with pytest.raises(ValueError):
+        c.decode(np.zeros((0, dim), np.uint16), np.zeros(0, np.int32))
+    kv1, sc1 = c.state()
+    assert np.array_equal(kv0, kv1) and np.array_equal(sc0, sc1)
+
+
 def test_decode_emission_timing_per_sequence():
     dim, H, r = 32, 16, 4
     c, _ = make(dim, H, r, 1, max_batch=6)
