@@ -595,7 +595,9 @@ def run_reference(args, rank, world):
     return {"impl": "reference", "metric": METRIC, "value": val, "unit": "entries/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD}, "cpu_baseline": cpu,
+            "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": arm.N, "entries_per_step": g,
+                       "l2": "not applicable: the oracle runs on the host cores",
+                       "parallelism": f"host threads x{arm.cores}"}, "cpu_baseline": cpu,
             "e2e": {"value": val, "unit": "entries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

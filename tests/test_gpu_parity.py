@@ -409,6 +409,42 @@ def test_decode_batch_beyond_one_token_tile(B, ratio, overlap):
     assert g.device_status() == 0
 
 
+@pytest.mark.parametrize("B", [4096, 4097])
+def test_decode_at_the_batch_limit_of_the_tensor_core_path(B):
+    """4096 sequences, the most the tensor-core decode takes in one call, and one more, which
+    runs the CUDA-core decode: states from four batched prefills of different lengths (so that
+    the sequences emit at different steps), then five steps against the oracle."""
+    layer = synthetic.Layer(256, 128, 4, 1, 1.0 / 16, gate_scale=2.0, rope_dim=64, fp4=1)
+    g, o = make_pair(13, layer, max_batch=B)
+    lens = [5, 6, 7, 8]
+    x, *_ = layer_inputs(13, layer, B, max(lens) + 5)
+    q = -(-B // len(lens))
+    sp0 = np.zeros(B, np.int32)
+    for i, n in enumerate(lens):
+        b0, b1 = i * q, min(B, (i + 1) * q)
+        xp = np.ascontiguousarray(x[b0:b1, :n])
+        o.prefill(xp, slot_offset=b0)
+        g.prefill(dev_bits(xp), slot_offset=b0, prequant=False)
+        sp0[b0:b1] = n
+    emitted_any = 0
+    for k in range(5):
+        sp = (sp0 + k).astype(np.int32)
+        xt = np.ascontiguousarray(x[np.arange(B), sp])
+        r = o.decode(xt, sp)
+        d = g.decode(dev_bits(xt), torch.from_numpy(sp).to(DEV))
+        em = d["emitted"].cpu().numpy()
+        assert np.array_equal(em, r["emitted"]), k
+        rows = np.flatnonzero(em)
+        emitted_any += rows.size
+        if rows.size:
+            check_entries(to_np(d, rows=rows), r["prequant"][rows], 1, f"decode B={B} step {k}")
+    assert emitted_any == B + q  # positions n .. n+4 complete one group each, two from n = 7
+    kg, sg = (t.cpu().numpy() for t in g.state_export())
+    ko, so = o.state()
+    assert np.allclose(kg, ko, rtol=2e-5, atol=2e-5 * np.abs(ko).max(initial=1.0))
+    assert g.device_status() == 0
+
+
 # ---- decode calls queued back to back (launches that start before the previous one ends) -----
 
 def _decode_setup(seed, layers, B, pos_hi):
