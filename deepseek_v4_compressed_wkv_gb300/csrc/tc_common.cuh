@@ -125,34 +125,18 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// TMA store of a 3-D box from this CTA's shared memory (rows past the tensor's extent are not
-// written), and the bulk-group bookkeeping: commit, then wait until the shared memory has been
+// Bulk-group bookkeeping of the TMA stores: commit, then wait until the shared memory has been
 // read.  Shared-memory writes by threads must be made visible to the copy engine first.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-                   (uint64_t)map),
-               "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void named_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
 
 // Distributed shared memory: the address of the same shared variable in CTA `rank` of the
-// cluster; an asynchronous 4-byte store there that completes its share of the transaction
-// count of an mbarrier in that CTA; the split cluster barrier (arrive, later wait).
+// cluster; a 16-byte load from such an address; the split cluster barrier (arrive, later wait).
 __device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
   return r;
-}
-__device__ __forceinline__ void st_async_f32(uint32_t remote, float v, uint32_t remote_bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote),
-               "r"(__float_as_uint(v)), "r"(remote_bar)
-               : "memory");
 }
 __device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
   float4 v;
@@ -170,11 +154,6 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
-// Hint: fetch `bytes` (a multiple of 16, 16-byte aligned) into L2.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)src), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
                                             uint64_t* bar) {
   asm volatile(
@@ -188,13 +167,6 @@ __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
 }
 
-// Hint: fetch one tile of a tensor map into L2 (no shared memory, no completion to wait for).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int c0, int c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"((uint64_t)map), "r"(c0),
-               "r"(c1)
-               : "memory");
-}
-
 // Programmatic dependent launch.  griddep_wait: block until the grids this launch depends on
 // have completed and their writes are visible (returns at once when the launch did not ask
 // for early start).  griddep_launch_dependents: this CTA no longer holds back the start of
@@ -204,21 +176,9 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with 128-byte swizzle:
-// rows of 128 bytes, 8-row core groups 1024 bytes apart (stride byte offset), descriptor
-// version 1, layout SWIZZLE_128B (2).  The leading byte offset is unused for this layout.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)1u << 16;
-  d |= (uint64_t)(1024u >> 4) << 32;
-  d |= (uint64_t)1u << 46;
-  d |= (uint64_t)2u << 61;
-  return d;
-}
-
-// The same for 64-byte swizzle: rows of 64 bytes (32 bf16), 8-row groups 512 bytes apart,
-// layout SWIZZLE_64B (4).
+// Shared-memory matrix descriptor of a K-major bf16 tile with 64-byte swizzle: rows of 64 bytes
+// (32 bf16), 8-row core groups 512 bytes apart (stride byte offset), descriptor version 1,
+// layout SWIZZLE_64B (4).  The leading byte offset is unused for this layout.
 __device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
