@@ -77,6 +77,40 @@ def test_prefill_chunks_then_decode(dim, H, ratio, overlap, B, chunks):
     assert g.device_status() == 0
 
 
+def _random_chains(n, seed=2027):
+    """Seeded random chunk chains: shape, ratio and chunk lengths drawn so that chunks start
+    anywhere in a group, span zero to several token tiles, and mix both projection paths."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        ratio, overlap = [(1, 0), (2, 0), (3, 0), (4, 1), (4, 0), (8, 0), (16, 0), (128, 0)][rng.integers(8)]
+        dim = int(rng.choice([128, 256]))
+        H = int(rng.choice([32, 64, 128, 128, 256]))
+        B = int(rng.integers(1, 4))
+        lens = tuple(int(v) for v in rng.integers(1, 700, size=int(rng.integers(2, 5))))
+        out.append((dim, H, ratio, overlap, B, lens))
+    return out
+
+
+@pytest.mark.parametrize("dim,H,ratio,overlap,B,chunks", _random_chains(12))
+def test_random_chunk_chains(dim, H, ratio, overlap, B, chunks):
+    layer = synthetic.Layer(dim, H, ratio, overlap, 1.0 / math.sqrt(dim), gate_scale=2.0, rope_dim=min(64, H), fp4=1)
+    g, o = make_pair(17, layer, max_batch=B)
+    x, *_ = layer_inputs(17, layer, B, sum(chunks))
+    p0 = 0
+    for n in chunks:
+        xc = np.ascontiguousarray(x[:, p0:p0 + n])
+        ref = o.prefill(xc, start_pos=p0)
+        got = g.prefill(dev_bits(xc), start_pos=p0)
+        torch.cuda.synchronize()
+        assert (got is None) == (ref["G"] == 0)
+        if ref["G"]:
+            check_entries(to_np(got), ref["prequant"], 1, f"chunk at {p0} (+{n})")
+        p0 += n
+    check_state(g, o, "state after the chain")
+    assert g.device_status() == 0
+
+
 def test_prefill_into_cache_rows():
     layer = synthetic.Layer(256, 128, 4, 1, 1.0 / 16, gate_scale=2.0, rope_dim=64, fp4=1)
     B, rows = 2, 100
