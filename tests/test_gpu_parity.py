@@ -473,7 +473,7 @@ DECODE_PAIR = [synthetic.Layer(512, 512, 4, 1, 1.0 / 22, gate_scale=2.0, rope_di
                synthetic.Layer(512, 512, 16, 0, 1.0 / 22, gate_scale=2.0, rope_dim=64, fp4=1, weight_stream=3)]
 
 
-def _check_steps(pairs, seed, sp0, steps, outs):
+def _check_steps(pairs, seed, sp0, steps, outs, layers=DECODE_PAIR):
     # the entries of all steps of a layer are checked together: the 2-ulp share is a property
     # of a sample, and one step may emit a single entry
     got = [[] for _ in pairs]
@@ -481,7 +481,7 @@ def _check_steps(pairs, seed, sp0, steps, outs):
     for k in range(steps):
         sp = (sp0 + k).astype(np.int32)
         for li, (g, o) in enumerate(pairs):
-            xt = _step_inputs(seed, DECODE_PAIR[li], sp)
+            xt = _step_inputs(seed, layers[li], sp)
             r = o.decode(xt, sp)
             d = outs[k][li]
             em = d["emitted"].cpu().numpy()
@@ -518,15 +518,22 @@ def test_decode_steps_queued_without_host_sync():
     _check_steps(pairs, seed, sp0, steps, outs)
 
 
-def test_decode_steps_in_a_cuda_graph():
-    """The same steps captured once in a CUDA graph and replayed: identical to the oracle."""
-    seed, B, steps = 23, 40, 12
-    sp0, pairs = _decode_setup(seed, DECODE_PAIR, B, 97)
+@pytest.mark.parametrize("case", ["small", "decode_workload"])
+def test_decode_steps_in_a_cuda_graph(case):
+    """The same steps captured once in a CUDA graph and replayed (the way bench.py times decode):
+    identical to the oracle.  "decode_workload" is the benchmark's pair of Flash-width
+    compressors (ratio 4 overlapped and ratio 128, dim 4096, head_dim 512) with 128 sequences
+    at positions up to 8191."""
+    if case == "small":
+        layers, seed, B, pos_hi, steps = DECODE_PAIR, 23, 40, 97, 12
+    else:
+        layers, seed, B, pos_hi, steps = synthetic.DECODE.layers, 25, synthetic.DECODE.batch, 8191, 12
+    sp0, pairs = _decode_setup(seed, layers, B, pos_hi)
     xs = {}
     for k in range(steps):
         sp = (sp0 + k).astype(np.int32)
         for li in range(2):
-            xs[k, li] = (dev_bits(_step_inputs(seed, DECODE_PAIR[li], sp)), torch.from_numpy(sp).to(DEV))
+            xs[k, li] = (dev_bits(_step_inputs(seed, layers[li], sp)), torch.from_numpy(sp).to(DEV))
     outs = [[{"emitted": torch.empty(B, dtype=torch.uint8, device=DEV),
               **pairs[li][0]._alloc_out(B, DEV, prequant=True)} for li in range(2)] for k in range(steps)]
 
@@ -542,7 +549,7 @@ def test_decode_steps_in_a_cuda_graph():
     pairs[1][0].decode(*xs[0, 1])
     torch.cuda.synchronize()
     for li, (g, _) in enumerate(pairs):
-        layer = DECODE_PAIR[li]
+        layer = layers[li]
         g.state_reset()
         for b in range(B):
             s = int(sp0[b])
@@ -556,7 +563,7 @@ def test_decode_steps_in_a_cuda_graph():
         run()
     graph.replay()
     torch.cuda.synchronize()
-    _check_steps(pairs, seed, sp0, steps, outs)
+    _check_steps(pairs, seed, sp0, steps, outs, layers)
 
 
 def test_decode_rollback_and_reset_between_steps():
