@@ -57,3 +57,16 @@ def test_two_gloo_ranks_barrier_and_max_over_ranks():
 def test_reference_arm_runs_on_rank_zero_only():
     import bench
     assert bench.run_reference(type("A", (), {"warmup": 0, "steps": 1})(), rank=1, world=2) is None
+
+
+def test_clock_record_rejection_rules():
+    """A throttled or clock-locked timed region is re-measured; a power cap alone is kept."""
+    import bench
+    ok = {"sm_mhz": 2050.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    assert bench.clock_rejection(ok) is None
+    assert bench.clock_rejection(None) is None
+    assert bench.clock_rejection({**ok, "reasons": ["hw_slowdown", "sw_power_cap"]}) == ["hw_slowdown"]
+    assert bench.clock_rejection({**ok, "reasons": ["sw_thermal_slowdown"]}) == ["sw_thermal_slowdown"]
+    assert bench.clock_rejection({"sm_mhz": 1100.0, "sm_max_mhz": 2070.0, "reasons": []}) == \
+        ["sm_clock_below_max_without_reason"]
+    assert bench.clock_rejection({"sm_mhz": 1100.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}) is None
