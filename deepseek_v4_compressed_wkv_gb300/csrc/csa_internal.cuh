@@ -101,6 +101,15 @@ inline Chunk make_chunk(int p0, int N, int ratio) {
 // projection kernel overwrites any state slot.
 inline bool chunk_needs_carry(const Chunk& k, int overlap) { return k.G > 0 && (k.a > 0 || (overlap && k.g0 > 0)); }
 
+// SMs of the current device, the one a launch goes to (152 on a GB300, used if the query fails).
+inline int current_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      n <= 0)
+    return 152;
+  return n;
+}
+
 // Kernel-side view of the epilogue parameters.
 struct EpiParams {
   const float* gain;      // [H]

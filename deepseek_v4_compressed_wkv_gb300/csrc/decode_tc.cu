@@ -655,12 +655,7 @@ __global__ void __launch_bounds__(kFinThreads, 5) decode_finish_kernel(const Fin
 
 // Number of K slices: about one CTA per SM for a 128-token block, at least one K block per CTA.
 int decode_tc_slices(const csa_compressor* c) {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
-  }
+  const int sms = current_sm_count();
   const int nkb = c->dim / dtc::kKb;
   int ks = sms / c->pk.ntiles;
   if (ks > nkb) ks = nkb;
@@ -763,12 +758,7 @@ cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, 
   }
   {
     FinParams P;
-    static int sms = 0;
-    if (!sms) {
-      int dev = 0;
-      cudaGetDevice(&dev);
-      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
-    }
+    const int sms = current_sm_count();
     P.B = B;
     P.ks = ks / decode_tc_cluster(ks);  // partial sums left after the on-chip additions
     P.ncol = c->pk.cols();

@@ -474,12 +474,7 @@ int owned_tokens(const csa_compressor* c, int tok) {
 // of 256 tokens per SM); the indexer's 128-wide compressor (4 packed tiles) takes the 128-token
 // tile, 4 x 34 = 136 CTAs in one wave instead of 76 CTAs of 224 tokens.
 int prefill_tok(const csa_compressor* c, int B, int N) {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
-  }
+  const int sms = current_sm_count();
   int best = tc::kTokMax;
   long long best_cost = -1;
   for (int tok : {256, 224, 128}) {
