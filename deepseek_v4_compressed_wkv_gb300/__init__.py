@@ -140,6 +140,17 @@ def _u16(t):
     return t.view(torch.int16) if t.dtype == torch.bfloat16 else t
 
 
+def _on_current_device(*tensors):
+    """The library launches on the current CUDA device: every tensor it reads or writes must
+    live there (a pointer into another GPU's memory would fault)."""
+    dev = torch.cuda.current_device()
+    for t in tensors:
+        if t is not None and (not t.is_cuda or t.device.index != dev):
+            raise CSAError(f"tensor on {t.device}, but the current CUDA device is cuda:{dev}")
+
+
+
+
 class Compressor:
     """One compressor instance (one attention layer's wkv / wgate / norm / state)."""
 
@@ -191,10 +202,27 @@ class Compressor:
                  prequant=torch.empty(rows, H, dtype=torch.bfloat16, device=device) if prequant else None)
         return d
 
+    def _check_out(self, d, rows):
+        """Caller-provided outputs: the library writes `rows` rows of each array given, so each
+        must be a contiguous CUDA tensor of the right type holding at least that many."""
+        H = self.head_dim
+        widths = {"latent": H, "codes": H // 2, "scales": H // self.scale_block, "prequant": H}
+        types = {"latent": torch.bfloat16, "codes": torch.uint8, "scales": torch.uint8, "prequant": torch.bfloat16}
+        if d.get("latent") is None:
+            raise CSAError("out['latent'] is required")
+        for k, t in d.items():
+            if t is None or k not in widths:
+                continue
+            if t.dtype != types[k]:
+                raise CSAError(f"out['{k}'] must be {types[k]}")
+            if t.numel() < rows * widths[k]:
+                raise CSAError(f"out['{k}'] holds {t.numel()} elements, the call writes {rows} x {widths[k]}")
+        _on_current_device(*[t for t in d.values() if t is not None])
+
     @staticmethod
     def _out_struct(d):
-        return Out(_dptr(d["latent"]).value, _dptr(d["codes"]).value, _dptr(d["scales"]).value,
-                   _dptr(d["prequant"]).value)
+        return Out(_dptr(d["latent"]).value, _dptr(d.get("codes")).value, _dptr(d.get("scales")).value,
+                   _dptr(d.get("prequant")).value)
 
     def prefill(self, x, slot_offset: int = 0, out=None, prequant: bool = True, stream=None, start_pos: int = 0):
         """x bf16 [B, N, dim] CUDA: tokens start_pos .. start_pos+N-1 of each sequence (start_pos > 0:
@@ -205,8 +233,11 @@ class Compressor:
         if D != self.dim or x.dtype != torch.bfloat16:
             raise CSAError("x must be bf16 [B, N, dim]")
         G = (start_pos + N) // self.ratio - start_pos // self.ratio
+        _on_current_device(x)
         if out is None:
             out = self._alloc_out(max(B * G, 1), x.device, prequant)
+        else:
+            self._check_out(out, B * G)
         o = self._out_struct(out)
         g = _check(self._lib.csa_compress_prefill(self._h, _dptr(_u16(x)), B, N, start_pos, slot_offset,
                                                   ctypes.byref(o), _stream(stream)), "csa_compress_prefill")
@@ -227,6 +258,8 @@ class Compressor:
         lat = cache["latent"]
         if lat.dim() != 3 or lat.shape[0] != B or lat.shape[2] != self.head_dim:
             raise CSAError("cache['latent'] must be [B, rows, head_dim]")
+        _on_current_device(x)
+        self._check_out({k: cache.get(k) for k in ("latent", "codes", "scales", "prequant")}, B * lat.shape[1])
         o = self._out_struct({k: cache.get(k) for k in ("latent", "codes", "scales", "prequant")})
         return _check(self._lib.csa_compress_prefill_into(self._h, _dptr(_u16(x)), B, N, start_pos, slot_offset,
                                                           ctypes.byref(o), lat.shape[1], _stream(stream)),
@@ -238,10 +271,18 @@ class Compressor:
         B, D = x_tok.shape
         if D != self.dim or x_tok.dtype != torch.bfloat16 or start_pos.dtype != torch.int32:
             raise CSAError("x_tok must be bf16 [B, dim] and start_pos int32 [B]")
+        if start_pos.numel() != B:
+            raise CSAError(f"start_pos has {start_pos.numel()} elements for {B} sequences")
+        _on_current_device(x_tok, start_pos)
         if out is None:
             out = self._alloc_out(B, x_tok.device, prequant)
+        else:
+            self._check_out(out, B)
         if emitted is None:
             emitted = torch.empty(B, dtype=torch.uint8, device=x_tok.device)
+        elif emitted.dtype != torch.uint8 or emitted.numel() < B:
+            raise CSAError("emitted must be uint8 with at least B elements")
+        _on_current_device(emitted)
         o = self._out_struct(out)
         _check(self._lib.csa_compress_decode(self._h, _dptr(_u16(x_tok)), B, _dptr(start_pos), _dptr(emitted),
                                              ctypes.byref(o), _stream(stream)), "csa_compress_decode")
@@ -283,6 +324,9 @@ def fp4_e4m3_roundtrip(x, stream=None):
     """bf16 CUDA tensor (size a multiple of 16) -> (codes u8 [n/2], scales u8 [n/16], out bf16 [n])."""
     lib = load_library()
     x = x.contiguous().view(-1)
+    if x.dtype != torch.bfloat16 or x.numel() % 16:
+        raise CSAError("x must be bf16 with a multiple of 16 elements")
+    _on_current_device(x)
     nb = x.numel() // 16
     codes = torch.empty(nb * 8, dtype=torch.uint8, device=x.device)
     scales = torch.empty(nb, dtype=torch.uint8, device=x.device)
@@ -297,6 +341,9 @@ def fp4_e8m0_roundtrip(x, stream=None):
     scales u8 [n/32] e8m0 bytes, out bf16 [n])."""
     lib = load_library()
     x = x.contiguous().view(-1)
+    if x.dtype != torch.bfloat16 or x.numel() % 32:
+        raise CSAError("x must be bf16 with a multiple of 32 elements")
+    _on_current_device(x)
     nb = x.numel() // 32
     codes = torch.empty(nb * 16, dtype=torch.uint8, device=x.device)
     scales = torch.empty(nb, dtype=torch.uint8, device=x.device)

@@ -361,6 +361,14 @@ def test_errors_are_reported_not_raised_on_the_device():
     lib = csa.load_library()
     assert lib.csa_compress_prefill(g.handle, x.data_ptr(), 1, 8, -1, 0, None, None) == -1  # negative start_pos
     assert lib.csa_compress_prefill(g.handle, x.data_ptr(), 1, 8, 5, 0, None, None) == -1  # entries but no out
+    # the binding refuses outputs too small for what the call writes, and mismatched lengths
+    small = g._alloc_out(1, DEV)
+    with pytest.raises(csa.CSAError, match="holds"):
+        g.prefill(torch.zeros(2, 8, 128, dtype=torch.bfloat16, device=DEV), out=small)  # 4 entries
+    with pytest.raises(csa.CSAError, match="start_pos has"):
+        g.decode(torch.zeros(2, 128, dtype=torch.bfloat16, device=DEV), torch.zeros(3, dtype=torch.int32, device=DEV))
+    with pytest.raises(csa.CSAError, match="multiple of 16"):
+        csa.fp4_e4m3_roundtrip(torch.zeros(24, dtype=torch.bfloat16, device=DEV))
     # empty calls are argument errors that enqueue nothing (the oracle rejects them alike)
     n0 = g.kernel_launches()
     assert lib.csa_compress_prefill(g.handle, x.data_ptr(), 1, 0, 0, 0, None, None) == -1
