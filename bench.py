@@ -39,7 +39,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--decode-steps", type=int, default=64)
+    ap.add_argument("--decode-steps", type=int, default=0,
+                    help="decode steps timed (0: the batched decode workload's 512)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--decode-only", action="store_true",
                     help="run and print only the decode measurement (for profiling)")
@@ -498,7 +499,7 @@ def bench_decode(args, torch, csa, synthetic, device, peaks, world, rank):
             outs = c._alloc_out(B, device, prequant=False)
             pair.append((c, outs))
         layers.append(pair)
-    steps = n_layers * max(1, -(-args.decode_steps // n_layers))
+    steps = n_layers * max(1, -(-(args.decode_steps or wl.decode_steps) // n_layers))
     xs = [torch.from_numpy(np.stack([synthetic.tokens(wl.seed, rank * B + b, int(sp0[b]) + k, int(sp0[b]) + k + 1,
                                                       wl.layers[0].dim)[0] for b in range(B)])).to(torch.bfloat16)
           .to(device) for k in range(8)]
