@@ -16,9 +16,9 @@
 //    TMEM and issues tcgen05.mma, warps 2-9 drain the chunk accumulators, the cluster of 4 K
 //    slices adds its sums through distributed shared memory and stores them with TMA.  The
 //    weights are not written by any kernel that can precede a decode launch in early-start
-//    mode, so warp 0 fetches the first stages' weight tiles (and prefetches the rest of the
-//    slice into L2) before it waits for the preceding kernel; the tokens, and every write,
-//    come after that wait.
+//    mode, so warp 0 fetches the first stages' weight tiles (and prefetches the next stages into
+//    L2) before it waits for the preceding kernel; the tokens, and every write, come after
+//    that wait.
 //
 //  * decode_finish_kernel, one CTA per sequence: adds the K slices' partial sums in slice order
 //    (a deterministic split-K reduction) into the token's state slot, applies the restart at
@@ -49,6 +49,7 @@ constexpr int kTok = 128;                               // tokens per CTA (MMA N
 constexpr int kKb = 64;                                 // K granularity of the slice split
 constexpr int kKs = 32;                                 // K per stage (one 64-byte swizzle row of bf16)
 constexpr int kStages = 4;
+constexpr int kPrefetchStages = 4;                     // weight stages fetched into L2 beyond the ring
 constexpr int kChunkSteps = 4;                          // stages per accumulator chunk (K = 128)
 constexpr int kPlaneBytes = kRows * kKs * 2;            // 8 KB
 static_assert(kRows == kPlaneTileRows && kKs == kPlaneTileK, "a stage is one tile of the plane layout");
@@ -126,12 +127,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nkb32 = P.nkb_total * (kKb / kKs), kb0 = k0 / kKs;
       const __nv_bfloat16* wt = P.w + plane_stage_elem(nkb32, tile, kb0);  // this slice's stages, contiguous
       constexpr int kW = 3 * kPlaneBytes;
-      // weights of the first stages into the ring, the rest of the slice into L2
+      // weights of the first stages into the ring and of the next kPrefetchStages into L2.  A
+      // longer L2 prefetch was slower: the copy engine works through the queued prefetches
+      // before the token tiles that the MMAs wait for after the wait below
       for (int t = 0; t < npre; ++t) {
         mbar_arrive_expect_tx(&full[t], kStageBytes);
         bulk_load_hint(smem + t * kStageBytes, wt + (size_t)t * (kW / 2), kW, &full[t], stream_pol);
       }
-      for (int t = npre; t < nstep; ++t) bulk_prefetch_l2_hint(wt + (size_t)t * (kW / 2), kW, stream_pol);
+      for (int t = npre; t < min(nstep, npre + kPrefetchStages); ++t)
+        bulk_prefetch_l2_hint(wt + (size_t)t * (kW / 2), kW, stream_pol);
       griddep_wait();  // the tokens may come from the preceding kernel
       griddep_launch_dependents();
       for (int t = 0; t < npre; ++t)
