@@ -166,8 +166,7 @@ int prefill_call(csa_compressor* c, const uint16_t* x, int B, int N, int start_p
     cudaStream_t s = (cudaStream_t)stream;
     const long long M = (long long)B * N;
     const csa_out o = out ? *out : csa_out{nullptr, nullptr, nullptr, nullptr};
-    CSA_CUDA(csa::invalidate_decode_acc(c, slot_offset, B, s), "invalidate decode running values");
-    if (csa::prefill_tc_supported(c, x)) {
+    if (csa::prefill_tc_supported(c, x)) {  // the kernel marks the decode running values invalid
       rc = ensure_scratch(c, csa::prefill_tc_scratch_bytes(c, B, N, ck), s);
       if (rc) return rc;
       if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
@@ -177,6 +176,7 @@ int prefill_call(csa_compressor* c, const uint16_t* x, int B, int N, int start_p
       c->launches += csa::chunk_needs_carry(ck, c->overlap) + 1 + (ck.G > 0);
       return ck.G;
     }
+    CSA_CUDA(csa::invalidate_decode_acc(c, slot_offset, B, s), "invalidate decode running values");
     rc = ensure_scratch(c, (size_t)M * c->pk.cols() * sizeof(float), s);
     if (rc) return rc;
     if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");

@@ -84,9 +84,7 @@ int noalloc_call(csa_compressor* c, const uint16_t* x, int B, int N, int start_p
     }
     base = g_addr[dev];
   }
-  cudaStream_t s = (cudaStream_t)stream;
-  if (csa::invalidate_decode_acc(c, slot_offset, B, s) != cudaSuccess)
-    return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: marking the decode running values failed");
+  cudaStream_t s = (cudaStream_t)stream;  // the kernel marks the sequences' decode running values invalid
   csa_out o = out ? *out : csa_out{nullptr, nullptr, nullptr, nullptr};
   if (csa::launch_prefill_tc(c, x, B, N, slot_offset, ck, o, base, s) != cudaSuccess)
     return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: kernel launch failed");

@@ -76,6 +76,7 @@ struct Params {
   const float* carry;      // [B][1 + overlap][3][H] running softmax values of the candidates
                            // of the first groups that are earlier than the chunk, or null
   int* flag;
+  int* acc_pos;            // [max_batch] decode running values: marked invalid for the call's sequences
   long long state_elems, pooled_elems;  // extents checked by the bounds-checked build
 };
 
@@ -221,21 +222,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       // and written the carried values; a no-op for a launch without that predecessor
       griddep_wait();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      // the prefill rewrites the sequence's state: its decode running values are no longer valid
+      if (ftile == 0 && tt == 0 && et == 0) P.acc_pos[P.slot_offset + b] = -1;
+      if (P.ape && row / P.pk.ft >= P.pk.nk / 2) {
+        // wgate(x) + the positional bias of each token's place in its group (score rows only),
+        // added in registers before staging, the loads independent of one another: column c
+        // holds the token at position ratio * g0 + t0 + c (halo columns wrap harmlessly)
+        const float* ab = P.ape + ftile * kRows + row;
+        const int r = P.ratio;
+        int sl = ((P.ratio * P.g0 + t0 + 128 * h) % r + r) % r;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          if (i < hcols) acc[i] += __ldg(ab + (size_t)sl * P.ncol);
+          sl = sl + 1 == r ? 0 : sl + 1;
+        }
+      }
       float* stg = (float*)smem;  // [128 packed rows][kSmemStride] f32, reuses the stage buffers
 #pragma unroll
       for (int i = 0; i < 128; ++i)
         if (i < hcols) stg[row * kSmemStride + 128 * h + i] = acc[i];
-      if (P.ape && row / P.pk.ft >= P.pk.nk / 2) {
-        // wgate(x) + the positional bias of each token's place in its group (score rows only):
-        // column c holds the token at position ratio * g0 + t0 + c (halo columns wrap harmlessly)
-        const float* ab = P.ape + ftile * kRows + row;
-        const int r = P.ratio;
-        int sl = ((P.ratio * P.g0 + t0 + 128 * h) % r + r) % r;
-        for (int i = 0; i < hcols; ++i) {
-          stg[row * kSmemStride + 128 * h + i] += __ldg(ab + (size_t)sl * P.ncol);
-          sl = sl + 1 == r ? 0 : sl + 1;
-        }
-      }
       epi_sync();
 
       const Packing& pk = P.pk;
@@ -382,6 +387,9 @@ __global__ void __launch_bounds__(128) chunk_carry_kernel(const float* __restric
                                                           int slots, int slot_offset, Chunk ck,
                                                           float* __restrict__ carry, long long carry_elems,
                                                           int* flag) {
+  // started early behind the preceding kernel, which may write the state read here (and the
+  // tokens that the projection launched behind this kernel reads): both wait for it here
+  griddep_wait();
   griddep_launch_dependents();
   const int b = blockIdx.y, f = blockIdx.x * blockDim.x + threadIdx.x;
   const int ncol = pk.cols(), H = pk.H;
@@ -518,15 +526,23 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
   P.carry = nullptr;
   P.ape = c->ape_set ? c->ape : nullptr;
   P.flag = c->dev_flag;
+  P.acc_pos = c->dec_acc_pos;
   P.state_elems = (long long)c->opt.max_batch * c->slots * P.ncol;
   P.pooled_elems = (long long)B * P.ntt * P.GT * c->H;
   P.w = c->w_planes;
   if (chunk_needs_carry(ck, c->overlap)) {
     float* carry = (float*)((uint8_t*)scratch + carry_offset((size_t)B * P.ntt * P.GT * c->H * sizeof(uint16_t)));
-    chunk_carry_kernel<<<dim3((c->H + 127) / 128, B), 128, 0, s>>>(c->state, c->pk, c->overlap, c->slots, slot_offset,
-                                                                  ck, carry, (long long)B * (1 + c->overlap) * 3 * c->H,
-                                                                  c->dev_flag);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchAttribute early[1];
+    early[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    early[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cc = {};
+    cc.gridDim = dim3((c->H + 127) / 128, B);
+    cc.blockDim = dim3(128, 1, 1);
+    cc.stream = s;
+    cc.attrs = early;
+    cc.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cc, chunk_carry_kernel, (const float*)c->state, c->pk, c->overlap, c->slots,
+                                       slot_offset, ck, carry, (long long)B * (1 + c->overlap) * 3 * c->H, c->dev_flag);
     if (e != cudaSuccess) return e;
     P.carry = carry;
   }

@@ -205,3 +205,42 @@ def test_long_context_in_two_chunks_sampled(layer_idx, split):
         ref = o.prefill_groups(x[0], [gfirst + j for j in loc])
         check_entries({k: v[0][loc] for k, v in gn.items()}, ref["prequant"], 1, f"long chunk from group {gfirst}")
     assert g.device_status() == 0
+
+
+@pytest.mark.parametrize("ratio,overlap", [(16, 0), (4, 1)])
+def test_chunk_rewriting_decoded_positions_then_decode(ratio, overlap):
+    """Decode steps, then a chunk that rewrites the last three decoded positions with other tokens,
+    then decode again across the end of the group: the decode must pool the rewritten tokens (the
+    running values it kept before the chunk summarise the old ones and may not be reused)."""
+    layer = synthetic.Layer(256, 128, ratio, overlap, 1.0 / 16, gate_scale=2.0, rope_dim=64, fp4=1)
+    B, p_start = 4, 2 * ratio + 5
+    g, o = make_pair(19, layer, max_batch=B)
+    x, *_ = layer_inputs(19, layer, B, 3 * ratio + 16)
+    y, *_ = layer_inputs(29, layer, B, 3 * ratio + 16)  # the rewriting tokens
+    xp = np.ascontiguousarray(x[:, :p_start])
+    o.prefill(xp)
+    g.prefill(dev_bits(xp), prequant=False)
+
+    def decode(p, src):
+        sp = np.full(B, p, np.int32)
+        xt = np.ascontiguousarray(src[:, p])
+        r = o.decode(xt, sp)
+        d = g.decode(dev_bits(xt), torch.from_numpy(sp).to(DEV))
+        em = d["emitted"].cpu().numpy()
+        assert np.array_equal(em, r["emitted"]), p
+        if em.any():
+            check_entries(to_np(d, rows=np.flatnonzero(em)), r["prequant"][np.flatnonzero(em)], 1, f"decode at {p}")
+        return int(em.sum())
+
+    for p in range(p_start, p_start + 6):
+        decode(p, x)
+    p1 = p_start + 6
+    yc = np.ascontiguousarray(y[:, p1 - 3:p1])
+    ref = o.prefill(yc, start_pos=p1 - 3)
+    got = g.prefill(dev_bits(yc), start_pos=p1 - 3)
+    if ref["G"]:
+        check_entries(to_np(got), ref["prequant"], 1, "rewriting chunk")
+    emitted = sum(decode(p, x) for p in range(p1, p1 + ratio))
+    assert emitted >= B  # the group completes within the steps
+    check_state(g, o, "state after the chunk and the decode steps")
+    assert g.device_status() == 0
