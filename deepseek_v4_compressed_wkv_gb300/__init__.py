@@ -248,6 +248,21 @@ class Compressor:
                "prequant": (B, g, H)}
         return {k: (None if v is None else v[:B * g].view(*shp[k])) for k, v in out.items()}
 
+    def prefill_noalloc(self, x, out, slot_offset: int = 0, start_pos: int = 0, stream=None):
+        """The same prefill through the entry point that allocates no device memory (its scratch
+        is a fixed array in the library; tensor-core shapes up to that array's size).  `out` is
+        required (the caller owns every buffer); returns the entries per sequence."""
+        B, N, D = x.shape
+        if D != self.dim or x.dtype != torch.bfloat16:
+            raise CSAError("x must be bf16 [B, N, dim]")
+        _on_current_device(x)
+        G = (start_pos + N) // self.ratio - start_pos // self.ratio
+        self._check_out(out, B * G)
+        o = self._out_struct(out)
+        return _check(self._lib.csa_compress_prefill_noalloc(self._h, _dptr(_u16(x)), B, N, start_pos, slot_offset,
+                                                             ctypes.byref(o), _stream(stream)),
+                      "csa_compress_prefill_noalloc")
+
     def prefill_into(self, x, cache, start_pos: int = 0, slot_offset: int = 0, stream=None) -> int:
         """Prefill (or a chunk at start_pos) writing entry g of sequence b into row g of
         cache["latent"][b] ([B, rows, H] bf16; optional "codes" [B, rows, H/2], "scales"
