@@ -12,7 +12,7 @@
 //  * decode_proj_kernel, grid (packed tile, K slice, 128-token block): accumulates the slice in
 //    K chunks of 128 (TMEM, promoted to f32 registers as in the prefill kernel) and writes its
 //    partial sums.  Roles (320 threads): warp 0 issues the loads (one bulk copy of the three
-//    pre-swizzled plane tiles and one TMA token tile of K = 32 per stage, 4 stages), warp 1 owns
+//    pre-swizzled plane tiles and one TMA token tile of K = 32 per stage, 6 stages), warp 1 owns
 //    TMEM and issues tcgen05.mma, warps 2-9 drain the chunk accumulators, the cluster of 4 K
 //    slices adds its sums through distributed shared memory and stores them with TMA.  The
 //    weights are not written by any kernel that can precede a decode launch in early-start
@@ -48,14 +48,14 @@ constexpr int kRows = 128;                              // packed rows per tile 
 constexpr int kTok = 128;                               // tokens per CTA (MMA N)
 constexpr int kKb = 64;                                 // K granularity of the slice split
 constexpr int kKs = 32;                                 // K per stage (one 64-byte swizzle row of bf16)
-constexpr int kStages = 4;
-constexpr int kPrefetchStages = 4;                     // weight stages fetched into L2 beyond the ring
+constexpr int kStages = 6;
+constexpr int kPrefetchStages = 2;                     // weight stages fetched into L2 beyond the ring
 constexpr int kChunkSteps = 4;                          // stages per accumulator chunk (K = 128)
 constexpr int kPlaneBytes = kRows * kKs * 2;            // 8 KB
 static_assert(kRows == kPlaneTileRows && kKs == kPlaneTileK, "a stage is one tile of the plane layout");
 constexpr int kXBytes = kTok * kKs * 2;                 // 8 KB
 constexpr int kStageBytes = 3 * kPlaneBytes + kXBytes;  // 32 KB
-constexpr int kRingBytes = kStages * kStageBytes;       // 128 KB
+constexpr int kRingBytes = kStages * kStageBytes;       // 192 KB
 constexpr int kPartBytes = kTok * kRows * 4;            // one CTA's partial sums, staged in the ring
 static_assert(kPartBytes <= kRingBytes, "the partial tile is staged in the free ring");
 constexpr int kEpiThreads = 256;
