@@ -80,28 +80,31 @@ def max_over_ranks(v, world, device):
     return float(t.item())
 
 
-def profiled_traffic(summary, key):
-    """DRAM bytes (read + write) that an ncu capture measured for a kernel, from its summary under
-    profiles/, or None when the kernel's sources no longer hash as they did at the capture."""
+def sources_hash(files):
+    """First 16 hex digits of the sha256 of the library sources `files`, concatenated in order."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", summary)
-    if not os.path.exists(path):
-        return None
-    fields = {}
-    with open(path) as f:
-        for line in f:
-            k, _, v = line.strip().partition(": ")
-            if v:
-                fields[k] = v.strip()
-    srcs = {"prefill_tc_flash_csa.md": "prefill_tc.cu", "decode_tc_batched.md": "decode_tc.cu"}[summary]
     csrc = os.path.join(ROOT, "deepseek_v4_compressed_wkv_gb300", "csrc")
     m = hashlib.sha256()
-    for fn in (srcs, "tc_common.cuh", "csa_internal.cuh", "kernels.h"):
+    for fn in files:
         with open(os.path.join(csrc, fn), "rb") as f:
             m.update(f.read())
-    if m.hexdigest()[:16] != fields.get("sources_sha256_16") or key not in fields:
+    return m.hexdigest()[:16]
+
+
+def profiled_traffic(entry, key):
+    """DRAM bytes (read + write) that an ncu capture measured for a kernel, from
+    profiles/traffic.json, or None when the kernel's sources no longer hash as they did at the
+    capture (the counters then describe another kernel)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
         return None
-    return int(fields[key])
+    with open(path) as f:
+        rec = json.load(f).get(entry)
+    if not rec or key not in rec:
+        return None
+    if sources_hash(rec["sources"]) != rec.get("sources_sha256_16"):
+        return None
+    return int(rec[key])
 
 
 def load_peaks():
@@ -275,7 +278,7 @@ def run_ours(args, rank, world, local):
     if tc:
         peak = peaks["bf16_tflops"] / 3.0
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": profiled_traffic("prefill_tc_flash_csa.md", "traffic_bytes_per_launch"),
+                "traffic": profiled_traffic("prefill_tc_flash_csa", "traffic_bytes_per_launch"),
                 "kernel": "csa_prefill_tc (projection + fused pool/norm/RoPE/fp4)",
                 "peak_basis": f"{peaks['source']} bf16 dense {peaks['bf16_tflops']} TFLOP/s / 3 bf16 passes"}
     else:
@@ -562,7 +565,7 @@ def bench_decode(args, torch, csa, synthetic, device, peaks, world, rank):
             "launch": "cuda graph" if graph is not None else "eager",
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"],
-                         "traffic": profiled_traffic("decode_tc_batched.md", "traffic_bytes_per_step"),
+                         "traffic": profiled_traffic("decode_tc_batched", "traffic_bytes_per_step"),
                          "algorithmic_bytes_per_step": alg}}
 
 

@@ -9,7 +9,8 @@ is present, calls fail with an error.
     c = Compressor(dim=4096, head_dim=512, ratio=4, overlap=1)
     c.set_weights(wkv, wgate, gain)          # f32 CUDA tensors [C, dim], [C, dim], [H]
     out = c.prefill(x)                       # x bf16 CUDA [B, N, dim] -> dict of tensors or None
-    step = c.decode(x_tok, start_pos)        # x_tok bf16 [B, dim], start_pos int32 CUDA [B]
+    step = c.decode(x_tok, start_pos)        # x_tok bf16 [B, dim]; start_pos int32 [B] on the host
+                                             # (returns the emitting count) or on the device
 """
 from __future__ import annotations
 
@@ -29,8 +30,9 @@ _lock = threading.Lock()
 _lib = None
 
 # every entry point declared in include/csa.h
-ABI_FUNCTIONS = ("csa_options_default", "csa_compressor_create", "csa_compressor_set_weights",
-                 "csa_compress_prefill", "csa_compress_decode", "csa_state_reset", "csa_state_elems",
+ABI_FUNCTIONS = ("csa_options_default", "csa_compressor_create", "csa_compressor_create_ex",
+                 "csa_compressor_set_weights", "csa_compress_prefill", "csa_compress_decode",
+                 "csa_compress_decode_dev", "csa_state_reset", "csa_state_elems",
                  "csa_state_export", "csa_device_status", "csa_compressor_destroy", "csa_last_error",
                  "csa_fp4_e4m3_roundtrip", "csa_rope_table", "csa_set_profile_events", "csa_kernel_launches",
                  "csa_uses_tensor_cores", "csa_compress_prefill_noalloc", "csa_compress_prefill_into",
@@ -77,10 +79,12 @@ def load_library(build_if_missing: bool = True):
         P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
         sig = {
             "csa_options_default": ([P], None),
-            "csa_compressor_create": ([I, I, I, I, P, P], I),
+            "csa_compressor_create": ([I, I, I, I, P], I),
+            "csa_compressor_create_ex": ([I, I, I, I, P, P], I),
             "csa_compressor_set_weights": ([P, P, P, P, P], I),
             "csa_compress_prefill": ([P, P, I, I, I, I, P, P], I),
             "csa_compress_decode": ([P, P, I, P, P, P, P], I),
+            "csa_compress_decode_dev": ([P, P, I, P, P, P, P], I),
             "csa_state_reset": ([P, I, I, P], I),
             "csa_state_elems": ([P], I64),
             "csa_state_export": ([P, P, P, P], I),
@@ -159,8 +163,8 @@ class Compressor:
         self.dim, self.head_dim, self.ratio, self.overlap = dim, head_dim, ratio, overlap
         self.options = default_options(**options)
         h = ctypes.c_void_p()
-        _check(self._lib.csa_compressor_create(dim, head_dim, ratio, overlap, ctypes.byref(self.options),
-                                               ctypes.byref(h)), "csa_compressor_create")
+        _check(self._lib.csa_compressor_create_ex(dim, head_dim, ratio, overlap, ctypes.byref(self.options),
+                                                  ctypes.byref(h)), "csa_compressor_create_ex")
         self._h = h
 
     def close(self):
@@ -281,28 +285,56 @@ class Compressor:
                       "csa_compress_prefill_into")
 
     def decode(self, x_tok, start_pos, out=None, emitted=None, prequant: bool = True, stream=None):
-        """x_tok bf16 [B, dim], start_pos int32 CUDA [B].  Returns a dict with emitted u8 [B]
-        and latent/codes/scales/prequant [B, ...] (rows valid where emitted)."""
+        """One decode step: x_tok bf16 CUDA [B, dim]; start_pos int32 [B], either on the host (a
+        numpy array, a list or a CPU tensor: csa_compress_decode, which returns the number of
+        emitting sequences) or a CUDA tensor (csa_compress_decode_dev, for positions that live on
+        the device and for graph capture).  Returns a dict with latent/codes/scales/prequant
+        [B, ...] (rows valid where emitted), emitted u8 [B] (a CPU tensor for host positions
+        unless a device `emitted` is given, else on the device) and, for host positions, count."""
         B, D = x_tok.shape
-        if D != self.dim or x_tok.dtype != torch.bfloat16 or start_pos.dtype != torch.int32:
-            raise CSAError("x_tok must be bf16 [B, dim] and start_pos int32 [B]")
-        if start_pos.numel() != B:
-            raise CSAError(f"start_pos has {start_pos.numel()} elements for {B} sequences")
-        _on_current_device(x_tok, start_pos)
+        if D != self.dim or x_tok.dtype != torch.bfloat16:
+            raise CSAError("x_tok must be bf16 [B, dim]")
+        on_device = isinstance(start_pos, torch.Tensor) and start_pos.is_cuda
+        if on_device:
+            if start_pos.dtype != torch.int32 or start_pos.numel() != B:
+                raise CSAError(f"start_pos must be int32 with {B} elements")
+            _on_current_device(x_tok, start_pos)
+        else:
+            import numpy as np
+            sp = np.ascontiguousarray(start_pos.numpy() if isinstance(start_pos, torch.Tensor) else start_pos,
+                                      dtype=np.int32).reshape(-1)
+            if sp.size != B:
+                raise CSAError(f"start_pos has {sp.size} elements for {B} sequences")
+            _on_current_device(x_tok)
         if out is None:
             out = self._alloc_out(B, x_tok.device, prequant)
         else:
             self._check_out(out, B)
-        if emitted is None:
-            emitted = torch.empty(B, dtype=torch.uint8, device=x_tok.device)
-        elif emitted.dtype != torch.uint8 or emitted.numel() < B:
-            raise CSAError("emitted must be uint8 with at least B elements")
-        _on_current_device(emitted)
         o = self._out_struct(out)
-        _check(self._lib.csa_compress_decode(self._h, _dptr(_u16(x_tok)), B, _dptr(start_pos), _dptr(emitted),
-                                             ctypes.byref(o), _stream(stream)), "csa_compress_decode")
+        if on_device:
+            if emitted is None:
+                emitted = torch.empty(B, dtype=torch.uint8, device=x_tok.device)
+            elif emitted.dtype != torch.uint8 or emitted.numel() < B or not emitted.is_cuda:
+                raise CSAError("emitted must be a uint8 CUDA tensor with at least B elements")
+            _on_current_device(emitted)
+            _check(self._lib.csa_compress_decode_dev(self._h, _dptr(_u16(x_tok)), B, _dptr(start_pos),
+                                                     ctypes.byref(o), _dptr(emitted), _stream(stream)),
+                   "csa_compress_decode_dev")
+            d = dict(out)
+            d["emitted"] = emitted
+            return d
+        if emitted is None:
+            emitted = torch.empty(B, dtype=torch.uint8)
+        elif emitted.dtype != torch.uint8 or emitted.numel() < B or not emitted.is_contiguous():
+            raise CSAError("emitted must be a contiguous uint8 tensor with at least B elements")
+        if emitted.is_cuda:
+            _on_current_device(emitted)
+        n = _check(self._lib.csa_compress_decode(self._h, _dptr(_u16(x_tok)), B, ctypes.c_void_p(sp.ctypes.data),
+                                                 ctypes.byref(o), ctypes.c_void_p(emitted.data_ptr()),
+                                                 _stream(stream)), "csa_compress_decode")
         d = dict(out)
         d["emitted"] = emitted
+        d["count"] = n
         return d
 
     def state_reset(self, slot_begin: int = 0, slot_count: int | None = None, stream=None):

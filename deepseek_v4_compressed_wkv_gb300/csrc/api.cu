@@ -109,6 +109,7 @@ void free_all(csa_compressor* c) {
   cudaFree(c->dec_part);
   cudaFree(c->dec_acc);
   cudaFree(c->dec_acc_pos);
+  cudaFree(c->dec_pos);
 }
 
 int ensure_scratch(csa_compressor* c, size_t bytes, cudaStream_t s) {
@@ -126,12 +127,24 @@ int ensure_scratch(csa_compressor* c, size_t bytes, cudaStream_t s) {
   return CSA_OK;
 }
 
+// Every call on a handle launches on the current device with pointers into the handle's device
+// memory: a call made while another device is current would use them on the wrong GPU.
+int check_device(const csa_compressor* c, const char* what) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != c->device)
+    return fail(CSA_ERR_ARG, "%s: the handle lives on device %d but device %d is current", what, c->device, dev);
+  return CSA_OK;
+}
+
 // Checks shared by the prefill entry points; on success fills the call geometry.  cache_rows < 0:
 // entries go to out [B][G][..]; else to rows start_pos / ratio .. of a cache [B][cache_rows][..].
 int check_prefill(const csa_compressor* c, const uint16_t* x, int B, int N, int start_pos, int slot_offset,
                   const csa_out* out, int cache_rows, const char* what, csa::Chunk* ck) {
   if (!c) return fail(CSA_ERR_ARG, "%s: handle is NULL", what);
   if (!c->weights_set) return fail(CSA_ERR_STATE, "%s: weights not set", what);
+  if (int rc = check_device(c, what)) return rc;
   if (B < 1 || N < 1) return fail(CSA_ERR_ARG, "%s: B (%d) and N (%d) must be >= 1", what, B, N);
   if (start_pos < 0 || (long long)start_pos + N > 0x7fffffffLL)
     return fail(CSA_ERR_ARG, "%s: start_pos %d must be >= 0 and start_pos + N must fit in int32", what, start_pos);
@@ -167,10 +180,12 @@ int prefill_call(csa_compressor* c, const uint16_t* x, int B, int N, int start_p
     const long long M = (long long)B * N;
     const csa_out o = out ? *out : csa_out{nullptr, nullptr, nullptr, nullptr};
     if (csa::prefill_tc_supported(c, x)) {  // the kernel marks the decode running values invalid
-      rc = ensure_scratch(c, csa::prefill_tc_scratch_bytes(c, B, N, ck), s);
+      const csa::PrefillPlan plan = csa::prefill_tc_plan(c, B, N, ck);
+      rc = ensure_scratch(c, plan.bytes, s);
       if (rc) return rc;
       if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
-      CSA_CUDA(csa::launch_prefill_tc(c, x, B, N, slot_offset, ck, o, c->scratch, s), "tensor-core prefill launch");
+      CSA_CUDA(csa::launch_prefill_tc(c, x, B, N, slot_offset, ck, plan, o, c->scratch, c->scratch_bytes, s),
+               "tensor-core prefill launch");
       if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
       // the carry kernel (a chunk), the projection kernel, the entry kernel
       c->launches += csa::chunk_needs_carry(ck, c->overlap) + 1 + (ck.G > 0);
@@ -193,6 +208,50 @@ int prefill_call(csa_compressor* c, const uint16_t* x, int B, int N, int start_p
   } catch (...) {
     return fail(CSA_ERR_INTERNAL, "%s: unexpected exception", what);
   }
+}
+
+int check_decode(const csa_compressor* c, const uint16_t* x_tok, int B, const csa_out* out, const char* what) {
+  if (!c) return fail(CSA_ERR_ARG, "%s: handle is NULL", what);
+  if (!c->weights_set) return fail(CSA_ERR_STATE, "%s: weights not set", what);
+  if (int rc = check_device(c, what)) return rc;
+  if (B < 1 || B > c->opt.max_batch)
+    return fail(CSA_ERR_ARG, "%s: B %d must be in [1, max_batch=%d]", what, B, c->opt.max_batch);
+  if (!x_tok || !out || !out->latent) return fail(CSA_ERR_ARG, "%s: x_tok and out->latent are required", what);
+  return CSA_OK;
+}
+
+// The decode kernels of one step, positions and emission flags in device memory (emitted may be
+// null: the host form fills its own).
+int decode_call(csa_compressor* c, const uint16_t* x_tok, int B, const int32_t* start_pos, const csa_out& out,
+                uint8_t* emitted, cudaStream_t s) {
+  if (csa::decode_tc_supported(c, x_tok, B)) {
+    // split-K partial sums: [slices][B][2C] f32, grown on first use (a later call of the same
+    // or smaller B allocates nothing)
+    const int ks = csa::decode_tc_slices(c);
+    const size_t bytes = (size_t)ks * B * c->pk.cols() * sizeof(float);
+    if (c->dec_part_bytes < bytes) {
+      CSA_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+      cudaFree(c->dec_part);
+      c->dec_part = nullptr;
+      c->dec_part_bytes = 0;
+      CSA_CUDA(cudaMalloc(&c->dec_part, bytes), "cudaMalloc(decode partial sums)");
+      c->dec_part_bytes = bytes;
+    }
+    if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
+    CSA_CUDA(csa::launch_decode_tc(c, x_tok, B, start_pos, c->dec_part, ks, out, emitted, c->dec_early_start, s),
+             "tensor-core decode launch");
+    if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
+    c->dec_early_start = true;
+    c->launches += 2;
+    return CSA_OK;
+  }
+  CSA_CUDA(csa::invalidate_decode_acc(c, 0, B, s), "invalidate decode running values");
+  if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
+  CSA_CUDA(csa::launch_projection_ffma(c, x_tok, B, c->state, 1, start_pos, 0, 0, s), "decode projection launch");
+  if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
+  CSA_CUDA(csa::launch_decode_emit(c, start_pos, B, out, emitted, s), "decode emit launch");
+  c->launches += 2;
+  return CSA_OK;
 }
 
 }  // namespace
@@ -236,7 +295,11 @@ int csa_rope_table(const csa_options* opt, int pos0, int npos, float* cos_out, f
   return CSA_OK;
 }
 
-int csa_compressor_create(int dim, int H, int ratio, int overlap, const csa_options* opt, csa_compressor** out) {
+int csa_compressor_create(int dim, int H, int ratio, int overlap, csa_compressor** out) {
+  return csa_compressor_create_ex(dim, H, ratio, overlap, nullptr, out);
+}
+
+int csa_compressor_create_ex(int dim, int H, int ratio, int overlap, const csa_options* opt, csa_compressor** out) {
   try {
     if (!out) return fail(CSA_ERR_ARG, "csa_compressor_create: out is NULL");
     *out = nullptr;
@@ -264,7 +327,10 @@ int csa_compressor_create(int dim, int H, int ratio, int overlap, const csa_opti
     c->pk = pk;
     c->slots = overlap ? 8 : ratio;
     c->weights_set = false;
-    cudaGetDevice(&c->device);
+    if (cudaError_t ed = cudaGetDevice(&c->device); ed != cudaSuccess) {
+      delete c;
+      return cuda_fail(ed, "cudaGetDevice");
+    }
     const size_t ncol = pk.cols();
     cudaError_t e = cudaSuccess;
     auto alloc = [&](void** p, size_t bytes) {
@@ -277,6 +343,7 @@ int csa_compressor_create(int dim, int H, int ratio, int overlap, const csa_opti
     alloc((void**)&c->dev_flag, sizeof(int));
     alloc((void**)&c->dec_acc, (size_t)o.max_batch * 3 * H * sizeof(float));
     alloc((void**)&c->dec_acc_pos, (size_t)o.max_batch * sizeof(int));
+    alloc((void**)&c->dec_pos, (size_t)o.max_batch * sizeof(int32_t));
     if (o.rope_dim > 0) {
       const size_t n = (size_t)o.max_pos * (o.rope_dim / 2);
       alloc((void**)&c->rope_cos, n * sizeof(float));
@@ -312,6 +379,7 @@ int csa_compressor_set_weights(csa_compressor* c, const float* wkv, const float*
   if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
   if (!wkv || !gain) return fail(CSA_ERR_ARG, "wkv and norm_gain are required");
   if (!wgate && c->ratio > 1) return fail(CSA_ERR_ARG, "wgate is required at ratio > 1");
+  if (int rc = check_device(c, "csa_compressor_set_weights")) return rc;
   cudaStream_t s = (cudaStream_t)stream;
   CSA_CUDA(csa::launch_pack_weights(c, wkv, wgate, s), "pack_weights launch");
   c->launches += 1;
@@ -323,6 +391,7 @@ int csa_compressor_set_weights(csa_compressor* c, const float* wkv, const float*
 
 int csa_compressor_set_gate_bias(csa_compressor* c, const float* ape, csa_stream_t stream) {
   if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
+  if (int rc = check_device(c, "csa_compressor_set_gate_bias")) return rc;
   if (!ape) {
     c->ape_set = false;
     return CSA_OK;
@@ -346,48 +415,65 @@ int csa_compress_prefill_into(csa_compressor* c, const uint16_t* x, int B, int N
   return prefill_call(c, x, B, N, start_pos, slot_offset, cache, cache_rows, stream, "csa_compress_prefill_into");
 }
 
-int csa_compress_decode(csa_compressor* c, const uint16_t* x_tok, int B, const int32_t* start_pos, uint8_t* emitted,
-                        const csa_out* out, csa_stream_t stream) {
+int csa_compress_decode(csa_compressor* c, const uint16_t* x_tok, int B, const int32_t* start_pos,
+                        const csa_out* out, uint8_t* emitted, csa_stream_t stream) {
   NvtxRange range("csa_compress_decode");
-  if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
-  if (!c->weights_set) return fail(CSA_ERR_STATE, "weights not set");
-  if (B < 1 || B > c->opt.max_batch) return fail(CSA_ERR_ARG, "B %d must be in [1, max_batch=%d]", B, c->opt.max_batch);
-  if (!x_tok || !start_pos || !emitted || !out || !out->latent)
-    return fail(CSA_ERR_ARG, "x_tok, start_pos, emitted and out->latent are required");
-  cudaStream_t s = (cudaStream_t)stream;
-  if (csa::decode_tc_supported(c, x_tok, B)) {
-    // split-K partial sums: [slices][B][2C] f32, grown on first use (a later call of the same
-    // or smaller B allocates nothing)
-    const int ks = csa::decode_tc_slices(c);
-    const size_t bytes = (size_t)ks * B * c->pk.cols() * sizeof(float);
-    if (c->dec_part_bytes < bytes) {
-      CSA_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
-      cudaFree(c->dec_part);
-      c->dec_part = nullptr;
-      c->dec_part_bytes = 0;
-      CSA_CUDA(cudaMalloc(&c->dec_part, bytes), "cudaMalloc(decode partial sums)");
-      c->dec_part_bytes = bytes;
+  try {
+    if (int rc = check_decode(c, x_tok, B, out, "csa_compress_decode")) return rc;
+    if (!start_pos) return fail(CSA_ERR_ARG, "csa_compress_decode: start_pos (host) is required");
+    // the positions are on the host: validate them here, count the emitting sequences ("None"
+    // for the others) and fill a host emitted array; a device emitted array is left to the kernels
+    int count = 0;
+    const int r = c->ratio;
+    for (int b = 0; b < B; ++b) {
+      const long long p = start_pos[b];
+      if (p < 0) return fail(CSA_ERR_ARG, "csa_compress_decode: start_pos[%d] = %lld is negative", b, p);
+      if ((p + 1) % r == 0) {
+        if (c->opt.rope_dim > 0 && p + 1 - r >= c->opt.max_pos)
+          return fail(CSA_ERR_ARG, "csa_compress_decode: entry position %lld of sequence %d exceeds the RoPE table (max_pos %d)",
+                      p + 1 - r, b, c->opt.max_pos);
+        ++count;
+      }
     }
-    if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
-    CSA_CUDA(csa::launch_decode_tc(c, x_tok, B, start_pos, c->dec_part, ks, *out, emitted, c->dec_early_start, s),
-             "tensor-core decode launch");
-    if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
-    c->dec_early_start = true;
-    c->launches += 2;
-    return CSA_OK;
+    uint8_t* emitted_dev = nullptr;
+    if (emitted) {
+      cudaPointerAttributes pa;
+      if (cudaPointerGetAttributes(&pa, emitted) == cudaSuccess &&
+          (pa.type == cudaMemoryTypeDevice || pa.type == cudaMemoryTypeManaged)) {
+        emitted_dev = emitted;
+      } else {
+        cudaGetLastError();  // an unregistered host pointer may leave an error behind on old drivers
+        for (int b = 0; b < B; ++b) emitted[b] = (start_pos[b] + 1) % r == 0 ? 1 : 0;
+      }
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    // a copy from ordinary host memory is staged before cudaMemcpyAsync returns: the caller may
+    // reuse start_pos at once, and this call's copy is ordered before its kernels
+    CSA_CUDA(cudaMemcpyAsync(c->dec_pos, start_pos, (size_t)B * sizeof(int32_t), cudaMemcpyHostToDevice, s),
+             "copy start_pos to the device");
+    int rc = decode_call(c, x_tok, B, c->dec_pos, *out, emitted_dev, s);
+    return rc ? rc : count;
+  } catch (...) {
+    return fail(CSA_ERR_INTERNAL, "csa_compress_decode: unexpected exception");
   }
-  CSA_CUDA(csa::invalidate_decode_acc(c, 0, B, s), "invalidate decode running values");
-  if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
-  CSA_CUDA(csa::launch_projection_ffma(c, x_tok, B, c->state, 1, start_pos, 0, 0, s), "decode projection launch");
-  if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
-  CSA_CUDA(csa::launch_decode_emit(c, start_pos, B, *out, emitted, s), "decode emit launch");
-  c->launches += 2;
-  return CSA_OK;
+}
+
+int csa_compress_decode_dev(csa_compressor* c, const uint16_t* x_tok, int B, const int32_t* start_pos,
+                            const csa_out* out, uint8_t* emitted, csa_stream_t stream) {
+  NvtxRange range("csa_compress_decode_dev");
+  try {
+    if (int rc = check_decode(c, x_tok, B, out, "csa_compress_decode_dev")) return rc;
+    if (!start_pos || !emitted) return fail(CSA_ERR_ARG, "csa_compress_decode_dev: start_pos and emitted are required");
+    return decode_call(c, x_tok, B, start_pos, *out, emitted, (cudaStream_t)stream);
+  } catch (...) {
+    return fail(CSA_ERR_INTERNAL, "csa_compress_decode_dev: unexpected exception");
+  }
 }
 
 int csa_state_reset(csa_compressor* c, int slot_begin, int slot_count, csa_stream_t stream) {
   NvtxRange range("csa_state_reset");
   if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
+  if (int rc = check_device(c, "csa_state_reset")) return rc;
   if (slot_begin < 0 || slot_count < 0 || (long long)slot_begin + slot_count > c->opt.max_batch)
     return fail(CSA_ERR_ARG, "slots [%d, %d) outside [0, %d)", slot_begin, slot_begin + slot_count, c->opt.max_batch);
   CSA_CUDA(csa::invalidate_decode_acc(c, slot_begin, slot_count, (cudaStream_t)stream),
@@ -405,6 +491,7 @@ int64_t csa_state_elems(const csa_compressor* c) {
 int csa_state_export(const csa_compressor* c, float* kv, float* score, csa_stream_t stream) {
   if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
   if (!kv || !score) return fail(CSA_ERR_ARG, "kv and score are required");
+  if (int rc = check_device(c, "csa_state_export")) return rc;
   CSA_CUDA(csa::launch_state_export(c, kv, score, (cudaStream_t)stream), "state export launch");
   const_cast<csa_compressor*>(c)->launches += 1;
   return CSA_OK;
@@ -431,13 +518,14 @@ int64_t csa_kernel_launches(const csa_compressor* c) {
 
 int csa_device_status(csa_compressor* c, csa_stream_t stream) {
   if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
+  if (int rc = check_device(c, "csa_device_status")) return rc;
   cudaStream_t s = (cudaStream_t)stream;
   int flag = 0;
   CSA_CUDA(cudaMemcpyAsync(&flag, c->dev_flag, sizeof(int), cudaMemcpyDeviceToHost, s), "read device flag");
   CSA_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
   if (!flag) return CSA_OK;
   CSA_CUDA(cudaMemsetAsync(c->dev_flag, 0, sizeof(int), s), "clear device flag");
-  return fail(CSA_ERR_DEVICE, "device flag 0x%x:%s%s%s%s", flag, (flag & 1) ? " negative start_pos;" : "",
+  return fail((flag & 4) ? CSA_ERR_TIMEOUT : CSA_ERR_DEVICE, "device flag 0x%x:%s%s%s%s", flag, (flag & 1) ? " negative start_pos;" : "",
               (flag & 2) ? " entry position beyond the RoPE table;" : "", (flag & 4) ? " wait budget exhausted;" : "",
               (flag & 8) ? " index out of bounds (bounds-checked build);" : "");
 }

@@ -89,8 +89,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kStages;
   uint64_t* c_full = empty + kStages;
   uint64_t* c_empty = c_full + 2;
-  uint32_t* tmem_slot = (uint32_t*)(c_empty + 2);
+  uint64_t* mma_done = c_empty + 2;  // clean-up after an abort: the issued MMAs have completed
+  uint32_t* tmem_slot = (uint32_t*)(mma_done + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  int* issued_s = (int*)(tmem_slot + 2);  // stages the producer issued (read by the clean-up)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x, ks = blockIdx.y, tb = blockIdx.z * kTok;
@@ -109,6 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&c_full[i], 1);
       mbar_init(&c_empty[i], kEpiThreads / 32);
     }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_map(&map_x);
@@ -119,6 +122,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  float acc[kTok / 2];  // epilogue warps: this thread's row over half of the token columns
+#pragma unroll
+  for (int i = 0; i < kTok / 2; ++i) acc[i] = 0.0f;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -150,13 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(st + 3 * kPlaneBytes, &map_x, k0 + t * kKs, tb, &full[s]);
         ++issued;
       }
-      if (*abort_flag) {  // let the copies already in flight land before the ring is reused or left
-        for (int t = max(0, issued - kStages); t < issued; ++t) {
-          const uint64_t t1 = globaltimer();
-          while (!mbar_try_wait(&full[t % kStages], (t / kStages) & 1) && globaltimer() - t1 < kWaitNs) {
-          }
-        }
-      }
+      *issued_s = issued;
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -187,12 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // drain each chunk into f32 registers, in chunk order; then store the partial sums
+    // drain each chunk into f32 registers, in chunk order (staged for the reduction below)
     const int q = warp & 3, h = (warp - 2) >> 2;
-    const int row = 32 * q + lane;
-    float acc[kTok / 2];
-#pragma unroll
-    for (int i = 0; i < kTok / 2; ++i) acc[i] = 0.0f;
     bool ok = true;
     for (int c = 0; c < nch; ++c) {
       const int buf = c & 1;
@@ -213,20 +209,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&c_empty[buf]);
     }
-    if (!ok && threadIdx.x == 64) atomicOr(P.flag, 4);
-    // every MMA has completed and every load has landed: the ring is free.  Stage the partial
-    // sums as [token][packed row]
-    float* stg = reinterpret_cast<float*>(smem);
-#pragma unroll
-    for (int i = 0; i < kTok / 2; ++i) stg[((kTok / 2) * h + i) * kRows + row] = acc[i];
+    (void)ok;  // a failed wait has raised the abort flag
   }
 
   tc_fence_before();
-  __syncthreads();
-  if (*abort_flag && threadIdx.x == 0) atomicOr(P.flag, 4);
+  __syncthreads();  // every role has left its loop; the flag no longer changes
+  if (*abort_flag) {
+    // a wait ran out: the copies in flight land and the issued MMAs complete before the TMEM is
+    // freed and the ring is reused (this call's results are undefined; the flag says so)
+    drain_after_abort(warp == 0 && lane == 0, warp == 1 && lane == 0, full, kStages, *issued_s, mma_done);
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0) atomicOr(P.flag, 4);
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  if (warp >= 2) {
+    // every MMA has completed and every load has landed: the ring is free.  Stage the partial
+    // sums as [token][packed row]
+    const int h = (warp - 2) >> 2, row = 32 * (warp & 3) + lane;
+    float* stg = reinterpret_cast<float*>(smem);
+#pragma unroll
+    for (int i = 0; i < kTok / 2; ++i) stg[((kTok / 2) * h + i) * kRows + row] = acc[i];
   }
   // The cs K slices of the cluster are added on chip: CTA r adds tokens [r * 128 / cs, ...) of
   // the cs staged tiles in slice order (distributed shared memory) and stores that part of the
@@ -290,7 +296,7 @@ struct FinParams {
   Packing pk;
   EpiParams ep;
   csa_out out;               // rows indexed by sequence
-  uint8_t* emitted;          // [B]
+  uint8_t* emitted;          // [B], or null (the caller learns the emissions on the host)
   float* acc;                // non-overlapped: [max_batch][3][H] running max, denominator and
                              // numerator of the open group over its tokens so far
   int* acc_pos;              // [max_batch] position of the last token in acc (-1: not valid)
@@ -590,7 +596,7 @@ __global__ void __launch_bounds__(kFinThreads, 5) decode_finish_kernel(const Fin
       if (in_bounds((long long)((st - P.state) + (size_t)4 * ncol + i), P.state_elems, P.flag))
         st[(size_t)4 * ncol + i] = padded_kind_value(pk, i % ncol);
   if (tid == 0) {
-    P.emitted[b] = pool ? 1 : 0;
+    if (P.emitted) P.emitted[b] = pool ? 1 : 0;
     if (p < 0) atomicOr(P.flag, 1);
     if (emit && !pool) atomicOr(P.flag, 2);
     if (!P.overlap) P.acc_pos[b] = p >= 0 ? p : -1;

@@ -27,9 +27,20 @@ cudaError_t launch_fp4_e8m0_roundtrip(const uint16_t* in, long long nb, uint8_t*
 
 // Tensor-core prefill (prefill_tc.cu): projection + pool + norm + RoPE + fp4 + state update.
 bool prefill_tc_supported(const csa_compressor* c, const void* x);
-size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N, const Chunk& ck);
+// The launch geometry of one call, fixed once so that the scratch it is given and the launch
+// agree: the token tile and the scratch bytes it needs (the pooled values [B][token tiles]
+// [groups per tile][H] bf16 and, for a chunk whose first group has earlier candidates, their
+// running softmax values [B][1 + overlap][3][H] f32 after them).
+struct PrefillPlan {
+  int tok;       // token tile: 256, 224 or 128
+  size_t bytes;  // scratch bytes
+};
+PrefillPlan prefill_tc_plan(const csa_compressor* c, int B, int N, const Chunk& ck);
+// scratch_bytes: the capacity of `scratch` (>= plan.bytes), the extent the bounds-checked build
+// checks the kernels' scratch stores against.
 cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset,
-                              const Chunk& ck, const csa_out& out, void* scratch, cudaStream_t s);
+                              const Chunk& ck, const PrefillPlan& plan, const csa_out& out, void* scratch,
+                              size_t scratch_bytes, cudaStream_t s);
 
 // Tensor-core decode (decode_tc.cu): two launches, the projection of one token per sequence
 // (split over K, partial sums to `part`), then one CTA per sequence for the reduction into its

@@ -259,7 +259,8 @@ __global__ void prefill_state_kernel(const float* __restrict__ proj, int N, Chun
 }
 
 // Decode: pool + epilogue for the sequences whose token completed a group; one warp per
-// sequence.  The projection of this step's tokens is already in their state slots.
+// sequence.  The projection of this step's tokens is already in their state slots.  emitted may
+// be null (the caller learns the emissions on the host).
 __global__ __launch_bounds__(128) void decode_emit_kernel(const int32_t* __restrict__ start_pos, int B, int ratio,
                                                           int overlap, Packing pk, float* __restrict__ state, int slots,
                                                           EpiParams ep, csa_out out, uint8_t* __restrict__ emitted,
@@ -272,7 +273,7 @@ __global__ __launch_bounds__(128) void decode_emit_kernel(const int32_t* __restr
   float* st = state + (size_t)b * slots * ncol;
   if (p < 0) {
     if (lane == 0) {
-      emitted[b] = 0;
+      if (emitted) emitted[b] = 0;
       atomicOr(flag, 1);
     }
     return;
@@ -284,7 +285,7 @@ __global__ __launch_bounds__(128) void decode_emit_kernel(const int32_t* __restr
   const long long pos = (long long)p + 1 - ratio;
   const bool pos_ok = ep.rope_dim == 0 || pos < ep.max_pos;
   if (lane == 0) {
-    emitted[b] = (emit && pos_ok) ? 1 : 0;
+    if (emitted) emitted[b] = (emit && pos_ok) ? 1 : 0;
     if (emit && !pos_ok) atomicOr(flag, 2);
   }
   if (!emit || !pos_ok) return;

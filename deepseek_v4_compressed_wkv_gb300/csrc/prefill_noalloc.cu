@@ -54,42 +54,51 @@ namespace {
 
 int noalloc_call(csa_compressor* c, const uint16_t* x, int B, int N, int start_pos, int slot_offset,
                  const csa_out* out, csa_stream_t stream) {
-  csa::Chunk ck;
-  const int rc =
-      csa_internal_check_prefill(c, x, B, N, start_pos, slot_offset, out, "csa_compress_prefill_noalloc", &ck);
-  if (rc) return rc;
-  if (!csa::prefill_tc_supported(c, x))
-    return csa_internal_fail(CSA_ERR_ARG,
-                             "csa_compress_prefill_noalloc: this shape runs the CUDA-core projection, whose "
-                             "scratch is not preallocated (needs 128-row packed tiles, ratio <= 256, 16-byte "
-                             "aligned x)");
-  const size_t bytes = csa::prefill_tc_scratch_bytes(c, B, N, ck);
-  if (bytes > kScratchBytes)
-    return csa_internal_fail(CSA_ERR_ARG,
-                             "csa_compress_prefill_noalloc: B x N too large for the preallocated scratch "
-                             "(limit: 16 MiB of pooled values and, for a chunk, carried softmax values)");
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-    return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: no current device");
-  void* base = nullptr;
-  {
-    // set-up, once per device, with that device current: the device address of the array
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_addr[dev]) {
-      void* p = nullptr;
-      cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-      if (e != cudaSuccess || !p)
-        return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: cudaGetSymbolAddress failed");
-      g_addr[dev] = p;
+  try {
+    csa::Chunk ck;
+    // also checks that the handle's device is the current one: the array used below is that
+    // device's copy
+    const int rc =
+        csa_internal_check_prefill(c, x, B, N, start_pos, slot_offset, out, "csa_compress_prefill_noalloc", &ck);
+    if (rc) return rc;
+    if (!csa::prefill_tc_supported(c, x))
+      return csa_internal_fail(CSA_ERR_ARG,
+                               "csa_compress_prefill_noalloc: this shape runs the CUDA-core projection, whose "
+                               "scratch is not preallocated (needs 128-row packed tiles, ratio <= 256, 16-byte "
+                               "aligned x)");
+    // the one launch geometry used both for this size check and for the launch below
+    const csa::PrefillPlan plan = csa::prefill_tc_plan(c, B, N, ck);
+    if (plan.bytes > kScratchBytes)
+      return csa_internal_fail(CSA_ERR_ARG,
+                               "csa_compress_prefill_noalloc: B x N too large for the preallocated scratch "
+                               "(limit: 16 MiB of pooled values and, for a chunk, carried softmax values)");
+    const int dev = c->device;
+    if (dev < 0 || dev >= kMaxDevices)
+      return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: device index out of range");
+    void* base = nullptr;
+    {
+      // set-up, once per device, with that device current (the check above): the device address
+      // of the array
+      std::lock_guard<std::mutex> lock(g_mu);
+      if (!g_addr[dev]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+          return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: cudaGetSymbolAddress failed");
+        g_addr[dev] = p;
+      }
+      base = g_addr[dev];
     }
-    base = g_addr[dev];
+    cudaStream_t s = (cudaStream_t)stream;  // the kernel marks the sequences' decode running values invalid
+    csa_out o = out ? *out : csa_out{nullptr, nullptr, nullptr, nullptr};
+    // the array's capacity is the extent the bounds-checked build checks the scratch stores against
+    if (csa::launch_prefill_tc(c, x, B, N, slot_offset, ck, plan, o, base, kScratchBytes, s) != cudaSuccess)
+      return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: kernel launch failed");
+    c->launches += csa::chunk_needs_carry(ck, c->overlap) + 1 + (ck.G > 0);
+    return ck.G;
+  } catch (...) {
+    return csa_internal_fail(CSA_ERR_INTERNAL, "csa_compress_prefill_noalloc: unexpected exception");
   }
-  cudaStream_t s = (cudaStream_t)stream;  // the kernel marks the sequences' decode running values invalid
-  csa_out o = out ? *out : csa_out{nullptr, nullptr, nullptr, nullptr};
-  if (csa::launch_prefill_tc(c, x, B, N, slot_offset, ck, o, base, s) != cudaSuccess)
-    return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: kernel launch failed");
-  c->launches += csa::chunk_needs_carry(ck, c->overlap) + 1 + (ck.G > 0);
-  return ck.G;
 }
 
 }  // namespace

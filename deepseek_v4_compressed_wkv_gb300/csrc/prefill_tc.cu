@@ -33,6 +33,9 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <cstdlib>
+
 #include "csa_internal.cuh"
 #include "kernels.h"
 #include "tc_common.cuh"
@@ -78,6 +81,9 @@ struct Params {
   int* flag;
   int* acc_pos;            // [max_batch] decode running values: marked invalid for the call's sequences
   long long state_elems, pooled_elems;  // extents checked by the bounds-checked build
+  unsigned long long wait_ns;           // budget of each device-side wait
+  int test_stall;          // bounds-checked build only: the producer never issues the last stage
+                           // (a test of the time-out path); 0 otherwise
 };
 
 struct EntryParams {
@@ -105,14 +111,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kStages;
   uint64_t* chunk_full = empty + kStages;  // [2]: chunk accumulator ready for the epilogue
   uint64_t* chunk_empty = chunk_full + 2;  // [2]: chunk accumulator drained, free for the MMAs
-  uint32_t* tmem_slot = (uint32_t*)(chunk_empty + 2);
+  uint64_t* mma_done = chunk_empty + 2;    // clean-up after an abort: the issued MMAs have completed
+  uint32_t* tmem_slot = (uint32_t*)(mma_done + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  int* issued_s = (int*)(tmem_slot + 2);  // stages the producer issued (read by the clean-up)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ftile = blockIdx.x, tt = blockIdx.y, b = blockIdx.z;
   const int nkb = P.K / kKb;
   const int nch = (nkb + kChunkKb - 1) / kChunkKb;
   const int t0 = tt * P.T - P.halo;  // virtual index (from the open group's start) of the tile's token 0
+#ifdef CSA_DEBUG_BOUNDS
+  const uint64_t kWait = P.wait_ns;  // the time-out test shortens the waits
+#else
+  constexpr uint64_t kWait = kWaitNs;
+#endif
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -123,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&chunk_full[i], 1);
       mbar_init(&chunk_empty[i], kEpiThreads / 32);
     }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_map(&map_x);
@@ -140,20 +154,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int kb = 0; kb < nkb; ++kb) {
         const int s = kb % kStages;
-        if (kb >= kStages && !mbar_wait(&empty[s], ((kb / kStages) & 1) ^ 1, abort_flag)) break;
+        if (kb >= kStages && !mbar_wait(&empty[s], ((kb / kStages) & 1) ^ 1, abort_flag, kWait)) break;
+#ifdef CSA_DEBUG_BOUNDS
+        if (P.test_stall && kb == nkb - 1) break;  // test of the time-out path: the last stage never comes
+#endif
         uint8_t* st = smem + s * kStageBytes;
         mbar_arrive_expect_tx(&full[s], kStageBytes);
         bulk_load(st, P.w + plane_stage_elem(P.K / kKb, ftile, kb), 3 * kPlaneBytes, &full[s]);
         tma_load_3d(st + 3 * kPlaneBytes, &map_x, kb * kKb, t0 - P.a, b, &full[s]);
         ++issued;
       }
-      if (*abort_flag) {  // let the copies already in flight land before the CTA exits
-        for (int kb = max(0, issued - kStages); kb < issued; ++kb) {
-          const uint64_t t1 = globaltimer();
-          while (!mbar_try_wait(&full[kb % kStages], (kb / kStages) & 1) && globaltimer() - t1 < kWaitNs) {
-          }
-        }
-      }
+      *issued_s = issued;
     }
   } else if (warp == 1) {
     // ---- MMA issuer
@@ -162,13 +173,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int c = 0; c < nch && ok; ++c) {
         const int buf = c & 1;
-        if (c >= 2 && !mbar_wait(&chunk_empty[buf], ((c >> 1) - 1) & 1, abort_flag)) break;
+        if (c >= 2 && !mbar_wait(&chunk_empty[buf], ((c >> 1) - 1) & 1, abort_flag, kWait)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * kTok);
         const int kb0 = c * kChunkKb, kb1 = min(nkb, kb0 + kChunkKb);
         for (int kb = kb0; kb < kb1; ++kb) {
           const int s = kb % kStages;
-          if (!mbar_wait(&full[s], (kb / kStages) & 1, abort_flag)) {
+          if (!mbar_wait(&full[s], (kb / kStages) & 1, abort_flag, kWait)) {
             ok = false;
             break;
           }
@@ -197,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int c = 0; c < nch; ++c) {
       const int buf = c & 1;
-      if (!mbar_wait(&chunk_full[buf], (c >> 1) & 1, abort_flag)) {
+      if (!mbar_wait(&chunk_full[buf], (c >> 1) & 1, abort_flag, kWait)) {
         ok = false;
         break;
       }
@@ -350,8 +361,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
-  if (*abort_flag && threadIdx.x == 0) atomicOr(P.flag, 4);
+  __syncthreads();  // every role has left its loop; the flag no longer changes
+  if (*abort_flag) {
+    // a wait ran out: the copies in flight land and the issued MMAs complete before the TMEM is
+    // freed and the CTA leaves (this call's outputs are undefined; the flag says so)
+    drain_after_abort(warp == 0 && lane == 0, warp == 1 && lane == 0, full, kStages, *issued_s, mma_done);
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0) atomicOr(P.flag, 4);
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -500,7 +518,7 @@ int prefill_tok(const csa_compressor* c, int B, int N) {
 
 template <int TOK>
 cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset, const Chunk& ck,
-                       const csa_out& out, void* scratch, cudaStream_t s) {
+                       const csa_out& out, void* scratch, size_t scratch_bytes, cudaStream_t s) {
   using namespace tc;
   auto encode = tcx::get_encode();
   if (!encode) return cudaErrorNotSupported;
@@ -528,10 +546,27 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
   P.flag = c->dev_flag;
   P.acc_pos = c->dec_acc_pos;
   P.state_elems = (long long)c->opt.max_batch * c->slots * P.ncol;
-  P.pooled_elems = (long long)B * P.ntt * P.GT * c->H;
+  // the pooled values' extent, for the bounds-checked build: what this launch writes, but never
+  // past the scratch it was given (the carried values, when present, follow the pooled ones)
+  const size_t pooled_bytes = (size_t)B * P.ntt * P.GT * c->H * sizeof(uint16_t);
+  const bool has_carry = chunk_needs_carry(ck, c->overlap);
+  P.pooled_elems = (long long)(std::min(pooled_bytes, has_carry ? std::min(carry_offset(pooled_bytes), scratch_bytes)
+                                                                : scratch_bytes) / sizeof(uint16_t));
   P.w = c->w_planes;
-  if (chunk_needs_carry(ck, c->overlap)) {
-    float* carry = (float*)((uint8_t*)scratch + carry_offset((size_t)B * P.ntt * P.GT * c->H * sizeof(uint16_t)));
+  P.wait_ns = tcx::kWaitNs;
+  P.test_stall = 0;
+#ifdef CSA_DEBUG_BOUNDS
+  // the time-out test: the producer leaves out the last stage, and the waits give up sooner
+  if (getenv("CSA_TEST_STALL_LAST_STAGE")) {
+    P.test_stall = 1;
+    P.wait_ns = 200000000ull;
+  }
+#endif
+  if (has_carry) {
+    const size_t coff = carry_offset(pooled_bytes);
+    const long long carry_elems = (long long)std::min<size_t>((size_t)B * (1 + c->overlap) * 3 * c->H,
+                                                              scratch_bytes > coff ? (scratch_bytes - coff) / 4 : 0);
+    float* carry = (float*)((uint8_t*)scratch + coff);
     cudaLaunchAttribute early[1];
     early[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     early[0].val.programmaticStreamSerializationAllowed = 1;
@@ -542,7 +577,7 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
     cc.attrs = early;
     cc.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cc, chunk_carry_kernel, (const float*)c->state, c->pk, c->overlap, c->slots,
-                                       slot_offset, ck, carry, (long long)B * (1 + c->overlap) * 3 * c->H, c->dev_flag);
+                                       slot_offset, ck, carry, carry_elems, c->dev_flag);
     if (e != cudaSuccess) return e;
     P.carry = carry;
   }
@@ -604,27 +639,30 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
 
 }  // namespace
 
-// Bytes of scratch a prefill call of B x N tokens needs: the pooled values ([B][token tiles]
-// [groups per tile][H] bf16) and, for a chunk whose first group has earlier candidates, their
-// running softmax values ([B][1 + overlap][3][H] f32).
-size_t prefill_tc_scratch_bytes(const csa_compressor* c, int B, int N, const Chunk& ck) {
-  const int T = owned_tokens(c, prefill_tok(c, B, ck.a + N));
+PrefillPlan prefill_tc_plan(const csa_compressor* c, int B, int N, const Chunk& ck) {
+  PrefillPlan plan;
+  plan.tok = prefill_tok(c, B, ck.a + N);
+  const int T = owned_tokens(c, plan.tok);
   const int GT = T / c->ratio;
   const int ntt = (ck.a + N + T - 1) / T;
   const size_t pooled = (size_t)B * ntt * GT * c->H * sizeof(uint16_t);
-  return chunk_needs_carry(ck, c->overlap) ? carry_offset(pooled) + (size_t)B * (1 + c->overlap) * 3 * c->H * 4
-                                           : pooled;
+  plan.bytes = chunk_needs_carry(ck, c->overlap)
+                   ? carry_offset(pooled) + (size_t)B * (1 + c->overlap) * 3 * c->H * sizeof(float)
+                   : pooled;
+  return plan;
 }
 
 cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset,
-                              const Chunk& ck, const csa_out& out, void* scratch, cudaStream_t s) {
-  switch (prefill_tok(c, B, ck.a + N)) {
+                              const Chunk& ck, const PrefillPlan& plan, const csa_out& out, void* scratch,
+                              size_t scratch_bytes, cudaStream_t s) {
+  if (scratch_bytes < plan.bytes) return cudaErrorInvalidValue;
+  switch (plan.tok) {
     case 224:
-      return launch_tok<224>(c, x, B, N, slot_offset, ck, out, scratch, s);
+      return launch_tok<224>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s);
     case 128:
-      return launch_tok<128>(c, x, B, N, slot_offset, ck, out, scratch, s);
+      return launch_tok<128>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s);
     default:
-      return launch_tok<256>(c, x, B, N, slot_offset, ck, out, scratch, s);
+      return launch_tok<256>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s);
   }
 }
 

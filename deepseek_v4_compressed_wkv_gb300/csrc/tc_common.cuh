@@ -58,20 +58,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase of `parity` to complete, at most kWaitNs; on time-out raises the CTA's
-// abort flag (so the other roles stop too) and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// Waits for the phase of `parity` to complete, at most wait_ns; on time-out raises the CTA's
+// abort flag (so the other roles stop too) and returns false.  Also returns false, at once,
+// once another role has raised the flag.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t wait_ns = kWaitNs) {
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 63u) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitNs) {
+      if (globaltimer() - t0 > wait_ns) {
         *abort_flag = 1;
         return false;
       }
     }
   }
+}
+
+// Waits for the phase of `parity` at most wait_ns, whatever the abort flag says (the clean-up
+// after an abort waits for work already started); false on time-out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t wait_ns = kWaitNs) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > wait_ns) return false;
+  return true;
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
@@ -237,6 +248,22 @@ __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
 
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Clean-up of a warp-specialised CTA after one of its roles gave up on a wait (the abort flag is
+// set), run by every thread between two __syncthreads once every role has left its loop, before
+// the CTA frees its TMEM or reuses its stage ring: the producer lets the last `ring` copies it
+// issued land (completions of the full barriers of ring stages; an earlier copy was consumed
+// before a later one could reuse its stage), and the MMA issuer commits its issued MMAs to
+// `mma_done` (a fresh barrier, phase 0) and waits for them.  Both waits are bounded.
+__device__ __forceinline__ void drain_after_abort(bool producer, bool issuer, uint64_t* full, int ring, int issued,
+                                                  uint64_t* mma_done) {
+  if (producer)
+    for (int t = max(0, issued - ring); t < issued; ++t) mbar_wait_bounded(&full[t % ring], (t / ring) & 1);
+  if (issuer) {
+    mma_commit(mma_done);
+    mbar_wait_bounded(mma_done, 0);
+  }
 }
 
 inline PFN_cuTensorMapEncodeTiled_v12000 get_encode() {

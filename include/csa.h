@@ -95,15 +95,22 @@ typedef struct {
 /* Fills *opt with the defaults above. */
 void csa_options_default(csa_options* opt);
 
-/* Creates a compressor for x of width dim, latent width head_dim, group size ratio.
- * overlap = 1 selects the ratio-4 overlapped form (two branches of head_dim each) and
- * requires ratio == 4.  opt may be NULL (defaults).  Requirements: dim % 64 == 0,
- * head_dim % 16 == 0 and 16 <= head_dim <= 512, ratio >= 1, rope_dim even and
- * <= head_dim, max_batch >= 1.  Allocates device memory on the current device (state,
- * RoPE table) and builds the YaRN table on the host in double precision.
- * On success *out receives the handle. */
-int csa_compressor_create(int dim, int head_dim, int ratio, int overlap, const csa_options* opt,
-                          csa_compressor** out);
+/* Creates a compressor with the default options (csa_options_default) for x of width dim,
+ * latent width head_dim, group size ratio ("Pool token pairs", Compressor(dim, head_dim,
+ * ratio); "Compressed Sparse Attention - ratio m = 4": the overlapped form).  overlap = 1
+ * selects the ratio-4 overlapped form (two branches of head_dim each) and requires ratio == 4.
+ * Requirements: dim % 64 == 0, head_dim % 16 == 0 and 16 <= head_dim <= 512, ratio >= 1.
+ * Allocates device memory on the current device (weights, state, RoPE table), which becomes the
+ * handle's device: every later call on the handle must be made with that device current
+ * (otherwise it returns CSA_ERR_ARG).  Builds the YaRN table on the host in double precision.
+ * On success *out receives the handle; on failure *out is NULL and nothing stays allocated. */
+int csa_compressor_create(int dim, int head_dim, int ratio, int overlap, csa_compressor** out);
+
+/* The same with explicit options; opt may be NULL (defaults).  Further requirements: rope_dim
+ * even and <= head_dim, max_batch >= 1, fp4 in {0, 1, 2} (2: head_dim % 32 == 0), eps >= 0,
+ * valid RoPE constants when rope_dim > 0. */
+int csa_compressor_create_ex(int dim, int head_dim, int ratio, int overlap, const csa_options* opt,
+                             csa_compressor** out);
 
 /* Copies the weights into library-owned, re-laid-out buffers.
  *  wkv   [C][dim] f32 dev, C = (1 + overlap) * head_dim ("Module compress" linear_f32 layout);
@@ -159,15 +166,18 @@ int csa_compress_prefill_into(csa_compressor* c, const uint16_t* x, int B, int N
  * all device memory for their own pool up front, or code that enqueues work while a CUDA
  * graph is being captured.  Same arguments, results and return value as
  * csa_compress_prefill, but the tensor-core kernel's scratch lives in a device array built
- * into the library (16 MiB of pooled values, held by every GPU that loads the library until
- * the process exits).  It therefore needs:
+ * into the library (16 MiB, held by every GPU that loads the library until the process
+ * exits).  It therefore needs:
  *  - a shape that runs the tensor-core kernel (csa_uses_tensor_cores(c) == 1, x 16-byte
  *    aligned); other shapes return CSA_ERR_ARG;
- *  - B * ceil((a + N) / T) * (T / ratio) * head_dim * 2 <= 16 MiB, with a = start_pos % ratio
- *    and T the tokens a tile owns (the launch takes a tile of 224 or 256 tokens: at ratio 4
- *    overlapped T = 220 or 252, else the largest multiple of ratio <= the tile), plus, for a
- *    chunk whose first group has earlier candidates, B * head_dim * 12 bytes (rounded up to
- *    256); larger calls return CSA_ERR_ARG ("too large") without launching anything.
+ *  - scratch of at most 16 MiB: B * ceil((a + N) / T) * (T / ratio) * head_dim * 2 bytes of
+ *    pooled values, with a = start_pos % ratio and T the tokens a tile owns (the launch takes a
+ *    tile of 256, 224 or 128 tokens, chosen from the number of SMs of the device: at ratio 4
+ *    overlapped T = 252, 220 or 124, else the largest multiple of ratio <= the tile), plus, for
+ *    a chunk whose first group has earlier candidates, the carried softmax values, B * (1 +
+ *    overlap) * 3 * head_dim * 4 bytes (after the pooled values, rounded up to 256).  Because T
+ *    depends on the device, the CSA_ERR_ARG "too large" return is the authoritative check:
+ *    larger calls return it without launching anything.
  * The first call on each device looks up the array's device address (with that device
  * current); make that first call before any stream capture.  Every call shares the one
  * array: calls that overlap on the GPU (other streams, other handles) race, so serialise
@@ -175,17 +185,37 @@ int csa_compress_prefill_into(csa_compressor* c, const uint16_t* x, int B, int N
 int csa_compress_prefill_noalloc(csa_compressor* c, const uint16_t* x, int B, int N, int start_pos,
                                  int slot_offset, const csa_out* out, csa_stream_t stream);
 
-/* One decode step for sequences 0..B-1 (state slots 0..B-1), one token each; 1 <= B <= max_batch
- * (B = 0 returns CSA_ERR_ARG and enqueues nothing).
+/* One decode step for sequences 0..B-1 (state slots 0..B-1), one token each ("Pool token
+ * pairs", Compressor forward, decode branch: the token goes to state slot start_pos % ratio, and
+ * when (start_pos + 1) % ratio == 0 the group is pooled and emitted, otherwise the module returns
+ * None; "Module compress", compressor: "or None while a group is still filling").
  *  x_tok     [B][dim] bf16 dev
- *  start_pos [B] int32 dev: position of this token in its sequence (per sequence)
- *  emitted   [B] u8 dev: set to 1 where the token completed a group, else 0
- * Row b of out is written only where emitted[b] = 1.  start_pos 0 restarts the sequence
- * (the pages' prefill branch with one token).  Positions must be >= 0, and for emitted
- * rows the entry position start_pos + 1 - ratio must be < max_pos; a violation leaves the
- * row unwritten, sets emitted[b] = 0 and raises the flag read by csa_device_status. */
+ *  start_pos [B] int32 HOST: position of this token in its sequence (per sequence); 0 restarts
+ *            the sequence (the pages' prefill branch with one token).  The library copies the
+ *            array before returning, so the caller may reuse it at once.
+ *  out       rows [B][..] (dev); row b is written only where sequence b emits
+ *  emitted   [B] u8, HOST or dev, or NULL: 1 where the token completed a group, else 0 (a host
+ *            array is filled before the call returns; a device array is written by the kernels)
+ * Returns the number of emitting sequences (0 is the pages' None for every sequence), or a
+ * negative csa_status.  1 <= B <= max_batch; positions must be >= 0 and, for emitting
+ * sequences, the entry position start_pos + 1 - ratio must be < max_pos when RoPE is on:
+ * violations return CSA_ERR_ARG and enqueue nothing.  The copy of start_pos to the device is
+ * a host-to-device copy from ordinary host memory, which cannot be captured into a CUDA graph:
+ * graphs use csa_compress_decode_dev. */
 int csa_compress_decode(csa_compressor* c, const uint16_t* x_tok, int B, const int32_t* start_pos,
-                        uint8_t* emitted, const csa_out* out, csa_stream_t stream);
+                        const csa_out* out, uint8_t* emitted, csa_stream_t stream);
+
+/* The same decode step with the positions in device memory, for callers whose positions live on
+ * the device and for CUDA-graph capture (a replayed graph reads positions that device work has
+ * advanced between replays).  The pages have only the host form above; this one cannot return
+ * the count, because the positions are not known on the host when the call is enqueued.
+ *  start_pos [B] int32 dev
+ *  emitted   [B] u8 dev (required)
+ * Returns CSA_OK or a negative csa_status.  A position the kernels cannot handle (negative, or
+ * an entry position beyond the RoPE table) leaves its row unwritten, sets emitted[b] = 0 and
+ * raises the flag read by csa_device_status. */
+int csa_compress_decode_dev(csa_compressor* c, const uint16_t* x_tok, int B, const int32_t* start_pos,
+                            const csa_out* out, uint8_t* emitted, csa_stream_t stream);
 
 /* Resets state slots [slot_begin, slot_begin + slot_count): kv 0, score -inf. */
 int csa_state_reset(csa_compressor* c, int slot_begin, int slot_count, csa_stream_t stream);
@@ -201,9 +231,12 @@ int64_t csa_state_elems(const csa_compressor* c);
 int csa_state_export(const csa_compressor* c, float* kv, float* score, csa_stream_t stream);
 
 /* Reads and clears the device-side error flag of the handle (synchronises the stream).
- * Returns CSA_OK, or CSA_ERR_DEVICE if a kernel flagged something since the last call: bit 1 a
- * negative start_pos, bit 2 an entry position beyond the RoPE table, bit 4 a wait that gave up,
- * bit 8 (only in the bounds-checked build of the library) a store outside its buffer, skipped. */
+ * Returns CSA_OK if no kernel flagged anything since the last call; CSA_ERR_TIMEOUT if a
+ * device-side wait ran out of its time budget (flag bit 4: the kernel stopped its work, let its
+ * copies and tensor-core operations in flight finish and returned, leaving that call's outputs
+ * and state slots undefined; the handle stays usable); else CSA_ERR_DEVICE: bit 1 a negative
+ * start_pos, bit 2 an entry position beyond the RoPE table, bit 8 (only in the bounds-checked
+ * build of the library) a store outside its buffer, skipped. */
 int csa_device_status(csa_compressor* c, csa_stream_t stream);
 
 /* Frees the handle and its device memory (synchronises the device first). NULL is a no-op. */

@@ -48,8 +48,12 @@ def test_create_rejects_bad_shapes_without_a_device(args, frag):
     lib = csa.load_library()
     h = ctypes.c_void_p()
     o = csa.default_options()
-    rc = lib.csa_compressor_create(*args, ctypes.byref(o), ctypes.byref(h))
+    rc = lib.csa_compressor_create_ex(*args, ctypes.byref(o), ctypes.byref(h))
     assert rc == -1 and not h.value
+    assert frag in lib.csa_last_error().decode()
+    # the form without options checks the same shapes
+    h2 = ctypes.c_void_p()
+    assert lib.csa_compressor_create(*args, ctypes.byref(h2)) == -1 and not h2.value
     assert frag in lib.csa_last_error().decode()
 
 
@@ -58,10 +62,10 @@ def test_create_rejects_bad_options():
     h = ctypes.c_void_p()
     for kw in (dict(rope_dim=63), dict(rope_dim=1024), dict(max_batch=0), dict(fp4=3), dict(fp4=-1)):
         o = csa.default_options(**kw)
-        assert lib.csa_compressor_create(4096, 512, 4, 1, ctypes.byref(o), ctypes.byref(h)) == -1
+        assert lib.csa_compressor_create_ex(4096, 512, 4, 1, ctypes.byref(o), ctypes.byref(h)) == -1
     # the power-of-two quantiser takes blocks of 32 features
     o = csa.default_options(fp4=2, rope_dim=16)
-    assert lib.csa_compressor_create(4096, 48, 4, 0, ctypes.byref(o), ctypes.byref(h)) == -1
+    assert lib.csa_compressor_create_ex(4096, 48, 4, 0, ctypes.byref(o), ctypes.byref(h)) == -1
     assert "multiple of 32" in lib.csa_last_error().decode()
 
 
@@ -69,6 +73,8 @@ def test_null_handle_calls_fail_cleanly():
     lib = csa.load_library()
     assert lib.csa_compress_prefill(None, None, 1, 4, 0, 0, None, None) == -1
     assert lib.csa_compress_decode(None, None, 1, None, None, None, None) == -1
+    assert lib.csa_compress_decode_dev(None, None, 1, None, None, None, None) == -1
+    assert lib.csa_compressor_create(256, 64, 4, 1, None) == -1  # no place for the handle
     assert lib.csa_state_reset(None, 0, 1, None) == -1
     assert lib.csa_state_elems(None) == -1
     assert lib.csa_compress_prefill_into(None, None, 1, 4, 0, 0, None, 8, None) == -1

@@ -3,7 +3,9 @@ kernel store with a computed index checks it against its buffer's extent and, in
 outside, skips the store and raises bit 8 of the device flag, which the parity tests read back
 through csa_device_status.  The cases run in a child process (the library is loaded once per
 process) with CSA_LIBRARY_VARIANT=bounds: small odd shapes on both projection paths, chains of
-chunks, cache rows, the gate bias, batches beyond one token block, and the indexer's quantiser."""
+chunks, cache rows, the gate bias, batches beyond one token block, the indexer's quantiser, the
+entry point that allocates nothing (its scratch stores checked against the fixed array's
+capacity), and the time-out path (a test hook of this build only)."""
 import os
 import subprocess
 import sys
@@ -30,7 +32,8 @@ def test_parity_cases_on_the_bounds_checked_build():
         "test_errors_are_reported_not_raised_on_the_device", "test_decode_steps_in_a_cuda_graph")]
     cases += [os.path.join(HERE, "test_gpu_chunks.py") + "::" + t for t in (
         "test_prefill_chunks_then_decode", "test_prefill_into_cache_rows")]
-    cases += [os.path.join(HERE, "test_gpu_gate_bias.py")]
+    cases += [os.path.join(HERE, "test_gpu_gate_bias.py"), os.path.join(HERE, "test_gpu_timeout.py"),
+              os.path.join(HERE, "test_zz_no_alloc.py")]
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider", *cases],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
