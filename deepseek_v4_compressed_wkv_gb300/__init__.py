@@ -296,8 +296,10 @@ class Compressor:
             raise CSAError("x_tok must be bf16 [B, dim]")
         on_device = isinstance(start_pos, torch.Tensor) and start_pos.is_cuda
         if on_device:
-            if start_pos.dtype != torch.int32 or start_pos.numel() != B:
-                raise CSAError(f"start_pos must be int32 with {B} elements")
+            if start_pos.numel() != B:
+                raise CSAError(f"start_pos has {start_pos.numel()} elements for {B} sequences")
+            if start_pos.dtype != torch.int32:
+                raise CSAError("start_pos must be int32")
             _on_current_device(x_tok, start_pos)
         else:
             import numpy as np

@@ -90,7 +90,7 @@ def check_entries(gpu: dict, ref_prequant: np.ndarray, fp4: int, what=""):
 def to_np(d: dict, rows=None):
     out = {}
     for k, v in d.items():
-        if v is None or k == "emitted":
+        if v is None or k in ("emitted", "count") or not isinstance(v, torch.Tensor):
             continue
         a = v.contiguous()
         a = host_bits(a) if a.dtype == torch.bfloat16 else a.cpu().numpy()
