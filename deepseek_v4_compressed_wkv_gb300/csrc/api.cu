@@ -225,10 +225,9 @@ int check_decode(const csa_compressor* c, const uint16_t* x_tok, int B, const cs
 int decode_call(csa_compressor* c, const uint16_t* x_tok, int B, const int32_t* start_pos, const csa_out& out,
                 uint8_t* emitted, cudaStream_t s) {
   if (csa::decode_tc_supported(c, x_tok, B)) {
-    // split-K partial sums: [slices][B][2C] f32, grown on first use (a later call of the same
-    // or smaller B allocates nothing)
-    const int ks = csa::decode_tc_slices(c);
-    const size_t bytes = (size_t)ks * B * c->pk.cols() * sizeof(float);
+    // split-K partial sums: [slices][B][2C] f32, grown on first use (a later call of the same or
+    // smaller B allocates nothing)
+    const size_t bytes = csa::decode_tc_part_bytes(c, B);
     if (c->dec_part_bytes < bytes) {
       CSA_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
       cudaFree(c->dec_part);
@@ -238,11 +237,11 @@ int decode_call(csa_compressor* c, const uint16_t* x_tok, int B, const int32_t* 
       c->dec_part_bytes = bytes;
     }
     if (c->prof_start) CSA_CUDA(cudaEventRecord(c->prof_start, s), "cudaEventRecord");
-    CSA_CUDA(csa::launch_decode_tc(c, x_tok, B, start_pos, c->dec_part, ks, out, emitted, c->dec_early_start, s),
+    CSA_CUDA(csa::launch_decode_tc(c, x_tok, B, start_pos, c->dec_part, out, emitted, c->dec_early_start, s),
              "tensor-core decode launch");
     if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
     c->dec_early_start = true;
-    c->launches += 2;
+    c->launches += csa::decode_tc_kernels_per_call();
     return CSA_OK;
   }
   CSA_CUDA(csa::invalidate_decode_acc(c, 0, B, s), "invalidate decode running values");
@@ -342,7 +341,7 @@ int csa_compressor_create_ex(int dim, int H, int ratio, int overlap, const csa_o
     alloc((void**)&c->state, (size_t)o.max_batch * c->slots * ncol * sizeof(float));
     alloc((void**)&c->dev_flag, sizeof(int));
     alloc((void**)&c->dec_acc, (size_t)o.max_batch * 3 * H * sizeof(float));
-    alloc((void**)&c->dec_acc_pos, (size_t)o.max_batch * sizeof(int));
+    alloc((void**)&c->dec_acc_pos, (size_t)o.max_batch * pk.ntiles * sizeof(int));
     alloc((void**)&c->dec_pos, (size_t)o.max_batch * sizeof(int32_t));
     if (o.rope_dim > 0) {
       const size_t n = (size_t)o.max_pos * (o.rope_dim / 2);
@@ -358,7 +357,7 @@ int csa_compressor_create_ex(int dim, int H, int ratio, int overlap, const csa_o
       }
     }
     if (e == cudaSuccess) e = cudaMemset(c->dev_flag, 0, sizeof(int));
-    if (e == cudaSuccess) e = cudaMemset(c->dec_acc_pos, 0xFF, (size_t)o.max_batch * sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(c->dec_acc_pos, 0xFF, (size_t)o.max_batch * pk.ntiles * sizeof(int));
     if (e == cudaSuccess && csa::launch_state_reset(c, 0, o.max_batch, 0) != cudaSuccess) e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {

@@ -422,7 +422,9 @@ struct csa_compressor {
   size_t dec_part_bytes;
   float* dec_acc;           // decode, non-overlapped: running softmax max / denominator / numerator
                             // of each sequence's open group [max_batch][3][H]
-  int* dec_acc_pos;         //   position of the last token folded in [max_batch] (-1: not valid)
+  int* dec_acc_pos;         //   position of the last token folded in [max_batch][ntiles] (-1: not
+                            //   valid); prefill invalidates every entry of its sequences, the
+                            //   decode keeps a sequence's in its first entry
   int32_t* dec_pos;         // [max_batch] device copy of the positions of a host-array decode call
   bool dec_early_start;     // the next decode may start its weight loads before the preceding
                             // kernel ends (false right after set_weights rewrote the planes)

@@ -299,7 +299,8 @@ struct FinParams {
   uint8_t* emitted;          // [B], or null (the caller learns the emissions on the host)
   float* acc;                // non-overlapped: [max_batch][3][H] running max, denominator and
                              // numerator of the open group over its tokens so far
-  int* acc_pos;              // [max_batch] position of the last token in acc (-1: not valid)
+  int* acc_pos;              // [max_batch][ntiles] position of the last token in acc (-1: not valid);
+                             // this kernel keeps a sequence's in its first entry
   const float* ape;          // packed gate positional bias [ratio][ncol] (zero at kv columns), or null
   long long state_elems, acc_elems;  // extents checked by the bounds-checked build
 };
@@ -488,7 +489,7 @@ __global__ void __launch_bounds__(kFinThreads, 5) decode_finish_kernel(const Fin
       num[gi][e] = 0.0f;
     }
   const bool open = !P.overlap && pp % P.ratio != 0;  // running values of an open group to continue
-  const bool use_acc = open && P.acc_pos[b] == p - 1;
+  const bool use_acc = open && P.acc_pos[(size_t)b * pk.ntiles] == p - 1;
 #pragma unroll
   for (int gi = 0; gi < kFinGroups; ++gi) {
     const int g = tid + gi * nthr;
@@ -599,7 +600,7 @@ __global__ void __launch_bounds__(kFinThreads, 5) decode_finish_kernel(const Fin
     if (P.emitted) P.emitted[b] = pool ? 1 : 0;
     if (p < 0) atomicOr(P.flag, 1);
     if (emit && !pool) atomicOr(P.flag, 2);
-    if (!P.overlap) P.acc_pos[b] = p >= 0 ? p : -1;
+    if (!P.overlap) P.acc_pos[(size_t)b * pk.ntiles] = p >= 0 ? p : -1;
   }
   if (P.overlap && !pool) return;
   __syncthreads();  // the token's row is complete in shared memory
@@ -686,13 +687,20 @@ bool decode_tc_supported(const csa_compressor* c, const void* x, int B) {
 
 cudaError_t invalidate_decode_acc(const csa_compressor* c, int first, int count, cudaStream_t s) {
   if (count <= 0) return cudaSuccess;
-  return cudaMemsetAsync(c->dec_acc_pos + first, 0xFF, (size_t)count * sizeof(int), s);
+  return cudaMemsetAsync(c->dec_acc_pos + (size_t)first * c->pk.ntiles, 0xFF,
+                         (size_t)count * c->pk.ntiles * sizeof(int), s);
 }
 
-cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, const int32_t* start_pos,
-                             float* part, int ks, const csa_out& out, uint8_t* emitted, bool early_start,
-                             cudaStream_t s) {
+size_t decode_tc_part_bytes(const csa_compressor* c, int B) {
+  return (size_t)decode_tc_slices(c) * B * c->pk.cols() * sizeof(float);
+}
+
+int decode_tc_kernels_per_call() { return 2; }
+
+cudaError_t launch_decode_tc(csa_compressor* c, const uint16_t* x, int B, const int32_t* start_pos, float* part,
+                             const csa_out& out, uint8_t* emitted, bool early_start, cudaStream_t s) {
   using namespace dtc;
+  const int ks = decode_tc_slices(c);
   auto encode = tcx::get_encode();
   if (!encode) return cudaErrorNotSupported;
   const size_t smem = (size_t)kRingBytes + 1024 + 1024;

@@ -42,17 +42,19 @@ cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B,
                               const Chunk& ck, const PrefillPlan& plan, const csa_out& out, void* scratch,
                               size_t scratch_bytes, cudaStream_t s);
 
-// Tensor-core decode (decode_tc.cu): two launches, the projection of one token per sequence
-// (split over K, partial sums to `part`), then one CTA per sequence for the reduction into its
-// state slot, the pool and the epilogue.  `early_start` lets the projection fetch its weights
+// Tensor-core decode (decode_tc.cu): two launches per call, the projection of one token per
+// sequence (split over K, partial sums to `part`), then one CTA per sequence for the reduction into
+// its state slot, the pool and the epilogue.  `early_start` lets the projection fetch its weights
 // before the preceding kernel in the stream has finished.
 bool decode_tc_supported(const csa_compressor* c, const void* x, int B);
 // Marks the decode running values of sequences [first, first + count) as not valid (their state
 // slots were rewritten by something other than the tensor-core decode).
 cudaError_t invalidate_decode_acc(const csa_compressor* c, int first, int count, cudaStream_t s);
 int decode_tc_slices(const csa_compressor* c);
-cudaError_t launch_decode_tc(const csa_compressor* c, const uint16_t* x, int B, const int32_t* start_pos,
-                             float* part, int nslices, const csa_out& out, uint8_t* emitted, bool early_start,
-                             cudaStream_t s);
+// Bytes of the split-K partial sums of a call of B sequences; kernels a call launches.
+size_t decode_tc_part_bytes(const csa_compressor* c, int B);
+int decode_tc_kernels_per_call();
+cudaError_t launch_decode_tc(csa_compressor* c, const uint16_t* x, int B, const int32_t* start_pos, float* part,
+                             const csa_out& out, uint8_t* emitted, bool early_start, cudaStream_t s);
 
 }  // namespace csa

@@ -79,7 +79,7 @@ struct Params {
   const float* carry;      // [B][1 + overlap][3][H] running softmax values of the candidates
                            // of the first groups that are earlier than the chunk, or null
   int* flag;
-  int* acc_pos;            // [max_batch] decode running values: marked invalid for the call's sequences
+  int* acc_pos;            // [max_batch][ntiles] decode running values: marked invalid for the call's sequences
   long long state_elems, pooled_elems;  // extents checked by the bounds-checked build
   unsigned long long wait_ns;           // budget of each device-side wait
   int test_stall;          // bounds-checked build only: the producer never issues the last stage
@@ -233,8 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // and written the carried values; a no-op for a launch without that predecessor
       griddep_wait();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      // the prefill rewrites the sequence's state: its decode running values are no longer valid
-      if (ftile == 0 && tt == 0 && et == 0) P.acc_pos[P.slot_offset + b] = -1;
+      // the prefill rewrites the sequence's state: its decode running values (kept per packed
+      // tile) are no longer valid
+      if (tt == 0 && et == 0) P.acc_pos[(size_t)(P.slot_offset + b) * P.pk.ntiles + ftile] = -1;
       if (P.ape && row / P.pk.ft >= P.pk.nk / 2) {
         // wgate(x) + the positional bias of each token's place in its group (score rows only),
         // added in registers before staging, the loads independent of one another: column c

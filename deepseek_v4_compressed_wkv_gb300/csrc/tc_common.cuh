@@ -63,6 +63,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // once another role has raised the flag.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint64_t wait_ns = kWaitNs) {
+  // a phase that has already completed returns at once: the timer is read only when the wait
+  // has to poll (reading %globaltimer on every call measured about 30 cycles per MMA in the
+  // tensor-core loops, which wait on a barrier per pipeline stage)
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -79,6 +83,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // Waits for the phase of `parity` at most wait_ns, whatever the abort flag says (the clean-up
 // after an abort waits for work already started); false on time-out.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t wait_ns = kWaitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity))
     if (globaltimer() - t0 > wait_ns) return false;
