@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--decode-layers", type=int, default=0,
                     help="layer instances rotated in the decode measurement (0: enough to exceed L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-long", action="store_true", help="skip the long-context prefill sweep")
     ap.add_argument("--clock-seconds", type=float, default=1.0,
                     help="seconds of untimed steps run under the clock sampler before the timed region")
     return ap.parse_args()
@@ -288,18 +289,47 @@ def run_ours(args, rank, world, local):
                 "traffic": None, "kernel": "gemm_ffma_kernel (f32 FMA projection)",
                 "peak_basis": f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 flop x {sm_clock:.0f} MHz"}
 
-    # end to end through the public call with host buffers (pinned): every step copies its x in
-    # (H2D), runs the prefill and copies latent + codes + scales out (D2H), all inside the timed
-    # region.  As a serving loop would, the steps are pipelined: step i+1's input copy (split over
-    # two copy streams) runs while step i computes, and step i's outputs go back on a third
-    # stream; inputs and outputs are double-buffered.
+    e2e_ms, h2d, d2h = measure_e2e(torch, comp, x, out, B * G, K, stream, world, device)
+
+    line = {"metric": METRIC, "value": value, "unit": "entries/s", "n_gpus": world, "steps": K,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": N, "entries_per_step": entries,
+                       "l2": "flushed between timed iterations (2x L2 buffer written)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "tokens_per_s": tokens_s, "kernel_ms": kms, "roofline": roof,
+            "e2e": {"value": entries / (e2e_ms * 1e-3), "unit": "entries/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches, "clocks": clk}
+    comp.close()
+    line["chunked_prefill"] = bench_chunked(args, torch, csa, synthetic, device, peaks, world)
+    line["other_prefill"] = [bench_prefill_workload(args, torch, csa, synthetic, device, peaks, world, wl)
+                             for wl in (synthetic.HCA, synthetic.INDEXER, synthetic.PAIRS)]
+    line["other_prefill"].append(bench_prefill_workload(args, torch, csa, synthetic, device, peaks, world,
+                                                        synthetic.FLASH_CSA, gate_bias=True))
+    if not args.no_long:
+        line["long_prefill"] = bench_long(args, torch, csa, synthetic, device, peaks, world)
+    if not args.no_decode:
+        line["decode"] = bench_decode(args, torch, csa, synthetic, device, peaks, world, rank)
+    return line
+
+
+def measure_e2e(torch, comp, x, out, rows, K, stream, world, device, start_pos=0):
+    """End to end through the public call with host buffers (pinned): every step copies its x in
+    (H2D), runs the prefill and copies latent + codes + scales out (D2H), all inside the timed
+    region.  As a serving loop would, the steps are pipelined: step i+1's input copy (split over two
+    copy streams) runs while step i computes, and step i's outputs go back on a third stream; inputs
+    and outputs are double-buffered.  Returns (ms per step, H2D bytes, D2H bytes per step)."""
     x_host = x.cpu().pin_memory()
-    x_dev = [torch.empty_like(x) for _ in range(2)]
-    outs2 = [out, comp._alloc_out(B * G, device, prequant=False)]
+    x_dev = [x, torch.empty_like(x)]
+    outs2 = [out, comp._alloc_out(rows, device, prequant=False)]
     host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items() if v is not None}
     h2d_streams = [torch.cuda.Stream(device) for _ in range(2)]
     d2h_stream = torch.cuda.Stream(device)
-    half = x.shape[1] // 2
+    # the two halves of each input copy: along the batch when there are several sequences, else
+    # along the tokens (each half one contiguous range)
+    ax = 0 if x.shape[0] > 1 else 1
+    half = x.shape[ax] // 2
 
     def e2e_steps(n):
         done = [None, None]  # compute of the step that last used buffer 0 / 1
@@ -311,8 +341,11 @@ def run_ours(args, rank, world, local):
                 with torch.cuda.stream(cs):
                     if done[j] is not None:
                         cs.wait_event(done[j])
-                    sl = slice(0, half) if part == 0 else slice(half, x.shape[1])
-                    x_dev[j][:, sl].copy_(x_host[:, sl], non_blocking=True)
+                    sl = slice(0, half) if part == 0 else slice(half, x.shape[ax])
+                    if ax == 0:
+                        x_dev[j][sl].copy_(x_host[sl], non_blocking=True)
+                    else:
+                        x_dev[j][:, sl].copy_(x_host[:, sl], non_blocking=True)
                     ev = torch.cuda.Event()
                     ev.record(cs)
                     copied.append(ev)
@@ -320,7 +353,7 @@ def run_ours(args, rank, world, local):
                 stream.wait_event(ev)
             if outs_done[j] is not None:
                 stream.wait_event(outs_done[j])
-            comp.prefill(x_dev[j], out=outs2[j], prequant=False)
+            comp.prefill(x_dev[j], out=outs2[j], prequant=False, start_pos=start_pos)
             ev = torch.cuda.Event()
             ev.record(stream)
             done[j] = ev
@@ -346,32 +379,48 @@ def run_ours(args, rank, world, local):
     e2e_ms = max_over_ranks(e2e_ev[0].elapsed_time(e2e_ev[1]), world, device) / K
     h2d = x.numel() * 2
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    return e2e_ms, h2d, d2h
 
-    line = {"metric": METRIC, "value": value, "unit": "entries/s", "n_gpus": world, "steps": K,
-            "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": N, "entries_per_step": entries,
-                       "l2": "flushed between timed iterations (2x L2 buffer written)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "tokens_per_s": tokens_s, "kernel_ms": kms, "roofline": roof,
-            "e2e": {"value": entries / (e2e_ms * 1e-3), "unit": "entries/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches, "clocks": clk}
-    comp.close()
-    line["chunked_prefill"] = bench_chunked(args, torch, csa, synthetic, device, peaks, world)
-    line["other_prefill"] = [bench_prefill_workload(args, torch, csa, synthetic, device, peaks, world, wl)
-                             for wl in (synthetic.HCA, synthetic.INDEXER, synthetic.PAIRS)]
-    line["other_prefill"].append(bench_prefill_workload(args, torch, csa, synthetic, device, peaks, world,
-                                                        synthetic.FLASH_CSA, gate_bias=True))
-    if not args.no_decode:
-        line["decode"] = bench_decode(args, torch, csa, synthetic, device, peaks, world, rank)
-    return line
+
+def time_prefill(torch, comp, x, out, K, stream, flush, world, device, start_pos=0):
+    """K prefill calls, each bracketed by CUDA events on the launching stream (ms per call, max over
+    ranks) and by the library's events around its projection kernel (ms, mean); a buffer of twice the
+    L2 is written between calls."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b_ in kev:  # torch creates an event on its first record; the library re-records it
+        a.record(stream)
+        b_.record(stream)
+    launches0 = comp.kernel_launches()
+    hold_gpu(flush)
+    for i in range(K):
+        flush.fill_(float(i))
+        comp.set_profile_events(*kev[i])
+        ev[i][0].record(stream)
+        comp.prefill(x, out=out, prequant=False, start_pos=start_pos)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    comp.set_profile_events(None, None)
+    ms = max_over_ranks(sum(a.elapsed_time(b_) for a, b_ in ev), world, device) / K
+    kms = statistics.mean(a.elapsed_time(b_) for a, b_ in kev)
+    return ms, kms, comp.kernel_launches() - launches0
+
+
+def prefill_line(name, comp, layer, B, N, G, ms, kms, world, peaks):
+    flops = 2.0 * B * N * layer.dim * 2 * layer.width
+    achieved = flops / (kms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"] / 3.0
+    return {"workload": name, "value": B * G * world / (ms * 1e-3), "unit": "entries/s", "ms_per_step": ms,
+            "tokens_per_s": B * N * world / (ms * 1e-3), "kernel_ms": kms, "tensor_cores": comp.uses_tensor_cores(),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak}}
 
 
 def bench_prefill_workload(args, torch, csa, synthetic, device, peaks, world, wl, gate_bias=False):
     """Prefill throughput of another compressor instance of the model (same kernels): the HCA
     layer (ratio 128), the indexer's 128-wide compressor, the ratio-2 layers; or of the Flash CSA
-    layer with a gate positional bias set (random, std 1)."""
+    layer with a gate positional bias set (random, std 1).  With an end-to-end figure through host
+    buffers and the oracle on the host cores beside it."""
     layer = wl.layers[0]
     B, N = wl.batch, wl.tokens[0]
     G = N // layer.ratio
@@ -388,32 +437,75 @@ def bench_prefill_workload(args, torch, csa, synthetic, device, peaks, world, wl
         comp.prefill(x, out=out, prequant=False)
     torch.cuda.synchronize()
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    for a, b_ in kev:
-        a.record(stream)
-        b_.record(stream)
-    hold_gpu(flush)
-    for i in range(K):
-        flush.fill_(float(i))
-        comp.set_profile_events(*kev[i])
-        ev[i][0].record(stream)
-        comp.prefill(x, out=out, prequant=False)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    comp.set_profile_events(None, None)
-    ms = max_over_ranks(sum(a.elapsed_time(b_) for a, b_ in ev), world, device) / K
-    kms = statistics.mean(a.elapsed_time(b_) for a, b_ in kev)
-    flops = 2.0 * B * N * layer.dim * 2 * layer.width
-    achieved = flops / (kms * 1e-3) / 1e12
-    peak = peaks["bf16_tflops"] / 3.0
-    tc = comp.uses_tensor_cores()
-    comp.close()
+    ms, kms, _ = time_prefill(torch, comp, x, out, K, stream, flush, world, device)
     name = wl.name + (", gate positional bias set" if gate_bias else "")
-    return {"workload": name, "value": B * G * world / (ms * 1e-3), "unit": "entries/s", "ms_per_step": ms,
-            "tokens_per_s": B * N * world / (ms * 1e-3), "kernel_ms": kms, "tensor_cores": bool(tc),
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak}}
+    line = prefill_line(name, comp, layer, B, N, G, ms, kms, world, peaks)
+    e2e_ms, h2d, d2h = measure_e2e(torch, comp, x, out, B * G, min(K, 5), stream, world, device)
+    line["e2e"] = {"value": B * G * world / (e2e_ms * 1e-3), "unit": "entries/s", "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h}
+    comp.close()
+    if not args.no_cpu_baseline and not gate_bias:
+        line["cpu_baseline"] = oracle_prefill_baseline(layer, wl.seed, B, N, min(N, 16 * 128 if layer.ratio == 128
+                                                                                 else 2048))
+    return line
+
+
+def bench_long(args, torch, csa, synthetic, device, peaks, world):
+    """The long-context prefill sweep: one sequence of 16384, 65536 and 131072 tokens through the
+    ratio-4 overlapped (Flash CSA) and the ratio-128 (HCA) compressors, and a batch of 8 sequences of
+    8192 tokens; 1% of the tokens are outliers (x20).  Each line times the prefill call (the inputs
+    are larger than L2, which is also flushed between calls) with the oracle's per-token time on the
+    host cores beside it (a prefix of 2048 tokens, extrapolated)."""
+    wl = synthetic.LONG
+    lines = []
+    props = torch.cuda.get_device_properties(device)
+    flush = torch.empty(int(2 * getattr(props, "L2_cache_size", 128 << 20)) // 4 + 1, dtype=torch.float32,
+                        device=device)
+    stream = torch.cuda.current_stream(device)
+    cases = [(1, n) for n in wl.tokens] + [wl.extra["batched"]]
+    cpu = {}
+    comps = []
+    for layer in wl.layers:
+        comp = csa.Compressor(layer.dim, layer.head_dim, layer.ratio, layer.overlap, max_batch=8,
+                              rope_dim=layer.rope_dim, fp4=layer.fp4)
+        wkv, wgate, gain = synthetic.weights(wl.seed, layer)
+        comp.set_weights(torch.from_numpy(wkv).to(device), torch.from_numpy(wgate).to(device),
+                         torch.from_numpy(gain).to(device))
+        comps.append(comp)
+    for B, N in cases:
+        # the tokens depend on the sequence and position only: one input serves both compressors
+        x = torch.from_numpy(np.stack([synthetic.tokens(wl.seed, b, 0, N, wl.layers[0].dim, wl.outlier_frac,
+                                                        wl.outlier_scale) for b in range(B)])) \
+            .to(torch.bfloat16).to(device)
+        for layer, comp in zip(wl.layers, comps):
+            G = N // layer.ratio
+            out = comp._alloc_out(B * G, device, prequant=False)
+            for _ in range(3):
+                comp.prefill(x, out=out, prequant=False)
+            torch.cuda.synchronize()
+            K = max(3, min(args.steps, 10 if B * N <= 65536 else 5))
+            ms, kms, _ = time_prefill(torch, comp, x, out, K, stream, flush, world, device)
+            name = (f"long-context prefill: B={B} N={N} dim={layer.dim} ratio={layer.ratio}"
+                    f"{' overlapped' if layer.overlap else ''}, 1% outlier tokens x20")
+            line = prefill_line(name, comp, layer, B, N, G, ms, kms, world, peaks)
+            line["steps"] = K
+            if not args.no_cpu_baseline:
+                key = layer.ratio
+                if key not in cpu:
+                    cpu[key] = oracle_prefill_rate(layer, wl.seed, 2048, outlier_frac=wl.outlier_frac)
+                dt, n = cpu[key]
+                t_all = dt * (B * N) / 2048
+                line["cpu_baseline"] = {"value": B * G / t_all, "unit": "entries/s", "cores": n, "kind": "oracle",
+                                        "tokens_per_s": B * N / t_all, "extrapolated": True,
+                                        "sample": f"prefill of a 2048-token prefix of sequence 0 "
+                                                  f"({2048 // layer.ratio} entries), {dt:.2f} s on {n} threads, "
+                                                  f"per-token time scaled to {B} x {N} tokens"}
+            lines.append(line)
+            del out
+        del x
+    for comp in comps:
+        comp.close()
+    return lines
 
 
 def bench_chunked(args, torch, csa, synthetic, device, peaks, world):
@@ -561,7 +653,9 @@ def bench_decode(args, torch, csa, synthetic, device, peaks, world, rank):
     for pair in layers:
         for c, _ in pair:
             c.close()
+    cpu = None if args.no_cpu_baseline or rank != 0 else oracle_decode_baseline(wl.seed)
     return {"steps_per_s": world / (ms * 1e-3) * 1.0, "ms_per_step": ms, "batch": B, "layers_rotated": n_layers,
+            "cpu_baseline": cpu,
             "launch": "cuda graph" if graph is not None else "eager",
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"],
@@ -570,6 +664,68 @@ def bench_decode(args, torch, csa, synthetic, device, peaks, world, rank):
 
 
 # ---------------------------------------------------------------------------------------------
+# The CPU oracle as it stands, timed on the host cores (a reported baseline, not a target).
+
+def oracle_prefill_rate(layer, seed, ntok, nthreads=None, outlier_frac=0.0):
+    """Seconds the oracle takes for a prefill of the first `ntok` tokens of sequence 0 of a workload
+    (a prefix of whole groups), and the threads it used."""
+    import torch
+
+    import oracle
+    import synthetic
+    x = synthetic.tokens(seed, 0, 0, ntok, layer.dim, outlier_frac)
+    xb = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)[None]
+    wkv, wgate, gain = synthetic.weights(seed, layer)
+    o = oracle.Compressor(layer.dim, layer.head_dim, layer.ratio, layer.overlap, rope_dim=layer.rope_dim,
+                          fp4=layer.fp4)
+    o.set_weights(wkv, wgate, gain)
+    n = nthreads or oracle.default_threads()
+    t0 = time.perf_counter()
+    o.prefill(xb, nthreads=n)
+    return time.perf_counter() - t0, n
+
+
+def oracle_prefill_baseline(layer, seed, B, N, prefix, outlier_frac=0.0):
+    """cpu_baseline of a prefill workload of B sequences of N tokens from a prefix of `prefix` tokens
+    (whole groups) of one sequence: the oracle's per-token time, extrapolated to the workload."""
+    dt, n = oracle_prefill_rate(layer, seed, prefix, outlier_frac=outlier_frac)
+    G = N // layer.ratio
+    t_all = dt * (B * N) / prefix
+    return {"value": B * G / t_all, "unit": "entries/s", "cores": n, "kind": "oracle",
+            "tokens_per_s": B * N / t_all, "extrapolated": prefix < B * N,
+            "sample": f"prefill of a {prefix}-token prefix of one sequence ({prefix // layer.ratio} entries), "
+                      f"{dt:.2f} s on {n} threads, per-token time scaled to {B} x {N} tokens"}
+
+
+def oracle_decode_baseline(seed, steps=2):
+    """cpu_baseline of the batched decode workload: whole steps (128 sequences through both
+    compressors) of the oracle at the workload's positions.  The oracle starts from a fresh state:
+    the work of a step does not depend on the state's values."""
+    import torch
+
+    import oracle
+    import synthetic
+    wl = synthetic.DECODE
+    B = wl.batch
+    sp0 = synthetic.start_positions(wl.seed, B, wl.start_pos_hi)
+    comps = []
+    for L in wl.layers:
+        wkv, wgate, gain = synthetic.weights(wl.seed, L)
+        o = oracle.Compressor(L.dim, L.head_dim, L.ratio, L.overlap, max_batch=B, rope_dim=L.rope_dim, fp4=L.fp4)
+        o.set_weights(wkv, wgate, gain)
+        comps.append(o)
+    n = oracle.default_threads()
+    xs = [torch.from_numpy(np.stack([synthetic.tokens(wl.seed, b, int(sp0[b]) + k, int(sp0[b]) + k + 1,
+                                                      wl.layers[0].dim)[0] for b in range(B)]))
+          .to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16) for k in range(steps)]
+    t0 = time.perf_counter()
+    for k in range(steps):
+        for o in comps:
+            o.decode(xs[k], (sp0 + k).astype(np.int32), nthreads=n)
+    dt = time.perf_counter() - t0
+    return {"value": steps / dt, "unit": "steps/s", "cores": n, "kind": "oracle",
+            "sample": f"{steps} whole steps (B={B}, both compressors), {dt:.2f} s on {n} threads"}
+
 
 class OracleArm:
     """The CPU oracle, as it stands, on the Flash CSA prefill workload: one step is the whole
@@ -601,6 +757,16 @@ def oracle_sample():
     g, dt = arm.step()
     return {"value": g / dt, "unit": "entries/s", "cores": arm.cores, "kind": "oracle",
             "sample": f"the whole workload: {g} entries ({arm.N} tokens), {dt:.2f} s on {arm.cores} threads"}
+
+
+def oracle_single_thread():
+    """The same oracle on one host thread, on a 256-token prefix of the Flash CSA workload."""
+    import synthetic
+    wl = synthetic.FLASH_CSA
+    layer = wl.layers[0]
+    dt, n = oracle_prefill_rate(layer, wl.seed, 256, nthreads=1)
+    return {"value": (256 // layer.ratio) / dt, "unit": "entries/s", "cores": 1, "kind": "oracle",
+            "sample": f"prefill of a 256-token prefix (64 entries) of the Flash CSA workload, {dt:.2f} s on 1 thread"}
 
 
 def run_reference(args, rank, world):
@@ -654,6 +820,7 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = oracle_sample()
+            line["cpu_baseline_single_thread"] = oracle_single_thread()
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
