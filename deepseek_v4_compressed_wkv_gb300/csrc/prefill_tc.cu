@@ -495,11 +495,19 @@ int owned_tokens(const csa_compressor* c, int tok) {
   return c->overlap ? tok - 4 : (tok / c->ratio) * c->ratio;
 }
 
-// The token tile of a launch: the one whose grid takes the fewest waves x tile tokens (one CTA
-// per SM), the larger on a tie.  At the Flash CSA shape the 224-token tile makes 16 x 19 = 304
-// CTAs, exactly two waves of 152 SMs, where 256 makes 272 (1.79 waves, the second wave a CTA
-// of 256 tokens per SM); the indexer's 128-wide compressor (4 packed tiles) takes the 128-token
-// tile, 4 x 34 = 136 CTAs in one wave instead of 76 CTAs of 224 tokens.
+// The token tile of a launch: the one whose grid takes the least time, counted as waves (one CTA
+// per SM) x the time of a K stage, which the shared-memory traffic of a stage bounds (the MMAs read
+// the 8 KB weight-plane tile and the token tile once per plane and K half, the copies write 24 KB
+// of planes and the token tile: 640 / 832 / 896 cycles at 128 bytes per cycle for tiles of 128 /
+// 224 / 256 tokens, against 384 / 672 / 768 cycles of MMA); the larger tile on a tie.  At the Flash
+// CSA shape the 224-token tile makes 16 x 19 = 304 CTAs, exactly two waves of 152 SMs; the
+// indexer's 128-wide compressor (4 packed tiles) takes the 128-token tile, one wave of 136 CTAs;
+// one long sequence through the ratio-128 compressor takes the 256-token tile.
+long long stage_cycles(int tok) {
+  const long long x_bytes = 64LL * tok;  // a token tile of K = 32 bf16
+  return (6 * (4096 + x_bytes) + 3 * 8192 + x_bytes) / 128;
+}
+
 int prefill_tok(const csa_compressor* c, int B, int N) {
   const int sms = current_sm_count();
   int best = tc::kTokMax;
@@ -508,7 +516,7 @@ int prefill_tok(const csa_compressor* c, int B, int N) {
     const int T = owned_tokens(c, tok);
     if (T < 1) continue;
     const long long ctas = (long long)c->pk.ntiles * ((N + T - 1) / T) * B;
-    const long long cost = (ctas + sms - 1) / sms * tok;
+    const long long cost = (ctas + sms - 1) / sms * stage_cycles(tok);
     if (best_cost < 0 || cost < best_cost) {
       best = tok;
       best_cost = cost;
