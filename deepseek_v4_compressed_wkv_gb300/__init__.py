@@ -47,7 +47,7 @@ class Options(ctypes.Structure):
     _fields_ = [("max_batch", ctypes.c_int), ("rope_dim", ctypes.c_int), ("rope_base", ctypes.c_float),
                 ("rope_factor", ctypes.c_float), ("rope_orig_len", ctypes.c_int), ("beta_fast", ctypes.c_float),
                 ("beta_slow", ctypes.c_float), ("max_pos", ctypes.c_int), ("fp4", ctypes.c_int),
-                ("eps", ctypes.c_float)]
+                ("eps", ctypes.c_float), ("prefill_split", ctypes.c_int)]
 
 
 class Out(ctypes.Structure):

@@ -92,6 +92,7 @@ bool check_options(const csa_options& o, int H, std::string& why) {
     why = buf;
   }
   else if (!(o.eps >= 0.0f)) why = "eps must be >= 0";
+  else if (o.prefill_split < 0 || o.prefill_split > 2) why = "prefill_split must be 0 (chosen per call), 1 or 2";
   else return true;
   return false;
 }
@@ -281,6 +282,7 @@ void csa_options_default(csa_options* o) {
   o->max_pos = 262144;
   o->fp4 = 1;
   o->eps = 1e-6f;
+  o->prefill_split = 0;
 }
 
 const char* csa_last_error(void) { return g_last_error.c_str(); }

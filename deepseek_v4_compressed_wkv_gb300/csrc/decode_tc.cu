@@ -84,7 +84,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     decode_proj_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_p,
                        const ProjParams P) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // 1 KB aligned (the swizzled tiles), offset from the shared array itself so that the compiler
+  // keeps the accesses through it in the shared state space
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = (uint64_t*)(smem + kRingBytes);
   uint64_t* empty = full + kStages;
   uint64_t* c_full = empty + kStages;

@@ -28,11 +28,12 @@ cudaError_t launch_fp4_e8m0_roundtrip(const uint16_t* in, long long nb, uint8_t*
 // Tensor-core prefill (prefill_tc.cu): projection + pool + norm + RoPE + fp4 + state update.
 bool prefill_tc_supported(const csa_compressor* c, const void* x);
 // The launch geometry of one call, fixed once so that the scratch it is given and the launch
-// agree: the token tile and the scratch bytes it needs (the pooled values [B][token tiles]
-// [groups per tile][H] bf16 and, for a chunk whose first group has earlier candidates, their
+// agree: the token tile, the K split and the scratch bytes it needs (the pooled values [B][token
+// tiles][groups per tile][H] bf16 and, for a chunk whose first group has earlier candidates, their
 // running softmax values [B][1 + overlap][3][H] f32 after them).
 struct PrefillPlan {
   int tok;       // token tile: 256, 224 or 128
+  int split;     // 1: one CTA per tile; 2: a cluster of two CTAs per tile, each half of K
   size_t bytes;  // scratch bytes
 };
 PrefillPlan prefill_tc_plan(const csa_compressor* c, int B, int N, const Chunk& ck);

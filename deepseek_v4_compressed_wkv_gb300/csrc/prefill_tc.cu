@@ -63,7 +63,11 @@ struct Tile {
   static_assert(TOK == 256 || TOK == 224 || TOK == 128, "token tile");
   static constexpr int kXBytes = TOK * kKb * 2;                  // 16 / 14 / 8 KB
   static constexpr int kStageBytes = 3 * kPlaneBytes + kXBytes;  // 40 / 38 / 32 KB (multiples of 1 KB)
-  static constexpr int kSmemStride = TOK + 1;                    // f32 staging row stride (bank-conflict free)
+  // f32 staging row stride: a multiple of 4 floats, so that the epilogue moves 16-byte vectors,
+  // and an odd number of 16-byte units, so that the vectors of 8 consecutive rows (a quarter-warp)
+  // fall in distinct banks
+  static constexpr int kSmemStride = TOK + 4;
+  static_assert(kSmemStride % 8 == 4, "16-byte rows, odd in 16-byte units");
   static_assert(kRows * kSmemStride * 4 <= kStages * kStageBytes, "staging must fit in the stage buffers");
   static_assert(kStageBytes % 1024 == 0, "stages keep the 1 KB alignment of the swizzled tiles");
 };
@@ -96,30 +100,43 @@ struct EntryParams {
   int* flag;
 };
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
 // ---- the kernel ----------------------------------------------------------------------------
+//
+// kSplit = 2 (a cluster of two CTAs per tile, the narrow compressors' grid): CTA r of the cluster
+// runs the K blocks [r K / 2, (r + 1) K / 2) and owns features [r F / 2, (r + 1) F / 2) of the
+// tile (F features per kind).  Each CTA stages its partial sums, copies the rows of the other
+// CTA's features into that CTA's shared memory (a bulk copy between the two CTAs), adds the
+// received half-K sums to its own (the lower K half first) and pools its features: a tile of
+// 128 x TOK outputs is then computed at the wide token tile by twice the CTAs.
 
-template <int kTok>
+template <int kTok, int kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap map_x, const Params P) {
+  static_assert(kSplit == 1 || kSplit == 2, "K split");
   constexpr int kStageBytes = Tile<kTok>::kStageBytes;
   constexpr int kSmemStride = Tile<kTok>::kSmemStride;
+  constexpr int kRecvRows = kSplit > 1 ? kRows / kSplit : 0;  // rows received from the other CTA
+  static_assert((kRows + kRecvRows) * kSmemStride * 4 <= kStages * kStageBytes,
+                "the staged and the received sums fit in the stage buffers");
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // 1 KB aligned (the swizzled tiles), offset from the shared array itself so that the compiler
+  // keeps the accesses through it in the shared state space
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = (uint64_t*)(smem + kStages * kStageBytes);
   uint64_t* empty = full + kStages;
   uint64_t* chunk_full = empty + kStages;  // [2]: chunk accumulator ready for the epilogue
   uint64_t* chunk_empty = chunk_full + 2;  // [2]: chunk accumulator drained, free for the MMAs
   uint64_t* mma_done = chunk_empty + 2;    // clean-up after an abort: the issued MMAs have completed
-  uint32_t* tmem_slot = (uint32_t*)(mma_done + 1);
+  uint64_t* recv_bar = mma_done + 1;       // kSplit 2: the other CTA's sums of this CTA's rows landed
+  uint32_t* tmem_slot = (uint32_t*)(recv_bar + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   int* issued_s = (int*)(tmem_slot + 2);  // stages the producer issued (read by the clean-up)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ftile = blockIdx.x, tt = blockIdx.y, b = blockIdx.z;
-  const int nkb = P.K / kKb;
-  const int nch = (nkb + kChunkKb - 1) / kChunkKb;
+  const int ftile = blockIdx.x / kSplit, rank = blockIdx.x % kSplit, tt = blockIdx.y, b = blockIdx.z;
+  const int nloc = P.K / kKb / kSplit;  // K blocks of this CTA: kb0 .. kb0 + nloc - 1
+  const int kb0 = rank * nloc;
+  const int nch = (nloc + kChunkKb - 1) / kChunkKb;
   const int t0 = tt * P.T - P.halo;  // virtual index (from the open group's start) of the tile's token 0
 #ifdef CSA_DEBUG_BOUNDS
   const uint64_t kWait = P.wait_ns;  // the time-out test shortens the waits
@@ -137,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&chunk_empty[i], kEpiThreads / 32);
     }
     mbar_init(mma_done, 1);
+    mbar_init(recv_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_map(&map_x);
@@ -148,15 +166,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+
   if (warp == 0) {
     // ---- producer: one x tile and three weight-plane tiles per stage
     if (lane == 0) {
       int issued = 0;
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kStages;
-        if (kb >= kStages && !mbar_wait(&empty[s], ((kb / kStages) & 1) ^ 1, abort_flag, kWait)) break;
+      for (int i = 0; i < nloc; ++i) {
+        const int s = i % kStages, kb = kb0 + i;
+        if (i >= kStages && !mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1, abort_flag, kWait)) break;
 #ifdef CSA_DEBUG_BOUNDS
-        if (P.test_stall && kb == nkb - 1) break;  // test of the time-out path: the last stage never comes
+        if (P.test_stall && i == nloc - 1) break;  // test of the time-out path: the last stage never comes
 #endif
         uint8_t* st = smem + s * kStageBytes;
         mbar_arrive_expect_tx(&full[s], kStageBytes);
@@ -176,10 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c >= 2 && !mbar_wait(&chunk_empty[buf], ((c >> 1) - 1) & 1, abort_flag, kWait)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * kTok);
-        const int kb0 = c * kChunkKb, kb1 = min(nkb, kb0 + kChunkKb);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          const int s = kb % kStages;
-          if (!mbar_wait(&full[s], (kb / kStages) & 1, abort_flag, kWait)) {
+        const int i0 = c * kChunkKb, i1 = min(nloc, i0 + kChunkKb);
+        for (int i = i0; i < i1; ++i) {
+          const int s = i % kStages;
+          if (!mbar_wait(&full[s], (i / kStages) & 1, abort_flag, kWait)) {
             ok = false;
             break;
           }
@@ -189,16 +208,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int p = 0; p < 3; ++p)
             for (int k = 0; k < kKb / 16; ++k)
               mma_bf16(d, sw64_desc(st + p * kPlaneBytes + k * 32), sw64_desc(xs + k * 32), idesc,
-                       (kb != kb0 || p != 0 || k != 0) ? 1u : 0u);
+                       (i != i0 || p != 0 || k != 0) ? 1u : 0u);
           mma_commit(&empty[s]);
         }
         if (ok) mma_commit(&chunk_full[buf]);  // arrives once this chunk's MMAs have completed
       }
     }
   } else {
-    // ---- epilogue (warps 2..9; warp w reads TMEM lanes 32*(w%4) .. +31, columns 128*h .. up to
-    //      128 columns)
-    const int et = threadIdx.x - 64;  // 0..255
+    // ---- epilogue (warps 2..9; warp w reads TMEM lanes 32*(w%4) .. +31, its packed row, and
+    //      columns 128*h .. up to 128 columns): the chunk accumulators into registers in chunk
+    //      order, then staged as [packed row][token] f32 in the stage buffers (idle once the last
+    //      chunk has completed)
     const int q = warp & 3, h = (warp - 2) >> 2;
     const int row = 32 * q + lane;
     const int hcols = h ? kTok - 128 : 128;  // a multiple of 32 (0: the 128-token tile's second half idles)
@@ -227,143 +247,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&chunk_empty[buf]);
     }
-    const bool have_acc = ok && !*abort_flag;
-    if (have_acc) {
-      // a chunk's carry kernel (the grid this launch may overlap) has finished reading the state
-      // and written the carried values; a no-op for a launch without that predecessor
-      griddep_wait();
+    if (ok && !*abort_flag) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      // the prefill rewrites the sequence's state: its decode running values (kept per packed
-      // tile) are no longer valid
-      if (tt == 0 && et == 0) P.acc_pos[(size_t)(P.slot_offset + b) * P.pk.ntiles + ftile] = -1;
-      if (P.ape && row / P.pk.ft >= P.pk.nk / 2) {
-        // wgate(x) + the positional bias of each token's place in its group (score rows only),
-        // added in registers before staging, the loads independent of one another: column c
-        // holds the token at position ratio * g0 + t0 + c (halo columns wrap harmlessly)
-        const float* ab = P.ape + ftile * kRows + row;
-        const int r = P.ratio;
-        int sl = ((P.ratio * P.g0 + t0 + 128 * h) % r + r) % r;
+      float* stg = (float*)smem;
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          if (i < hcols) acc[i] += __ldg(ab + (size_t)sl * P.ncol);
-          sl = sl + 1 == r ? 0 : sl + 1;
-        }
-      }
-      float* stg = (float*)smem;  // [128 packed rows][kSmemStride] f32, reuses the stage buffers
-#pragma unroll
-      for (int i = 0; i < 128; ++i)
-        if (i < hcols) stg[row * kSmemStride + 128 * h + i] = acc[i];
-      epi_sync();
-
-      const Packing& pk = P.pk;
-      const int F = pk.ft, r = P.ratio, G = P.G;
-      const int col0 = ftile * kRows;  // first packed column of this tile
-      // -- state: the new tokens (virtual index >= a) of the unfinished group and, overlapped,
-      //    of the last complete group that this tile owns; thread et < 128 writes packed
-      //    column col0 + et.  Virtual group G is absolute group gend.
-      if (et < kRows) {
-        const size_t st0 = (size_t)(P.slot_offset + b) * P.slots * P.ncol + col0 + et;
-        float* st = P.state + st0;
-        const int own0 = max(tt * P.T, P.a), own1 = min(tt * P.T + P.T, P.a + P.N);
-        auto put = [&](int tok, int slot) {
-          if (in_bounds((long long)(st0 + (size_t)slot * P.ncol), P.state_elems, P.flag))
-            st[(size_t)slot * P.ncol] = stg[et * kSmemStride + (tok - t0)];
-        };
-        if (!P.overlap) {
-          for (int tok = max(own0, r * G); tok < own1; ++tok) put(tok, tok - r * G);
-        } else {
-          const int qp = P.gend & 1;
-          for (int tok = max(own0, 4 * G); tok < own1; ++tok) put(tok, 4 * qp + tok - 4 * G);
-          if (G >= 1)
-            for (int tok = max(own0, 4 * G - 4); tok < min(own1, 4 * G); ++tok)
-              put(tok, 4 * (1 - qp) + tok - (4 * G - 4));
-          if (P.gend == 0 && tt == 0) {
-            const int kind = et / F;  // padded previous branch: kv 0, score -inf
-            const float pad = kind < pk.nk / 2 ? 0.0f : -INFINITY;
-            for (int i = 0; i < 4; ++i)
-              if (in_bounds((long long)(st0 + (size_t)(4 + i) * P.ncol), P.state_elems, P.flag))
-                st[(size_t)(4 + i) * P.ncol] = pad;
-          }
-        }
-      }
-      // -- pool every (feature, group) pair of the tile into bf16 scratch
-      uint16_t* pooled_tile = P.pooled + ((size_t)b * P.ntt + tt) * P.GT * pk.H;
-      for (int pr = et; pr < P.GT * F; pr += kEpiThreads) {
-        const int f = pr % F, g = pr / F;
-        const int j = tt * P.GT + g;
-        if (j >= G) break;  // pairs are visited in group order
-        float m = -INFINITY, den = 0.0f, num = 0.0f;
-        if (P.carry && j < 1 + P.overlap) {
-          // the chunk's first groups hold tokens earlier than the chunk (virtual index < a, or the
-          // halo): those arrive as running values; the rest are this tile's columns.  Group 0:
-          // branch A of tokens a..3 (non-overlapped: tokens a..ratio-1); overlapped group 1:
-          // branch B of tokens a..3 and branch A of tokens 4..7.
-          const float* cr = P.carry + ((size_t)b * (1 + P.overlap) + j) * 3 * pk.H + ftile * F + f;
-          const float mc = cr[0], dc = cr[pk.H], nc = cr[2 * pk.H];  // max, denominator, numerator
-          const int kk = P.overlap ? (KV_A * F + f) : (KV * F + f), ks = P.overlap ? (S_A * F + f) : (S * F + f);
-          const float* kv = stg + kk * kSmemStride + P.halo + 4 * j;
-          const float* sc = stg + ks * kSmemStride + P.halo + 4 * j;
-          const float* kB = stg + (KV_B * F + f) * kSmemStride + P.halo;
-          const float* sB = stg + (S_B * F + f) * kSmemStride + P.halo;
-          const int n = P.overlap ? 4 : r, i0 = j == 0 ? P.a : 0, iB = j == 1 ? P.a : 4;
-          m = mc;
-          for (int i = i0; i < n; ++i) m = fmaxf(m, sc[i]);
-          for (int i = iB; i < 4; ++i) m = fmaxf(m, sB[i]);
-          const float rs = expf(mc - m);  // 0 when nothing was carried (mc = -inf)
-          den = dc * rs;
-          num = nc * rs;
-          for (int i = iB; i < 4; ++i) {
-            const float e = expf(sB[i] - m);
-            den += e;
-            num = fmaf(e, kB[i], num);
-          }
-          for (int i = i0; i < n; ++i) {
-            const float e = expf(sc[i] - m);
-            den += e;
-            num = fmaf(e, kv[i], num);
-          }
-        } else if (P.overlap) {
-          const float* kA = stg + (KV_A * F + f) * kSmemStride + 4 * g + 4;
-          const float* sA = stg + (S_A * F + f) * kSmemStride + 4 * g + 4;
-          const float* kB = stg + (KV_B * F + f) * kSmemStride + 4 * g;
-          const float* sB = stg + (S_B * F + f) * kSmemStride + 4 * g;
-          const bool padB = P.g0 + j == 0;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            m = fmaxf(m, sA[i]);
-            if (!padB) m = fmaxf(m, sB[i]);
-          }
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float ea = expf(sA[i] - m);
-            den += ea;
-            num = fmaf(ea, kA[i], num);
-            if (!padB) {
-              const float eb = expf(sB[i] - m);
-              den += eb;
-              num = fmaf(eb, kB[i], num);
-            }
-          }
-        } else {
-          const float* kv = stg + (KV * F + f) * kSmemStride + r * g;
-          const float* sc = stg + (S * F + f) * kSmemStride + r * g;
-          for (int i = 0; i < r; ++i) m = fmaxf(m, sc[i]);
-          for (int i = 0; i < r; ++i) {
-            const float e = expf(sc[i] - m);
-            den += e;
-            num = fmaf(e, kv[i], num);
-          }
-        }
-        const size_t pi = (size_t)g * pk.H + ftile * F + f;
-        if (in_bounds((long long)((pooled_tile - P.pooled) + pi), P.pooled_elems, P.flag))
-          pooled_tile[pi] = bf16_bits(__fdiv_rn(num, den));
-      }
+      for (int i = 0; i < 128; i += 4)
+        if (i < hcols)
+          *reinterpret_cast<float4*>(stg + row * kSmemStride + 128 * h + i) =
+              make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
     }
   }
 
   tc_fence_before();
   __syncthreads();  // every role has left its loop; the flag no longer changes
-  if (*abort_flag) {
+  const bool aborted = *abort_flag != 0;
+  if (aborted) {
     // a wait ran out: the copies in flight land and the issued MMAs complete before the TMEM is
     // freed and the CTA leaves (this call's outputs are undefined; the flag says so)
     drain_after_abort(warp == 0 && lane == 0, warp == 1 && lane == 0, full, kStages, *issued_s, mma_done);
@@ -374,6 +272,220 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+
+  // ---- the pool, by all warps
+  const Packing& pk = P.pk;
+  const int F = pk.ft, hf = F / kSplit, f0 = rank * hf;  // this CTA's features of the tile
+  float* stg = (float*)smem;
+  if (!aborted) {
+    // a chunk's carry kernel (the grid this launch may overlap) has finished reading the state
+    // and written the carried values; a no-op for a launch without that predecessor
+    griddep_wait();
+    // the prefill rewrites the sequence's state: its decode running values (kept per packed
+    // tile) are no longer valid
+    if (rank == 0 && tt == 0 && threadIdx.x == 0) P.acc_pos[(size_t)(P.slot_offset + b) * pk.ntiles + ftile] = -1;
+  }
+  bool lost = false;  // the other CTA's sums never arrived
+  if constexpr (kSplit > 1) {
+    // the rows of the other CTA's features go to its shared memory (kind k's rows in a block of
+    // hf rows), its sums of this CTA's rows come back into `recv`; every CTA takes part whatever
+    // its state, so that neither waits on a barrier the other never reaches
+    constexpr uint32_t kRunBytesPerRow = kSmemStride * 4;
+    float* recv = stg + kRows * kSmemStride;
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(recv_bar, (uint32_t)(pk.nk * hf) * kRunBytesPerRow);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the staged sums, for the copy
+    cluster_arrive();
+    cluster_wait();  // both CTAs have staged their sums; neither uses its stage buffers any more
+    if (threadIdx.x == 0) {
+      const uint32_t peer = (uint32_t)(rank ^ 1);
+      const uint32_t peer_bar = cluster_map(recv_bar, peer);
+      for (int k = 0; k < pk.nk; ++k)
+        bulk_push_cluster(cluster_map(recv + k * hf * kSmemStride, peer),
+                          stg + (k * F + (int)peer * hf) * kSmemStride, (uint32_t)hf * kRunBytesPerRow, peer_bar);
+    }
+    lost = __syncthreads_or(!mbar_wait_bounded(recv_bar, 0, kWait));
+    if (lost && threadIdx.x == 0) atomicOr(P.flag, 4);
+  }
+  if (!aborted && !lost && (kSplit > 1 || P.ape)) {
+    // this CTA's rows: the two half-K sums added (the same sum in either order), then wgate(x) +
+    // the positional bias of each token's place in its group (score rows; column c holds the
+    // token at position ratio * g0 + t0 + c, halo columns wrap harmlessly).  Unsplit, only the
+    // score rows of a layer with the bias are visited.  Warp w takes rows w, w + 10, ..., its
+    // lanes the columns.
+    const float* recv = stg + kRows * kSmemStride;
+    const int kind0 = kSplit > 1 ? 0 : pk.nk / 2;
+    const int r = P.ratio, step = 32 % r;
+    const int sl0 = ((P.ratio * P.g0 + t0 + lane) % r + r) % r;
+    for (int rr = kind0 * hf + warp; rr < pk.nk * hf; rr += kThreads / 32) {
+      const int kind = rr / hf;
+      const int prow = kind * F + f0 + (rr - kind * hf);
+      float* srow = stg + prow * kSmemStride;
+      const float* rrow = recv + rr * kSmemStride;
+      const float* ab = P.ape && kind >= pk.nk / 2 ? P.ape + ftile * kRows + prow : nullptr;
+      // every load of the row before any store (the stores could otherwise alias the next loads)
+      constexpr int kCol = kTok / 32;
+      float v[kCol], w[kCol];
+#pragma unroll
+      for (int i = 0; i < kCol; ++i) {
+        v[i] = srow[lane + 32 * i];
+        w[i] = kSplit > 1 ? rrow[lane + 32 * i] : 0.0f;
+      }
+      if (ab) {
+        int sl = sl0;
+#pragma unroll
+        for (int i = 0; i < kCol; ++i) {
+          w[i] = kSplit > 1 ? v[i] + w[i] : v[i];
+          v[i] = __ldg(ab + (size_t)sl * P.ncol);
+          sl += step;
+          sl = sl >= r ? sl - r : sl;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kCol; ++i) srow[lane + 32 * i] = v[i] + w[i];
+    }
+  }
+  __syncthreads();
+
+  if (!aborted) {
+    const int r = P.ratio, G = P.G;
+    const int col0 = ftile * kRows;  // first packed column of this tile
+    // -- state: the new tokens (virtual index >= a) of the unfinished group and, overlapped,
+    //    of the last complete group that this tile owns; thread et < nk * hf writes one packed
+    //    column of this CTA's features.  Virtual group G is absolute group gend.
+    const int et = threadIdx.x;
+    if (et < pk.nk * hf) {
+      const int kind = et / hf, prow = kind * F + f0 + et % hf;
+      const size_t st0 = (size_t)(P.slot_offset + b) * P.slots * P.ncol + col0 + prow;
+      float* st = P.state + st0;
+      const float* srow = stg + prow * kSmemStride - t0;  // srow[tok]: the tile's column of token tok
+      const int own0 = max(tt * P.T, P.a), own1 = min(tt * P.T + P.T, P.a + P.N);
+      auto put = [&](int tok, int slot) {
+        if (in_bounds((long long)st0 + (long long)slot * P.ncol, P.state_elems, P.flag)) st[slot * P.ncol] = srow[tok];
+      };
+      if (!P.overlap) {
+        for (int tok = max(own0, r * G); tok < own1; ++tok) put(tok, tok - r * G);
+      } else {
+        const int qp = P.gend & 1;
+        for (int tok = max(own0, 4 * G); tok < own1; ++tok) put(tok, 4 * qp + tok - 4 * G);
+        if (G >= 1)
+          for (int tok = max(own0, 4 * G - 4); tok < min(own1, 4 * G); ++tok)
+            put(tok, 4 * (1 - qp) + tok - (4 * G - 4));
+        if (P.gend == 0 && tt == 0) {
+          const float pad = kind < pk.nk / 2 ? 0.0f : -INFINITY;  // padded previous branch: kv 0, score -inf
+          for (int i = 0; i < 4; ++i)
+            if (in_bounds((long long)st0 + (long long)(4 + i) * P.ncol, P.state_elems, P.flag)) st[(4 + i) * P.ncol] = pad;
+        }
+      }
+    }
+    // -- pool every (feature, group) pair of this CTA's features into bf16 scratch: thread t
+    //    takes feature f0 + t % hf and groups t / hf, t / hf + kThreads / hf, ... (hf divides the
+    //    320 threads: 16, 32 or 64), two groups per step whose chains are independent
+    uint16_t* pooled_tile = P.pooled + ((size_t)b * P.ntt + tt) * P.GT * pk.H;
+    const int f = f0 + (int)threadIdx.x % hf;
+    // a group all of whose candidates are this tile's columns
+    auto pool_tile = [&](int g, int j) -> float {
+      float m = -INFINITY, den = 0.0f, num = 0.0f;
+      if (P.overlap) {
+        // branch A: tokens 4g + 4 .. 4g + 7 of the tile, branch B: tokens 4g .. 4g + 3 (one
+        // 16-byte vector each)
+        const float4 a4 = *reinterpret_cast<const float4*>(stg + (KV_A * F + f) * kSmemStride + 4 * g + 4);
+        const float4 p4 = *reinterpret_cast<const float4*>(stg + (S_A * F + f) * kSmemStride + 4 * g + 4);
+        const float4 b4 = *reinterpret_cast<const float4*>(stg + (KV_B * F + f) * kSmemStride + 4 * g);
+        const float4 q4 = *reinterpret_cast<const float4*>(stg + (S_B * F + f) * kSmemStride + 4 * g);
+        const float kA[4] = {a4.x, a4.y, a4.z, a4.w}, sA[4] = {p4.x, p4.y, p4.z, p4.w};
+        const float kB[4] = {b4.x, b4.y, b4.z, b4.w}, sB[4] = {q4.x, q4.y, q4.z, q4.w};
+        const bool padB = P.g0 + j == 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          m = fmaxf(m, sA[i]);
+          if (!padB) m = fmaxf(m, sB[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float ea = expf(sA[i] - m);
+          den += ea;
+          num = fmaf(ea, kA[i], num);
+          if (!padB) {
+            const float eb = expf(sB[i] - m);
+            den += eb;
+            num = fmaf(eb, kB[i], num);
+          }
+        }
+      } else if (r % 2 == 0) {
+        // the group's ratio tokens as 8-byte pairs
+        const float2* kv = reinterpret_cast<const float2*>(stg + (KV * F + f) * kSmemStride + r * g);
+        const float2* sc = reinterpret_cast<const float2*>(stg + (S * F + f) * kSmemStride + r * g);
+        for (int i = 0; i < r / 2; ++i) m = fmaxf(m, fmaxf(sc[i].x, sc[i].y));
+        for (int i = 0; i < r / 2; ++i) {
+          const float2 s2 = sc[i], k2 = kv[i];
+          const float e0 = expf(s2.x - m), e1 = expf(s2.y - m);
+          den += e0;
+          num = fmaf(e0, k2.x, num);
+          den += e1;
+          num = fmaf(e1, k2.y, num);
+        }
+      } else {
+        const float* kv = stg + (KV * F + f) * kSmemStride + r * g;
+        const float* sc = stg + (S * F + f) * kSmemStride + r * g;
+        for (int i = 0; i < r; ++i) m = fmaxf(m, sc[i]);
+        for (int i = 0; i < r; ++i) {
+          const float e = expf(sc[i] - m);
+          den += e;
+          num = fmaf(e, kv[i], num);
+        }
+      }
+      return __fdiv_rn(num, den);
+    };
+    // a chunk's first groups hold tokens earlier than the chunk (virtual index < a, or the halo):
+    // those arrive as running values; the rest are this tile's columns.  Group 0: branch A of
+    // tokens a..3 (non-overlapped: tokens a..ratio-1); overlapped group 1: branch B of tokens
+    // a..3 and branch A of tokens 4..7.
+    auto pool_carried = [&](int j) -> float {
+      const float* cr = P.carry + ((size_t)b * (1 + P.overlap) + j) * 3 * pk.H + ftile * F + f;
+      const float mc = cr[0], dc = cr[pk.H], nc = cr[2 * pk.H];  // max, denominator, numerator
+      const int kk = P.overlap ? (KV_A * F + f) : (KV * F + f), ks = P.overlap ? (S_A * F + f) : (S * F + f);
+      const float* kv = stg + kk * kSmemStride + P.halo + 4 * j;
+      const float* sc = stg + ks * kSmemStride + P.halo + 4 * j;
+      const float* kB = stg + (KV_B * F + f) * kSmemStride + P.halo;
+      const float* sB = stg + (S_B * F + f) * kSmemStride + P.halo;
+      const int n = P.overlap ? 4 : r, i0 = j == 0 ? P.a : 0, iB = j == 1 ? P.a : 4;
+      float m = mc;
+      for (int i = i0; i < n; ++i) m = fmaxf(m, sc[i]);
+      for (int i = iB; i < 4; ++i) m = fmaxf(m, sB[i]);
+      const float rs = expf(mc - m);  // 0 when nothing was carried (mc = -inf)
+      float den = dc * rs, num = nc * rs;
+      for (int i = iB; i < 4; ++i) {
+        const float e = expf(sB[i] - m);
+        den += e;
+        num = fmaf(e, kB[i], num);
+      }
+      for (int i = i0; i < n; ++i) {
+        const float e = expf(sc[i] - m);
+        den += e;
+        num = fmaf(e, kv[i], num);
+      }
+      return __fdiv_rn(num, den);
+    };
+    auto put_pooled = [&](int g, float v) {
+      const size_t pi = (size_t)g * pk.H + ftile * F + f;
+      if (in_bounds((long long)((pooled_tile - P.pooled) + pi), P.pooled_elems, P.flag)) pooled_tile[pi] = bf16_bits(v);
+    };
+    const int gstep = kThreads / hf;
+    for (int g = (int)threadIdx.x / hf; g < P.GT; g += 2 * gstep) {
+      const int j = tt * P.GT + g;
+      if (j >= G) break;  // groups are visited in order
+      // the second group (never a carried one: gstep >= 5), or the first again when there is none
+      const bool two = g + gstep < P.GT && j + gstep < G;
+      const float v2 = two ? pool_tile(g + gstep, j + gstep) : 0.0f;
+      const float v1 = P.carry && j < 1 + P.overlap ? pool_carried(j) : pool_tile(g, j);
+      put_pooled(g, v1);
+      if (two) put_pooled(g + gstep, v2);
+    }
+  }
+  if constexpr (kSplit > 1) {
+    cluster_arrive();
+    cluster_wait();  // the other CTA has received this CTA's copy: its source may go
   }
 }
 
@@ -495,37 +607,105 @@ int owned_tokens(const csa_compressor* c, int tok) {
   return c->overlap ? tok - 4 : (tok / c->ratio) * c->ratio;
 }
 
-// The token tile of a launch: the one whose grid takes the least time, counted as waves (one CTA
-// per SM) x the time of a K stage, which the shared-memory traffic of a stage bounds (the MMAs read
-// the 8 KB weight-plane tile and the token tile once per plane and K half, the copies write 24 KB
-// of planes and the token tile: 640 / 832 / 896 cycles at 128 bytes per cycle for tiles of 128 /
-// 224 / 256 tokens, against 384 / 672 / 768 cycles of MMA); the larger tile on a tie.  At the Flash
-// CSA shape the 224-token tile makes 16 x 19 = 304 CTAs, exactly two waves of 152 SMs; the
-// indexer's 128-wide compressor (4 packed tiles) takes the 128-token tile, one wave of 136 CTAs;
-// one long sequence through the ratio-128 compressor takes the 256-token tile.
-long long stage_cycles(int tok) {
-  const long long x_bytes = 64LL * tok;  // a token tile of K = 32 bf16
-  return (6 * (4096 + x_bytes) + 3 * 8192 + x_bytes) / 128;
+// Time of one K stage of a CTA, in cycles: the six MMAs of 64-cycle units per 128 tokens, or the
+// round trip of the 5-stage ring (a stage's copy issued when its slot is freed, landed, consumed
+// by the MMAs, freed again), which measured about 750 cycles whatever the tile: the 128- and
+// 224-token tiles ran at that floor (0.46 and 0.86 of the MMA rate), the 256-token tile at its
+// 768 cycles of MMA (0.98-0.99).
+long long stage_cycles(int tok) { return std::max(3LL * tok, 750LL); }
+// The extra time of a K-split tile: the staged sums copied between the two CTAs and added.
+constexpr long long kSplitCycles = 2500;
+
+template <int TOK, int SPLIT>
+size_t smem_bytes() {
+  return (size_t)tc::kStages * tc::Tile<TOK>::kStageBytes + 1024 /* barriers */ + 1024 /* alignment */;
 }
 
-int prefill_tok(const csa_compressor* c, int B, int N) {
+template <int TOK, int SPLIT>
+cudaError_t set_smem_attr() {
+  static std::atomic<unsigned long long> attr_set{0};
+  return tcx::once_per_device(attr_set, [] {
+    return cudaFuncSetAttribute(tc::prefill_tc_kernel<TOK, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_bytes<TOK, SPLIT>());
+  });
+}
+
+// Clusters of two CTAs of the K-split kernel that the device holds at once (0 if it cannot say),
+// asked once per device and tile.
+template <int TOK>
+int split_clusters() {
+  static std::atomic<int> known[64];  // clusters + 1 per device; 0: not asked yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const int k = known[dev & 63].load();
+  if (k > 0) return k - 1;
+  int n = 0;
+  if (set_smem_attr<TOK, 2>() == cudaSuccess) {
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * current_sm_count(), 1, 1);
+    cfg.blockDim = dim3(tc::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes<TOK, 2>();
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void*)tc::prefill_tc_kernel<TOK, 2>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+  } else {
+    (void)cudaGetLastError();
+  }
+  known[dev & 63].store(n + 1);
+  return n;
+}
+
+int split_clusters_of(int tok) {
+  switch (tok) {
+    case 224:
+      return split_clusters<224>();
+    case 128:
+      return split_clusters<128>();
+    default:
+      return split_clusters<256>();
+  }
+}
+
+// The launch geometry with the least modelled time: waves (CTAs over the SMs, or clusters of two
+// over the clusters the device holds) x the K stages of a CTA x the stage time, plus the exchange
+// of a split tile; the larger tile, then the unsplit grid, on a tie.  At the Flash CSA shape the
+// 224-token tile makes 16 x 19 = 304 CTAs, exactly two waves of 152 SMs; the indexer's 128-wide
+// compressor (4 packed tiles) takes the 224-token tile split over K, 4 x 19 clusters of two in one
+// wave; one long sequence through the ratio-128 compressor takes the 256-token tile.
+PrefillPlan prefill_shape(const csa_compressor* c, int B, int N) {
   const int sms = current_sm_count();
-  int best = tc::kTokMax;
+  const int nkb = c->dim / tc::kKb;
+  const int force = c->opt.prefill_split;
+  PrefillPlan best{tc::kTokMax, 1, 0};
   long long best_cost = -1;
-  for (int tok : {256, 224, 128}) {
-    const int T = owned_tokens(c, tok);
-    if (T < 1) continue;
-    const long long ctas = (long long)c->pk.ntiles * ((N + T - 1) / T) * B;
-    const long long cost = (ctas + sms - 1) / sms * stage_cycles(tok);
-    if (best_cost < 0 || cost < best_cost) {
-      best = tok;
-      best_cost = cost;
+  for (int split : {1, 2}) {
+    if (force && split != force) continue;
+    if (split == 2 && (nkb % 2 != 0 || c->pk.ft % 2 != 0)) continue;
+    for (int tok : {256, 224, 128}) {
+      const int T = owned_tokens(c, tok);
+      if (T < 1) continue;
+      const long long ctas = (long long)c->pk.ntiles * ((N + T - 1) / T) * B * split;
+      const long long slots = split == 1 ? sms : 2LL * split_clusters_of(tok);
+      if (slots <= 0) continue;
+      const long long cost = (ctas + slots - 1) / slots * (nkb / split * stage_cycles(tok) + (split > 1 ? kSplitCycles : 0));
+      if (best_cost < 0 || cost < best_cost) {
+        best = PrefillPlan{tok, split, 0};
+        best_cost = cost;
+      }
     }
   }
   return best;
 }
 
-template <int TOK>
+template <int TOK, int SPLIT>
 cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset, const Chunk& ck,
                        const csa_out& out, void* scratch, size_t scratch_bytes, cudaStream_t s) {
   using namespace tc;
@@ -602,24 +782,30 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const size_t smem = (size_t)kStages * Tile<TOK>::kStageBytes + 1024 /* barriers */ + 1024 /* alignment */;
-  static std::atomic<unsigned long long> attr_set{0};
-  cudaError_t ea = tcx::once_per_device(attr_set, [] {
-    return cudaFuncSetAttribute(prefill_tc_kernel<TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)((size_t)kStages * Tile<TOK>::kStageBytes + 1024 + 1024));
-  });
+  cudaError_t ea = set_smem_attr<TOK, SPLIT>();
   if (ea != cudaSuccess) return ea;
-  cudaLaunchAttribute pdl[1];
-  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute pat[2];
+  int npat = 0;
+  if (P.carry) {  // started early only behind a chunk's carry kernel
+    pat[npat].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pat[npat].val.programmaticStreamSerializationAllowed = 1;
+    ++npat;
+  }
+  if (SPLIT > 1) {  // the two K halves of a tile: one cluster
+    pat[npat].id = cudaLaunchAttributeClusterDimension;
+    pat[npat].val.clusterDim.x = SPLIT;
+    pat[npat].val.clusterDim.y = 1;
+    pat[npat].val.clusterDim.z = 1;
+    ++npat;
+  }
   cudaLaunchConfig_t pc = {};
-  pc.gridDim = dim3(c->pk.ntiles, P.ntt, B);
+  pc.gridDim = dim3(c->pk.ntiles * SPLIT, P.ntt, B);
   pc.blockDim = dim3(kThreads, 1, 1);
-  pc.dynamicSmemBytes = smem;
+  pc.dynamicSmemBytes = smem_bytes<TOK, SPLIT>();
   pc.stream = s;
-  pc.attrs = pdl;
-  pc.numAttrs = P.carry ? 1 : 0;  // started early only behind a chunk's carry kernel
-  cudaError_t e = cudaLaunchKernelEx(&pc, prefill_tc_kernel<TOK>, mx, P);
+  pc.attrs = pat;
+  pc.numAttrs = npat;
+  cudaError_t e = cudaLaunchKernelEx(&pc, prefill_tc_kernel<TOK, SPLIT>, mx, P);
   if (e != cudaSuccess || P.G == 0) return e;
   // the entries: RMSNorm, RoPE and fp4, one CTA each, started early by programmatic dependent
   // launch (the pooled values are read after its wait)
@@ -649,8 +835,7 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
 }  // namespace
 
 PrefillPlan prefill_tc_plan(const csa_compressor* c, int B, int N, const Chunk& ck) {
-  PrefillPlan plan;
-  plan.tok = prefill_tok(c, B, ck.a + N);
+  PrefillPlan plan = prefill_shape(c, B, ck.a + N);
   const int T = owned_tokens(c, plan.tok);
   const int GT = T / c->ratio;
   const int ntt = (ck.a + N + T - 1) / T;
@@ -665,13 +850,17 @@ cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B,
                               const Chunk& ck, const PrefillPlan& plan, const csa_out& out, void* scratch,
                               size_t scratch_bytes, cudaStream_t s) {
   if (scratch_bytes < plan.bytes) return cudaErrorInvalidValue;
+  const bool split = plan.split == 2;
   switch (plan.tok) {
     case 224:
-      return launch_tok<224>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s);
+      return split ? launch_tok<224, 2>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s)
+                   : launch_tok<224, 1>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s);
     case 128:
-      return launch_tok<128>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s);
+      return split ? launch_tok<128, 2>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s)
+                   : launch_tok<128, 1>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s);
     default:
-      return launch_tok<256>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s);
+      return split ? launch_tok<256, 2>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s)
+                   : launch_tok<256, 1>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s);
   }
 }
 

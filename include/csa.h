@@ -77,6 +77,11 @@ typedef struct {
                           (e8m0) scale per 32 features, the indexer's keys (head_dim % 32 == 0);
                           0 = off */
   float eps;           /* RMSNorm epsilon; default 1e-6 */
+  int prefill_split;   /* launch geometry of the tensor-core prefill: 0 = chosen per call from a
+                          model of its time (default); 1 = one CTA per (packed tile, token tile);
+                          2 = a cluster of two CTAs per tile, each taking half of K (dim), the two
+                          partial sums added on chip.  The outputs agree within the rounding of
+                          that addition; a tuning knob, not a change of the method. */
 } csa_options;
 
 /* Output buffers of one call (dev).  Rows are entries: prefill [B][G][..], decode [B][..].

@@ -43,10 +43,11 @@ CHAINS = [
 ]
 
 
+@pytest.mark.parametrize("split", [1, 2])
 @pytest.mark.parametrize("dim,H,ratio,overlap,B,chunks", CHAINS)
-def test_prefill_chunks_then_decode(dim, H, ratio, overlap, B, chunks):
+def test_prefill_chunks_then_decode(dim, H, ratio, overlap, B, chunks, split):
     layer = synthetic.Layer(dim, H, ratio, overlap, 1.0 / math.sqrt(dim), gate_scale=2.0, rope_dim=min(64, H), fp4=1)
-    g, o = make_pair(11, layer, max_batch=B + 1)
+    g, o = make_pair(11, layer, max_batch=B + 1, split=split)
     P = sum(chunks)
     x, *_ = layer_inputs(11, layer, B, P + 5)
     p0 = 0

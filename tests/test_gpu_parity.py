@@ -45,9 +45,13 @@ def opts_of(layer, max_batch=1, max_pos=262144):
     return dict(max_batch=max_batch, rope_dim=layer.rope_dim, fp4=layer.fp4, max_pos=max_pos)
 
 
-def make_pair(seed, layer, max_batch=1, max_pos=262144):
+def make_pair(seed, layer, max_batch=1, max_pos=262144, split=0):
+    """The library's compressor and the oracle's, with the same synthetic weights.  split forces
+    the tensor-core prefill's launch geometry (1: one CTA per tile, 2: two CTAs of a cluster each
+    taking half of K; 0: chosen per call)."""
     wkv, wgate, gain = synthetic.weights(seed, layer)
-    g = csa.Compressor(layer.dim, layer.head_dim, layer.ratio, layer.overlap, **opts_of(layer, max_batch, max_pos))
+    g = csa.Compressor(layer.dim, layer.head_dim, layer.ratio, layer.overlap, prefill_split=split,
+                       **opts_of(layer, max_batch, max_pos))
     g.set_weights(torch.from_numpy(wkv).to(DEV), torch.from_numpy(wgate).to(DEV), torch.from_numpy(gain).to(DEV))
     o = oracle.Compressor(layer.dim, layer.head_dim, layer.ratio, layer.overlap, max_batch=max_batch,
                           rope_dim=layer.rope_dim, fp4=layer.fp4)
@@ -202,11 +206,12 @@ SMALL_FP4 = [(d, H, r, ov, B, N, 1) for d, H, r, ov, B, N in SMALL] + [
 ]
 
 
+@pytest.mark.parametrize("split", [1, 2])
 @pytest.mark.parametrize("dim,H,ratio,overlap,B,N,fp4", SMALL_FP4)
-def test_small_prefill_state_and_decode(dim, H, ratio, overlap, B, N, fp4):
+def test_small_prefill_state_and_decode(dim, H, ratio, overlap, B, N, fp4, split):
     layer = synthetic.Layer(dim, H, ratio, overlap, 1.0 / math.sqrt(dim), gate_scale=2.0,
                             rope_dim=min(64, H), fp4=fp4)
-    g, o = make_pair(5, layer, max_batch=B + 1)
+    g, o = make_pair(5, layer, max_batch=B + 1, split=split)
     x, *_ = layer_inputs(5, layer, B, N + 6)
     xp = np.ascontiguousarray(x[:, :N])
     ref = o.prefill(xp, slot_offset=1)
