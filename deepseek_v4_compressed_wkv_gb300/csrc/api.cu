@@ -188,8 +188,7 @@ int prefill_call(csa_compressor* c, const uint16_t* x, int B, int N, int start_p
       CSA_CUDA(csa::launch_prefill_tc(c, x, B, N, slot_offset, ck, plan, o, c->scratch, c->scratch_bytes, s),
                "tensor-core prefill launch");
       if (c->prof_stop) CSA_CUDA(cudaEventRecord(c->prof_stop, s), "cudaEventRecord");
-      // the carry kernel (a chunk), the projection kernel, the entry kernel
-      c->launches += csa::chunk_needs_carry(ck, c->overlap) + 1 + (ck.G > 0);
+      c->launches += plan.kernels;
       return ck.G;
     }
     CSA_CUDA(csa::invalidate_decode_acc(c, slot_offset, B, s), "invalidate decode running values");

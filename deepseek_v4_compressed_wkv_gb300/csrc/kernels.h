@@ -35,6 +35,7 @@ struct PrefillPlan {
   int tok;       // token tile: 256, 224 or 128
   int split;     // 1: one CTA per tile; 2: a cluster of two CTAs per tile, each half of K
   size_t bytes;  // scratch bytes
+  int kernels;   // kernels the call launches
 };
 PrefillPlan prefill_tc_plan(const csa_compressor* c, int B, int N, const Chunk& ck);
 // scratch_bytes: the capacity of `scratch` (>= plan.bytes), the extent the bounds-checked build

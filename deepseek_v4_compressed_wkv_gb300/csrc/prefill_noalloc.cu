@@ -94,7 +94,7 @@ int noalloc_call(csa_compressor* c, const uint16_t* x, int B, int N, int start_p
     // the array's capacity is the extent the bounds-checked build checks the scratch stores against
     if (csa::launch_prefill_tc(c, x, B, N, slot_offset, ck, plan, o, base, kScratchBytes, s) != cudaSuccess)
       return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: kernel launch failed");
-    c->launches += csa::chunk_needs_carry(ck, c->overlap) + 1 + (ck.G > 0);
+    c->launches += plan.kernels;
     return ck.G;
   } catch (...) {
     return csa_internal_fail(CSA_ERR_INTERNAL, "csa_compress_prefill_noalloc: unexpected exception");

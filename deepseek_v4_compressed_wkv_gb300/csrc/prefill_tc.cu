@@ -72,6 +72,17 @@ struct Tile {
   static_assert(kStageBytes % 1024 == 0, "stages keep the 1 KB alignment of the swizzled tiles");
 };
 
+struct EntryParams {
+  int B, G, GT, ntt, ratio;
+  int tpe;                 // threads per entry: H / 4 rounded up to a power of two
+  Chunk ck;
+  const uint16_t* pooled;  // [B][ntt][GT][H] bf16 bits
+  EpiParams ep;
+  csa_out out;
+  long long out_rows;      // rows of the outputs (checked by the bounds-checked build)
+  int* flag;
+};
+
 struct Params {
   int N, K, ratio, overlap, T, GT, halo, ntt, G, ncol, slots, slot_offset;
   int a, g0, gend;         // chunk geometry (Chunk): all 0 / G for a prefill from position 0
@@ -90,15 +101,85 @@ struct Params {
                            // (a test of the time-out path); 0 otherwise
 };
 
-struct EntryParams {
-  int G, GT, ntt, ratio;
-  Chunk ck;
-  const uint16_t* pooled;  // [B][ntt][GT][H] bf16 bits
-  EpiParams ep;
-  csa_out out;
-  long long out_rows;      // rows of the outputs (checked by the bounds-checked build)
-  int* flag;
+
+// ---- one entry's epilogue ---------------------------------------------------------------------
+//
+// The entries (b, j) take H / 4 threads each (rounded up to a power of two, `tpe`, an aligned
+// segment of lanes or whole warps); thread te of an entry takes features 4te..4te+3 of its pooled
+// values, then bf16, RMSNorm (the sum of squares over the entry's lanes, and over its warps in
+// order when it spans several), RoPE and the fp4 round trip (entry_epilogue_quad, whose fp4 blocks
+// are aligned groups of four or eight lanes).  entry_prepare reads what does not depend on the
+// projection (gain, RoPE factors), entry_finish the rest.
+
+struct EntryPrep {
+  int b, j, f;
+  bool live, act;
+  float gn[4], rc[2], rs[2];
 };
+
+__device__ __forceinline__ EntryPrep entry_prepare(const EntryParams& P, int e, int te) {
+  EntryPrep q;
+  const int H = P.ep.H, hr = P.ep.rope_dim >> 1, r0 = H - P.ep.rope_dim;
+  q.f = 4 * te;
+  q.live = e < P.B * P.G;
+  q.act = q.f < H;
+  q.b = q.live ? e / P.G : 0;
+  q.j = q.live ? e % P.G : 0;
+  const long long pos = (long long)P.ratio * (P.ck.g0 + q.j);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) q.gn[i] = 0.0f;
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    q.rc[u] = 1.0f;
+    q.rs[u] = 0.0f;
+  }
+  if (q.live && q.act) {
+    const float4 gg = __ldg(reinterpret_cast<const float4*>(P.ep.gain + q.f));
+    q.gn[0] = gg.x;
+    q.gn[1] = gg.y;
+    q.gn[2] = gg.z;
+    q.gn[3] = gg.w;
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      if (hr > 0 && q.f + 2 * u >= r0) {
+        q.rc[u] = __ldg(P.ep.rope_cos + pos * hr + ((q.f + 2 * u - r0) >> 1));
+        q.rs[u] = __ldg(P.ep.rope_sin + pos * hr + ((q.f + 2 * u - r0) >> 1));
+      }
+  }
+  return q;
+}
+
+// t: the thread's index in its CTA; wss: 4 floats of shared memory when tpe > 32 (then every thread
+// of the CTA calls this, it synchronises the CTA), else unused.  All 32 lanes of a warp call it.
+__device__ __forceinline__ void entry_finish(const EntryParams& P, const EntryPrep& q, int t, float* wss) {
+  const int H = P.ep.H, tpe = P.tpe, lane = t & 31;
+  const int tt = q.j / P.GT, g = q.j % P.GT;
+  float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (q.live && q.act) {
+    const uint2 u = __ldcg(reinterpret_cast<const uint2*>(P.pooled + (((size_t)q.b * P.ntt + tt) * P.GT + g) * H + q.f));
+    v[0] = __uint_as_float(u.x << 16);
+    v[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(u.y << 16);
+    v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+  }
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) ss = fmaf(v[i], v[i], ss);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1)
+    if (o < tpe) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (tpe > 32) {
+    if (lane == 0) wss[t >> 5] = ss;
+    __syncthreads();
+    const int w0 = ((t / tpe) * tpe) >> 5;
+    ss = wss[w0];
+    for (int w = 1; w < tpe / 32; ++w) ss += wss[w0 + w];
+  }
+  const float inv = rms_inv(ss, P.ep);
+  const long long row = P.ck.row(q.b, q.j);
+  const bool ok = q.live && in_bounds(row, P.out_rows, P.flag);
+  entry_epilogue_quad(v, q.act && ok, q.f, lane, inv, q.gn, q.rc, q.rs, P.ep, ok ? (size_t)row : 0, P.out);
+}
 
 // ---- the kernel ----------------------------------------------------------------------------
 //
@@ -307,13 +388,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     lost = __syncthreads_or(!mbar_wait_bounded(recv_bar, 0, kWait));
     if (lost && threadIdx.x == 0) atomicOr(P.flag, 4);
   }
-  if (!aborted && !lost && (kSplit > 1 || P.ape)) {
+  // Split without a gate bias, the received half-K sums are added where the state writes and the
+  // pool read them (`fold`); otherwise the pass below leaves this CTA's final values in stg.
+  const float* recv = stg + kRows * kSmemStride;
+  const bool fold = kSplit > 1 && !P.ape;
+  if (!aborted && !lost && (kSplit > 1 || P.ape) && !fold) {
     // this CTA's rows: the two half-K sums added (the same sum in either order), then wgate(x) +
     // the positional bias of each token's place in its group (score rows; column c holds the
     // token at position ratio * g0 + t0 + c, halo columns wrap harmlessly).  Unsplit, only the
     // score rows of a layer with the bias are visited.  Warp w takes rows w, w + 10, ..., its
     // lanes the columns.
-    const float* recv = stg + kRows * kSmemStride;
     const int kind0 = kSplit > 1 ? 0 : pk.nk / 2;
     const int r = P.ratio, step = 32 % r;
     const int sl0 = ((P.ratio * P.g0 + t0 + lane) % r + r) % r;
@@ -347,6 +431,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
+  // the final sum of packed row (kind, f) of this CTA's features at tile column col, one value or
+  // the four from col (col a multiple of 4)
+  auto at = [&](int kind, int f, int col) -> float {
+    float v = stg[(kind * F + f) * kSmemStride + col];
+    if (fold) v += recv[(kind * hf + f - f0) * kSmemStride + col];
+    return v;
+  };
+  auto at4 = [&](int kind, int f, int col) -> float4 {
+    float4 v = *reinterpret_cast<const float4*>(stg + (kind * F + f) * kSmemStride + col);
+    if (fold) {
+      const float4 w = *reinterpret_cast<const float4*>(recv + (kind * hf + f - f0) * kSmemStride + col);
+      v.x += w.x;
+      v.y += w.y;
+      v.z += w.z;
+      v.w += w.w;
+    }
+    return v;
+  };
+
   if (!aborted) {
     const int r = P.ratio, G = P.G;
     const int col0 = ftile * kRows;  // first packed column of this tile
@@ -358,10 +461,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kind = et / hf, prow = kind * F + f0 + et % hf;
       const size_t st0 = (size_t)(P.slot_offset + b) * P.slots * P.ncol + col0 + prow;
       float* st = P.state + st0;
-      const float* srow = stg + prow * kSmemStride - t0;  // srow[tok]: the tile's column of token tok
       const int own0 = max(tt * P.T, P.a), own1 = min(tt * P.T + P.T, P.a + P.N);
-      auto put = [&](int tok, int slot) {
-        if (in_bounds((long long)st0 + (long long)slot * P.ncol, P.state_elems, P.flag)) st[slot * P.ncol] = srow[tok];
+      auto put = [&](int tok, int slot) {  // token tok is the tile's column tok - t0
+        if (in_bounds((long long)st0 + (long long)slot * P.ncol, P.state_elems, P.flag))
+          st[slot * P.ncol] = at(kind, f0 + et % hf, tok - t0);
       };
       if (!P.overlap) {
         for (int tok = max(own0, r * G); tok < own1; ++tok) put(tok, tok - r * G);
@@ -389,10 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (P.overlap) {
         // branch A: tokens 4g + 4 .. 4g + 7 of the tile, branch B: tokens 4g .. 4g + 3 (one
         // 16-byte vector each)
-        const float4 a4 = *reinterpret_cast<const float4*>(stg + (KV_A * F + f) * kSmemStride + 4 * g + 4);
-        const float4 p4 = *reinterpret_cast<const float4*>(stg + (S_A * F + f) * kSmemStride + 4 * g + 4);
-        const float4 b4 = *reinterpret_cast<const float4*>(stg + (KV_B * F + f) * kSmemStride + 4 * g);
-        const float4 q4 = *reinterpret_cast<const float4*>(stg + (S_B * F + f) * kSmemStride + 4 * g);
+        const float4 a4 = at4(KV_A, f, 4 * g + 4), p4 = at4(S_A, f, 4 * g + 4);
+        const float4 b4 = at4(KV_B, f, 4 * g), q4 = at4(S_B, f, 4 * g);
         const float kA[4] = {a4.x, a4.y, a4.z, a4.w}, sA[4] = {p4.x, p4.y, p4.z, p4.w};
         const float kB[4] = {b4.x, b4.y, b4.z, b4.w}, sB[4] = {q4.x, q4.y, q4.z, q4.w};
         const bool padB = P.g0 + j == 0;
@@ -412,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             num = fmaf(eb, kB[i], num);
           }
         }
-      } else if (r % 2 == 0) {
+      } else if (r % 2 == 0 && !fold) {
         // the group's ratio tokens as 8-byte pairs
         const float2* kv = reinterpret_cast<const float2*>(stg + (KV * F + f) * kSmemStride + r * g);
         const float2* sc = reinterpret_cast<const float2*>(stg + (S * F + f) * kSmemStride + r * g);
@@ -426,13 +527,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           num = fmaf(e1, k2.y, num);
         }
       } else {
-        const float* kv = stg + (KV * F + f) * kSmemStride + r * g;
-        const float* sc = stg + (S * F + f) * kSmemStride + r * g;
-        for (int i = 0; i < r; ++i) m = fmaxf(m, sc[i]);
+        for (int i = 0; i < r; ++i) m = fmaxf(m, at(S, f, r * g + i));
         for (int i = 0; i < r; ++i) {
-          const float e = expf(sc[i] - m);
+          const float e = expf(at(S, f, r * g + i) - m);
           den += e;
-          num = fmaf(e, kv[i], num);
+          num = fmaf(e, at(KV, f, r * g + i), num);
         }
       }
       return __fdiv_rn(num, den);
@@ -444,26 +543,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto pool_carried = [&](int j) -> float {
       const float* cr = P.carry + ((size_t)b * (1 + P.overlap) + j) * 3 * pk.H + ftile * F + f;
       const float mc = cr[0], dc = cr[pk.H], nc = cr[2 * pk.H];  // max, denominator, numerator
-      const int kk = P.overlap ? (KV_A * F + f) : (KV * F + f), ks = P.overlap ? (S_A * F + f) : (S * F + f);
-      const float* kv = stg + kk * kSmemStride + P.halo + 4 * j;
-      const float* sc = stg + ks * kSmemStride + P.halo + 4 * j;
-      const float* kB = stg + (KV_B * F + f) * kSmemStride + P.halo;
-      const float* sB = stg + (S_B * F + f) * kSmemStride + P.halo;
+      const int kk = P.overlap ? KV_A : KV, ks = P.overlap ? S_A : S;
+      const int c0 = P.halo + 4 * j;  // this group's first column (branch A when overlapped)
       const int n = P.overlap ? 4 : r, i0 = j == 0 ? P.a : 0, iB = j == 1 ? P.a : 4;
       float m = mc;
-      for (int i = i0; i < n; ++i) m = fmaxf(m, sc[i]);
-      for (int i = iB; i < 4; ++i) m = fmaxf(m, sB[i]);
+      for (int i = i0; i < n; ++i) m = fmaxf(m, at(ks, f, c0 + i));
+      for (int i = iB; i < 4; ++i) m = fmaxf(m, at(S_B, f, P.halo + i));
       const float rs = expf(mc - m);  // 0 when nothing was carried (mc = -inf)
       float den = dc * rs, num = nc * rs;
       for (int i = iB; i < 4; ++i) {
-        const float e = expf(sB[i] - m);
+        const float e = expf(at(S_B, f, P.halo + i) - m);
         den += e;
-        num = fmaf(e, kB[i], num);
+        num = fmaf(e, at(KV_B, f, P.halo + i), num);
       }
       for (int i = i0; i < n; ++i) {
-        const float e = expf(sc[i] - m);
+        const float e = expf(at(ks, f, c0 + i) - m);
         den += e;
-        num = fmaf(e, kv[i], num);
+        num = fmaf(e, at(kk, f, c0 + i), num);
       }
       return __fdiv_rn(num, den);
     };
@@ -541,50 +637,15 @@ __global__ void __launch_bounds__(128) chunk_carry_kernel(const float* __restric
                   out + 3 * H, H);
 }
 
-// One CTA of 128 threads per entry (b, j): thread t takes features 4t..4t+3 of its pooled
-// values, then bf16, RMSNorm (the sum of squares over the CTA, warps in order), RoPE and the
-// fp4 round trip (entry_epilogue_quad).  The gain and RoPE factors (written before this launch's
-// predecessor started) are read before the wait for the projection kernel.
+// The entries in their own kernel: a CTA of 128 threads takes 128 / tpe consecutive entries (one
+// CTA per entry at H = 512); the gain and RoPE factors (written before this launch's predecessor
+// started) are read before the wait for the projection kernel.
 __global__ void __launch_bounds__(128) prefill_entry_kernel(const EntryParams P) {
   __shared__ float wss[4];
-  const int e = blockIdx.x, t = threadIdx.x, lane = t & 31, f = 4 * t;
-  const int b = e / P.G, j = e % P.G, tt = j / P.GT, g = j % P.GT;
-  const int H = P.ep.H, hr = P.ep.rope_dim >> 1, r0 = H - P.ep.rope_dim;
-  const bool act = f < H;
-  const long long pos = (long long)P.ratio * (P.ck.g0 + j);
-  float gn[4] = {0.0f, 0.0f, 0.0f, 0.0f}, rc[2] = {1.0f, 1.0f}, rs[2] = {0.0f, 0.0f};
-  if (act) {
-    const float4 gg = __ldg(reinterpret_cast<const float4*>(P.ep.gain + f));
-    gn[0] = gg.x;
-    gn[1] = gg.y;
-    gn[2] = gg.z;
-    gn[3] = gg.w;
-#pragma unroll
-    for (int u = 0; u < 2; ++u)
-      if (hr > 0 && f + 2 * u >= r0) {
-        rc[u] = __ldg(P.ep.rope_cos + pos * hr + ((f + 2 * u - r0) >> 1));
-        rs[u] = __ldg(P.ep.rope_sin + pos * hr + ((f + 2 * u - r0) >> 1));
-      }
-  }
+  const int t = threadIdx.x;
+  const EntryPrep q = entry_prepare(P, blockIdx.x * (128 / P.tpe) + t / P.tpe, t % P.tpe);
   griddep_wait();  // the pooled values of the projection kernel
-  float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  if (act) {
-    const uint2 u = __ldcg(reinterpret_cast<const uint2*>(P.pooled + (((size_t)b * P.ntt + tt) * P.GT + g) * H + f));
-    v[0] = __uint_as_float(u.x << 16);
-    v[1] = __uint_as_float(u.x & 0xFFFF0000u);
-    v[2] = __uint_as_float(u.y << 16);
-    v[3] = __uint_as_float(u.y & 0xFFFF0000u);
-  }
-  float ss = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) ss = fmaf(v[i], v[i], ss);
-  ss = warp_sum(ss);
-  if (lane == 0) wss[t >> 5] = ss;
-  __syncthreads();
-  const float inv = rms_inv(wss[0] + wss[1] + wss[2] + wss[3], P.ep);
-  const long long row = P.ck.row(b, j);
-  if (!in_bounds(row, P.out_rows, P.flag)) return;  // the same for the whole CTA
-  entry_epilogue_quad(v, act, f, lane, inv, gn, rc, rs, P.ep, (size_t)row, P.out);
+  entry_finish(P, q, t, wss);
 }
 
 }  // namespace tc
@@ -684,7 +745,7 @@ PrefillPlan prefill_shape(const csa_compressor* c, int B, int N) {
   const int sms = current_sm_count();
   const int nkb = c->dim / tc::kKb;
   const int force = c->opt.prefill_split;
-  PrefillPlan best{tc::kTokMax, 1, 0};
+  PrefillPlan best{tc::kTokMax, 1, 0, 0};
   long long best_cost = -1;
   for (int split : {1, 2}) {
     if (force && split != force) continue;
@@ -697,7 +758,7 @@ PrefillPlan prefill_shape(const csa_compressor* c, int B, int N) {
       if (slots <= 0) continue;
       const long long cost = (ctas + slots - 1) / slots * (nkb / split * stage_cycles(tok) + (split > 1 ? kSplitCycles : 0));
       if (best_cost < 0 || cost < best_cost) {
-        best = PrefillPlan{tok, split, 0};
+        best = PrefillPlan{tok, split, 0, 0};
         best_cost = cost;
       }
     }
@@ -782,6 +843,22 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  // the entries: RMSNorm, RoPE and fp4, in their own kernel, started early by programmatic
+  // dependent launch (the pooled values are read after its wait)
+  EntryParams Q;
+  Q.B = B;
+  Q.G = P.G;
+  Q.GT = P.GT;
+  Q.ntt = P.ntt;
+  Q.ratio = c->ratio;
+  Q.tpe = 4;
+  while (Q.tpe < c->H / 4) Q.tpe *= 2;
+  Q.ck = ck;
+  Q.pooled = P.pooled;
+  Q.out_rows = (long long)B * ck.bstride;
+  Q.flag = c->dev_flag;
+  Q.ep = epi_params(c);
+  Q.out = out;
   cudaError_t ea = set_smem_attr<TOK, SPLIT>();
   if (ea != cudaSuccess) return ea;
   cudaLaunchAttribute pat[2];
@@ -807,24 +884,12 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
   pc.numAttrs = npat;
   cudaError_t e = cudaLaunchKernelEx(&pc, prefill_tc_kernel<TOK, SPLIT>, mx, P);
   if (e != cudaSuccess || P.G == 0) return e;
-  // the entries: RMSNorm, RoPE and fp4, one CTA each, started early by programmatic dependent
-  // launch (the pooled values are read after its wait)
-  EntryParams Q;
-  Q.G = P.G;
-  Q.GT = P.GT;
-  Q.ntt = P.ntt;
-  Q.ratio = c->ratio;
-  Q.ck = ck;
-  Q.pooled = P.pooled;
-  Q.out_rows = (long long)B * ck.bstride;
-  Q.flag = c->dev_flag;
-  Q.ep = epi_params(c);
-  Q.out = out;
+  const long long ctas = ((long long)B * P.G + 128 / Q.tpe - 1) / (128 / Q.tpe);
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((long long)B * P.G), 1, 1);
+  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
   cfg.blockDim = dim3(128, 1, 1);
   cfg.stream = s;
   cfg.attrs = at;
@@ -843,6 +908,8 @@ PrefillPlan prefill_tc_plan(const csa_compressor* c, int B, int N, const Chunk& 
   plan.bytes = chunk_needs_carry(ck, c->overlap)
                    ? carry_offset(pooled) + (size_t)B * (1 + c->overlap) * 3 * c->H * sizeof(float)
                    : pooled;
+  // the carry kernel (a chunk), the projection kernel, the entry kernel
+  plan.kernels = chunk_needs_carry(ck, c->overlap) + 1 + (ck.G > 0);
   return plan;
 }
 
