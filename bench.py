@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--decode-only", action="store_true",
                     help="run and print only the decode measurement (for profiling)")
+    ap.add_argument("--other-only", choices=["hca", "indexer", "pairs"], default=None,
+                    help="run and print only the prefill of that other compressor instance (for profiling)")
     ap.add_argument("--decode-layers", type=int, default=0,
                     help="layer instances rotated in the decode measurement (0: enough to exceed L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -815,6 +817,17 @@ def main():
         d = bench_decode(args, torch, csa, synthetic, torch.device("cuda", local), load_peaks(), world, rank)
         if rank == 0:
             print(json.dumps({"decode": d}), flush=True)
+        return
+    if args.other_only:
+        import torch
+
+        import deepseek_v4_compressed_wkv_gb300 as csa
+        import synthetic
+        torch.cuda.set_device(local)
+        wl = {"hca": synthetic.HCA, "indexer": synthetic.INDEXER, "pairs": synthetic.PAIRS}[args.other_only]
+        o = bench_prefill_workload(args, torch, csa, synthetic, torch.device("cuda", local), load_peaks(), world, wl)
+        if rank == 0:
+            print(json.dumps({"other_prefill": [o]}), flush=True)
         return
     line = run_ours(args, rank, world, local)
     if rank == 0:
