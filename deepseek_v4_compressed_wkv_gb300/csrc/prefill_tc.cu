@@ -513,13 +513,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             num = fmaf(eb, kB[i], num);
           }
         }
-      } else if (r % 2 == 0 && !fold) {
-        // the group's ratio tokens as 8-byte pairs
+      } else if (r % 2 == 0) {
+        // the group's ratio tokens as 8-byte pairs (and the received half-K sums beside them)
         const float2* kv = reinterpret_cast<const float2*>(stg + (KV * F + f) * kSmemStride + r * g);
         const float2* sc = reinterpret_cast<const float2*>(stg + (S * F + f) * kSmemStride + r * g);
-        for (int i = 0; i < r / 2; ++i) m = fmaxf(m, fmaxf(sc[i].x, sc[i].y));
+        const float2* kv2 = reinterpret_cast<const float2*>(recv + (KV * hf + f - f0) * kSmemStride + r * g);
+        const float2* sc2 = reinterpret_cast<const float2*>(recv + (S * hf + f - f0) * kSmemStride + r * g);
+        auto pair = [&](const float2* own, const float2* got, int i) {
+          float2 v = own[i];
+          if (fold) {
+            const float2 w = got[i];
+            v.x += w.x;
+            v.y += w.y;
+          }
+          return v;
+        };
         for (int i = 0; i < r / 2; ++i) {
-          const float2 s2 = sc[i], k2 = kv[i];
+          const float2 s2 = pair(sc, sc2, i);
+          m = fmaxf(m, fmaxf(s2.x, s2.y));
+        }
+        for (int i = 0; i < r / 2; ++i) {
+          const float2 s2 = pair(sc, sc2, i), k2 = pair(kv, kv2, i);
           const float e0 = expf(s2.x - m), e1 = expf(s2.y - m);
           den += e0;
           num = fmaf(e0, k2.x, num);
@@ -674,8 +688,11 @@ int owned_tokens(const csa_compressor* c, int tok) {
 // 224-token tiles ran at that floor (0.46 and 0.86 of the MMA rate), the 256-token tile at its
 // 768 cycles of MMA (0.98-0.99).
 long long stage_cycles(int tok) { return std::max(3LL * tok, 750LL); }
-// The extra time of a K-split tile: the staged sums copied between the two CTAs and added.
-constexpr long long kSplitCycles = 2500;
+// Per CTA besides its K stages (from per-CTA timestamps at about 1.9 GHz): the first stage landing,
+// the last chunk drained, the staging and the pool, about 3.5 us; a K-split CTA adds the cluster
+// barrier, the copy between the two CTAs and the received sums it reads, about 2.6 us.
+constexpr long long kTileCycles = 6700;
+constexpr long long kSplitCycles = 5000;
 
 template <int TOK, int SPLIT>
 size_t smem_bytes() {
@@ -736,8 +753,9 @@ int split_clusters_of(int tok) {
 }
 
 // The launch geometry with the least modelled time: waves (CTAs over the SMs, or clusters of two
-// over the clusters the device holds) x the K stages of a CTA x the stage time, plus the exchange
-// of a split tile; the larger tile, then the unsplit grid, on a tie.  At the Flash CSA shape the
+// over the clusters the device holds) x the time of a CTA (its K stages x the stage time, plus the
+// rest of a tile and the exchange of a split tile); the larger tile, then the unsplit grid, on a
+// tie.  At the Flash CSA shape the
 // 224-token tile makes 16 x 19 = 304 CTAs, exactly two waves of 152 SMs; the indexer's 128-wide
 // compressor (4 packed tiles) takes the 224-token tile split over K, 4 x 19 clusters of two in one
 // wave; one long sequence through the ratio-128 compressor takes the 256-token tile.
@@ -756,7 +774,8 @@ PrefillPlan prefill_shape(const csa_compressor* c, int B, int N) {
       const long long ctas = (long long)c->pk.ntiles * ((N + T - 1) / T) * B * split;
       const long long slots = split == 1 ? sms : 2LL * split_clusters_of(tok);
       if (slots <= 0) continue;
-      const long long cost = (ctas + slots - 1) / slots * (nkb / split * stage_cycles(tok) + (split > 1 ? kSplitCycles : 0));
+      const long long cost =
+          (ctas + slots - 1) / slots * (nkb / split * stage_cycles(tok) + kTileCycles + (split > 1 ? kSplitCycles : 0));
       if (best_cost < 0 || cost < best_cost) {
         best = PrefillPlan{tok, split, 0, 0};
         best_cost = cost;
