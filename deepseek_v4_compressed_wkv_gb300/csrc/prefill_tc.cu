@@ -3,8 +3,9 @@
 // epilogue.  The pre-pool kv / score values live only in TMEM and shared memory.
 //
 // GEMM orientation: the packed weight rows are the MMA's M side (128 rows = one packed tile:
-// ft features x nk kinds), the tokens its N side (a tile of 256, 224 or 128, whichever fills
-// the SMs in fewer waves x tile tokens), K = dim.  The f32 weights
+// ft features x nk kinds), the tokens its N side (a tile of 256, 224 or 128), K = dim; a tile is
+// one CTA, or for compressors with few packed tiles a cluster of two CTAs that each take half of
+// K (the launch geometry with the least modelled time, prefill_shape).  The f32 weights
 // enter as three bf16 planes whose sum is exact (w = p0 + p1 + p2), so three bf16 MMAs into
 // one f32 accumulator give the f32 product (x is bf16, so every partial product is exact):
 // the f32 projection of "Pool token pairs" (x.float(), wkv(x), wgate(x)) and the f32 x . w^T
@@ -18,12 +19,13 @@
 // half that of an f32 FMA GEMM; chunks of 256 are 4% faster (chunks of 512: another 2%).
 //
 // Roles (320 threads): warp 0 issues the TMA loads (x tile shared by all three planes, one
-// tile per plane), warp 1 owns TMEM and issues tcgen05.mma, warps 2-9 run the epilogue (warps
-// w and w+4 share TMEM lane quarter w%4 and split the 256 token columns).
-// One CTA computes one (packed tile, token tile) and leaves its pooled values in scratch; the
-// entries are then normalised, rotated and quantised by prefill_entry_kernel, one CTA per entry
-// over all SMs (the RMSNorm needs all H features, and one SM finishing a token tile's 63
-// entries alone took about as long as a quarter of the projection).
+// tile per plane), warp 1 owns TMEM and issues tcgen05.mma, warps 2-9 drain the chunk
+// accumulators (warps w and w+4 share TMEM lane quarter w%4 and split the token columns) and
+// stage the sums in the idle stage buffers; once the TMEM is freed all ten warps write the state
+// tokens and pool.  A tile's CTA (or pair) leaves its pooled values in scratch; the entries are
+// then normalised, rotated and quantised by prefill_entry_kernel over all SMs (the RMSNorm needs
+// all H features, and one SM finishing a token tile's 63 entries alone took about as long as a
+// quarter of the projection).
 //
 // A chunk at position p0 > 0 (Chunk) tiles the tokens from the start of the open group: the
 // first tile's leading a = p0 % ratio token columns (and the overlapped halo) are earlier
@@ -100,7 +102,6 @@ struct Params {
   int test_stall;          // bounds-checked build only: the producer never issues the last stage
                            // (a test of the time-out path); 0 otherwise
 };
-
 
 // ---- one entry's epilogue ---------------------------------------------------------------------
 //
