@@ -583,15 +583,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (in_bounds((long long)((pooled_tile - P.pooled) + pi), P.pooled_elems, P.flag)) pooled_tile[pi] = bf16_bits(v);
     };
     const int gstep = kThreads / hf;
-    for (int g = (int)threadIdx.x / hf; g < P.GT; g += 2 * gstep) {
-      const int j = tt * P.GT + g;
-      if (j >= G) break;  // groups are visited in order
-      // the second group (never a carried one: gstep >= 5), or the first again when there is none
-      const bool two = g + gstep < P.GT && j + gstep < G;
-      const float v2 = two ? pool_tile(g + gstep, j + gstep) : 0.0f;
-      const float v1 = P.carry && j < 1 + P.overlap ? pool_carried(j) : pool_tile(g, j);
-      put_pooled(g, v1);
-      if (two) put_pooled(g + gstep, v2);
+    if (!P.overlap && r == 2 && !P.carry) {
+      // pairs of tokens ("Pool token pairs"): one 16-byte load holds groups 2p and 2p + 1, the
+      // additions in the order of the general loop below
+      for (int p = (int)threadIdx.x / hf; 2 * p < P.GT; p += gstep) {
+        const int g = 2 * p, j = tt * P.GT + g;
+        if (j >= G) break;
+        const float4 s4 = at4(S, f, 4 * p), k4 = at4(KV, f, 4 * p);
+        const float m0 = fmaxf(s4.x, s4.y), m1 = fmaxf(s4.z, s4.w);
+        const float a0 = expf(s4.x - m0), b0 = expf(s4.y - m0), a1 = expf(s4.z - m1), b1 = expf(s4.w - m1);
+        put_pooled(g, __fdiv_rn(fmaf(b0, k4.y, fmaf(a0, k4.x, 0.0f)), (0.0f + a0) + b0));
+        if (g + 1 < P.GT && j + 1 < G)
+          put_pooled(g + 1, __fdiv_rn(fmaf(b1, k4.w, fmaf(a1, k4.z, 0.0f)), (0.0f + a1) + b1));
+      }
+    } else {
+      for (int g = (int)threadIdx.x / hf; g < P.GT; g += 2 * gstep) {
+        const int j = tt * P.GT + g;
+        if (j >= G) break;  // groups are visited in order
+        // the second group (never a carried one: gstep >= 5), or the first again when there is none
+        const bool two = g + gstep < P.GT && j + gstep < G;
+        const float v2 = two ? pool_tile(g + gstep, j + gstep) : 0.0f;
+        const float v1 = P.carry && j < 1 + P.overlap ? pool_carried(j) : pool_tile(g, j);
+        put_pooled(g, v1);
+        if (two) put_pooled(g + gstep, v2);
+      }
     }
   }
   if constexpr (kSplit > 1) {
