@@ -596,6 +596,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (g + 1 < P.GT && j + 1 < G)
           put_pooled(g + 1, __fdiv_rn(fmaf(b1, k4.w, fmaf(a1, k4.z, 0.0f)), (0.0f + a1) + b1));
       }
+    } else if (!P.overlap && r >= 64 && r % 8 == 0 && !P.carry && hf % 16 == 0) {
+      // long groups (ratio 128: two per 256-token tile): two adjacent threads per (feature, group),
+      // each over half of the group's tokens from the group's maximum (the pair's), the two
+      // halves' sums added once.  The 16 pairs of a warp share their group (16 divides hf), so whole
+      // warps iterate together and the pair exchanges are full-warp shuffles.
+      const int q = (int)threadIdx.x >> 1, part = (int)threadIdx.x & 1;
+      const int qstep = (kThreads / 2) / hf;  // groups per step: 2 (hf 64) or 5 (hf 32)
+      const int fq = f0 + q % hf, half = r / 2;
+      if (q < qstep * hf) {
+        for (int g = q / hf; g < P.GT; g += qstep) {
+          const int j = tt * P.GT + g;
+          if (j >= G) break;
+          const int c0 = r * g + half * part;  // this thread's first column
+          float m = -INFINITY;
+          for (int i = 0; i < half; i += 4) {
+            const float4 v = at4(S, fq, c0 + i);
+            m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+          }
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+          float den = 0.0f, num = 0.0f;
+          for (int i = 0; i < half; i += 4) {
+            const float4 sv = at4(S, fq, c0 + i), kv = at4(KV, fq, c0 + i);
+            const float e0 = expf(sv.x - m), e1 = expf(sv.y - m), e2 = expf(sv.z - m), e3 = expf(sv.w - m);
+            den += e0;
+            num = fmaf(e0, kv.x, num);
+            den += e1;
+            num = fmaf(e1, kv.y, num);
+            den += e2;
+            num = fmaf(e2, kv.z, num);
+            den += e3;
+            num = fmaf(e3, kv.w, num);
+          }
+          den += __shfl_xor_sync(0xffffffffu, den, 1);  // the same sum in both threads of the pair
+          num += __shfl_xor_sync(0xffffffffu, num, 1);
+          if (part == 0) {
+            const size_t pi = (size_t)g * pk.H + ftile * F + fq;
+            if (in_bounds((long long)((pooled_tile - P.pooled) + pi), P.pooled_elems, P.flag))
+              pooled_tile[pi] = bf16_bits(__fdiv_rn(num, den));
+          }
+        }
+      }
     } else {
       for (int g = (int)threadIdx.x / hf; g < P.GT; g += 2 * gstep) {
         const int j = tt * P.GT + g;

@@ -187,6 +187,7 @@ SMALL = [
     (128, 64, 2, 0, 3, 2 * 70 + 1),
     (256, 512, 4, 1, 2, 128 + 5),
     (256, 512, 128, 0, 2, 128 * 3 + 77),
+    (256, 256, 64, 0, 2, 64 * 9 + 13),  # long groups at ratio 64 (the two-thread pool, four groups a tile)
     (192, 256, 8, 0, 1, 8 * 40),
     (128, 64, 1, 0, 2, 37),
     (128, 32, 3, 0, 1, 2),
