@@ -302,7 +302,8 @@ def run_ours(args, rank, world, local):
             "tokens_per_s": tokens_s, "kernel_ms": kms, "roofline": roof,
             "e2e": {"value": entries / (e2e_ms * 1e-3), "unit": "entries/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches, "clocks": clk}
+            "gpu_launches": launches, "clocks": clk,
+            "launch_geometry": comp.prefill_geometry(B, N) if tc else None}
     comp.close()
     line["chunked_prefill"] = bench_chunked(args, torch, csa, synthetic, device, peaks, world)
     line["other_prefill"] = [bench_prefill_workload(args, torch, csa, synthetic, device, peaks, world, wl)
@@ -414,6 +415,7 @@ def prefill_line(name, comp, layer, B, N, G, ms, kms, world, peaks):
     peak = peaks["bf16_tflops"] / 3.0
     return {"workload": name, "value": B * G * world / (ms * 1e-3), "unit": "entries/s", "ms_per_step": ms,
             "tokens_per_s": B * N * world / (ms * 1e-3), "kernel_ms": kms, "tensor_cores": comp.uses_tensor_cores(),
+            "launch_geometry": comp.prefill_geometry(B, N) if comp.uses_tensor_cores() else None,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak}}
 
@@ -555,10 +557,12 @@ def bench_chunked(args, torch, csa, synthetic, device, peaks, world):
     flops = 2.0 * B * N * layer.dim * 2 * layer.width
     achieved = flops / (kms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"] / 3.0
+    geometry = comp.prefill_geometry(B, N, p0)
     comp.close()
     return {"workload": f"Flash CSA chunk: B={B}, {N} tokens at start_pos {p0} after a {p0}-token prefill",
             "value": B * G * world / (ms * 1e-3), "unit": "entries/s", "ms_per_step": ms, "steps": K,
             "tokens_per_s": B * N * world / (ms * 1e-3), "kernel_ms": kms, "gpu_launches": launches,
+            "launch_geometry": geometry,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": None,
                          "kernel": "chunk_carry_kernel + csa_prefill_tc (projection + fused pool)"}}

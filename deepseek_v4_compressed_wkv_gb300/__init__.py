@@ -36,6 +36,7 @@ ABI_FUNCTIONS = ("csa_options_default", "csa_compressor_create", "csa_compressor
                  "csa_state_export", "csa_device_status", "csa_compressor_destroy", "csa_last_error",
                  "csa_fp4_e4m3_roundtrip", "csa_rope_table", "csa_set_profile_events", "csa_kernel_launches",
                  "csa_uses_tensor_cores", "csa_compress_prefill_noalloc", "csa_compress_prefill_into",
+                 "csa_prefill_geometry",
                  "csa_fp4_e8m0_roundtrip", "csa_compressor_set_gate_bias")
 
 
@@ -98,6 +99,7 @@ def load_library(build_if_missing: bool = True):
             "csa_set_profile_events": ([P, P, P], I),
             "csa_kernel_launches": ([P], I64),
             "csa_uses_tensor_cores": ([P], I),
+            "csa_prefill_geometry": ([P, I, I, I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)], I),
             "csa_compress_prefill_noalloc": ([P, P, I, I, I, I, P, P], I),
             "csa_compress_prefill_into": ([P, P, I, I, I, I, P, I, P], I),
         }
@@ -361,6 +363,14 @@ class Compressor:
 
     def uses_tensor_cores(self) -> bool:
         return bool(_check(self._lib.csa_uses_tensor_cores(self._h), "csa_uses_tensor_cores"))
+
+    def prefill_geometry(self, B: int, N: int, start_pos: int = 0) -> dict:
+        """The tensor-core prefill's launch geometry for B sequences of N tokens at start_pos:
+        {"token_tile": 256 | 224 | 128, "k_split": 1 | 2}."""
+        tok, split = ctypes.c_int(), ctypes.c_int()
+        _check(self._lib.csa_prefill_geometry(self._h, B, N, start_pos, ctypes.byref(tok), ctypes.byref(split)),
+               "csa_prefill_geometry")
+        return {"token_tile": tok.value, "k_split": split.value}
 
     def kernel_launches(self) -> int:
         return _check(self._lib.csa_kernel_launches(self._h), "csa_kernel_launches")

@@ -516,6 +516,23 @@ int64_t csa_kernel_launches(const csa_compressor* c) {
   return c->launches;
 }
 
+int csa_prefill_geometry(const csa_compressor* c, int B, int N, int start_pos, int* token_tile, int* k_split) {
+  try {
+    if (!c || !token_tile || !k_split) return fail(CSA_ERR_ARG, "csa_prefill_geometry: NULL argument");
+    if (B < 1 || N < 1 || start_pos < 0) return fail(CSA_ERR_ARG, "csa_prefill_geometry: bad shape");
+    if (int rc = check_device(c, "csa_prefill_geometry")) return rc;
+    static const uint16_t aligned[8] = {};
+    if (!csa::prefill_tc_supported(c, aligned))
+      return fail(CSA_ERR_STATE, "csa_prefill_geometry: this compressor runs the CUDA-core projection");
+    const csa::PrefillPlan plan = csa::prefill_tc_plan(c, B, N, csa::make_chunk(start_pos, N, c->ratio));
+    *token_tile = plan.tok;
+    *k_split = plan.split;
+    return CSA_OK;
+  } catch (...) {
+    return fail(CSA_ERR_INTERNAL, "csa_prefill_geometry: unexpected exception");
+  }
+}
+
 int csa_device_status(csa_compressor* c, csa_stream_t stream) {
   if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
   if (int rc = check_device(c, "csa_device_status")) return rc;

@@ -280,6 +280,14 @@ int csa_uses_tensor_cores(const csa_compressor* c);
 /* Number of kernels this handle has enqueued since it was created (all calls). */
 int64_t csa_kernel_launches(const csa_compressor* c);
 
+/* The launch geometry a tensor-core prefill of B sequences of N tokens at start_pos would use on
+ * the current device (no counterpart on the pages; for tuning and measurement): *token_tile = the
+ * tokens per tile including the overlapped halo (256, 224 or 128), *k_split = 1 (one CTA per tile)
+ * or 2 (a cluster of two CTAs per tile, each half of dim).  Returns CSA_OK, CSA_ERR_ARG for a
+ * NULL pointer or a bad shape, or CSA_ERR_STATE when the shape runs the CUDA-core projection
+ * (csa_uses_tensor_cores(c) == 0).  Host only: nothing is enqueued. */
+int csa_prefill_geometry(const csa_compressor* c, int B, int N, int start_pos, int* token_tile, int* k_split);
+
 /* Host-only: the YaRN RoPE table the library uploads ("Module compress", yarn_freqs_cis):
  * cos_out, sin_out [npos][rope_dim/2] f32 host for positions pos0..pos0+npos-1, computed in
  * double precision and rounded once to f32. */

@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import deepseek_v4_compressed_wkv_gb300 as csa
 import synthetic
 from _util import layer_inputs
 from test_gpu_parity import DEV, check_entries, dev_bits, make_pair, to_np
@@ -62,3 +63,31 @@ def test_pool_token_pairs_ratio2_prefill():
     assert ref["G"] == N // 2
     check_entries(to_np(got), ref["prequant"], 1, "pairs prefill")
     assert g.device_status() == 0
+
+
+def test_launch_geometry_of_the_measured_instances():
+    """The launch geometry the prefill chooses (csa_prefill_geometry): the indexer's 4 packed tiles
+    split over K at the 224-token tile (76 clusters of two CTAs fill the 152 SMs), the Flash CSA
+    layer's 16 tiles one CTA each at 224 tokens (two full waves), HCA and one long ratio-128
+    sequence at the 256-token tile; a forced split is reported as forced, and a shape the
+    CUDA-core projection runs is refused."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    def geo(wl, **opt):
+        L = wl.layers[0]
+        c = csa.Compressor(L.dim, L.head_dim, L.ratio, L.overlap, max_batch=max(wl.batch, 1), **opt)
+        try:
+            return c.prefill_geometry(wl.batch, wl.tokens[0])
+        finally:
+            c.close()
+    if sms == 152:  # the choices below are the model's for the 152-SM part
+        assert geo(synthetic.INDEXER) == {"token_tile": 224, "k_split": 2}
+        assert geo(synthetic.FLASH_CSA) == {"token_tile": 224, "k_split": 1}
+        assert geo(synthetic.HCA) == {"token_tile": 256, "k_split": 1}
+    assert geo(synthetic.INDEXER, prefill_split=1)["k_split"] == 1
+    assert geo(synthetic.FLASH_CSA, prefill_split=2)["k_split"] == 2
+    narrow = csa.Compressor(128, 32, 3, 0, rope_dim=16)  # packed tile narrower than 128 rows: the CUDA-core projection
+    try:
+        with pytest.raises(csa.CSAError):
+            narrow.prefill_geometry(1, 30)
+    finally:
+        narrow.close()
