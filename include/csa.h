@@ -153,7 +153,11 @@ int csa_compressor_set_gate_bias(csa_compressor* c, const float* ape, csa_stream
  *    group (and, overlapped, of the last complete group).
  * Entry j of sequence b (group start_pos / ratio + j, RoPE position ratio * that group) goes to
  * row b * G + j of out ([B][G][..]).  Returns G (0 means "no entry", the pages' None) or a
- * negative csa_status.  Requires ratio * (last group) < max_pos when RoPE is on. */
+ * negative csa_status.  Requires ratio * (last group) < max_pos when RoPE is on.
+ * The launch geometry (token tile, K split; csa_prefill_geometry) is chosen per call on the host.
+ * The first prefill on a device also sets the kernels' shared-memory attribute and asks the
+ * device how many two-CTA clusters it holds; make it before capturing prefill calls into a CUDA
+ * graph. */
 int csa_compress_prefill(csa_compressor* c, const uint16_t* x, int B, int N, int start_pos, int slot_offset,
                          const csa_out* out, csa_stream_t stream);
 
