@@ -245,3 +245,43 @@ def test_chunk_rewriting_decoded_positions_then_decode(ratio, overlap):
     assert emitted >= B  # the group completes within the steps
     check_state(g, o, "state after the chunk and the decode steps")
     assert g.device_status() == 0
+
+
+@pytest.mark.parametrize("split", [1, 2])
+def test_prefill_and_chunk_in_a_cuda_graph(split):
+    """A prefill and a chunk continuing it, captured once in a CUDA graph after one eager pass (the
+    library sets its kernel attributes, queries the device and sizes its scratch on first use) and
+    replayed twice: the entries equal the eager pass's bit for bit and the oracle's within the
+    parity tolerance, in both launch geometries."""
+    layer = synthetic.Layer(256, 128, 4, 1, 1.0 / math.sqrt(256), gate_scale=2.0, rope_dim=64, fp4=1)
+    B, N1, N2 = 2, 4 * 45 + 2, 4 * 20 + 3
+    g, o = make_pair(29, layer, max_batch=B, split=split)
+    x, *_ = layer_inputs(29, layer, B, N1 + N2)
+    x1, x2 = (dev_bits(np.ascontiguousarray(x[:, a:b])) for a, b in ((0, N1), (N1, N1 + N2)))
+    outs = [g._alloc_out(B * ((p + n) // 4 - p // 4), DEV, prequant=True) for p, n in ((0, N1), (N1, N2))]
+
+    def run():
+        g.prefill(x1, start_pos=0, out=outs[0])
+        g.prefill(x2, start_pos=N1, out=outs[1])
+
+    run()
+    torch.cuda.synchronize()
+    eager = [to_np(ob) for ob in outs]
+    for ob in outs:
+        for t in ob.values():
+            t.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    for k, ob in enumerate(outs):
+        got = to_np(ob)
+        for key in eager[k]:
+            assert np.array_equal(got[key], eager[k][key]), (k, key)
+    r1 = o.prefill(np.ascontiguousarray(x[:, :N1]))
+    r2 = o.prefill(np.ascontiguousarray(x[:, N1:]), start_pos=N1)
+    check_entries(to_np(outs[0]), r1["prequant"], 1, "graph prefill")
+    check_entries(to_np(outs[1]), r2["prequant"], 1, "graph chunk")
+    assert g.device_status() == 0
