@@ -61,7 +61,10 @@ static_assert(kPartBytes <= kRingBytes, "the partial tile is staged in the free 
 constexpr int kEpiThreads = 256;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kTmemCols = 2 * kTok;
-constexpr int kFinThreads = 128;  // one warp per SM sub-partition: fits beside a projection CTA
+// One warp per SM sub-partition: fits beside a projection CTA, whose three warps on a sub-partition
+// (135 registers each) leave room for one finish warp (87 registers).  More registers in either kernel
+// break that overlap: at 142 projection registers a decode step measured 0.254 of HBM instead of 0.29.
+constexpr int kFinThreads = 128;
 
 __device__ __forceinline__ void add4(float4& a, const float4& v) {
   a.x += v.x;

@@ -322,7 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t r[32];
           tmem_ld32(base + 32 * j, r);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[32 * j + i] += __uint_as_float(r[i]);
+          for (int i = 0; i < 32; i += 2)
+            fadd2(acc[32 * j + i], acc[32 * j + i + 1], __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
         }
       }
       tc_fence_before();
