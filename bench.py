@@ -565,7 +565,7 @@ def bench_chunked(args, torch, csa, synthetic, device, peaks, world):
             "launch_geometry": geometry,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": None,
-                         "kernel": "chunk_carry_kernel + csa_prefill_tc (projection + fused pool)"}}
+                         "kernel": "csa_prefill_tc (projection + fused pool, the carried candidates read from the state)"}}
 
 
 def bench_decode(args, torch, csa, synthetic, device, peaks, world, rank):

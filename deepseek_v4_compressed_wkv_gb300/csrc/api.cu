@@ -110,6 +110,7 @@ void free_all(csa_compressor* c) {
   cudaFree(c->dec_part);
   cudaFree(c->dec_acc);
   cudaFree(c->dec_acc_pos);
+  cudaFree(c->prefill_order);
   cudaFree(c->dec_pos);
 }
 
@@ -343,6 +344,7 @@ int csa_compressor_create_ex(int dim, int H, int ratio, int overlap, const csa_o
     alloc((void**)&c->dev_flag, sizeof(int));
     alloc((void**)&c->dec_acc, (size_t)o.max_batch * 3 * H * sizeof(float));
     alloc((void**)&c->dec_acc_pos, (size_t)o.max_batch * pk.ntiles * sizeof(int));
+    alloc((void**)&c->prefill_order, (size_t)o.max_batch * pk.ntiles * 2 * sizeof(int));
     alloc((void**)&c->dec_pos, (size_t)o.max_batch * sizeof(int32_t));
     if (o.rope_dim > 0) {
       const size_t n = (size_t)o.max_pos * (o.rope_dim / 2);
@@ -359,6 +361,7 @@ int csa_compressor_create_ex(int dim, int H, int ratio, int overlap, const csa_o
     }
     if (e == cudaSuccess) e = cudaMemset(c->dev_flag, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(c->dec_acc_pos, 0xFF, (size_t)o.max_batch * pk.ntiles * sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(c->prefill_order, 0, (size_t)o.max_batch * pk.ntiles * 2 * sizeof(int));
     if (e == cudaSuccess && csa::launch_state_reset(c, 0, o.max_batch, 0) != cudaSuccess) e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
@@ -479,6 +482,11 @@ int csa_state_reset(csa_compressor* c, int slot_begin, int slot_count, csa_strea
   CSA_CUDA(csa::invalidate_decode_acc(c, slot_begin, slot_count, (cudaStream_t)stream),
            "invalidate decode running values");
   CSA_CUDA(csa::launch_state_reset(c, slot_begin, slot_count, (cudaStream_t)stream), "state reset launch");
+  // the chunk ordering counters are zero after every call that completed; a call that timed out
+  // may have left one set
+  CSA_CUDA(cudaMemsetAsync(c->prefill_order + (size_t)slot_begin * c->pk.ntiles * 2, 0,
+                           (size_t)slot_count * c->pk.ntiles * 2 * sizeof(int), (cudaStream_t)stream),
+           "reset chunk ordering counters");
   c->launches += slot_count > 0;
   return CSA_OK;
 }

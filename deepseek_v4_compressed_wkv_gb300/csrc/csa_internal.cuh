@@ -426,6 +426,8 @@ struct csa_compressor {
                             //   valid); prefill invalidates every entry of its sequences, the
                             //   decode keeps a sequence's in its first entry
   int32_t* dec_pos;         // [max_batch] device copy of the positions of a host-array decode call
+  int* prefill_order;       // [max_batch][ntiles][2] counters ordering a chunk's state read before
+                            // its later tiles' state writes (zero between calls)
   bool dec_early_start;     // the next decode may start its weight loads before the preceding
                             // kernel ends (false right after set_weights rewrote the planes)
   cudaEvent_t prof_start, prof_stop;  // optional events around the dominant kernel

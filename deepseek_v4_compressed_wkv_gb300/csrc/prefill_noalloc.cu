@@ -17,8 +17,7 @@
 namespace {
 
 // Largest scratch this entry point can use: the pooled bf16 values (B * token tiles * groups *
-// H * 2 bytes) and, for a chunk at start_pos > 0, the carried softmax values of its first group
-// (B * H * 12 bytes, after the pooled values).  Every GPU that loads the library holds the
+// H * 2 bytes).  Every GPU that loads the library holds the
 // array until the process exits.
 constexpr size_t kScratchBytes = 16u << 20;
 
@@ -71,7 +70,7 @@ int noalloc_call(csa_compressor* c, const uint16_t* x, int B, int N, int start_p
     if (plan.bytes > kScratchBytes)
       return csa_internal_fail(CSA_ERR_ARG,
                                "csa_compress_prefill_noalloc: B x N too large for the preallocated scratch "
-                               "(limit: 16 MiB of pooled values and, for a chunk, carried softmax values)");
+                               "(limit: 16 MiB of pooled values)");
     const int dev = c->device;
     if (dev < 0 || dev >= kMaxDevices)
       return csa_internal_fail(CSA_ERR_CUDA, "csa_compress_prefill_noalloc: device index out of range");

@@ -29,9 +29,10 @@
 //
 // A chunk at position p0 > 0 (Chunk) tiles the tokens from the start of the open group: the
 // first tile's leading a = p0 % ratio token columns (and the overlapped halo) are earlier
-// tokens, whose contribution to the first group (overlapped: the first two groups) arrives as
-// running softmax values computed from the state before this kernel (chunk_carry_kernel);
-// their x rows read as zeros and their columns are not pooled.
+// tokens, whose contribution to the first group (overlapped: the first two groups) the first
+// tile's CTAs read from the state as running softmax values, before any CTA of the call rewrites
+// those slots (a later tile that writes the state waits for that read: a counter per sequence,
+// packed tile and K half); their x rows read as zeros and their columns are not pooled.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -93,8 +94,9 @@ struct Params {
   Packing pk;
   float* state;
   uint16_t* pooled;        // [B][ntt][GT][H] bf16 bits
-  const float* carry;      // [B][1 + overlap][3][H] running softmax values of the candidates
-                           // of the first groups that are earlier than the chunk, or null
+  int carry;               // the first groups have candidates earlier than the chunk (in the state)
+  int order_writers;       // carry: later token tiles of a sequence that write the state
+  int* order;              // carry: [max_batch][ntiles][2] counters, the first tile's state read done
   int* flag;
   int* acc_pos;            // [max_batch][ntiles] decode running values: marked invalid for the call's sequences
   long long state_elems, pooled_elems;  // extents checked by the bounds-checked build
@@ -213,6 +215,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = (uint32_t*)(recv_bar + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   int* issued_s = (int*)(tmem_slot + 2);  // stages the producer issued (read by the clean-up)
+  int* order_seen = (int*)(tmem_slot + 3);  // a chunk's later tile: the first tile's state read was
+                                            // already done when the stages started
+  // a chunk's first tile: the running softmax values (max, denominator, numerator) of the carried
+  // candidates of group j and feature f0 + i at [3 * (j * hf + i)], at most 2 x 32 or 64 values
+  float* carried = (float*)(tmem_slot + 4);
+  static_assert(16 * 8 + 16 + 3 * 64 * 4 <= 1024, "barriers, flags and carried values fit their region");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ftile = blockIdx.x / kSplit, rank = blockIdx.x % kSplit, tt = blockIdx.y, b = blockIdx.z;
@@ -238,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(mma_done, 1);
     mbar_init(recv_bar, 1);
     *abort_flag = 0;
+    *order_seen = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_map(&map_x);
   }
@@ -301,6 +310,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     //      columns 128*h .. up to 128 columns): the chunk accumulators into registers in chunk
     //      order, then staged as [packed row][token] f32 in the stage buffers (idle once the last
     //      chunk has completed)
+    if (P.carry) {
+      // idle until the first chunk completes: the first tile reads the candidates it carries
+      // from the state (their running values, for the pool), then lets the later tiles of the
+      // sequence rewrite it; a later tile looks whether that read is already done (then its state
+      // writes need not wait)
+      const int e = (int)threadIdx.x - 64;
+      if (tt == 0) {
+        const int F = P.pk.ft, hf = F / kSplit, f0 = rank * hf, j = e / hf;
+        if (j < 1 + P.overlap) {
+          const int f = f0 + e % hf;
+          const float* sq = P.state + (size_t)(P.slot_offset + b) * P.slots * P.ncol + ftile * kRows + f;
+          // candidate i of group j: group 0 takes, overlapped, branch B of group g0 - 1 (parity
+          // (g0 - 1) % 2; none for g0 = 0, the padded branch) and branch A of the open group's
+          // tokens before p0 (parity g0 % 2, slots 0 .. a - 1), non-overlapped those tokens;
+          // overlapped group 1 takes branch B of those tokens
+          const int open = 4 * (P.g0 & 1), prev = 4 * ((P.g0 + 1) & 1);
+          const int nprev = P.overlap && j == 0 && P.g0 > 0 ? 4 : 0, n = nprev + P.a;
+          auto cand = [&](int i, bool score) -> float {
+            int slot, kind;
+            if (!P.overlap) {
+              slot = i;
+              kind = score ? S : KV;
+            } else if (i < nprev) {
+              slot = prev + i;
+              kind = score ? S_B : KV_B;
+            } else {
+              slot = open + i - nprev;
+              kind = j == 0 ? (score ? S_A : KV_A) : (score ? S_B : KV_B);
+            }
+            return sq[(size_t)slot * P.ncol + kind * F];
+          };
+          float m = -INFINITY, den = 0.0f, num = 0.0f;
+          for (int i = 0; i < n; ++i) m = fmaxf(m, cand(i, true));
+          if (m > -INFINITY)
+            for (int i = 0; i < n; ++i) {
+              const float x = expf(cand(i, true) - m);
+              den += x;
+              num = fmaf(x, cand(i, false), num);
+            }
+          carried[3 * e] = m;
+          carried[3 * e + 1] = den;
+          carried[3 * e + 2] = num;
+        }
+        // every value read (and used) before the later tiles may write: the epilogue warps meet,
+        // then one thread signals
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+        if (e == 0 && P.order_writers > 0)
+          counter_release_add(P.order + ((size_t)(P.slot_offset + b) * P.pk.ntiles + ftile) * 2 + rank,
+                              P.order_writers);
+      } else if (e == 0) {
+        *order_seen = counter_ready(P.order + ((size_t)(P.slot_offset + b) * P.pk.ntiles + ftile) * 2 + rank);
+      }
+    }
     const int q = warp & 3, h = (warp - 2) >> 2;
     const int row = 32 * q + lane;
     const int hcols = h ? kTok - 128 : 128;  // a multiple of 32 (0: the 128-token tile's second half idles)
@@ -361,10 +423,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Packing& pk = P.pk;
   const int F = pk.ft, hf = F / kSplit, f0 = rank * hf;  // this CTA's features of the tile
   float* stg = (float*)smem;
+  // the state slots of the sequence's unfinished group (and, overlapped, of the last complete
+  // group) that this tile rewrites: virtual tokens [max(own0, s_lo), own1)
+  const int own0 = max(tt * P.T, P.a), own1 = min(tt * P.T + P.T, P.a + P.N);
+  const int s_lo = P.overlap ? 4 * P.G - (P.G >= 1 ? 4 : 0) : P.ratio * P.G;
+  int* order = P.carry ? P.order + ((size_t)(P.slot_offset + b) * pk.ntiles + ftile) * 2 + rank : nullptr;
   if (!aborted) {
-    // a chunk's carry kernel (the grid this launch may overlap) has finished reading the state
-    // and written the carried values; a no-op for a launch without that predecessor
-    griddep_wait();
     // the prefill rewrites the sequence's state: its decode running values (kept per packed
     // tile) are no longer valid
     if (rank == 0 && tt == 0 && threadIdx.x == 0) P.acc_pos[(size_t)(P.slot_offset + b) * pk.ntiles + ftile] = -1;
@@ -452,6 +516,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     return v;
   };
 
+  // a later tile that rewrites state slots waits until the first tile has read its carried
+  // candidates (also when aborted, so that the counter returns to zero); a wait that runs out
+  // leaves the state unwritten and raises the time-out bit
+  bool late = false;
+  if (P.carry && tt > 0 && max(own0, s_lo) < own1) {
+    late = __syncthreads_or(threadIdx.x == 0 && !(*order_seen ? (atomicSub(order, 1), true) : counter_take(order, kWait)));
+    if (late && threadIdx.x == 0) atomicOr(P.flag, 4);
+  }
   if (!aborted) {
     const int r = P.ratio, G = P.G;
     const int col0 = ftile * kRows;  // first packed column of this tile
@@ -459,11 +531,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     //    of the last complete group that this tile owns; thread et < nk * hf writes one packed
     //    column of this CTA's features.  Virtual group G is absolute group gend.
     const int et = threadIdx.x;
-    if (et < pk.nk * hf) {
+    if (et < pk.nk * hf && !late) {
       const int kind = et / hf, prow = kind * F + f0 + et % hf;
       const size_t st0 = (size_t)(P.slot_offset + b) * P.slots * P.ncol + col0 + prow;
       float* st = P.state + st0;
-      const int own0 = max(tt * P.T, P.a), own1 = min(tt * P.T + P.T, P.a + P.N);
       auto put = [&](int tok, int slot) {  // token tok is the tile's column tok - t0
         if (in_bounds((long long)st0 + (long long)slot * P.ncol, P.state_elems, P.flag))
           st[slot * P.ncol] = at(kind, f0 + et % hf, tok - t0);
@@ -553,12 +624,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __fdiv_rn(num, den);
     };
     // a chunk's first groups hold tokens earlier than the chunk (virtual index < a, or the halo):
-    // those arrive as running values; the rest are this tile's columns.  Group 0: branch A of
-    // tokens a..3 (non-overlapped: tokens a..ratio-1); overlapped group 1: branch B of tokens
-    // a..3 and branch A of tokens 4..7.
+    // those arrive as the running values read while the stages streamed; the rest are this tile's columns.  Group 0:
+    // branch A of tokens a..3 (non-overlapped: tokens a..ratio-1); overlapped group 1: branch B
+    // of tokens a..3 and branch A of tokens 4..7.
     auto pool_carried = [&](int j) -> float {
-      const float* cr = P.carry + ((size_t)b * (1 + P.overlap) + j) * 3 * pk.H + ftile * F + f;
-      const float mc = cr[0], dc = cr[pk.H], nc = cr[2 * pk.H];  // max, denominator, numerator
+      const float* cv = carried + 3 * (j * hf + f - f0);
+      const float mc = cv[0], dc = cv[1], nc = cv[2];  // max, denominator, numerator
       const int kk = P.overlap ? KV_A : KV, ks = P.overlap ? S_A : S;
       const int c0 = P.halo + 4 * j;  // this group's first column (branch A when overlapped)
       const int n = P.overlap ? 4 : r, i0 = j == 0 ? P.a : 0, iB = j == 1 ? P.a : 4;
@@ -657,58 +728,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Running softmax values (max, denominator, numerator) per feature of the candidates of a
-// chunk's first groups that are earlier than the chunk, from the state (absolute group g0 is
-// the open group, its tokens before p0 in slots 0 .. a-1, overlapped of parity g0 % 2):
-//  [b][0]: group g0 - the open group's earlier tokens (overlapped: their branch A) and,
-//          overlapped, branch B of group g0 - 1 (parity (g0 - 1) % 2; none for g0 = 0, the
-//          padded branch);
-//  [b][1]: overlapped only, group g0 + 1 - branch B of the open group's earlier tokens.
-// Layout [B][1 + overlap][3][H] f32; an empty set gives (-inf, 0, 0).  Grid (H / 128, B), one
-// thread per feature.  The projection kernel that follows starts at once (programmatic
-// dependent launch): it reads these values, and writes state slots, only after its wait.
-template <class Cand>
-__device__ __forceinline__ void running_softmax(int n, Cand cand, float* out, int H) {
-  float m = -INFINITY, den = 0.0f, num = 0.0f;
-  for (int i = 0; i < n; ++i) m = fmaxf(m, *cand(i, true));
-  if (m > -INFINITY)
-    for (int i = 0; i < n; ++i) {
-      const float e = expf(*cand(i, true) - m);
-      den += e;
-      num = fmaf(e, *cand(i, false), num);
-    }
-  out[0] = m;
-  out[H] = den;
-  out[2 * H] = num;
-}
-
-__global__ void __launch_bounds__(128) chunk_carry_kernel(const float* __restrict__ state, Packing pk, int overlap,
-                                                          int slots, int slot_offset, Chunk ck,
-                                                          float* __restrict__ carry, long long carry_elems,
-                                                          int* flag) {
-  // started early behind the preceding kernel, which may write the state read here (and the
-  // tokens that the projection launched behind this kernel reads): both wait for it here
-  griddep_wait();
-  griddep_launch_dependents();
-  const int b = blockIdx.y, f = blockIdx.x * blockDim.x + threadIdx.x;
-  const int ncol = pk.cols(), H = pk.H;
-  if (f >= H) return;
-  const float* st = state + (size_t)(slot_offset + b) * slots * ncol;
-  float* out = carry + (size_t)b * (1 + overlap) * 3 * H + f;
-  if (!in_bounds((long long)((size_t)(b + 1) * (1 + overlap) * 3 * H) - 1, carry_elems, flag)) return;
-  if (!overlap) {
-    running_softmax(ck.a, [&](int i, bool score) { return st + (size_t)i * ncol + pk.col(score ? S : KV, f); }, out, H);
-    return;
-  }
-  const int open = 4 * (ck.g0 & 1), prev = 4 * ((ck.g0 + 1) & 1), nprev = ck.g0 > 0 ? 4 : 0;
-  running_softmax(nprev + ck.a, [&](int i, bool score) {
-    return i < nprev ? st + (size_t)(prev + i) * ncol + pk.col(score ? S_B : KV_B, f)
-                     : st + (size_t)(open + i - nprev) * ncol + pk.col(score ? S_A : KV_A, f);
-  }, out, H);
-  running_softmax(ck.a, [&](int i, bool score) { return st + (size_t)(open + i) * ncol + pk.col(score ? S_B : KV_B, f); },
-                  out + 3 * H, H);
-}
-
 // The entries in their own kernel: a CTA of 128 threads takes 128 / tpe consecutive entries (one
 // CTA per entry at H = 512); the gain and RoPE factors (written before this launch's predecessor
 // started) are read before the wait for the projection kernel.
@@ -731,9 +750,15 @@ bool prefill_tc_supported(const csa_compressor* c, const void* x) {
 
 namespace {
 
-// Offset of the carried running softmax values ([B][1 + overlap][3][H] f32) after the pooled
-// scratch.
-size_t carry_offset(size_t pooled_bytes) { return (pooled_bytes + 255) & ~(size_t)255; }
+// The token tiles after the first that rewrite state slots of a chunk whose first tile reads
+// candidates from the state (the kernel's own test, for tiles 1 .. ntt - 1).
+int order_writers(const csa_compressor* c, const tc::Params& P, int N) {
+  const int s_lo = c->overlap ? 4 * P.G - (P.G >= 1 ? 4 : 0) : c->ratio * P.G;
+  int n = 0;
+  for (int tt = 1; tt < P.ntt; ++tt)
+    n += std::max(std::max(tt * P.T, P.a), s_lo) < std::min(tt * P.T + P.T, P.a + N);
+  return n;
+}
 
 // Tokens of a tile owned by it (the overlapped tile also loads the 4 tokens before it).
 int owned_tokens(const csa_compressor* c, int tok) {
@@ -868,17 +893,17 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
   P.pk = c->pk;
   P.state = c->state;
   P.pooled = (uint16_t*)scratch;
-  P.carry = nullptr;
+  P.carry = chunk_needs_carry(ck, c->overlap);
+  P.order_writers = P.carry ? order_writers(c, P, N) : 0;
+  P.order = c->prefill_order;
   P.ape = c->ape_set ? c->ape : nullptr;
   P.flag = c->dev_flag;
   P.acc_pos = c->dec_acc_pos;
   P.state_elems = (long long)c->opt.max_batch * c->slots * P.ncol;
   // the pooled values' extent, for the bounds-checked build: what this launch writes, but never
-  // past the scratch it was given (the carried values, when present, follow the pooled ones)
+  // past the scratch it was given
   const size_t pooled_bytes = (size_t)B * P.ntt * P.GT * c->H * sizeof(uint16_t);
-  const bool has_carry = chunk_needs_carry(ck, c->overlap);
-  P.pooled_elems = (long long)(std::min(pooled_bytes, has_carry ? std::min(carry_offset(pooled_bytes), scratch_bytes)
-                                                                : scratch_bytes) / sizeof(uint16_t));
+  P.pooled_elems = (long long)(std::min(pooled_bytes, scratch_bytes) / sizeof(uint16_t));
   P.w = c->w_planes;
   P.wait_ns = tcx::kWaitNs;
   P.test_stall = 0;
@@ -889,25 +914,6 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
     P.wait_ns = 200000000ull;
   }
 #endif
-  if (has_carry) {
-    const size_t coff = carry_offset(pooled_bytes);
-    const long long carry_elems = (long long)std::min<size_t>((size_t)B * (1 + c->overlap) * 3 * c->H,
-                                                              scratch_bytes > coff ? (scratch_bytes - coff) / 4 : 0);
-    float* carry = (float*)((uint8_t*)scratch + coff);
-    cudaLaunchAttribute early[1];
-    early[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    early[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cc = {};
-    cc.gridDim = dim3((c->H + 127) / 128, B);
-    cc.blockDim = dim3(128, 1, 1);
-    cc.stream = s;
-    cc.attrs = early;
-    cc.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cc, chunk_carry_kernel, (const float*)c->state, c->pk, c->overlap, c->slots,
-                                       slot_offset, ck, carry, carry_elems, c->dev_flag);
-    if (e != cudaSuccess) return e;
-    P.carry = carry;
-  }
   CUtensorMap mx;
   {
     // x: [B][N][dim] bf16; out-of-range tokens (the halo before token 0, the tail past N) read as 0
@@ -938,13 +944,8 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
   Q.out = out;
   cudaError_t ea = set_smem_attr<TOK, SPLIT>();
   if (ea != cudaSuccess) return ea;
-  cudaLaunchAttribute pat[2];
+  cudaLaunchAttribute pat[1];
   int npat = 0;
-  if (P.carry) {  // started early only behind a chunk's carry kernel
-    pat[npat].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    pat[npat].val.programmaticStreamSerializationAllowed = 1;
-    ++npat;
-  }
   if (SPLIT > 1) {  // the two K halves of a tile: one cluster
     pat[npat].id = cudaLaunchAttributeClusterDimension;
     pat[npat].val.clusterDim.x = SPLIT;
@@ -981,12 +982,9 @@ PrefillPlan prefill_tc_plan(const csa_compressor* c, int B, int N, const Chunk& 
   const int T = owned_tokens(c, plan.tok);
   const int GT = T / c->ratio;
   const int ntt = (ck.a + N + T - 1) / T;
-  const size_t pooled = (size_t)B * ntt * GT * c->H * sizeof(uint16_t);
-  plan.bytes = chunk_needs_carry(ck, c->overlap)
-                   ? carry_offset(pooled) + (size_t)B * (1 + c->overlap) * 3 * c->H * sizeof(float)
-                   : pooled;
-  // the carry kernel (a chunk), the projection kernel, the entry kernel
-  plan.kernels = chunk_needs_carry(ck, c->overlap) + 1 + (ck.G > 0);
+  plan.bytes = (size_t)B * ntt * GT * c->H * sizeof(uint16_t);
+  // the projection kernel, the entry kernel
+  plan.kernels = 1 + (ck.G > 0);
   return plan;
 }
 

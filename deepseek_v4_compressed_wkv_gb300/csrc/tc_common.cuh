@@ -196,6 +196,31 @@ __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
 // have completed and their writes are visible (returns at once when the launch did not ask
 // for early start).  griddep_launch_dependents: this CTA no longer holds back the start of
 // the next launch in the stream (it starts once every CTA has said so or exited).
+// A counter in global memory that orders CTAs of one grid: the signalling CTA adds with release
+// semantics (its earlier memory accesses, and those of its threads before a CTA barrier, come
+// first); the waiting CTA polls with acquire loads, at most wait_ns, and takes one unit.
+__device__ __forceinline__ void counter_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// True when the counter already holds a unit (an acquire load, no wait).
+__device__ __forceinline__ bool counter_ready(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v > 0;
+}
+__device__ __forceinline__ bool counter_take(int* p, uint64_t wait_ns) {
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v > 0) break;
+    if (globaltimer() - t0 > wait_ns) return false;
+    __nanosleep(256);
+  }
+  atomicSub(p, 1);
+  return true;
+}
+
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -182,9 +182,7 @@ int csa_compress_prefill_into(csa_compressor* c, const uint16_t* x, int B, int N
  *  - scratch of at most 16 MiB: B * ceil((a + N) / T) * (T / ratio) * head_dim * 2 bytes of
  *    pooled values, with a = start_pos % ratio and T the tokens a tile owns (the launch takes a
  *    tile of 256, 224 or 128 tokens, chosen from the number of SMs of the device: at ratio 4
- *    overlapped T = 252, 220 or 124, else the largest multiple of ratio <= the tile), plus, for
- *    a chunk whose first group has earlier candidates, the carried softmax values, B * (1 +
- *    overlap) * 3 * head_dim * 4 bytes (after the pooled values, rounded up to 256).  Because T
+ *    overlapped T = 252, 220 or 124, else the largest multiple of ratio <= the tile).  Because T
  *    depends on the device, the CSA_ERR_ARG "too large" return is the authoritative check:
  *    larger calls return it without launching anything.
  * The first call on each device looks up the array's device address (with that device
@@ -226,7 +224,10 @@ int csa_compress_decode(csa_compressor* c, const uint16_t* x_tok, int B, const i
 int csa_compress_decode_dev(csa_compressor* c, const uint16_t* x_tok, int B, const int32_t* start_pos,
                             const csa_out* out, uint8_t* emitted, csa_stream_t stream);
 
-/* Resets state slots [slot_begin, slot_begin + slot_count): kv 0, score -inf. */
+/* Resets state slots [slot_begin, slot_begin + slot_count): kv 0, score -inf.  It also clears,
+ * for those sequences, the library's own per-call bookkeeping (the decode running values, and
+ * the counters that order a chunk's state read before its state writes, which a call that
+ * returned CSA_ERR_TIMEOUT may have left set). */
 int csa_state_reset(csa_compressor* c, int slot_begin, int slot_count, csa_stream_t stream);
 
 /* Number of float elements of each of the two exported state arrays. */
