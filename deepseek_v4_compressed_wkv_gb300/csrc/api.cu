@@ -550,9 +550,10 @@ int csa_device_status(csa_compressor* c, csa_stream_t stream) {
   CSA_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
   if (!flag) return CSA_OK;
   CSA_CUDA(cudaMemsetAsync(c->dev_flag, 0, sizeof(int), s), "clear device flag");
-  return fail((flag & 4) ? CSA_ERR_TIMEOUT : CSA_ERR_DEVICE, "device flag 0x%x:%s%s%s%s", flag, (flag & 1) ? " negative start_pos;" : "",
-              (flag & 2) ? " entry position beyond the RoPE table;" : "", (flag & 4) ? " wait budget exhausted;" : "",
-              (flag & 8) ? " index out of bounds (bounds-checked build);" : "");
+  return fail((flag & 4) ? CSA_ERR_TIMEOUT : CSA_ERR_DEVICE, "device flag 0x%x:%s%s%s%s%s", flag,
+              (flag & 1) ? " negative start_pos;" : "", (flag & 2) ? " entry position beyond the RoPE table;" : "",
+              (flag & 4) ? " wait budget exhausted;" : "", (flag & 8) ? " index out of bounds (bounds-checked build);" : "",
+              (flag & 16) ? " chunk ordering counters left set (bounds-checked build);" : "");
 }
 
 void csa_compressor_destroy(csa_compressor* c) {

@@ -84,6 +84,8 @@ struct EntryParams {
   csa_out out;
   long long out_rows;      // rows of the outputs (checked by the bounds-checked build)
   int* flag;
+  const int* order;        // a chunk with carried candidates: the call's ordering counters (the
+  int order_n;             // bounds-checked build checks that each is back at zero), else null
 };
 
 struct Params {
@@ -736,6 +738,13 @@ __global__ void __launch_bounds__(128) prefill_entry_kernel(const EntryParams P)
   const int t = threadIdx.x;
   const EntryPrep q = entry_prepare(P, blockIdx.x * (128 / P.tpe) + t / P.tpe, t % P.tpe);
   griddep_wait();  // the pooled values of the projection kernel
+#ifdef CSA_DEBUG_BOUNDS
+  // the projection grid has completed: every counter that ordered the first tile's state read
+  // before a later tile's state writes was taken as often as it was released
+  if (P.order && blockIdx.x == 0)
+    for (int i = t; i < P.order_n; i += 128)
+      if (P.order[i] != 0) atomicOr(P.flag, 16);
+#endif
   entry_finish(P, q, t, wss);
 }
 
@@ -940,6 +949,8 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
   Q.pooled = P.pooled;
   Q.out_rows = (long long)B * ck.bstride;
   Q.flag = c->dev_flag;
+  Q.order = P.carry ? c->prefill_order + (size_t)slot_offset * c->pk.ntiles * 2 : nullptr;
+  Q.order_n = B * c->pk.ntiles * 2;
   Q.ep = epi_params(c);
   Q.out = out;
   cudaError_t ea = set_smem_attr<TOK, SPLIT>();

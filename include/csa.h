@@ -246,7 +246,10 @@ int csa_state_export(const csa_compressor* c, float* kv, float* score, csa_strea
  * copies and tensor-core operations in flight finish and returned, leaving that call's outputs
  * and state slots undefined; the handle stays usable); else CSA_ERR_DEVICE: bit 1 a negative
  * start_pos, bit 2 an entry position beyond the RoPE table, bit 8 (only in the bounds-checked
- * build of the library) a store outside its buffer, skipped. */
+ * build of the library) a store outside its buffer, skipped, bit 16 (that build only) a counter
+ * ordering a prefill chunk's state read before its state writes not back at zero after the call.
+ * A time-out (bit 4) is also raised when a chunk's later token tile waited in vain for its first
+ * tile's state read; it then leaves the state unwritten. */
 int csa_device_status(csa_compressor* c, csa_stream_t stream);
 
 /* Frees the handle and its device memory (synchronises the device first). NULL is a no-op. */
