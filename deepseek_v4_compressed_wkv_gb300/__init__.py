@@ -48,7 +48,7 @@ class Options(ctypes.Structure):
     _fields_ = [("max_batch", ctypes.c_int), ("rope_dim", ctypes.c_int), ("rope_base", ctypes.c_float),
                 ("rope_factor", ctypes.c_float), ("rope_orig_len", ctypes.c_int), ("beta_fast", ctypes.c_float),
                 ("beta_slow", ctypes.c_float), ("max_pos", ctypes.c_int), ("fp4", ctypes.c_int),
-                ("eps", ctypes.c_float), ("prefill_split", ctypes.c_int)]
+                ("eps", ctypes.c_float), ("prefill_split", ctypes.c_int), ("prefill_pair", ctypes.c_int)]
 
 
 class Out(ctypes.Structure):
@@ -99,7 +99,8 @@ def load_library(build_if_missing: bool = True):
             "csa_set_profile_events": ([P, P, P], I),
             "csa_kernel_launches": ([P], I64),
             "csa_uses_tensor_cores": ([P], I),
-            "csa_prefill_geometry": ([P, I, I, I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)], I),
+            "csa_prefill_geometry": ([P, I, I, I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                                      ctypes.POINTER(ctypes.c_int)], I),
             "csa_compress_prefill_noalloc": ([P, P, I, I, I, I, P, P], I),
             "csa_compress_prefill_into": ([P, P, I, I, I, I, P, I, P], I),
         }
@@ -366,11 +367,11 @@ class Compressor:
 
     def prefill_geometry(self, B: int, N: int, start_pos: int = 0) -> dict:
         """The tensor-core prefill's launch geometry for B sequences of N tokens at start_pos:
-        {"token_tile": 256 | 224 | 128, "k_split": 1 | 2}."""
-        tok, split = ctypes.c_int(), ctypes.c_int()
-        _check(self._lib.csa_prefill_geometry(self._h, B, N, start_pos, ctypes.byref(tok), ctypes.byref(split)),
-               "csa_prefill_geometry")
-        return {"token_tile": tok.value, "k_split": split.value}
+        {"token_tile": 256 | 224 | 128, "k_split": 1 | 2, "cta_pair": 1 | 2}."""
+        tok, split, pair = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+        _check(self._lib.csa_prefill_geometry(self._h, B, N, start_pos, ctypes.byref(tok), ctypes.byref(split),
+                                              ctypes.byref(pair)), "csa_prefill_geometry")
+        return {"token_tile": tok.value, "k_split": split.value, "cta_pair": pair.value}
 
     def kernel_launches(self) -> int:
         return _check(self._lib.csa_kernel_launches(self._h), "csa_kernel_launches")

@@ -93,6 +93,7 @@ bool check_options(const csa_options& o, int H, std::string& why) {
   }
   else if (!(o.eps >= 0.0f)) why = "eps must be >= 0";
   else if (o.prefill_split < 0 || o.prefill_split > 2) why = "prefill_split must be 0 (chosen per call), 1 or 2";
+  else if (o.prefill_pair != 0 && o.prefill_pair != 2) why = "prefill_pair must be 0 (one CTA per packed tile) or 2";
   else return true;
   return false;
 }
@@ -283,6 +284,7 @@ void csa_options_default(csa_options* o) {
   o->fp4 = 1;
   o->eps = 1e-6f;
   o->prefill_split = 0;
+  o->prefill_pair = 0;
 }
 
 const char* csa_last_error(void) { return g_last_error.c_str(); }
@@ -524,7 +526,8 @@ int64_t csa_kernel_launches(const csa_compressor* c) {
   return c->launches;
 }
 
-int csa_prefill_geometry(const csa_compressor* c, int B, int N, int start_pos, int* token_tile, int* k_split) {
+int csa_prefill_geometry(const csa_compressor* c, int B, int N, int start_pos, int* token_tile, int* k_split,
+                         int* cta_pair) {
   try {
     if (!c || !token_tile || !k_split) return fail(CSA_ERR_ARG, "csa_prefill_geometry: NULL argument");
     if (B < 1 || N < 1 || start_pos < 0) return fail(CSA_ERR_ARG, "csa_prefill_geometry: bad shape");
@@ -535,6 +538,7 @@ int csa_prefill_geometry(const csa_compressor* c, int B, int N, int start_pos, i
     const csa::PrefillPlan plan = csa::prefill_tc_plan(c, B, N, csa::make_chunk(start_pos, N, c->ratio));
     *token_tile = plan.tok;
     *k_split = plan.split;
+    if (cta_pair) *cta_pair = plan.pair;
     return CSA_OK;
   } catch (...) {
     return fail(CSA_ERR_INTERNAL, "csa_prefill_geometry: unexpected exception");

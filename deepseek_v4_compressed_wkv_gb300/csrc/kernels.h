@@ -36,6 +36,8 @@ struct PrefillPlan {
   int split;     // 1: one CTA per tile; 2: a cluster of two CTAs per tile, each half of K
   size_t bytes;  // scratch bytes
   int kernels;   // kernels the call launches
+  int pair = 1;  // split 1: 2 when two CTAs (two packed tiles) share one MMA of M = 256 and the
+                 // token tile, each loading half of its tokens
 };
 PrefillPlan prefill_tc_plan(const csa_compressor* c, int B, int N, const Chunk& ck);
 // scratch_bytes: the capacity of `scratch` (>= plan.bytes), the extent the bounds-checked build

@@ -51,7 +51,6 @@ using namespace tcx;
 constexpr int kRows = 128;           // packed rows per tile (MMA M)
 constexpr int kTokMax = 256;         // tokens per tile including the halo (MMA N): 256, 224 or 128
 constexpr int kKb = 32;              // K elements per stage (one 64-byte swizzle row of bf16)
-constexpr int kStages = 5;
 constexpr int kPlaneBytes = kRows * kKb * 2;          // 8 KB
 static_assert(kRows == kPlaneTileRows && kKb == kPlaneTileK, "a stage is one tile of the plane layout");
 constexpr int kChunkKb = 8;         // K blocks per accumulator chunk (K = 256)
@@ -59,13 +58,17 @@ constexpr int kEpiThreads = 256;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kTmemCols = 512;      // two chunk accumulators of up to 256 columns (a power of two)
 
-// The sizes that follow from the token tile.  Epilogue warp half h drains token columns
+// The sizes that follow from the token tile and from whether a pair of CTAs shares it (PAIR = 2:
+// one MMA of M = 256 over two packed tiles, each CTA loading half of the tile's tokens, so that a
+// stage is smaller and more of them are in flight).  Epilogue warp half h drains token columns
 // [128 h, min(128 h + 128, TOK)).
-template <int TOK>
+template <int TOK, int PAIR = 1>
 struct Tile {
   static_assert(TOK == 256 || TOK == 224 || TOK == 128, "token tile");
-  static constexpr int kXBytes = TOK * kKb * 2;                  // 16 / 14 / 8 KB
-  static constexpr int kStageBytes = 3 * kPlaneBytes + kXBytes;  // 40 / 38 / 32 KB (multiples of 1 KB)
+  static_assert(PAIR == 1 || PAIR == 2, "CTA pair");
+  static constexpr int kXBytes = TOK / PAIR * kKb * 2;           // 16 / 14 / 8 KB (a pair: half)
+  static constexpr int kStageBytes = 3 * kPlaneBytes + kXBytes;  // 40 / 38 / 32 KB (a pair: 32 / 31 / 28)
+  static constexpr int kStages = PAIR > 1 ? 6 : 5;               // up to 200 KB
   // f32 staging row stride: a multiple of 4 floats, so that the epilogue moves 16-byte vectors,
   // and an odd number of 16-byte units, so that the vectors of 8 consecutive rows (a quarter-warp)
   // fall in distinct banks
@@ -195,12 +198,16 @@ __device__ __forceinline__ void entry_finish(const EntryParams& P, const EntryPr
 // received half-K sums to its own (the lower K half first) and pools its features: a tile of
 // 128 x TOK outputs is then computed at the wide token tile by twice the CTAs.
 
-template <int kTok, int kSplit>
+template <int kTok, int kSplit, int kPair>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap map_x, const Params P) {
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                      const Params P) {
   static_assert(kSplit == 1 || kSplit == 2, "K split");
-  constexpr int kStageBytes = Tile<kTok>::kStageBytes;
-  constexpr int kSmemStride = Tile<kTok>::kSmemStride;
+  static_assert(kSplit == 1 || kPair == 1, "a K split or a CTA pair, not both");
+  constexpr bool kP = kPair > 1;
+  constexpr int kStages = Tile<kTok, kPair>::kStages;
+  constexpr int kStageBytes = Tile<kTok, kPair>::kStageBytes;
+  constexpr int kSmemStride = Tile<kTok, kPair>::kSmemStride;
   constexpr int kRecvRows = kSplit > 1 ? kRows / kSplit : 0;  // rows received from the other CTA
   static_assert((kRows + kRecvRows) * kSmemStride * 4 <= kStages * kStageBytes,
                 "the staged and the received sums fit in the stage buffers");
@@ -222,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // a chunk's first tile: the running softmax values (max, denominator, numerator) of the carried
   // candidates of group j and feature f0 + i at [3 * (j * hf + i)], at most 2 x 32 or 64 values
   float* carried = (float*)(tmem_slot + 4);
-  static_assert(16 * 8 + 16 + 3 * 64 * 4 <= 1024, "barriers, flags and carried values fit their region");
+  static_assert((2 * kStages + 6) * 8 + 16 + 3 * 64 * 4 <= 1024, "barriers, flags and carried values fit their region");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ftile = blockIdx.x / kSplit, rank = blockIdx.x % kSplit, tt = blockIdx.y, b = blockIdx.z;
@@ -230,6 +237,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb0 = rank * nloc;
   const int nch = (nloc + kChunkKb - 1) / kChunkKb;
   const int t0 = tt * P.T - P.halo;  // virtual index (from the open group's start) of the tile's token 0
+  // a CTA pair: the even CTA (the leader) issues the MMAs for both; each loads its packed tile's
+  // weight planes and half of the token tile (the leader the first half)
+  const int prank = kP ? (int)(blockIdx.x & 1) : 0;
+  const bool leader = prank == 0;
 #ifdef CSA_DEBUG_BOUNDS
   const uint64_t kWait = P.wait_ns;  // the time-out test shortens the waits
 #else
@@ -243,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&chunk_full[i], 1);
-      mbar_init(&chunk_empty[i], kEpiThreads / 32);
+      mbar_init(&chunk_empty[i], kPair * kEpiThreads / 32);  // a pair: the leader's counts both CTAs' warps
     }
     mbar_init(mma_done, 1);
     mbar_init(recv_bar, 1);
@@ -251,11 +262,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     *order_seen = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_map(&map_x);
+    if constexpr (kP) prefetch_map(&map_w);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 1) {
+    if constexpr (kP)
+      tmem_alloc_pair(tmem_slot, kTmemCols);
+    else
+      tmem_alloc(tmem_slot, kTmemCols);
+  }
   griddep_launch_dependents();  // the entry kernel may be scheduled; it waits for this grid
   tc_fence_before();
   __syncthreads();
+  if constexpr (kP) {
+    cluster_arrive();
+    cluster_wait();  // both CTAs' barriers are initialised before either's copies complete on them
+  }
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -271,27 +292,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (P.test_stall && i == nloc - 1) break;  // test of the time-out path: the last stage never comes
 #endif
         uint8_t* st = smem + s * kStageBytes;
-        mbar_arrive_expect_tx(&full[s], kStageBytes);
-        bulk_load(st, P.w + plane_stage_elem(P.K / kKb, ftile, kb), 3 * kPlaneBytes, &full[s]);
-        tma_load_3d(st + 3 * kPlaneBytes, &map_x, kb * kKb, t0 - P.a, b, &full[s]);
+        if constexpr (kP) {
+          // both CTAs' copies complete on the leader's barrier, which expects the bytes of both
+          const uint32_t fb = cluster_map(&full[s], 0);
+          if (leader) mbar_arrive_expect_tx(&full[s], 2 * kStageBytes);
+          tma_load_3d_pair(st, &map_w, 0, (3 * kPlaneBytes / 512) * (ftile * (P.K / kKb) + kb), 0, fb);
+          tma_load_3d_pair(st + 3 * kPlaneBytes, &map_x, kb * kKb, t0 - P.a + prank * (kTok / 2), b, fb);
+        } else {
+          mbar_arrive_expect_tx(&full[s], kStageBytes);
+          bulk_load(st, P.w + plane_stage_elem(P.K / kKb, ftile, kb), 3 * kPlaneBytes, &full[s]);
+          tma_load_3d(st + 3 * kPlaneBytes, &map_x, kb * kKb, t0 - P.a, b, &full[s]);
+        }
         ++issued;
       }
       *issued_s = issued;
     }
   } else if (warp == 1) {
-    // ---- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(kRows, kTok);
+    // ---- MMA issuer (a pair: the leader's, for both CTAs)
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_bf16(kRows * kPair, kTok);
       bool ok = true;
       for (int c = 0; c < nch && ok; ++c) {
         const int buf = c & 1;
-        if (c >= 2 && !mbar_wait(&chunk_empty[buf], ((c >> 1) - 1) & 1, abort_flag, kWait)) break;
+        if (c >= 2 && !mbar_wait<kP>(&chunk_empty[buf], ((c >> 1) - 1) & 1, abort_flag, kWait)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * kTok);
         const int i0 = c * kChunkKb, i1 = min(nloc, i0 + kChunkKb);
         for (int i = i0; i < i1; ++i) {
           const int s = i % kStages;
-          if (!mbar_wait(&full[s], (i / kStages) & 1, abort_flag, kWait)) {
+          if (!mbar_wait<kP>(&full[s], (i / kStages) & 1, abort_flag, kWait)) {
             ok = false;
             break;
           }
@@ -299,12 +328,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st = smem_addr(smem + s * kStageBytes);
           const uint32_t xs = st + 3 * kPlaneBytes;
           for (int p = 0; p < 3; ++p)
-            for (int k = 0; k < kKb / 16; ++k)
-              mma_bf16(d, sw64_desc(st + p * kPlaneBytes + k * 32), sw64_desc(xs + k * 32), idesc,
-                       (i != i0 || p != 0 || k != 0) ? 1u : 0u);
-          mma_commit(&empty[s]);
+            for (int k = 0; k < kKb / 16; ++k) {
+              const uint64_t a = sw64_desc(st + p * kPlaneBytes + k * 32), bd = sw64_desc(xs + k * 32);
+              const uint32_t en = (i != i0 || p != 0 || k != 0) ? 1u : 0u;
+              if constexpr (kP)
+                mma_bf16_pair(d, a, bd, idesc, en);
+              else
+                mma_bf16(d, a, bd, idesc, en);
+            }
+          if constexpr (kP)
+            mma_commit_pair_multicast(&empty[s], 0x3);  // both CTAs' producers may refill the stage
+          else
+            mma_commit(&empty[s]);
         }
-        if (ok) mma_commit(&chunk_full[buf]);  // arrives once this chunk's MMAs have completed
+        if (ok) {  // arrives once this chunk's MMAs have completed
+          if constexpr (kP)
+            mma_commit_pair_multicast(&chunk_full[buf], 0x3);
+          else
+            mma_commit(&chunk_full[buf]);
+        }
       }
     }
   } else {
@@ -392,7 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&chunk_empty[buf]);
+      if (lane == 0) {
+        if constexpr (kP)
+          mbar_arrive_remote(cluster_map(&chunk_empty[buf], 0));  // the leader's MMAs may reuse it
+        else
+          mbar_arrive(&chunk_empty[buf]);
+      }
     }
     if (ok && !*abort_flag) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -411,12 +458,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (aborted) {
     // a wait ran out: the copies in flight land and the issued MMAs complete before the TMEM is
     // freed and the CTA leaves (this call's outputs are undefined; the flag says so)
-    drain_after_abort(warp == 0 && lane == 0, warp == 1 && lane == 0, full, kStages, *issued_s, mma_done);
+    if constexpr (kP) {
+      // the leader's barriers count both CTAs' copies of the stages it expected, and only it
+      // issued MMAs; the other CTA's copies of stages the leader never expected are given time
+      // to land (a bounded pause: nothing waits for them)
+      if (warp == 0 && lane == 0) {
+        if (leader) {
+          for (int t = max(0, *issued_s - kStages); t < *issued_s; ++t)
+            mbar_wait_bounded(&full[t % kStages], (t / kStages) & 1);
+        } else {
+          const uint64_t t0 = globaltimer();
+          while (globaltimer() - t0 < 50000ull) __nanosleep(1000);
+        }
+      }
+      if (warp == 1 && lane == 0 && leader) {
+        mma_commit_pair(mma_done);
+        mbar_wait_bounded(mma_done, 0);
+      }
+    } else {
+      drain_after_abort(warp == 0 && lane == 0, warp == 1 && lane == 0, full, kStages, *issued_s, mma_done);
+    }
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0) atomicOr(P.flag, 4);
   }
-  if (warp == 1) {
+  if (warp == 1 && !kP) {  // a pair frees its TMEM at the end, after both CTAs are done with it
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -728,6 +794,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_arrive();
     cluster_wait();  // the other CTA has received this CTA's copy: its source may go
   }
+  if constexpr (kP) {
+    tc_fence_before();
+    cluster_arrive();
+    cluster_wait();  // the leader's MMAs into this CTA's TMEM and its arrivals on this CTA's barriers are over
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc_pair(tmem, kTmemCols);
+    }
+  }
 }
 
 // The entries in their own kernel: a CTA of 128 threads takes 128 / tpe consecutive entries (one
@@ -786,17 +861,18 @@ long long stage_cycles(int tok) { return std::max(3LL * tok, 750LL); }
 constexpr long long kTileCycles = 6700;
 constexpr long long kSplitCycles = 5000;
 
-template <int TOK, int SPLIT>
+template <int TOK, int SPLIT, int PAIR>
 size_t smem_bytes() {
-  return (size_t)tc::kStages * tc::Tile<TOK>::kStageBytes + 1024 /* barriers */ + 1024 /* alignment */;
+  using T = tc::Tile<TOK, PAIR>;
+  return (size_t)T::kStages * T::kStageBytes + 1024 /* barriers */ + 1024 /* alignment */;
 }
 
-template <int TOK, int SPLIT>
+template <int TOK, int SPLIT, int PAIR>
 cudaError_t set_smem_attr() {
   static std::atomic<unsigned long long> attr_set{0};
   return tcx::once_per_device(attr_set, [] {
-    return cudaFuncSetAttribute(tc::prefill_tc_kernel<TOK, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)smem_bytes<TOK, SPLIT>());
+    return cudaFuncSetAttribute(tc::prefill_tc_kernel<TOK, SPLIT, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_bytes<TOK, SPLIT, PAIR>());
   });
 }
 
@@ -810,7 +886,7 @@ int split_clusters() {
   const int k = known[dev & 63].load();
   if (k > 0) return k - 1;
   int n = 0;
-  if (set_smem_attr<TOK, 2>() == cudaSuccess) {
+  if (set_smem_attr<TOK, 2, 1>() == cudaSuccess) {
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 2;
@@ -819,10 +895,10 @@ int split_clusters() {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * current_sm_count(), 1, 1);
     cfg.blockDim = dim3(tc::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem_bytes<TOK, 2>();
+    cfg.dynamicSmemBytes = smem_bytes<TOK, 2, 1>();
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, (const void*)tc::prefill_tc_kernel<TOK, 2>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, (const void*)tc::prefill_tc_kernel<TOK, 2, 1>, &cfg) != cudaSuccess) {
       (void)cudaGetLastError();
       n = 0;
     }
@@ -874,10 +950,12 @@ PrefillPlan prefill_shape(const csa_compressor* c, int B, int N) {
       }
     }
   }
+  // asked for, unsplit tiles run as CTA pairs wherever the packed tiles pair up
+  if (c->opt.prefill_pair == 2 && best.split == 1 && c->pk.ntiles % 2 == 0) best.pair = 2;
   return best;
 }
 
-template <int TOK, int SPLIT>
+template <int TOK, int SPLIT, int PAIR>
 cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N, int slot_offset, const Chunk& ck,
                        const csa_out& out, void* scratch, size_t scratch_bytes, cudaStream_t s) {
   using namespace tc;
@@ -928,10 +1006,26 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
     // x: [B][N][dim] bf16; out-of-range tokens (the halo before token 0, the tail past N) read as 0
     cuuint64_t dims[3] = {(cuuint64_t)c->dim, (cuuint64_t)N, (cuuint64_t)B};
     cuuint64_t strides[2] = {(cuuint64_t)c->dim * 2, (cuuint64_t)N * c->dim * 2};
-    cuuint32_t box[3] = {kKb, TOK, 1};
+    cuuint32_t box[3] = {kKb, TOK / PAIR, 1};  // a pair: each CTA loads half of the tile's tokens
     cuuint32_t es[3] = {1, 1, 1};
     if (encode(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)x, dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  CUtensorMap mw = mx;  // read only by a CTA pair
+  if (PAIR > 1) {
+    // the weight planes as the contiguous 24 KB stages they are stored in (already the swizzled
+    // image a stage holds, so copied as they are), seen as rows of 512 bytes: a stage (the three
+    // planes of one tile and K block) is 48 rows
+    const int nkb = c->dim / kKb;
+    constexpr int kW = 256, kWRows = 3 * kPlaneBytes / (2 * kW);
+    cuuint64_t dims[3] = {(cuuint64_t)kW, (cuuint64_t)c->pk.ntiles * nkb * kWRows, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)kW * 2, (cuuint64_t)c->pk.ntiles * nkb * kWRows * kW * 2};
+    cuuint32_t box[3] = {kW, kWRows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (encode(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)c->w_planes, dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -953,13 +1047,13 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
   Q.order_n = B * c->pk.ntiles * 2;
   Q.ep = epi_params(c);
   Q.out = out;
-  cudaError_t ea = set_smem_attr<TOK, SPLIT>();
+  cudaError_t ea = set_smem_attr<TOK, SPLIT, PAIR>();
   if (ea != cudaSuccess) return ea;
   cudaLaunchAttribute pat[1];
   int npat = 0;
-  if (SPLIT > 1) {  // the two K halves of a tile: one cluster
+  if (SPLIT > 1 || PAIR > 1) {  // the two K halves of a tile, or two packed tiles sharing the MMA: one cluster
     pat[npat].id = cudaLaunchAttributeClusterDimension;
-    pat[npat].val.clusterDim.x = SPLIT;
+    pat[npat].val.clusterDim.x = SPLIT * PAIR;
     pat[npat].val.clusterDim.y = 1;
     pat[npat].val.clusterDim.z = 1;
     ++npat;
@@ -967,11 +1061,11 @@ cudaError_t launch_tok(const csa_compressor* c, const uint16_t* x, int B, int N,
   cudaLaunchConfig_t pc = {};
   pc.gridDim = dim3(c->pk.ntiles * SPLIT, P.ntt, B);
   pc.blockDim = dim3(kThreads, 1, 1);
-  pc.dynamicSmemBytes = smem_bytes<TOK, SPLIT>();
+  pc.dynamicSmemBytes = smem_bytes<TOK, SPLIT, PAIR>();
   pc.stream = s;
   pc.attrs = pat;
   pc.numAttrs = npat;
-  cudaError_t e = cudaLaunchKernelEx(&pc, prefill_tc_kernel<TOK, SPLIT>, mx, P);
+  cudaError_t e = cudaLaunchKernelEx(&pc, prefill_tc_kernel<TOK, SPLIT, PAIR>, mx, mw, P);
   if (e != cudaSuccess || P.G == 0) return e;
   const long long ctas = ((long long)B * P.G + 128 / Q.tpe - 1) / (128 / Q.tpe);
   cudaLaunchAttribute at[1];
@@ -1003,18 +1097,21 @@ cudaError_t launch_prefill_tc(const csa_compressor* c, const uint16_t* x, int B,
                               const Chunk& ck, const PrefillPlan& plan, const csa_out& out, void* scratch,
                               size_t scratch_bytes, cudaStream_t s) {
   if (scratch_bytes < plan.bytes) return cudaErrorInvalidValue;
-  const bool split = plan.split == 2;
+  if (plan.pair == 2 && (plan.split != 1 || c->pk.ntiles % 2 != 0)) return cudaErrorInvalidValue;
+  const int kind = plan.split == 2 ? 2 : plan.pair == 2 ? 1 : 0;  // split, pair, one CTA per tile
+#define CSA_LAUNCH_TOK(T)                                                                                         \
+  return kind == 2   ? launch_tok<T, 2, 1>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s)          \
+         : kind == 1 ? launch_tok<T, 1, 2>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s)          \
+                     : launch_tok<T, 1, 1>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s)
   switch (plan.tok) {
     case 224:
-      return split ? launch_tok<224, 2>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s)
-                   : launch_tok<224, 1>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s);
+      CSA_LAUNCH_TOK(224);
     case 128:
-      return split ? launch_tok<128, 2>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s)
-                   : launch_tok<128, 1>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s);
+      CSA_LAUNCH_TOK(128);
     default:
-      return split ? launch_tok<256, 2>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s)
-                   : launch_tok<256, 1>(c, x, B, N, slot_offset, ck, out, scratch, scratch_bytes, s);
+      CSA_LAUNCH_TOK(256);
   }
+#undef CSA_LAUNCH_TOK
 }
 
 }  // namespace csa

@@ -82,6 +82,11 @@ typedef struct {
                           2 = a cluster of two CTAs per tile, each taking half of K (dim), the two
                           partial sums added on chip.  The outputs agree within the rounding of
                           that addition; a tuning knob, not a change of the method. */
+  int prefill_pair;    /* 0 = one CTA per packed tile (default); 2 = where a tile is not split
+                          over K and the packed tiles pair up, two CTAs (a cluster of two) share
+                          one tcgen05 MMA of M = 256 rows, each holding its packed tile's weights
+                          and half of the token tile.  The same products and additions; a tuning
+                          knob (on GB300 it measured 2-3 % slower at the configurations here). */
 } csa_options;
 
 /* Output buffers of one call (dev).  Rows are entries: prefill [B][G][..], decode [B][..].
@@ -291,10 +296,12 @@ int64_t csa_kernel_launches(const csa_compressor* c);
 /* The launch geometry a tensor-core prefill of B sequences of N tokens at start_pos would use on
  * the current device (no counterpart on the pages; for tuning and measurement): *token_tile = the
  * tokens per tile including the overlapped halo (256, 224 or 128), *k_split = 1 (one CTA per tile)
- * or 2 (a cluster of two CTAs per tile, each half of dim).  Returns CSA_OK, CSA_ERR_ARG for a
+ * or 2 (a cluster of two CTAs per tile, each half of dim), *cta_pair (may be NULL) = 1, or 2 when
+ * two CTAs share one MMA of 256 rows (option prefill_pair).  Returns CSA_OK, CSA_ERR_ARG for a
  * NULL pointer or a bad shape, or CSA_ERR_STATE when the shape runs the CUDA-core projection
  * (csa_uses_tensor_cores(c) == 0).  Host only: nothing is enqueued. */
-int csa_prefill_geometry(const csa_compressor* c, int B, int N, int start_pos, int* token_tile, int* k_split);
+int csa_prefill_geometry(const csa_compressor* c, int B, int N, int start_pos, int* token_tile, int* k_split,
+                         int* cta_pair);
 
 /* Host-only: the YaRN RoPE table the library uploads ("Module compress", yarn_freqs_cis):
  * cos_out, sin_out [npos][rope_dim/2] f32 host for positions pos0..pos0+npos-1, computed in

@@ -39,7 +39,7 @@ def test_default_options():
     assert (o.max_batch, o.rope_dim, o.rope_base, o.rope_factor, o.rope_orig_len) == (128, 64, 160000.0, 16.0, 4096)
     assert (o.beta_fast, o.beta_slow, o.max_pos, o.fp4) == (32.0, 1.0, 262144, 1)
     assert abs(o.eps - 1e-6) < 1e-12
-    assert o.prefill_split == 0
+    assert o.prefill_split == 0 and o.prefill_pair == 0
 
 
 @pytest.mark.parametrize("args,frag", [((100, 512, 4, 1), "dim"), ((4096, 500, 4, 0), "head_dim"),
@@ -62,7 +62,7 @@ def test_create_rejects_bad_options():
     lib = csa.load_library()
     h = ctypes.c_void_p()
     for kw in (dict(rope_dim=63), dict(rope_dim=1024), dict(max_batch=0), dict(fp4=3), dict(fp4=-1),
-               dict(prefill_split=3), dict(prefill_split=-1)):
+               dict(prefill_split=3), dict(prefill_split=-1), dict(prefill_pair=1), dict(prefill_pair=3)):
         o = csa.default_options(**kw)
         assert lib.csa_compressor_create_ex(4096, 512, 4, 1, ctypes.byref(o), ctypes.byref(h)) == -1
     # the power-of-two quantiser takes blocks of 32 features

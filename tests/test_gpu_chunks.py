@@ -43,11 +43,11 @@ CHAINS = [
 ]
 
 
-@pytest.mark.parametrize("split", [1, 2])
+@pytest.mark.parametrize("split,pair", [(1, 0), (2, 0), (1, 2)])
 @pytest.mark.parametrize("dim,H,ratio,overlap,B,chunks", CHAINS)
-def test_prefill_chunks_then_decode(dim, H, ratio, overlap, B, chunks, split):
+def test_prefill_chunks_then_decode(dim, H, ratio, overlap, B, chunks, split, pair):
     layer = synthetic.Layer(dim, H, ratio, overlap, 1.0 / math.sqrt(dim), gate_scale=2.0, rope_dim=min(64, H), fp4=1)
-    g, o = make_pair(11, layer, max_batch=B + 1, split=split)
+    g, o = make_pair(11, layer, max_batch=B + 1, split=split, pair=pair)
     P = sum(chunks)
     x, *_ = layer_inputs(11, layer, B, P + 5)
     p0 = 0

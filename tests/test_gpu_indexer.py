@@ -80,11 +80,14 @@ def test_launch_geometry_of_the_measured_instances():
         finally:
             c.close()
     if sms == 152:  # the choices below are the model's for the 152-SM part
-        assert geo(synthetic.INDEXER) == {"token_tile": 224, "k_split": 2}
-        assert geo(synthetic.FLASH_CSA) == {"token_tile": 224, "k_split": 1}
-        assert geo(synthetic.HCA) == {"token_tile": 256, "k_split": 1}
+        assert geo(synthetic.INDEXER) == {"token_tile": 224, "k_split": 2, "cta_pair": 1}
+        assert geo(synthetic.FLASH_CSA) == {"token_tile": 224, "k_split": 1, "cta_pair": 1}
+        assert geo(synthetic.HCA) == {"token_tile": 256, "k_split": 1, "cta_pair": 1}
     assert geo(synthetic.INDEXER, prefill_split=1)["k_split"] == 1
     assert geo(synthetic.FLASH_CSA, prefill_split=2)["k_split"] == 2
+    # CTA pairs where asked for and the tiles are not split
+    assert geo(synthetic.FLASH_CSA, prefill_pair=2)["cta_pair"] == 2
+    assert geo(synthetic.INDEXER, prefill_pair=2, prefill_split=2)["cta_pair"] == 1
     narrow = csa.Compressor(128, 32, 3, 0, rope_dim=16)  # packed tile narrower than 128 rows: the CUDA-core projection
     try:
         with pytest.raises(csa.CSAError):

@@ -45,13 +45,14 @@ def opts_of(layer, max_batch=1, max_pos=262144):
     return dict(max_batch=max_batch, rope_dim=layer.rope_dim, fp4=layer.fp4, max_pos=max_pos)
 
 
-def make_pair(seed, layer, max_batch=1, max_pos=262144, split=0):
+def make_pair(seed, layer, max_batch=1, max_pos=262144, split=0, pair=0):
     """The library's compressor and the oracle's, with the same synthetic weights.  split forces
     the tensor-core prefill's launch geometry (1: one CTA per tile, 2: two CTAs of a cluster each
-    taking half of K; 0: chosen per call)."""
+    taking half of K; 0: chosen per call); pair = 2 asks for two CTAs sharing one MMA of 256 rows
+    where the tiles are not split."""
     wkv, wgate, gain = synthetic.weights(seed, layer)
     g = csa.Compressor(layer.dim, layer.head_dim, layer.ratio, layer.overlap, prefill_split=split,
-                       **opts_of(layer, max_batch, max_pos))
+                       prefill_pair=pair, **opts_of(layer, max_batch, max_pos))
     g.set_weights(torch.from_numpy(wkv).to(DEV), torch.from_numpy(wgate).to(DEV), torch.from_numpy(gain).to(DEV))
     o = oracle.Compressor(layer.dim, layer.head_dim, layer.ratio, layer.overlap, max_batch=max_batch,
                           rope_dim=layer.rope_dim, fp4=layer.fp4)
@@ -207,12 +208,12 @@ SMALL_FP4 = [(d, H, r, ov, B, N, 1) for d, H, r, ov, B, N in SMALL] + [
 ]
 
 
-@pytest.mark.parametrize("split", [1, 2])
+@pytest.mark.parametrize("split,pair", [(1, 0), (2, 0), (1, 2)])
 @pytest.mark.parametrize("dim,H,ratio,overlap,B,N,fp4", SMALL_FP4)
-def test_small_prefill_state_and_decode(dim, H, ratio, overlap, B, N, fp4, split):
+def test_small_prefill_state_and_decode(dim, H, ratio, overlap, B, N, fp4, split, pair):
     layer = synthetic.Layer(dim, H, ratio, overlap, 1.0 / math.sqrt(dim), gate_scale=2.0,
                             rope_dim=min(64, H), fp4=fp4)
-    g, o = make_pair(5, layer, max_batch=B + 1, split=split)
+    g, o = make_pair(5, layer, max_batch=B + 1, split=split, pair=pair)
     x, *_ = layer_inputs(5, layer, B, N + 6)
     xp = np.ascontiguousarray(x[:, :N])
     ref = o.prefill(xp, slot_offset=1)
@@ -269,6 +270,30 @@ def test_flash_csa_prefill_full():
     ref = o.prefill(x)
     frac, mx = check_entries(to_np(got), ref["prequant"], 1, "Flash CSA prefill")
     assert ref["G"] == 1024
+
+
+def test_cta_pairs_give_the_single_cta_results():
+    """Two CTAs sharing one MMA of 256 rows (prefill_pair = 2) form the same products and add them
+    in the same order as one CTA per packed tile: the Flash CSA prefill's entries (before and after
+    fp4) and its state are bit-identical, and a chunk continuing it is too."""
+    wl = synthetic.FLASH_CSA
+    layer = wl.layers[0]
+    x, *_ = layer_inputs(wl.seed, layer, 1, 4096 + 300)
+    res = []
+    for pair in (0, 2):
+        g, _ = make_pair(wl.seed, layer, pair=pair)
+        assert g.prefill_geometry(1, 4096)["cta_pair"] == (2 if pair else 1)
+        a = g.prefill(dev_bits(np.ascontiguousarray(x[:, :4096])))
+        b = g.prefill(dev_bits(np.ascontiguousarray(x[:, 4096:])), start_pos=4096)
+        torch.cuda.synchronize()
+        res.append((a, b, [t.cpu() for t in g.state_export()]))
+        assert g.device_status() == 0
+        g.close()
+    (a0, b0, s0), (a1, b1, s1) = res
+    for k in ("latent", "codes", "scales", "prequant"):
+        assert torch.equal(a0[k].cpu(), a1[k].cpu()), k
+        assert torch.equal(b0[k].cpu(), b1[k].cpu()), k
+    assert all(torch.equal(u, v) for u, v in zip(s0, s1))
 
 
 def sampled_groups(G, k, seed):
