@@ -50,6 +50,9 @@ def parse():
                     help="layer instances rotated in the decode measurement (0: enough to exceed L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-long", action="store_true", help="skip the long-context prefill sweep")
+    ap.add_argument("--prefill-pair", action="store_true",
+                    help="prefill compressors with the option prefill_pair = 2 (two CTAs sharing one MMA of 256 "
+                         "rows where the tiles pair up; off by default, measured slower): for profiling it")
     ap.add_argument("--clock-seconds", type=float, default=1.0,
                     help="seconds of untimed steps run under the clock sampler before the timed region")
     return ap.parse_args()
@@ -190,12 +193,13 @@ def hold_gpu(flush, n=64):
         flush.fill_(float(-i))
 
 
-def make_inputs(torch, csa, synthetic, layer, seed, B, N, rank, device):
+def make_inputs(torch, csa, synthetic, layer, seed, B, N, rank, device, args=None):
     x = np.stack([synthetic.tokens(seed, rank * B + b, 0, N, layer.dim) for b in range(B)])
     xb = torch.from_numpy(x).to(torch.bfloat16).to(device)
     wkv, wgate, gain = synthetic.weights(seed, layer)
+    opts = {"prefill_pair": 2} if args is not None and getattr(args, "prefill_pair", False) else {}
     comp = csa.Compressor(layer.dim, layer.head_dim, layer.ratio, layer.overlap, max_batch=max(B, 1),
-                          rope_dim=layer.rope_dim, fp4=layer.fp4)
+                          rope_dim=layer.rope_dim, fp4=layer.fp4, **opts)
     comp.set_weights(torch.from_numpy(wkv).to(device), torch.from_numpy(wgate).to(device),
                      torch.from_numpy(gain).to(device))
     return comp, xb
@@ -215,7 +219,7 @@ def run_ours(args, rank, world, local):
     layer = wl.layers[0]
     B, N = 1, wl.tokens[0]
     G = N // layer.ratio
-    comp, x = make_inputs(torch, csa, synthetic, layer, wl.seed, B, N, rank, device)
+    comp, x = make_inputs(torch, csa, synthetic, layer, wl.seed, B, N, rank, device, args)
     H = layer.head_dim
     out = comp._alloc_out(B * G, device, prequant=False)
     stream = torch.cuda.current_stream(device)
@@ -428,7 +432,7 @@ def bench_prefill_workload(args, torch, csa, synthetic, device, peaks, world, wl
     layer = wl.layers[0]
     B, N = wl.batch, wl.tokens[0]
     G = N // layer.ratio
-    comp, x = make_inputs(torch, csa, synthetic, layer, wl.seed, B, N, 0, device)
+    comp, x = make_inputs(torch, csa, synthetic, layer, wl.seed, B, N, 0, device, args)
     if gate_bias:
         ape = torch.randn(layer.ratio, layer.width, generator=torch.Generator().manual_seed(7)).to(device)
         comp.set_gate_bias(ape)
@@ -520,7 +524,7 @@ def bench_chunked(args, torch, csa, synthetic, device, peaks, world):
     wl = synthetic.FLASH_CSA
     layer = wl.layers[0]
     B, N, p0 = 1, wl.tokens[0], wl.tokens[0] + 2
-    comp, x = make_inputs(torch, csa, synthetic, layer, wl.seed, B, N, 0, device)
+    comp, x = make_inputs(torch, csa, synthetic, layer, wl.seed, B, N, 0, device, args)
     G = (p0 + N) // layer.ratio - p0 // layer.ratio
     out = comp._alloc_out(B * G, device, prequant=False)
     stream = torch.cuda.current_stream(device)
