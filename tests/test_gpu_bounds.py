@@ -31,7 +31,7 @@ def test_parity_cases_on_the_bounds_checked_build():
         "test_small_prefill_state_and_decode", "test_decode_batch_beyond_one_token_tile",
         "test_errors_are_reported_not_raised_on_the_device", "test_decode_steps_in_a_cuda_graph")]
     cases += [os.path.join(HERE, "test_gpu_chunks.py") + "::" + t for t in (
-        "test_prefill_chunks_then_decode", "test_prefill_into_cache_rows")]
+        "test_prefill_chunks_then_decode", "test_prefill_into_cache_rows", "test_chunk_of_many_sequences_across_waves")]
     cases += [os.path.join(HERE, "test_gpu_gate_bias.py"), os.path.join(HERE, "test_gpu_timeout.py"),
               os.path.join(HERE, "test_zz_no_alloc.py")]
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider", *cases],

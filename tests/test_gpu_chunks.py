@@ -112,6 +112,29 @@ def test_random_chunk_chains(dim, H, ratio, overlap, B, chunks):
     assert g.device_status() == 0
 
 
+@pytest.mark.parametrize("split,pair", [(1, 0), (1, 2)])
+def test_chunk_of_many_sequences_across_waves(split, pair):
+    """A chunk whose first token tile reads candidates from the state that its later tiles rewrite,
+    for 64 sequences at once: the grid (packed tiles x token tiles x sequences) runs in several
+    waves, so a later tile's CTA may start before or long after the first tile of its sequence;
+    it writes the state only once that tile has read it.  Entries and state against the oracle,
+    and no time-out."""
+    layer = synthetic.Layer(256, 128, 4, 1, 1.0 / 16, gate_scale=2.0, rope_dim=64, fp4=1)
+    B, p0, n = 64, 4 * 20 + 2, 4 * 75 + 1  # the chunk starts two tokens into a group
+    g, o = make_pair(31, layer, max_batch=B, split=split, pair=pair)
+    x, *_ = layer_inputs(31, layer, B, p0 + n)
+    for q0, q1 in ((0, p0), (p0, p0 + n)):
+        xc = np.ascontiguousarray(x[:, q0:q1])
+        ref = o.prefill(xc, start_pos=q0)
+        got = g.prefill(dev_bits(xc), start_pos=q0)
+        torch.cuda.synchronize()
+        check_entries(to_np(got), ref["prequant"], 1, f"chunk at {q0} (+{q1 - q0})")
+    T = g.prefill_geometry(B, n, p0)["token_tile"] - 4  # tokens a tile owns (overlapped: less the halo)
+    assert -(-(p0 % 4 + n) // T) >= 2  # several token tiles per sequence
+    check_state(g, o, "state after the chunk")
+    assert g.device_status() == 0
+
+
 def test_prefill_into_cache_rows():
     layer = synthetic.Layer(256, 128, 4, 1, 1.0 / 16, gate_scale=2.0, rope_dim=64, fp4=1)
     B, rows = 2, 100
