@@ -523,10 +523,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lost && threadIdx.x == 0) atomicOr(P.flag, 4);
   }
   // Split without a gate bias, the received half-K sums are added where the state writes and the
-  // pool read them (`fold`); otherwise the pass below leaves this CTA's final values in stg.
+  // pool read them (`fold`); unsplit and overlapped, so is the gate bias (`fold_bias`: the token in
+  // tile column c has group position c % 4, as the tile starts on a group); otherwise the pass
+  // below leaves this CTA's final values in stg.
   const float* recv = stg + kRows * kSmemStride;
   const bool fold = kSplit > 1 && !P.ape;
-  if (!aborted && !lost && (kSplit > 1 || P.ape) && !fold) {
+  const bool fold_bias = kSplit == 1 && P.ape && P.overlap;
+  if (!aborted && !lost && (kSplit > 1 || P.ape) && !fold && !fold_bias) {
     // this CTA's rows: the two half-K sums added (the same sum in either order), then wgate(x) +
     // the positional bias of each token's place in its group (score rows; column c holds the
     // token at position ratio * g0 + t0 + c, halo columns wrap harmlessly).  Unsplit, only the
@@ -567,15 +570,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // the final sum of packed row (kind, f) of this CTA's features at tile column col, one value or
   // the four from col (col a multiple of 4)
+  // the bias of packed row prow at group position sl (zero at the kv rows)
+  auto bias = [&](int prow, int sl) { return __ldg(P.ape + (size_t)sl * P.ncol + ftile * kRows + prow); };
   auto at = [&](int kind, int f, int col) -> float {
     float v = stg[(kind * F + f) * kSmemStride + col];
     if (fold) v += recv[(kind * hf + f - f0) * kSmemStride + col];
+    if (fold_bias && kind >= pk.nk / 2) v += bias(kind * F + f, (t0 + col) & 3);
     return v;
   };
+  // the four group positions' biases of this thread's pool feature (col is a multiple of 4, so
+  // position i is element i), for the score kinds
+  const int fpool = f0 + (int)threadIdx.x % hf;
+  float4 bias4[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  if (fold_bias)
+    for (int u = 0; u < 2; ++u)
+      bias4[u] = make_float4(bias((S_A + u) * F + fpool, 0), bias((S_A + u) * F + fpool, 1),
+                             bias((S_A + u) * F + fpool, 2), bias((S_A + u) * F + fpool, 3));
   auto at4 = [&](int kind, int f, int col) -> float4 {
     float4 v = *reinterpret_cast<const float4*>(stg + (kind * F + f) * kSmemStride + col);
     if (fold) {
       const float4 w = *reinterpret_cast<const float4*>(recv + (kind * hf + f - f0) * kSmemStride + col);
+      v.x += w.x;
+      v.y += w.y;
+      v.z += w.z;
+      v.w += w.w;
+    }
+    if (fold_bias && kind >= S_A) {  // f is this thread's pool feature
+      const float4 w = bias4[kind - S_A];
       v.x += w.x;
       v.y += w.y;
       v.z += w.z;
