@@ -33,7 +33,7 @@ _lib = None
 ABI_FUNCTIONS = ("csa_options_default", "csa_compressor_create", "csa_compressor_create_ex",
                  "csa_compressor_set_weights", "csa_compress_prefill", "csa_compress_decode",
                  "csa_compress_decode_dev", "csa_state_reset", "csa_state_elems",
-                 "csa_state_export", "csa_device_status", "csa_compressor_destroy", "csa_last_error",
+                 "csa_state_export", "csa_state_import", "csa_device_status", "csa_compressor_destroy", "csa_last_error",
                  "csa_fp4_e4m3_roundtrip", "csa_rope_table", "csa_set_profile_events", "csa_kernel_launches",
                  "csa_uses_tensor_cores", "csa_compress_prefill_noalloc", "csa_compress_prefill_into",
                  "csa_prefill_geometry",
@@ -89,6 +89,7 @@ def load_library(build_if_missing: bool = True):
             "csa_state_reset": ([P, I, I, P], I),
             "csa_state_elems": ([P], I64),
             "csa_state_export": ([P, P, P, P], I),
+            "csa_state_import": ([P, P, P, P], I),
             "csa_device_status": ([P, P], I),
             "csa_compressor_destroy": ([P], None),
             "csa_last_error": ([], ctypes.c_char_p),
@@ -355,6 +356,17 @@ class Compressor:
         mb, H = self.options.max_batch, self.head_dim
         shape = (mb, 2, 4, 2 * H) if self.overlap else (mb, self.ratio, H)
         return kv.view(shape), sc.view(shape)
+
+    def state_import(self, kv, score, stream=None):
+        """Replaces the whole state with kv and score (f32 CUDA tensors in the layout state_export
+        returns, e.g. another handle's)."""
+        n = _check(self._lib.csa_state_elems(self._h), "csa_state_elems")
+        kv, score = kv.contiguous(), score.contiguous()
+        for t in (kv, score):
+            if t.dtype != torch.float32 or not t.is_cuda or t.numel() != n:
+                raise CSAError(f"state arrays must be f32 CUDA tensors of {n} elements")
+            _on_current_device(t)
+        _check(self._lib.csa_state_import(self._h, _dptr(kv), _dptr(score), _stream(stream)), "csa_state_import")
 
     def set_profile_events(self, start=None, stop=None):
         """torch.cuda.Event pair (enable_timing=True) recorded around the dominant kernel."""

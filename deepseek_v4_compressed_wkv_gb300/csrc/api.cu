@@ -507,6 +507,20 @@ int csa_state_export(const csa_compressor* c, float* kv, float* score, csa_strea
   return CSA_OK;
 }
 
+int csa_state_import(csa_compressor* c, const float* kv, const float* score, csa_stream_t stream) {
+  if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
+  if (!kv || !score) return fail(CSA_ERR_ARG, "kv and score are required");
+  if (int rc = check_device(c, "csa_state_import")) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int mb = c->opt.max_batch;
+  CSA_CUDA(csa::launch_state_import(c, kv, score, s), "state import launch");
+  CSA_CUDA(csa::invalidate_decode_acc(c, 0, mb, s), "invalidate decode running values");
+  CSA_CUDA(cudaMemsetAsync(c->prefill_order, 0, (size_t)mb * c->pk.ntiles * 2 * sizeof(int), s),
+           "reset chunk ordering counters");
+  c->launches += 1;
+  return CSA_OK;
+}
+
 int csa_set_profile_events(csa_compressor* c, csa_event_t start, csa_event_t stop) {
   if (!c) return fail(CSA_ERR_ARG, "handle is NULL");
   if ((start == nullptr) != (stop == nullptr)) return fail(CSA_ERR_ARG, "set both events or neither");

@@ -20,6 +20,7 @@ cudaError_t launch_decode_emit(const csa_compressor* c, const int32_t* start_pos
                                uint8_t* emitted, cudaStream_t s);
 cudaError_t launch_state_reset(const csa_compressor* c, int slot_begin, int count, cudaStream_t s);
 cudaError_t launch_state_export(const csa_compressor* c, float* kv, float* score, cudaStream_t s);
+cudaError_t launch_state_import(const csa_compressor* c, const float* kv, const float* score, cudaStream_t s);
 cudaError_t launch_fp4_roundtrip(const uint16_t* in, long long nb, uint8_t* codes, uint8_t* scales, uint16_t* out,
                                  cudaStream_t s);
 cudaError_t launch_fp4_e8m0_roundtrip(const uint16_t* in, long long nb, uint8_t* codes, uint8_t* scales,

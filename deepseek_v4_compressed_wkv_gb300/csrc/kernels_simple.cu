@@ -334,6 +334,21 @@ __global__ void state_export_kernel(const float* __restrict__ state, Packing pk,
   }
 }
 
+// The inverse of state_export_kernel: the logical arrays written back into the packed state.
+__global__ void state_import_kernel(float* __restrict__ state, Packing pk, int overlap, size_t rows,
+                                    const float* __restrict__ kv, const float* __restrict__ score) {
+  const int W = (1 + overlap) * pk.H, ncol = pk.cols();
+  const size_t n = rows * W;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = i / W;
+    const int c = (int)(i % W);
+    const int br = c / pk.H, f = c % pk.H;
+    float* row = state + r * ncol;
+    row[pk.col(overlap ? (br ? KV_B : KV_A) : KV, f)] = kv[i];
+    row[pk.col(overlap ? (br ? S_B : S_A) : S, f)] = score[i];
+  }
+}
+
 __global__ void fp4_roundtrip_kernel(const uint16_t* __restrict__ in, long long nb, uint8_t* __restrict__ codes,
                                      uint8_t* __restrict__ scales, uint16_t* __restrict__ out) {
   for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nb; b += (long long)gridDim.x * blockDim.x) {
@@ -445,6 +460,12 @@ cudaError_t launch_state_reset(const csa_compressor* c, int slot_begin, int coun
 cudaError_t launch_state_export(const csa_compressor* c, float* kv, float* score, cudaStream_t s) {
   const size_t rows = (size_t)c->opt.max_batch * c->slots;
   state_export_kernel<<<grid_cap(rows * c->width, 256), 256, 0, s>>>(c->state, c->pk, c->overlap, rows, kv, score);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_state_import(const csa_compressor* c, const float* kv, const float* score, cudaStream_t s) {
+  const size_t rows = (size_t)c->opt.max_batch * c->slots;
+  state_import_kernel<<<grid_cap(rows * c->width, 256), 256, 0, s>>>(c->state, c->pk, c->overlap, rows, kv, score);
   return cudaGetLastError();
 }
 

@@ -245,6 +245,13 @@ int64_t csa_state_elems(const csa_compressor* c);
  * pages keep the state out of checkpoints). */
 int csa_state_export(const csa_compressor* c, float* kv, float* score, csa_stream_t stream);
 
+/* The inverse of csa_state_export: replaces the whole state (every sequence's slots) with kv and
+ * score (dev, csa_state_elems floats each, the logical layout above), e.g. a session moved from
+ * another handle of the same shape and options.  The decode running values kept between calls
+ * are marked stale (the next decode rebuilds them from the slots, as after a prefill), and the
+ * chunk ordering counters are cleared.  Returns CSA_OK or a negative csa_status. */
+int csa_state_import(csa_compressor* c, const float* kv, const float* score, csa_stream_t stream);
+
 /* Reads and clears the device-side error flag of the handle (synchronises the stream).
  * Returns CSA_OK if no kernel flagged anything since the last call; CSA_ERR_TIMEOUT if a
  * device-side wait ran out of its time budget (flag bit 4: the kernel stopped its work, let its

@@ -743,3 +743,46 @@ def test_decode_rollback_and_reset_between_steps():
         assert got[li], li
         merged = {kk: np.concatenate([gd[kk] for gd in got[li]]) for kk in got[li][0]}
         check_entries(merged, np.concatenate(ref[li]), 1, f"rollback/reset layer {li}")
+
+
+@pytest.mark.parametrize("li", [0, 1])
+def test_state_moves_to_another_handle(li):
+    """csa_state_import: the state exported from one handle and imported into another of the same
+    shape continues the same sessions.  Both handles then decode the same tokens: the overlapped
+    compressor's entries are bit-identical to the first handle's; the non-overlapped one rebuilds
+    its running softmax values from the imported slots (the same softmax in another order), so its
+    entries are checked against the oracle, which continues the sessions as well."""
+    seed, B = 41, 16
+    layer = DECODE_PAIR[li]
+    sp0, ((g, o),) = _decode_setup(seed, [layer], B, 61)
+    for k in range(3):  # a few steps first, so that the running values are in use
+        sp = (sp0 + k).astype(np.int32)
+        xt = _step_inputs(seed, layer, sp)
+        o.decode(xt, sp)
+        g.decode(dev_bits(xt), torch.from_numpy(sp).to(DEV))
+    h, _ = make_pair(seed, layer, max_batch=B)
+    kv, sc = g.state_export()
+    h.state_import(kv, sc)
+    k2, s2 = h.state_export()
+    assert torch.equal(kv, k2) and torch.equal(sc, s2)
+    got, ref = [], []
+    for k in range(3, 3 + 2 * layer.ratio):
+        sp = (sp0 + k).astype(np.int32)
+        xt = _step_inputs(seed, layer, sp)
+        r = o.decode(xt, sp)
+        a = g.decode(dev_bits(xt), torch.from_numpy(sp).to(DEV))
+        b_ = h.decode(dev_bits(xt), torch.from_numpy(sp).to(DEV))
+        em = b_["emitted"].cpu().numpy()
+        assert np.array_equal(em, r["emitted"]) and np.array_equal(em, a["emitted"].cpu().numpy())
+        rows = np.flatnonzero(em)
+        if rows.size:
+            if layer.overlap:
+                assert torch.equal(a["latent"][rows], b_["latent"][rows])
+            got.append(to_np(b_, rows=rows))
+            ref.append(r["prequant"][rows])
+    assert got
+    merged = {kk: np.concatenate([gd[kk] for gd in got]) for kk in got[0]}
+    check_entries(merged, np.concatenate(ref), 1, "decode after the state moved")
+    assert g.device_status() == 0 and h.device_status() == 0
+    with pytest.raises(csa.CSAError):
+        h.state_import(kv[:-1], sc)
