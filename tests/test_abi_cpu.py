@@ -79,6 +79,8 @@ def test_null_handle_calls_fail_cleanly():
     assert lib.csa_compressor_create(256, 64, 4, 1, None) == -1  # no place for the handle
     assert lib.csa_state_reset(None, 0, 1, None) == -1
     assert lib.csa_state_elems(None) == -1
+    assert lib.csa_state_export(None, None, None, None) == -1
+    assert lib.csa_state_import(None, None, None, None) == -1
     assert lib.csa_compress_prefill_into(None, None, 1, 4, 0, 0, None, 8, None) == -1
     assert lib.csa_compress_prefill_noalloc(None, None, 1, 4, 0, 0, None, None) == -1
     assert lib.csa_compressor_set_gate_bias(None, None, None) == -1
