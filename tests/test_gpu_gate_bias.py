@@ -24,11 +24,14 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("split", [1, 2])
+@pytest.mark.parametrize("split,pair", [(1, 0), (2, 0), (1, 2)])
 @pytest.mark.parametrize("dim,H,ratio,overlap,B,N,Nc", SHAPES)
-def test_gate_bias_prefill_chunk_decode(dim, H, ratio, overlap, B, N, Nc, split):
+def test_gate_bias_prefill_chunk_decode(dim, H, ratio, overlap, B, N, Nc, split, pair):
+    """The bias where the prefill adds it (overlapped and one CTA per tile: where the pool and the
+    state writes read the scores; otherwise in a pass over the staged rows), in decode and in the
+    CUDA-core path, against the oracle's biased logits."""
     layer = synthetic.Layer(dim, H, ratio, overlap, 1.0 / math.sqrt(dim), gate_scale=2.0, rope_dim=min(64, H), fp4=1)
-    g, o = make_pair(13, layer, max_batch=B, split=split)
+    g, o = make_pair(13, layer, max_batch=B, split=split, pair=pair)
     ape = np.random.default_rng(ratio).standard_normal((ratio, (1 + overlap) * H)).astype(np.float32) * 2
     g.set_gate_bias(torch.from_numpy(ape).to(DEV))
     o.set_gate_bias(ape)
